@@ -1,0 +1,254 @@
+/*
+ * minite.h -- C ABI of the native-NVFP4 W4A4 MoE expert MLP (GB300, sm_103a).
+ *
+ * The path: per-token NVFP4 quantization fused into the MoE permutation and
+ * into the routing-weighted SwiGLU, a block-scaled grouped GEMM over experts
+ * that reads contiguous expert buffers and device-side offsets, and the
+ * combine back to token order.
+ *
+ * Sources. "miniTE Technical Report: Stable and Efficient Reinforcement
+ * Learning with Native NVFP4" (summary page), section "Follow the numerical
+ * execution path" (per-token activation scaling) and section "Two
+ * complementary interventions" (amax computed during permutation and during
+ * weighted SwiGLU; scale-layout conversion fused with quantization;
+ * contiguous buffers with device-side metadata). "miniTE accélère le RL en
+ * NVFP4 sur B300", lead (W4A4) and section "Diagnostic, alignement et noyaux
+ * rapides" (grouped GEMMs over the experts of a MoE layer).
+ *
+ * Common rules for every entry point:
+ *  - Pointers named *device* are CUDA device pointers owned by the caller.
+ *    The library allocates no memory and keeps no pointer after a call
+ *    returns. Buffers must not overlap unless stated.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *    never synchronizes the host. Host-detectable errors (null pointers, bad
+ *    shapes, bad alignment) are returned before anything is enqueued.
+ *  - Errors found on the device (routing ids out of range, a pipeline wait
+ *    that timed out) are OR-ed as bits (1 << code) into `*status`, a caller
+ *    owned device int32 that the caller zeroes and reads after its own
+ *    synchronization. `status` may be NULL, in which case they are dropped.
+ *  - BF16 tensors are raw 16-bit patterns (`const void*`), row-major.
+ *  - NVFP4 data: codes are packed E2M1, two per byte, element 2i in the low
+ *    nibble; scale factors (SF) are unsigned E4M3 bytes, one per 16 elements
+ *    along the blocked dimension, stored in 128-row x 4-column atoms of
+ *    512 bytes: for a region with rows padded to 128 and Kc = roundup(K/16, 4)
+ *    SF columns, the SF of row r, column c is at byte
+ *      ((r/128)*(Kc/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4.
+ *    Padding bytes are written as 0. Dequantized value = e2m1(code) * sf / g.
+ *  - Global scale g (FP32): 2688 / amax of the row (activations) or of the
+ *    whole group (weights), capped at FLT_MAX; 1 when amax is 0.
+ *  - Base pointers must be 16-byte aligned; the GEMM operands 128-byte.
+ */
+#ifndef MINITE_H
+#define MINITE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* minite_stream_t;
+
+typedef enum {
+  MINITE_OK = 0,
+  MINITE_ERR_INVALID_ARG = 1,      /* null pointer, bad enum, bad alignment, small workspace */
+  MINITE_ERR_UNSUPPORTED_SHAPE = 2,/* a size rule below is violated */
+  MINITE_ERR_CUDA = 3,             /* a CUDA launch or runtime call failed */
+  MINITE_ERR_TIMEOUT = 4,          /* device: a pipeline wait gave up (status bit 1<<4) */
+  MINITE_ERR_BAD_ROUTING = 5       /* device: a routing id outside [0, E) (status bit 1<<5) */
+} minite_status_t;
+
+enum { MINITE_SCALE_PER_ROW = 0, MINITE_SCALE_PER_GROUP = 1 };
+enum { MINITE_ALONG_COLS = 0, MINITE_ALONG_ROWS = 1 };
+enum { MINITE_OUT_BF16 = 0, MINITE_OUT_FP32 = 1 };
+enum { MINITE_OP_QUANTIZE = 0, MINITE_OP_PERMUTE_QUANT = 1 };
+
+/*
+ * minite_quantize_nvfp4 -- NVFP4 quantization of `groups` BF16 matrices.
+ *
+ * Cites: per-token activation scaling ("Follow the numerical execution
+ * path"); swizzled scale layout written by the quantizer itself ("Two
+ * complementary interventions").
+ *
+ * x:           device, BF16 [groups, rows, cols].
+ * scale_mode:  MINITE_SCALE_PER_ROW: one g per quantized row (activations);
+ *              MINITE_SCALE_PER_GROUP: one g per group from the amax of the
+ *              whole group (one expert's weight matrix).
+ * orientation: MINITE_ALONG_COLS: blocks of 16 along cols; the quantized
+ *              matrix of a group is x[g] itself, [rows, cols].
+ *              MINITE_ALONG_ROWS: blocks of 16 along rows; the quantized
+ *              matrix is x[g] transposed, [cols, rows] (the dgrad layout of a
+ *              forward weight).
+ *              Let (Rq, Cq) be the quantized matrix's shape: (rows, cols) or
+ *              (cols, rows).
+ * gscale_in:   device float [groups] or NULL. PER_GROUP only: use these g
+ *              instead of computing the amax (re-quantizing a weight in the
+ *              other orientation with the same global scale).
+ * codes:       device, uint8 [groups, Rq, Cq/2].
+ * sf:          device, uint8 [groups, roundup(Rq,128) * roundup(Cq/16,4)].
+ * gscale_out:  device float, [groups*Rq] (PER_ROW) or [groups] (PER_GROUP).
+ *              May equal gscale_in.
+ * workspace:   device, >= minite_workspace_bytes(MINITE_OP_QUANTIZE, groups,
+ *              0, 0, 0) bytes (PER_GROUP without gscale_in only; else NULL ok).
+ * Shape rules: Cq % 16 == 0 (blocks), Rq % 2 == 0 when ALONG_ROWS, all > 0.
+ */
+int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows, int64_t cols,
+                          int scale_mode, int orientation, const float* gscale_in,
+                          uint8_t* codes, uint8_t* sf, float* gscale_out,
+                          void* workspace, size_t ws_bytes, int32_t* status,
+                          minite_stream_t stream);
+
+/*
+ * minite_moe_permute_quant -- MoE permutation fused with per-token amax,
+ * NVFP4 quantization and the SF swizzle, in one pass over x.
+ *
+ * Cites: "Two complementary interventions" (amax during permutation,
+ * contiguous buffers, device-side metadata, fused scale layout) and "Follow
+ * the numerical execution path" (per-token scales).
+ *
+ * Permuted rows are ordered by (expert, token, slot). Row p holds the
+ * quantization of token perm_src[p]; a token routed to k experts appears in
+ * k rows with identical codes, SF and g. Pairs with an id outside [0, E) are
+ * dropped (status bit 1<<MINITE_ERR_BAD_ROUTING, dest_row = -1), so the used
+ * rows are [0, expert_offsets[E]) and later rows are left untouched.
+ *
+ * x:              device, BF16 [T, H].
+ * topk_ids:       device, int32 [T, k].
+ * topk_w:         device, float [T, k], or NULL (then perm_w must be NULL).
+ * codes:          device, uint8 [T*k, H/2].
+ * sf:             device, uint8 [(T*k + 128*E) * roundup(H/16,4)]. Expert e's
+ *                 rows occupy the padded row range [sf_row_offsets[e],
+ *                 sf_row_offsets[e+1]) (local row = p - expert_offsets[e]).
+ * row_g:          device, float [T*k].
+ * expert_offsets: device, int32 [E+1], exclusive prefix of expert counts.
+ * sf_row_offsets: device, int32 [E+1], prefix of counts rounded up to 128.
+ * perm_src:       device, int32 [T*k], token of each permuted row.
+ * dest_row:       device, int32 [T, k], permuted row of each (token, slot).
+ * perm_w:         device, float [T*k], routing weight of each row, or NULL.
+ * workspace:      device, >= minite_workspace_bytes(MINITE_OP_PERMUTE_QUANT,
+ *                 T, H, E, k) bytes; contents on entry are ignored.
+ * Shape rules: H % 64 == 0, 1 <= E <= 1024, 1 <= k <= 32, T >= 1,
+ * T*k < 2^31.
+ */
+int minite_moe_permute_quant(const void* x, const int32_t* topk_ids, const float* topk_w,
+                             int64_t T, int64_t H, int32_t E, int32_t k,
+                             uint8_t* codes, uint8_t* sf, float* row_g,
+                             int32_t* expert_offsets, int32_t* sf_row_offsets,
+                             int32_t* perm_src, int32_t* dest_row, float* perm_w,
+                             void* workspace, size_t ws_bytes, int32_t* status,
+                             minite_stream_t stream);
+
+/*
+ * minite_grouped_gemm_nvfp4 -- block-scaled FP4 x FP4 grouped GEMM over
+ * experts, one launch for all experts.
+ *
+ * Cites: "Diagnostic, alignement et noyaux rapides" (grouped GEMMs for MoE);
+ * "Two complementary interventions" (contiguous expert buffers, device-side
+ * metadata: the host never learns the per-expert row counts).
+ *
+ * For every row m in [0, expert_offsets[E]) of expert e (offsets[e] <= m <
+ * offsets[e+1]) and n in [0, N):
+ *   out[m, n] = sum_k (a(m,k) * sfa(m,k/16)) * (b_e(n,k) * sfb_e(n,k/16))
+ *               / (a_g[m] * b_g[e])
+ * with a, b the E2M1 values; accumulation in FP32 on the tensor cores in a
+ * fixed K order with no split-K, so a row's result depends only on its own
+ * codes and its expert's weights.
+ *
+ * a_codes:  device, uint8 [M_total, K/2], rows in permuted order.
+ * a_sf:     device, SF of A in per-expert padded regions (sf_row_offsets).
+ * a_g:      device, float [M_total], per-row global scales.
+ * b_codes:  device, uint8 [E, N, K/2] (K-major weights).
+ * b_sf:     device, uint8 [E, roundup(N,128) * roundup(K/16,4)].
+ * b_g:      device, float [E].
+ * expert_offsets, sf_row_offsets: device, int32 [E+1] (as produced by
+ *           minite_moe_permute_quant; for a dense GEMM {0, M} and
+ *           {0, roundup(M,128)}).
+ * M_total:  number of rows of a_codes / out (upper bound of offsets[E]).
+ * out:      device, [M_total, N] BF16 (round to nearest even) or FP32; rows
+ *           at or beyond offsets[E] are not written.
+ * Shape rules: K % 64 == 0, N % 32 == 0, 1 <= E <= 1024, M_total < 2^31,
+ * a_codes/b_codes 16-byte aligned with K/2 % 16 == 0.
+ */
+int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_g,
+                              const uint8_t* b_codes, const uint8_t* b_sf, const float* b_g,
+                              const int32_t* expert_offsets, const int32_t* sf_row_offsets,
+                              int64_t M_total, int64_t N, int64_t K, int32_t E,
+                              void* out, int out_dtype, int32_t* status,
+                              minite_stream_t stream);
+
+/*
+ * minite_swiglu_weighted_quant -- routing-weighted SwiGLU with the per-row
+ * amax and NVFP4 requantization fused into the same pass.
+ *
+ * Cites: "Two complementary interventions" (amax computed during weighted
+ * SwiGLU, fused scale layout).
+ *
+ * For each used row m (< expert_offsets[E]):
+ *   h = (silu(gate) * up) * w,  gate = gate_up[m, 0:I], up = gate_up[m, I:2I],
+ *   silu(v) = v / (1 + exp(-v)), w = perm_w[m] (1 if perm_w is NULL),
+ * all in FP32 with a specified exponential (Cody-Waite reduction, degree-7
+ * Taylor polynomial, inputs clamped to [-87, 88]); then h is quantized per
+ * row exactly as minite_quantize_nvfp4 PER_ROW, with the SF written into the
+ * per-expert padded regions given by sf_row_offsets.
+ *
+ * gate_up: device, BF16 [M, 2I].  perm_w: device float [M] or NULL.
+ * codes:   device, uint8 [M, I/2].  sf: as for the permute output with I in
+ *          place of H.  row_g: device, float [M].
+ * Shape rules: I % 64 == 0, 1 <= E <= 1024.
+ */
+int minite_swiglu_weighted_quant(const void* gate_up, const float* perm_w,
+                                 int64_t M, int64_t I, int32_t E,
+                                 const int32_t* expert_offsets, const int32_t* sf_row_offsets,
+                                 uint8_t* codes, uint8_t* sf, float* row_g,
+                                 int32_t* status, minite_stream_t stream);
+
+/*
+ * minite_moe_combine -- unpermute: y[t] = BF16(sum_{j<k} D[dest_row[t,j]]),
+ * summed in FP32 in slot order starting from 0; dropped pairs (dest_row < 0)
+ * are skipped. The routing weight is already inside D (applied in the
+ * SwiGLU).
+ *
+ * expert_out: device, BF16 [M, N], rows in permuted order.
+ * dest_row:   device, int32 [T, k]; entries >= M are skipped and reported
+ *             as status bit 1<<MINITE_ERR_BAD_ROUTING.
+ * y:          device, BF16 [T, N]; must not overlap expert_out.
+ * Shape rules: N % 8 == 0, 1 <= k <= 32.
+ */
+int minite_moe_combine(const void* expert_out, const int32_t* dest_row,
+                       int64_t T, int64_t M, int64_t N, int32_t k, void* y,
+                       int32_t* status, minite_stream_t stream);
+
+/* Workspace bytes needed by `op` (MINITE_OP_QUANTIZE: a = groups;
+ * MINITE_OP_PERMUTE_QUANT: a = T, b = H, E, k). 0 means none needed. */
+size_t minite_workspace_bytes(int op, int64_t a, int64_t b, int32_t E, int32_t k);
+
+/* Static description of a status code. */
+const char* minite_status_string(int status);
+
+/* Library version, "major.minor.patch". */
+const char* minite_version(void);
+
+/*
+ * Test hooks: the element-wise converters and the specified exponential
+ * exactly as the kernels above use them, over n values, so that they can be
+ * compared with an independent CPU implementation across the whole float32
+ * range. out_e2m1 receives one 4-bit code per byte; out_e4m3 one code per
+ * byte (inputs must be >= 0 and finite).
+ */
+int minite_test_convert(const float* in, int64_t n, uint8_t* out_e2m1, uint8_t* out_e4m3,
+                        float* out_exp, minite_stream_t stream);
+
+/*
+ * Test hook for failure detection: sets the time budget of every bounded
+ * pipeline wait in the GEMM (nanoseconds; 0 restores the default of 2 s).
+ * Process-wide; takes effect at the next launch.
+ */
+void minite_set_wait_budget_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MINITE_H */

@@ -1,0 +1,338 @@
+// Device-side building blocks shared by the minite kernels (sm_103a):
+// NVFP4 scalar conversions, the warp-level row quantizer, the specified
+// exponential, and thin inline-PTX wrappers for mbarrier, TMA and tcgen05.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/minite.h"
+
+namespace minite {
+
+constexpr int kWarp = 32;
+constexpr float kE2M1Max = 6.0f;
+constexpr float kGlobalNumerator = 2688.0f;  // 448 (E4M3 max) * 6 (E2M1 max)
+constexpr float kFltMax = 3.402823466e+38f;
+
+__device__ __forceinline__ void set_status(int32_t* status, int code) {
+  if (status) atomicOr(status, 1 << code);
+}
+
+// ----------------------------------------------------------------------------
+// BF16 / scalar format conversions
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Round to nearest even onto the E2M1 grid, saturating at +-6, sign kept.
+// Returns one byte holding `lo` in bits 0..3 and `hi` in bits 4..7.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(out) : "f"(lo), "f"(hi));
+  return out & 0xFFu;
+}
+
+// Non-negative finite float -> unsigned E4M3 code (nearest even, saturate 448).
+__device__ __forceinline__ uint32_t cvt_e4m3(float s) {
+  uint16_t out;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(out) : "f"(s), "f"(0.0f));
+  return out & 0xFFu;
+}
+
+// Unsigned E4M3 code (never 0x7F) -> float, exact.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  uint32_t e = (c >> 3) & 0xF, m = c & 7;
+  if (e == 0) return __fmul_rn(static_cast<float>(m), 0.001953125f);  // m * 2^-9
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));              // (1+m/8) * 2^(e-7)
+}
+
+// g = min(2688 / amax, FLT_MAX) for amax > 0, else 1.
+__device__ __forceinline__ float global_scale(float amax) {
+  if (!(amax > 0.0f)) return 1.0f;
+  return fminf(__fdiv_rn(kGlobalNumerator, amax), kFltMax);
+}
+
+// One 16-element block: scale code from its amax and the row's global scale,
+// and the factor that maps elements onto the E2M1 grid (0 when sf == 0).
+struct BlockScale {
+  uint32_t sf;
+  float enc;
+};
+__device__ __forceinline__ BlockScale block_scale(float amax_b, float g) {
+  BlockScale r;
+  float s = __fmul_rn(__fdiv_rn(amax_b, kE2M1Max), g);
+  r.sf = cvt_e4m3(s);
+  r.enc = r.sf ? fminf(__fdiv_rn(g, e4m3_value(r.sf)), kFltMax) : 0.0f;
+  return r;
+}
+
+// 8 consecutive elements -> 4 bytes of packed codes (element 0 in the low nibble).
+__device__ __forceinline__ uint32_t encode8(const float (&v)[8], float enc, bool zero) {
+  if (zero) return 0u;
+  uint32_t b0 = cvt_e2m1x2(__fmul_rn(v[0], enc), __fmul_rn(v[1], enc));
+  uint32_t b1 = cvt_e2m1x2(__fmul_rn(v[2], enc), __fmul_rn(v[3], enc));
+  uint32_t b2 = cvt_e2m1x2(__fmul_rn(v[4], enc), __fmul_rn(v[5], enc));
+  uint32_t b3 = cvt_e2m1x2(__fmul_rn(v[6], enc), __fmul_rn(v[7], enc));
+  return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+}
+
+__device__ __forceinline__ float amax8(const float (&v)[8]) {
+  float m = fabsf(v[0]);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&v)[8]) {
+  v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+  v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Byte offset of the scale of (row r, SF column c) in a region with kc SF
+// columns: 128-row x 4-column atoms of 512 bytes.
+__device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t kc) {
+  return ((r >> 7) * (kc >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+// ----------------------------------------------------------------------------
+// Warp-level row quantizer. A row of C elements is split in chunks of 256;
+// in chunk j lane l holds elements [256j + 8l, 256j + 8l + 8). Lanes 2b, 2b+1
+// share one 16-element block; lanes 8a..8a+7 share one 4-column SF atom word.
+// ----------------------------------------------------------------------------
+
+template <int NCH>
+struct RowQuant {
+  uint32_t codes[NCH];  // this lane's 4 code bytes per chunk
+  uint32_t sfword[NCH]; // valid on lanes 8a: the 4 SF bytes of blocks 4a..4a+3
+};
+
+// v[j][i]: element (256j + 8*lane + i); elements at or beyond C must be 0.
+template <int NCH>
+__device__ __forceinline__ void quantize_row_warp(const float (&v)[NCH][8], int C, float g,
+                                                  RowQuant<NCH>& out) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const bool valid = (256 * j + 8 * lane) < C;
+    float am = amax8(v[j]);
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    BlockScale bs = block_scale(am, g);
+    uint32_t sf = valid ? bs.sf : 0u;
+    out.codes[j] = encode8(v[j], bs.enc, !valid || sf == 0);
+    // gather the SF bytes of lanes 8a, 8a+2, 8a+4, 8a+6 into lane 8a
+    uint32_t s1 = __shfl_down_sync(0xffffffffu, sf, 2);
+    uint32_t s2 = __shfl_down_sync(0xffffffffu, sf, 4);
+    uint32_t s3 = __shfl_down_sync(0xffffffffu, sf, 6);
+    out.sfword[j] = sf | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  }
+}
+
+// Write one quantized row: codes at codes_row (C/2 bytes), SF words into the
+// swizzled region `sf_base` at local row r with kc SF columns.
+template <int NCH>
+__device__ __forceinline__ void store_row_warp(const RowQuant<NCH>& q, int C, uint8_t* codes_row,
+                                               uint8_t* sf_base, int64_t r, int kc) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int e0 = 256 * j + 8 * lane;
+    if (e0 < C) *reinterpret_cast<uint32_t*>(codes_row + e0 / 2) = q.codes[j];
+    const int col = 16 * j + (lane >> 1);  // SF column of this lane's block
+    if ((lane & 7) == 0 && col < kc) {
+      *reinterpret_cast<uint32_t*>(sf_base + sf_offset(r, col, kc)) = q.sfword[j];
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// The specified exponential: Cody-Waite reduction with a two-part ln 2 and a
+// degree-7 Taylor polynomial, every step one IEEE float operation rounded to
+// nearest (no contraction), inputs clamped to [-87, 88].
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ float exp_spec(float x) {
+  constexpr float kLog2e = 1.44269502162933349609375f;   // float32(log2 e)
+  constexpr float kLn2Hi = 0.693145751953125f;           // ln 2 cut to 15 significant bits
+  constexpr float kLn2Lo = 1.428606765330187045e-06f;    // float32(ln 2 - kLn2Hi)
+  x = fminf(fmaxf(x, -87.0f), 88.0f);
+  const float n = rintf(__fmul_rn(x, kLog2e));
+  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, kLn2Hi)), __fmul_rn(n, kLn2Lo));
+  float p = 1.0f / 5040.0f;
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  const int ni = static_cast<int>(n);
+  return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(ni + 127) << 23));
+}
+
+// ----------------------------------------------------------------------------
+// mbarrier / TMA / tcgen05 wrappers (inline PTX)
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: true when the phase with `parity` completed; false when
+// `budget_ns` passed since the wait began, or *abort became non-zero first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
+                                          volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  // try_wait itself suspends the thread for a while before failing, so the
+  // abort flag and the clock are checked after every failed attempt
+  const uint64_t start = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (globaltimer() - start > budget_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(desc)) : "memory");
+}
+
+// 2-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_t* bar, int x,
+                                            int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)),
+         "r"(x), "r"(y)
+      : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+         "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Whole warp: allocate `ncols` TMEM columns, address written to *dst (smem).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(smem_u32(dst)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// Make `bar` track completion of all prior tcgen05 async ops of this thread.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+      :: "r"(smem_u32(bar)) : "memory");
+}
+
+// Copy one 512-byte scale-factor atom (32 rows x 16 bytes) from shared memory
+// into 4 TMEM columns, replicated into the four 32-lane quarters.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
+               :: "r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T with NVFP4 block scales from TMEM.
+__device__ __forceinline__ void tc_mma_nvfp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa_tmem,
+                                             uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+         "r"(accumulate)
+      : "memory");
+}
+
+// Warp: load 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+      " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+      " [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start, leading and stride
+// byte offsets in 16-byte units, version 1 at bit 46, layout in bits 61..63.
+enum : uint64_t { kLayoutNone = 0, kLayoutSwizzle128B = 2 };
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint64_t layout) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
+}
+
+}  // namespace minite

@@ -1,0 +1,286 @@
+// minite_moe_permute_quant: MoE token permutation fused with the per-token
+// amax, NVFP4 quantization and the scale-layout swizzle.
+//
+// The miniTE report summary, section "Two complementary interventions",
+// computes the amax during the permutation (so no separate scan of the
+// activations), writes experts into contiguous buffers described by
+// device-side metadata, and fuses the scale-layout conversion into
+// quantization. Per-token scales follow its section "Follow the numerical
+// execution path".
+//
+// Three launches, no host synchronization:
+//   permute_hist_kernel   per token-chunk expert histogram -> table[e][chunk]
+//                         (also resets the scan's completion counter).
+//   permute_scan_kernel   one block per expert: exclusive prefix of its
+//                         chunk counts; the last block to finish turns the
+//                         expert totals into expert_offsets / sf_row_offsets.
+//   permute_quant_kernel  one block per chunk: stable rank of every
+//                         (token, slot) pair inside the chunk, then each token
+//                         is read once, quantized once in registers and its
+//                         codes / scales written to its k destination rows.
+#include "common.cuh"
+#include "host_util.h"
+
+namespace minite {
+
+constexpr int kPermThreads = 256;
+
+struct PermWs {
+  uint32_t* counter;  // scan completion counter
+  int32_t* totals;    // [E]
+  int32_t* table;     // [E][nchunks]
+};
+
+static size_t perm_ws_bytes(int64_t T, int E, int k) {
+  const int64_t ct = permute_chunk_tokens(k);
+  const int64_t nchunks = (T + ct - 1) / ct;
+  return 256 + static_cast<size_t>(E) * 4 + 256 + static_cast<size_t>(E) * nchunks * 4;
+}
+
+static PermWs perm_ws(void* ws, int E) {
+  PermWs w;
+  char* p = static_cast<char*>(ws);
+  w.counter = reinterpret_cast<uint32_t*>(p);
+  w.totals = reinterpret_cast<int32_t*>(p + 256);
+  w.table = reinterpret_cast<int32_t*>(p + 256 + ((static_cast<size_t>(E) * 4 + 255) & ~size_t(255)));
+  return w;
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(
+    const int32_t* __restrict__ ids, int64_t T, int k, int E, int ct, int nchunks,
+    int32_t* __restrict__ table, uint32_t* __restrict__ counter, int32_t* status) {
+  extern __shared__ int32_t hist[];
+  const int c = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  if (c == 0 && threadIdx.x == 0) *counter = 0u;
+  __syncthreads();
+  const int64_t p0 = static_cast<int64_t>(c) * ct * k;
+  const int64_t p1 = min(static_cast<int64_t>(c + 1) * ct, T) * k;
+  bool bad = false;
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else bad = true;
+  }
+  if (bad) set_status(status, MINITE_ERR_BAD_ROUTING);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    table[static_cast<int64_t>(e) * nchunks + c] = hist[e];
+}
+
+// Exclusive scan of one value per thread over a 256-thread block; returns the
+// block total through *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int s = lane < (kPermThreads / 32) ? warp_sums[lane] : 0;
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += t;
+    }
+    if (lane < (kPermThreads / 32)) warp_sums[lane] = si - s;
+    if (lane == 31) warp_sums[32] = si;
+  }
+  __syncthreads();
+  const int res = warp_sums[wid] + incl - v;
+  *total = warp_sums[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_scan_kernel(
+    int32_t* __restrict__ table, int nchunks, int E, uint32_t* __restrict__ counter,
+    int32_t* __restrict__ totals, int32_t* __restrict__ expert_offsets,
+    int32_t* __restrict__ sf_row_offsets) {
+  __shared__ int warp_sums[33];
+  __shared__ int is_last;
+  const int e = blockIdx.x;
+  int32_t* row = table + static_cast<int64_t>(e) * nchunks;
+  int carry = 0;
+  for (int base = 0; base < nchunks; base += kPermThreads) {
+    const int i = base + threadIdx.x;
+    const int v = i < nchunks ? row[i] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, warp_sums, &tot);
+    if (i < nchunks) row[i] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) {
+    totals[e] = carry;
+    __threadfence();
+    is_last = (atomicAdd(counter, 1u) == static_cast<uint32_t>(E - 1));
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  int off = 0, sfoff = 0;
+  for (int base = 0; base < E; base += kPermThreads) {
+    const int i = base + threadIdx.x;
+    const int cnt = i < E ? __ldcg(totals + i) : 0;
+    int tot, tot_pad;
+    const int ex = block_exclusive_scan(cnt, warp_sums, &tot);
+    const int ex_pad = block_exclusive_scan((cnt + 127) & ~127, warp_sums, &tot_pad);
+    if (i < E) {
+      expert_offsets[i] = off + ex;
+      sf_row_offsets[i] = sfoff + ex_pad;
+    }
+    off += tot;
+    sfoff += tot_pad;
+  }
+  if (threadIdx.x == 0) {
+    expert_offsets[E] = off;
+    sf_row_offsets[E] = sfoff;
+  }
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(kPermThreads) permute_quant_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
+    const float* __restrict__ topk_w, int64_t T, int H, int E, int k, int ct, int nchunks,
+    const int32_t* __restrict__ table, const int32_t* __restrict__ expert_offsets,
+    const int32_t* __restrict__ sf_row_offsets, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ sf, float* __restrict__ row_g, int32_t* __restrict__ perm_src,
+    int32_t* __restrict__ dest_row, float* __restrict__ perm_w) {
+  extern __shared__ int32_t sm[];
+  int32_t* s_off = sm;                // [E+1]
+  int32_t* s_sfoff = sm + (E + 1);    // [E+1]
+  int32_t* s_id = sm + 2 * (E + 1);   // [ct*k]
+  int32_t* s_dest = s_id + ct * k;    // [ct*k]
+  const int c = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, wid = tid >> 5;
+  const int kc = ((H / 16) + 3) & ~3;
+  for (int i = tid; i <= E; i += blockDim.x) {
+    s_off[i] = expert_offsets[i];
+    s_sfoff[i] = sf_row_offsets[i];
+  }
+  const int64_t t0 = static_cast<int64_t>(c) * ct;
+  const int ntok = static_cast<int>(min(static_cast<int64_t>(ct), T - t0));
+  const int npairs = ntok * k;
+  for (int p = tid; p < npairs; p += blockDim.x) s_id[p] = ids[t0 * k + p];
+  __syncthreads();
+
+  // stable rank of each pair among the chunk's pairs with the same expert
+  for (int p = tid; p < npairs; p += blockDim.x) {
+    const int e = s_id[p];
+    int dest = -1;
+    if (e >= 0 && e < E) {
+      int rank = 0;
+      for (int q = 0; q < p; ++q) rank += (s_id[q] == e);
+      dest = s_off[e] + table[static_cast<int64_t>(e) * nchunks + c] + rank;
+      const int64_t t = t0 + p / k;
+      perm_src[dest] = static_cast<int32_t>(t);
+      if (perm_w) perm_w[dest] = topk_w[t0 * k + p];
+    }
+    s_dest[p] = dest;
+    dest_row[t0 * k + p] = dest;
+  }
+  __syncthreads();
+
+  // each token: one read, one quantization, k scattered writes
+  const int nwarps = blockDim.x >> 5;
+  for (int tl = wid; tl < ntok; tl += nwarps) {
+    const uint16_t* xr = x + (t0 + tl) * H;
+    float v[NCH][8];
+    float am = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int e0 = 256 * j + 8 * lane;
+      if (e0 < H) {
+        uint4 u = __ldcs(reinterpret_cast<const uint4*>(xr + e0));
+        unpack_bf16x8(u, v[j]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[j][i] = 0.0f;
+      }
+      am = fmaxf(am, amax8(v[j]));
+    }
+    const float g = global_scale(warp_max(am));
+    RowQuant<NCH> q;
+    quantize_row_warp<NCH>(v, H, g, q);
+    for (int j = 0; j < k; ++j) {
+      const int d = s_dest[tl * k + j];
+      if (d < 0) continue;
+      const int e = s_id[tl * k + j];
+      const int64_t r = static_cast<int64_t>(s_sfoff[e]) + (d - s_off[e]);
+      store_row_warp<NCH>(q, H, codes + static_cast<int64_t>(d) * (H / 2), sf, r, kc);
+      if (lane == 0) row_g[d] = g;
+    }
+  }
+
+  // zero the scale bytes of each expert's padding rows
+  for (int e = c; e < E; e += gridDim.x) {
+    const int cnt = s_off[e + 1] - s_off[e];
+    const int pad = ((cnt + 127) & ~127) - cnt;
+    const int words = kc / 4;
+    for (int i = tid; i < pad * words; i += blockDim.x) {
+      const int64_t r = static_cast<int64_t>(s_sfoff[e]) + cnt + i / words;
+      *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * (i % words), kc)) = 0u;
+    }
+  }
+}
+
+}  // namespace minite
+
+using namespace minite;
+
+namespace minite {
+size_t permute_workspace_bytes(int64_t T, int32_t E, int32_t k) { return perm_ws_bytes(T, E, k); }
+}  // namespace minite
+
+extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
+                                        const float* topk_w, int64_t T, int64_t H, int32_t E,
+                                        int32_t k, uint8_t* codes, uint8_t* sf, float* row_g,
+                                        int32_t* expert_offsets, int32_t* sf_row_offsets,
+                                        int32_t* perm_src, int32_t* dest_row, float* perm_w,
+                                        void* workspace, size_t ws_bytes, int32_t* status,
+                                        minite_stream_t stream) {
+  if (!x || !topk_ids || !codes || !sf || !row_g || !expert_offsets || !sf_row_offsets ||
+      !perm_src || !dest_row || !workspace)
+    return MINITE_ERR_INVALID_ARG;
+  if ((topk_w == nullptr) != (perm_w == nullptr)) return MINITE_ERR_INVALID_ARG;
+  if (T < 1 || H < 64 || H % 64 != 0 || H > 4096 || E < 1 || E > 1024 || k < 1 || k > 32)
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (T * k >= (int64_t(1) << 31) || (T * k + 128 * int64_t(E)) * ((H / 16 + 3) & ~3) >= (int64_t(1) << 40))
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(workspace, 256))
+    return MINITE_ERR_INVALID_ARG;
+  if (ws_bytes < perm_ws_bytes(T, E, k)) return MINITE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int ct = permute_chunk_tokens(k);
+  const int nchunks = static_cast<int>((T + ct - 1) / ct);
+  PermWs w = perm_ws(workspace, E);
+
+  permute_hist_kernel<<<nchunks, kPermThreads, E * sizeof(int32_t), s>>>(
+      topk_ids, T, k, E, ct, nchunks, w.table, w.counter, status);
+  permute_scan_kernel<<<E, kPermThreads, 0, s>>>(w.table, nchunks, E, w.counter, w.totals,
+                                                 expert_offsets, sf_row_offsets);
+  const size_t smem = (2 * (E + 1) + 2 * ct * k) * sizeof(int32_t);
+  const int nch = static_cast<int>((H + 255) / 256);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  const int h = static_cast<int>(H);
+  switch (nch) {
+#define MINITE_CASE(N)                                                                     \
+  case N:                                                                                  \
+    permute_quant_kernel<N><<<nchunks, kPermThreads, smem, s>>>(                           \
+        xb, topk_ids, topk_w, T, h, E, k, ct, nchunks, w.table, expert_offsets,            \
+        sf_row_offsets, codes, sf, row_g, perm_src, dest_row, perm_w);                     \
+    break;
+    MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
+    MINITE_CASE(7) MINITE_CASE(8) MINITE_CASE(9) MINITE_CASE(10) MINITE_CASE(11)
+    MINITE_CASE(12) MINITE_CASE(13) MINITE_CASE(14) MINITE_CASE(15) MINITE_CASE(16)
+#undef MINITE_CASE
+    default: return MINITE_ERR_UNSUPPORTED_SHAPE;
+  }
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}

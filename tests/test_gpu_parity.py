@@ -1,0 +1,482 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle.
+
+Integer, code, scale and index outputs must match bit for bit. Grouped-GEMM
+outputs: FP32 within 2^-20 * sum_k |a_k b_k| of the exact result, BF16
+within one BF16 ulp of the correctly rounded exact result. Comparisons of
+permuted rows are keyed by (token, slot) through the permutation itself,
+which is compared exactly first.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _helpers import (assert_bf16_within_one_ulp, assert_fp32_within_bound, bf16_dev, np_dev,
+                      u16)
+from nvfp4_w4a4_moe_permute_gb300 import inputs as IN
+from nvfp4_w4a4_moe_permute_gb300 import minite as M
+from oracle import nvfp4_moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from nvfp4_w4a4_moe_permute_gb300 import build
+    build.build()
+    M.load()
+    M.minite_set_wait_budget_ns(0)
+    yield
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _rand_bf16(rng, shape, scale_spread=6):
+    x = rng.standard_normal(shape).astype(np.float32)
+    if len(shape) >= 2:
+        x *= np.exp2(rng.integers(-scale_spread, scale_spread + 1, shape[:-1] + (1,))).astype(np.float32)
+    return O.f32_to_bf16(x)
+
+
+# --------------------------------------------------------------------- converters
+
+def _sweep_bits():
+    parts = [np.arange(0, 2 ** 32, 257, dtype=np.uint64).astype(np.uint32)]
+    # every float32 within +-1024 ulps of each E2M1 midpoint and grid value,
+    # and of each E4M3 midpoint and value
+    vals = O.e4m3_decode(np.arange(127, dtype=np.uint8)).astype(np.float64)
+    pts = np.concatenate([O.E2M1_MAGNITUDES, (O.E2M1_MAGNITUDES[1:] + O.E2M1_MAGNITUDES[:-1]) / 2,
+                          vals, (vals[1:] + vals[:-1]) / 2, [448.0, 464.0, 480.0]])
+    base = pts.astype(np.float32).view(np.uint32).astype(np.int64)
+    near = (base[:, None] + np.arange(-1024, 1025)[None, :]).ravel()
+    near = near[(near >= 0) & (near < 2 ** 31)].astype(np.uint32)
+    parts.append(near)
+    parts.append(near | np.uint32(0x80000000))
+    b = np.concatenate(parts)
+    f = b.view(np.float32)
+    return f[np.isfinite(f)]
+
+
+def test_converters_bit_exact_over_float32_sweep():
+    v = _sweep_bits()
+    for lo in range(0, v.size, 1 << 23):
+        c = v[lo:lo + (1 << 23)]
+        x = np_dev(c)
+        e2 = torch.empty(c.size, dtype=torch.uint8, device="cuda")
+        e4 = torch.empty(c.size, dtype=torch.uint8, device="cuda")
+        ex = torch.empty(c.size, dtype=torch.float32, device="cuda")
+        M.minite_test_convert(x, e2, e4, ex)
+        torch.cuda.synchronize()
+        assert np.array_equal(e2.cpu().numpy(), O.e2m1_rn(c)), "E2M1"
+        pos = (c > 0) | ((c == 0) & ~np.signbit(c))  # scales are never -0
+        assert np.array_equal(e4.cpu().numpy()[pos], O.e4m3_rn_satfinite(c[pos])), "E4M3"
+        got = ex.cpu().numpy().view(np.uint32)
+        assert np.array_equal(got, O.exp_spec(c).view(np.uint32)), "exp_spec"
+
+
+# --------------------------------------------------------------------- quantize
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (3, 48), (37, 80), (128, 256), (130, 2048),
+                                       (200, 4096), (64, 1536), (129, 768)])
+def test_quantize_per_row_bit_exact(rows, cols):
+    rng = np.random.default_rng(rows * 7 + cols)
+    x = _rand_bf16(rng, (rows, cols))
+    x[0, :] = 0  # zero row
+    if rows > 2:
+        x[1, :] = O.f32_to_bf16(np.full(cols, 1e-40, dtype=np.float32))  # subnormal row
+        x[2, 5] = O.f32_to_bf16(np.array([3.0e38], dtype=np.float32))[0]
+    q = M.quantize(bf16_dev(x))
+    torch.cuda.synchronize()
+    codes, sf, g = O.quantize_per_row(O.bf16_to_f32(x))
+    assert np.array_equal(q["codes"].cpu().numpy(), codes)
+    assert np.array_equal(q["sf"].cpu().numpy(), O.swizzle_sf(sf))
+    assert np.array_equal(q["g"].cpu().numpy().view(np.uint32), g.view(np.uint32))
+
+
+@pytest.mark.parametrize("E,R,C", [(1, 32, 64), (3, 128, 256), (4, 100, 768), (2, 1536, 2048),
+                                   (5, 2048, 768)])
+def test_quantize_weights_per_expert_bit_exact(E, R, C):
+    rng = np.random.default_rng(E * 1000 + R + C)
+    w = O.f32_to_bf16((rng.standard_normal((E, R, C)) * 0.02).astype(np.float32))
+    q = M.quantize(bf16_dev(w), per_group=True)
+    torch.cuda.synchronize()
+    codes, _, sw, g = O.quantize_weights(w)
+    assert np.array_equal(q["codes"].cpu().numpy(), codes)
+    assert np.array_equal(q["sf"].cpu().numpy(), sw)
+    assert np.array_equal(q["g"].cpu().numpy().view(np.uint32), g.view(np.uint32))
+
+
+@pytest.mark.parametrize("E,R,C", [(1, 64, 128), (2, 96, 80), (3, 2048, 768), (1, 48, 200),
+                                   (2, 768, 1536)])
+def test_quantize_weights_along_rows_bit_exact(E, R, C):
+    rng = np.random.default_rng(E * 999 + R + C)
+    w = O.f32_to_bf16((rng.standard_normal((E, R, C)) * 0.02).astype(np.float32))
+    codes, _, sw, g = O.quantize_weights(w, along_rows=True)
+    wd = bf16_dev(w)
+    for g_in in (None, np_dev(g)):
+        q = M.quantize(wd, per_group=True, along_rows=True, g_in=g_in)
+        torch.cuda.synchronize()
+        assert np.array_equal(q["codes"].cpu().numpy(), codes)
+        assert np.array_equal(q["sf"].cpu().numpy(), sw)
+        assert np.array_equal(q["g"].cpu().numpy().view(np.uint32), g.view(np.uint32))
+
+
+# --------------------------------------------------------------------- permute
+
+def run_permute(x_u16, ids, w, E):
+    T, H = x_u16.shape
+    k = ids.shape[1]
+    mlp = M.MoEMLP(T, H, 64, E, k)
+    status = _status()
+    mlp.status = status
+    mlp.permute_quant(bf16_dev(x_u16), np_dev(ids), None if w is None else np_dev(w))
+    torch.cuda.synchronize()
+    return mlp, int(status.item())
+
+
+def check_permute(mlp, ref, H, check_rows=None):
+    off = ref["expert_offsets"]
+    Mu = int(off[-1])
+    assert np.array_equal(mlp.offsets.cpu().numpy(), off)
+    assert np.array_equal(mlp.sf_offsets.cpu().numpy(), ref["sf_row_offsets"])
+    assert np.array_equal(mlp.dest_row.cpu().numpy(), ref["dest_row"])
+    assert np.array_equal(mlp.perm_src.cpu().numpy()[:Mu], ref["perm_src"])
+    if ref["perm_w"] is not None:
+        assert np.array_equal(mlp.perm_w.cpu().numpy()[:Mu].view(np.uint32),
+                              ref["perm_w"].view(np.uint32))
+    rows = np.arange(Mu) if check_rows is None else check_rows
+    assert np.array_equal(mlp.a_codes.cpu().numpy()[rows], ref["codes"][rows])
+    assert np.array_equal(mlp.a_g.cpu().numpy()[rows].view(np.uint32), ref["row_g"][rows].view(np.uint32))
+    n_sf = ref["sf_swizzled"].size
+    assert np.array_equal(mlp.a_sf.cpu().numpy()[:n_sf], ref["sf_swizzled"])
+
+
+def test_permute_tiny_config():
+    d = IN.make_moe_inputs("tiny")
+    E = d["cfg"]["E"]
+    mlp, st = run_permute(d["x"], d["topk_ids"], d["topk_w"], E)
+    assert st == 0
+    check_permute(mlp, O.moe_permute_quant(d["x"], d["topk_ids"], d["topk_w"], E), d["cfg"]["H"])
+
+
+def test_permute_random_shapes_edge_cases():
+    rng = np.random.default_rng(42)
+    for trial in range(25):
+        T = int(rng.integers(1, 301))
+        E = int(rng.integers(1, 10))
+        k = int(rng.integers(1, 5))
+        H = int(rng.choice([64, 128, 192, 320]))
+        ids = rng.integers(0, E, (T, k)).astype(np.int32)
+        if trial % 5 == 1:
+            ids[:] = E - 1  # everything to one expert
+        if trial % 5 == 2 and E > 1:
+            ids[ids == 0] = 1  # an empty expert
+        if trial % 5 == 3:
+            ids[rng.random((T, k)) < 0.05] = E + 3  # bad ids: dropped, status bit set
+        w = rng.random((T, k)).astype(np.float32)
+        x = _rand_bf16(rng, (T, H))
+        mlp, st = run_permute(x, ids, w if trial % 2 else None, E)
+        bad = ((ids < 0) | (ids >= E)).any()
+        assert st == ((1 << M.ERR_BAD_ROUTING) if bad else 0)
+        check_permute(mlp, O.moe_permute_quant(x, ids, w if trial % 2 else None, E), H)
+
+
+def test_permute_qwen3_gate_up_layer_full_size():
+    d = IN.make_moe_inputs("gate_up", with_weights=False)
+    E = d["cfg"]["E"]
+    mlp, st = run_permute(d["x"], d["topk_ids"], d["topk_w"], E)
+    assert st == 0
+    check_permute(mlp, O.moe_permute_quant(d["x"], d["topk_ids"], d["topk_w"], E), d["cfg"]["H"])
+
+
+def test_permute_skewed_full_size_sampled_rows():
+    d = IN.make_moe_inputs("skewed", with_weights=False)
+    E = d["cfg"]["E"]
+    mlp, st = run_permute(d["x"], d["topk_ids"], d["topk_w"], E)
+    assert st == 0
+    ref = O.moe_permute_quant(d["x"], d["topk_ids"], d["topk_w"], E)
+    counts = np.diff(ref["expert_offsets"])
+    assert (counts == 0).sum() == d["cfg"]["n_empty"]
+    rng = np.random.default_rng(0)
+    rows = rng.choice(int(ref["expert_offsets"][-1]), 4096, replace=False)
+    check_permute(mlp, ref, d["cfg"]["H"], check_rows=np.sort(rows))
+
+
+# --------------------------------------------------------------------- grouped GEMM
+
+def make_gemm_case(counts, N, K, seed, act_scale=True):
+    rng = np.random.default_rng(seed)
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    sfo = np.concatenate([[0], np.cumsum((np.array(counts) + 127) // 128 * 128)]).astype(np.int32)
+    Mu = int(off[-1])
+    x = _rand_bf16(rng, (max(Mu, 1), K))
+    codes, sf, g = O.quantize_per_row(O.bf16_to_f32(x))
+    a_sw = O.place_sf_per_expert(sf[:Mu], off, sfo)
+    w = O.f32_to_bf16((rng.standard_normal((E, N, K)) * 0.02).astype(np.float32))
+    bc, bsf, bsw, bg = O.quantize_weights(w)
+    return dict(E=E, N=N, K=K, off=off, sfo=sfo, Mu=Mu, codes=codes, sf=sf, g=g, a_sw=a_sw,
+                bc=bc, bsf=bsf, bsw=bsw, bg=bg)
+
+
+def run_gemm(c, out_dtype, M_total=None):
+    Mt = M_total or max(c["Mu"], 1)
+    a_codes = torch.zeros((Mt, c["K"] // 2), dtype=torch.uint8, device="cuda")
+    a_codes[:c["codes"].shape[0]] = np_dev(c["codes"][:Mt])
+    a_sf = torch.zeros((Mt + 128 * c["E"]) * (c["K"] // 16), dtype=torch.uint8, device="cuda")
+    a_sf[:c["a_sw"].size] = np_dev(c["a_sw"])
+    a_g = torch.ones(Mt, dtype=torch.float32, device="cuda")
+    a_g[:c["g"].shape[0]] = np_dev(c["g"][:Mt])
+    out = torch.full((Mt, c["N"]), float("nan"), dtype=out_dtype, device="cuda")
+    st = _status()
+    M.minite_grouped_gemm_nvfp4(a_codes, a_sf, a_g, np_dev(c["bc"]), np_dev(c["bsw"]),
+                                np_dev(c["bg"]), np_dev(c["off"]), np_dev(c["sfo"]), out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return out
+
+
+def check_gemm(c, out, rows=None):
+    rows = np.arange(c["Mu"]) if rows is None else rows
+    y, bound = O.grouped_gemm_exact(c["codes"], c["sf"], c["g"], c["bc"], c["bsf"], c["bg"],
+                                    c["off"], rows=rows)
+    if out.dtype == torch.float32:
+        assert_fp32_within_bound(out.cpu().numpy()[rows], y, bound, "fp32 out")
+    else:
+        assert_bf16_within_one_ulp(u16(out)[rows], y, "bf16 out")
+
+
+GEMM_CASES = [
+    ([5], 32, 64), ([128], 128, 256), ([1, 0, 300, 17], 160, 320), ([0, 0, 0, 9], 384, 512),
+    ([129, 127], 256, 2048), ([3, 200, 1, 0, 64], 96, 768), ([257], 128, 128), ([40] * 9, 64, 192),
+]
+
+
+@pytest.mark.parametrize("counts,N,K", GEMM_CASES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_grouped_gemm_small(counts, N, K, dtype):
+    c = make_gemm_case(counts, N, K, seed=sum(counts) + N + K)
+    out = run_gemm(c, dtype)
+    check_gemm(c, out)
+    # rows of no expert (beyond offsets[E]) are not written
+    if out.shape[0] > c["Mu"]:
+        assert torch.isnan(out[c["Mu"]:].float()).all()
+
+
+def test_grouped_gemm_rows_beyond_used_are_untouched():
+    c = make_gemm_case([10, 20], 128, 256, seed=3)
+    out = run_gemm(c, torch.float32, M_total=100)
+    check_gemm(c, out)
+    assert torch.isnan(out[30:]).all()
+
+
+def test_grouped_gemm_one_hot_weights_reproduce_dequantized_activations():
+    rng = np.random.default_rng(9)
+    Mu, K, N = 200, 256, 32
+    x = _rand_bf16(rng, (Mu, K))
+    codes, sf, g = O.quantize_per_row(O.bf16_to_f32(x))
+    cols = rng.choice(K, N, replace=False)
+    w = np.zeros((1, N, K), dtype=np.float32)
+    w[0, np.arange(N), cols] = 6.0
+    bc, bsf, bsw, bg = O.quantize_weights(O.f32_to_bf16(w))
+    off = np.array([0, Mu], dtype=np.int32)
+    c = dict(E=1, N=N, K=K, off=off, sfo=np.array([0, 256], dtype=np.int32), Mu=Mu, codes=codes,
+             sf=sf, g=g, a_sw=O.place_sf_per_expert(sf, off, np.array([0, 256])), bc=bc,
+             bsf=bsf, bsw=bsw, bg=bg)
+    out = run_gemm(c, torch.float32).cpu().numpy()
+    xh = O.dequantize(codes, sf, g)
+    # one nonzero product per output: exact up to the final fp32 scaling
+    ref = (6.0 * xh[:, cols]).astype(np.float32).astype(np.float64)
+    assert np.allclose(out, ref, rtol=2.0 ** -22, atol=0)
+
+
+def test_grouped_gemm_dense_config_bf16_and_fp32():
+    d = IN.make_dense_inputs()
+    Mr, N, K = d["cfg"]["M"], d["cfg"]["N"], d["cfg"]["K"]
+    codes, sf, g = O.quantize_per_row(O.bf16_to_f32(d["a"]))
+    bc, bsf, bsw, bg = O.quantize_weights(d["w"][None])
+    off = np.array([0, Mr], dtype=np.int32)
+    sfo = np.array([0, Mr], dtype=np.int32)
+    c = dict(E=1, N=N, K=K, off=off, sfo=sfo, Mu=Mr, codes=codes, sf=sf, g=g,
+             a_sw=O.swizzle_sf(sf), bc=bc, bsf=bsf, bsw=bsw, bg=bg)
+    # the GPU quantizer reproduces the operands bit for bit
+    qa = M.quantize(bf16_dev(d["a"]))
+    torch.cuda.synchronize()
+    assert np.array_equal(qa["codes"].cpu().numpy(), codes)
+    rng = np.random.default_rng(1)
+    rows = np.sort(np.concatenate([rng.choice(Mr, 1024, replace=False), [0, Mr - 1]]))
+    for dt in (torch.float32, torch.bfloat16):
+        out = run_gemm(c, dt)
+        check_gemm(c, out, rows=np.unique(rows))
+
+
+def test_grouped_gemm_batch_invariance():
+    """A token's output row is bitwise identical whatever else is routed to its
+    expert (more rows, fewer rows, other experts)."""
+    base = make_gemm_case([70, 150, 33], 128, 512, seed=11)
+    out0 = run_gemm(base, torch.float32).cpu().numpy()
+    rng = np.random.default_rng(12)
+    extra = _rand_bf16(rng, (300, 512))
+    ec, esf, eg = O.quantize_per_row(O.bf16_to_f32(extra))
+    # expert 1 gets 300 more rows appended after its own; experts 0 and 2 unchanged
+    off0 = base["off"]
+    order = np.concatenate([np.arange(0, off0[2]), -1 - np.arange(300), np.arange(off0[2], off0[3])])
+    codes = np.concatenate([base["codes"][:off0[2]], ec, base["codes"][off0[2]:off0[3]]])
+    sf = np.concatenate([base["sf"][:off0[2]], esf, base["sf"][off0[2]:off0[3]]])
+    g = np.concatenate([base["g"][:off0[2]], eg, base["g"][off0[2]:off0[3]]])
+    counts = [70, 450, 33]
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    sfo = np.concatenate([[0], np.cumsum((np.array(counts) + 127) // 128 * 128)]).astype(np.int32)
+    c = dict(base, off=off, sfo=sfo, Mu=553, codes=codes, sf=sf, g=g,
+             a_sw=O.place_sf_per_expert(sf, off, sfo))
+    out1 = run_gemm(c, torch.float32).cpu().numpy()
+    keep = order >= 0
+    assert np.array_equal(out1[keep].view(np.uint32), out0[order[keep]].view(np.uint32))
+    # and alone: expert 1's first 5 rows routed with nothing else
+    c2 = dict(base, off=np.array([0, 0, 5, 5], dtype=np.int32),
+              sfo=np.array([0, 0, 128, 128], dtype=np.int32), Mu=5, codes=base["codes"][70:75],
+              sf=base["sf"][70:75], g=base["g"][70:75],
+              a_sw=O.place_sf_per_expert(base["sf"][70:75], np.array([0, 0, 5, 5]), np.array([0, 0, 128, 128])))
+    out2 = run_gemm(c2, torch.float32).cpu().numpy()
+    assert np.array_equal(out2[:5].view(np.uint32), out0[70:75].view(np.uint32))
+
+
+def test_grouped_gemm_inconsistent_offsets_are_reported_not_executed():
+    c = make_gemm_case([10, 20], 128, 256, seed=5)
+    c["off"] = np.array([0, 25, 20], dtype=np.int32)  # decreasing
+    Mt = 30
+    out = torch.full((Mt, 128), float("nan"), dtype=torch.float32, device="cuda")
+    st = _status()
+    M.minite_grouped_gemm_nvfp4(np_dev(c["codes"]), np_dev(np.resize(c["a_sw"], (Mt + 256) * 16)),
+                                np_dev(c["g"]), np_dev(c["bc"]), np_dev(c["bsw"]), np_dev(c["bg"]),
+                                np_dev(c["off"]), np_dev(c["sfo"]), out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1 << 1
+    assert torch.isnan(out).all()
+
+
+# --------------------------------------------------------------------- SwiGLU, combine
+
+@pytest.mark.parametrize("counts,I", [([3, 0, 130, 1], 64), ([256, 17], 768), ([1], 128),
+                                      ([100] * 5, 1536)])
+def test_swiglu_weighted_quant_bit_exact(counts, I):
+    rng = np.random.default_rng(len(counts) * 31 + I)
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    sfo = np.concatenate([[0], np.cumsum((np.array(counts) + 127) // 128 * 128)]).astype(np.int32)
+    Mu = int(off[-1])
+    Mt = Mu + 7
+    gu = O.f32_to_bf16((rng.standard_normal((Mt, 2 * I)) * 3).astype(np.float32))
+    gu[0, :I] = O.f32_to_bf16(np.linspace(-120, 120, I).astype(np.float32))  # clamp region
+    pw = rng.random(Mt).astype(np.float32)
+    for weights in (pw, None):
+        ref = O.swiglu_weighted_quant(gu, weights, off, sfo)
+        codes = torch.zeros((Mt, I // 2), dtype=torch.uint8, device="cuda")
+        sf = torch.full(((Mt + 128 * E) * (I // 16),), 0xAB, dtype=torch.uint8, device="cuda")
+        g = torch.zeros(Mt, dtype=torch.float32, device="cuda")
+        st = _status()
+        M.minite_swiglu_weighted_quant(bf16_dev(gu), None if weights is None else np_dev(weights),
+                                       E, np_dev(off), np_dev(sfo), codes, sf, g, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert np.array_equal(codes.cpu().numpy()[:Mu], ref["codes"])
+        assert np.array_equal(sf.cpu().numpy()[:ref["sf_swizzled"].size], ref["sf_swizzled"])
+        assert np.array_equal(g.cpu().numpy()[:Mu].view(np.uint32), ref["row_g"].view(np.uint32))
+
+
+@pytest.mark.parametrize("T,k,N", [(1, 1, 8), (64, 2, 64), (300, 8, 2048), (33, 5, 136)])
+def test_combine_bit_exact(T, k, N):
+    rng = np.random.default_rng(T * k + N)
+    Mr = T * k
+    D = O.f32_to_bf16(rng.standard_normal((Mr, N)).astype(np.float32))
+    dest = rng.permutation(Mr).reshape(T, k).astype(np.int32)
+    if T > 2:
+        dest[1, 0] = -1
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    st = _status()
+    M.minite_moe_combine(bf16_dev(D), np_dev(dest), y, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(u16(y), O.moe_combine(D, dest))
+
+
+# --------------------------------------------------------------------- whole MLP
+
+def _weights(d):
+    return (M.quantize(bf16_dev(d["w_gate_up"]), per_group=True),
+            M.quantize(bf16_dev(d["w_down"]), per_group=True))
+
+
+def test_mlp_tiny_stagewise_and_end_to_end():
+    d = IN.make_moe_inputs("tiny")
+    c = d["cfg"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    wgu, wd = _weights(d)
+    mlp = M.MoEMLP(T, H, I, E, k)
+    y = mlp.forward(bf16_dev(d["x"]), np_dev(d["topk_ids"]), np_dev(d["topk_w"]), wgu, wd)
+    torch.cuda.synchronize()
+    assert int(mlp.status.item()) == 0
+    ref = O.moe_mlp_forward(d["x"], d["topk_ids"], d["topk_w"], E,
+                            O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
+    p = ref["permute"]
+    Mu = int(p["expert_offsets"][-1])
+    check_permute(mlp, p, H)
+    gu_exact, _ = O.grouped_gemm_exact(p["codes"], p["sf"], p["row_g"],
+                                       *[O.quantize_weights(d["w_gate_up"])[i] for i in (0, 1)],
+                                       O.quantize_weights(d["w_gate_up"])[3], p["expert_offsets"])
+    assert_bf16_within_one_ulp(u16(mlp.gate_up)[:Mu], gu_exact, "gate_up")
+    yv = O.bf16_to_f32(u16(y)).astype(np.float64)
+    yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
+    assert np.linalg.norm(yv - yr) / np.linalg.norm(yr) < 2e-2
+
+
+def test_mlp_forward_full_size_sampled_tokens_match_oracle_chain():
+    """Full Qwen3-30B-A3B expert-MLP forward (4096 tokens). Per-token scaling
+    makes a token's output independent of the rest of the batch, so the oracle
+    runs the chain on a sample of tokens alone and the GPU's full-batch rows of
+    those tokens must agree within the chain tolerance."""
+    d = IN.make_moe_inputs("mlp")
+    c = d["cfg"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    wgu, wd = _weights(d)
+    mlp = M.MoEMLP(T, H, I, E, k)
+    y = mlp.forward(bf16_dev(d["x"]), np_dev(d["topk_ids"]), np_dev(d["topk_w"]), wgu, wd)
+    torch.cuda.synchronize()
+    assert int(mlp.status.item()) == 0
+    rng = np.random.default_rng(5)
+    tok = np.sort(rng.choice(T, 64, replace=False))
+    ref = O.moe_mlp_forward(d["x"][tok], d["topk_ids"][tok], d["topk_w"][tok], E,
+                            O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
+    yv = O.bf16_to_f32(u16(y)[tok]).astype(np.float64)
+    yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
+    rel = np.linalg.norm(yv - yr, axis=1) / np.linalg.norm(yr, axis=1)
+    assert rel.max() < 2e-2, rel.max()
+    same = (u16(y)[tok] == ref["y"]).mean()
+    assert same > 0.9, same
+
+
+# --------------------------------------------------------------------- failure detection
+
+def test_gemm_wait_timeout_sets_status_and_context_survives():
+    c = make_gemm_case([600, 300], 256, 2048, seed=21)
+    Mt = c["Mu"]
+    args = [np_dev(c["codes"]), np_dev(np.concatenate([c["a_sw"], np.zeros(256 * 128, np.uint8)])),
+            np_dev(c["g"]), np_dev(c["bc"]), np_dev(c["bsw"]), np_dev(c["bg"]), np_dev(c["off"]),
+            np_dev(c["sfo"])]
+    out = torch.zeros((Mt, 256), dtype=torch.float32, device="cuda")
+    st = _status()
+    try:
+        M.minite_set_wait_budget_ns(1)
+        M.minite_grouped_gemm_nvfp4(*args, out, st)
+        torch.cuda.synchronize()
+    finally:
+        M.minite_set_wait_budget_ns(0)
+    assert int(st.item()) & (1 << M.ERR_TIMEOUT)
+    st.zero_()
+    M.minite_grouped_gemm_nvfp4(*args, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    check_gemm(c, out)
