@@ -169,7 +169,7 @@ int minite_moe_permute_quant(const void* x, const int32_t* topk_ids, const float
  * out:      device, [M_total, N] BF16 (round to nearest even) or FP32; rows
  *           at or beyond offsets[E] are not written.
  * Shape rules: K % 64 == 0, N % 32 == 0, 1 <= E <= 1024, M_total < 2^31,
- * a_codes/b_codes 16-byte aligned with K/2 % 16 == 0.
+ * a_codes/b_codes 128-byte and out 32-byte aligned.
  */
 int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_g,
                               const uint8_t* b_codes, const uint8_t* b_sf, const float* b_g,

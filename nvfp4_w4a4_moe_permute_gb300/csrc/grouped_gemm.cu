@@ -8,21 +8,27 @@
 // report summary, section "Two complementary interventions").
 //
 // Design (sm_103a):
-//  * Tile 128 x BN (BN = 128) of the output, K consumed 256 elements (128
-//    bytes of packed E2M1) per pipeline stage; one tcgen05.mma of kind
-//    mxf4nvf4 with 4X block scaling covers K = 64, so a stage is 4 MMAs.
-//  * Warp 0: producer. TMA (128-byte swizzle) loads the A and B code tiles;
+//  * Output tile 128 x 256; K consumed 256 elements (128 bytes of packed
+//    E2M1) per pipeline stage; one tcgen05.mma of kind mxf4nvf4 with 4X block
+//    scaling covers K = 64 (M = 128, N = 256), so a stage is 4 MMAs.
+//  * Warp 0 (producer): TMA (128-byte swizzle) loads the A and B code tiles;
 //    plain bulk copies load the scale atoms, which the permutation and the
-//    quantizers already wrote in the MMA layout, so they need no reshuffle.
-//  * Warp 1: MMA issuer. Copies the scale atoms shared -> TMEM with
-//    tcgen05.cp (32x128b, replicated to the four lane quarters) and issues
-//    the MMAs into a TMEM accumulator; tcgen05.commit frees smem stages and
-//    publishes finished accumulators.
-//  * Warps 2..5: epilogue. tcgen05.ld the accumulator, multiply by
-//    1/(g_a[row] * g_w[e]), convert, and store rows of this expert only.
-//  * Two TMEM accumulators so the epilogue of one tile overlaps the main
-//    loop of the next; a static round-robin tile schedule over a grid of one
-//    CTA per SM. The tile list is derived on the device from expert_offsets.
+//    quantizers already wrote in the MMA layout.
+//  * Warp 1 (MMA issuer): one thread issues only MMAs and commits, with
+//    descriptors advanced by constant offsets, so the tensor pipe never waits
+//    on the issuing thread.
+//  * Warps 2..5 (scale warps): read each stage's scale atoms from shared
+//    memory and write them to a TMEM ring with tcgen05.st, replicated into
+//    the four 32-lane quarters (the layout a 32x128b.warpx4 copy produces).
+//    This keeps scale movement off the tensor pipe, where copies and MMAs
+//    would otherwise share issue bandwidth.
+//  * Warps 6..13 (epilogue): two warps per TMEM lane quarter, each draining
+//    128 of the 256 accumulator columns; the accumulator is released as soon
+//    as it is read, then rows are scaled by 1/(g_a[row] * g_w[e]), converted
+//    and stored for the rows of the tile's expert only.
+//  * TMEM: 256 accumulator columns + a 4-deep ring of 48 scale columns.
+//  * Static round-robin tile schedule over one CTA per SM; the tile list is
+//    derived on the device from expert_offsets.
 //  * Fixed K order, no split-K, one tile shape: a row's result depends only
 //    on its own codes and its expert's weights (batch invariance).
 //  * Every mbarrier wait is bounded by a %globaltimer budget; on expiry the
@@ -42,22 +48,25 @@ namespace minite {
 namespace gemm {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 256;
 constexpr int BK_BYTES = 128;                 // 256 E2M1 values per row per stage
-constexpr int STAGES = 6;
+constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK_BYTES;        // 16 KB
-constexpr int B_BYTES = BN * BK_BYTES;        // 16 KB
-constexpr int SF_ATOM = 512;                  // 128 rows x 4 scales
-constexpr int SFA_BYTES = 4 * SF_ATOM;        // 4 K-steps of 64
+constexpr int B_BYTES = BN * BK_BYTES;        // 32 KB
+constexpr int SF_ATOM = 512;                  // 128 rows x 4 scales (one K = 64 step)
+constexpr int SFA_BYTES = 4 * SF_ATOM;        // 4 K-steps
 constexpr int SFB_BYTES = 4 * SF_ATOM * (BN / 128);
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_WARPS = 14;
+constexpr int NUM_THREADS = NUM_WARPS * 32;
+constexpr int SF_WARP0 = 2, EPI_WARP0 = 6, NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COLS = BN;             // fp32 accumulator: one column per n
-constexpr uint32_t SFA_COL = 2 * ACC_COLS;    // 2 x 16 columns
-constexpr uint32_t SFB_COL = SFA_COL + 32;    // 2 x 16 columns (BN = 128)
+constexpr uint32_t ACC_COLS = BN;
+constexpr int NSF = 4;                                   // scale ring depth
+constexpr uint32_t SF_COLS = 16 + 16 * (BN / 128);       // A: 4 x 4 cols, B: 4 x 4 x (BN/128)
+constexpr uint32_t SF_COL0 = ACC_COLS;
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
-static_assert(SFB_COL + 32 <= TMEM_COLS, "TMEM budget");
+static_assert(SF_COL0 + NSF * SF_COLS <= TMEM_COLS, "TMEM budget");
 
 // Instruction descriptor of tcgen05.mma kind::mxf4nvf4: A and B E2M1 (format
 // code 1 in this kind), both K-major, UE4M3 scales (bit 23 clear), scale
@@ -70,8 +79,10 @@ constexpr uint32_t make_idesc() {
 struct Smem {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t sf_full[NSF];
+  uint64_t sf_empty[NSF];
+  uint64_t acc_full;
+  uint64_t acc_empty;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -121,6 +132,10 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, const int32_t* t
   return r;
 }
 
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -136,6 +151,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const int KSTEPS = p.K / 64;            // MMAs per tile
   const int atoms_per_rb = p.K / 64;      // scale atoms per 128-row block
   const int n_tiles = (p.N + BN - 1) / BN;
+  const int rb_per_expert = (p.N + 127) / 128;   // 128-row scale blocks of one weight
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_a);
@@ -144,10 +160,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&S.acc_full[b], 1);
-      mbar_init(&S.acc_empty[b], 4);
+    for (int b = 0; b < NSF; ++b) {
+      mbar_init(&S.sf_full[b], 4);
+      mbar_init(&S.sf_empty[b], 1);
     }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, NUM_EPI_WARPS);
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
     fence_mbar_init();
@@ -197,16 +215,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t armed[STAGES];
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) armed[s] = 0;
     if (lane == 0) {
+      uint32_t armed_mask = 0, armed_parity = 0;   // per stage: armed at least once, last parity
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const size_t sfb_expert = static_cast<size_t>((p.N + 127) / 128) * atoms_per_rb * SF_ATOM;
+      const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = decode_tile(t, n_tiles, tiles_prefix, p);
+        // the second 128-row scale block of B exists only inside the padded weight
+        const int nrb = min(BN / 128, rb_per_expert - tl.nt * (BN / 128));
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
           const int ks = min(4, KSTEPS - 4 * kt);
@@ -214,18 +232,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           uint8_t* sB = sA + A_BYTES;
           uint8_t* sSFA = sB + B_BYTES;
           uint8_t* sSFB = sSFA + SFA_BYTES;
-          mbar_arrive_expect_tx(&S.full[stage],
-                                A_BYTES + B_BYTES + 2 * static_cast<uint32_t>(ks) * SF_ATOM);
+          mbar_arrive_expect_tx(&S.full[stage], A_BYTES + B_BYTES +
+                                                    static_cast<uint32_t>(ks * (1 + nrb)) * SF_ATOM);
           tma_load_2d(sA, &tmap_a, &S.full[stage], kt * BK_BYTES, tl.row0);
           tma_load_2d(sB, &tmap_b, &S.full[stage], kt * BK_BYTES, tl.e * p.N + tl.nt * BN);
           bulk_load(sSFA,
                     p.a_sf + (static_cast<size_t>(tl.sf_rb) * atoms_per_rb + 4 * kt) * SF_ATOM,
                     ks * SF_ATOM, &S.full[stage]);
-          bulk_load(sSFB,
-                    p.b_sf + tl.e * sfb_expert +
-                        (static_cast<size_t>(tl.nt) * atoms_per_rb + 4 * kt) * SF_ATOM,
-                    ks * SF_ATOM, &S.full[stage]);
-          ++armed[stage];
+          for (int rb = 0; rb < nrb; ++rb)
+            bulk_load(sSFB + rb * 4 * SF_ATOM,
+                      p.b_sf + tl.e * sfb_expert +
+                          (static_cast<size_t>(tl.nt * (BN / 128) + rb) * atoms_per_rb + 4 * kt) *
+                              SF_ATOM,
+                      ks * SF_ATOM, &S.full[stage]);
+          armed_mask |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -236,112 +257,185 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       // drain: every armed stage's copies must have landed before exit
       volatile int no_abort = 0;
       for (int s = 0; s < STAGES; ++s)
-        if (armed[s]) mbar_wait(&S.full[s], (armed[s] - 1) & 1u, kDrainBudget, &no_abort);
+        if (armed_mask & (1u << s))
+          mbar_wait(&S.full[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc();
-      int stage = 0;
-      uint32_t phase = 0;
+      const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t bdesc0 = smem_desc(smem_u32(stages + A_BYTES), 16, 1024, kLayoutSwizzle128B);
+      int stage = 0, sfb = 0;
+      uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      int local = 0;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
-        const int buf = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
-        if (!mbar_wait(&S.acc_empty[buf], acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * ACC_COLS;
         for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag) ||
+              !mbar_wait(&S.sf_full[sfb], sf_phase, budget, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int ks = min(4, KSTEPS - 4 * kt);
-          uint8_t* sA = stages + stage * STAGE_BYTES;
-          uint8_t* sB = sA + A_BYTES;
-          uint8_t* sSFA = sB + B_BYTES;
-          uint8_t* sSFB = sSFA + SFA_BYTES;
-          const uint32_t sfa_t = tmem + SFA_COL + (kt & 1) * 16;
-          const uint32_t sfb_t = tmem + SFB_COL + (kt & 1) * 16;
-          for (int s = 0; s < ks; ++s) {
-            tc_cp_sf(sfa_t + 4 * s, smem_desc(smem_u32(sSFA + s * SF_ATOM), 0, 128, kLayoutNone));
-            tc_cp_sf(sfb_t + 4 * s, smem_desc(smem_u32(sSFB + s * SF_ATOM), 0, 128, kLayoutNone));
-          }
-          for (int s = 0; s < ks; ++s) {
-            const uint64_t ad = smem_desc(smem_u32(sA + 32 * s), 16, 1024, kLayoutSwizzle128B);
-            const uint64_t bd = smem_desc(smem_u32(sB + 32 * s), 16, 1024, kLayoutSwizzle128B);
-            tc_mma_nvfp4(d_tmem, ad, bd, idesc, sfa_t + 4 * s, sfb_t + 4 * s, (kt | s) != 0);
-          }
+          const uint64_t soff = static_cast<uint64_t>(stage * STAGE_BYTES) >> 4;
+          const uint32_t sf_t = tmem + SF_COL0 + sfb * SF_COLS;
+          for (int s = 0; s < ks; ++s)
+            tc_mma_nvfp4(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc, sf_t + 4 * s,
+                         sf_t + 16 + 4 * (BN / 128) * s, (kt | s) != 0);
           issued = true;
           tc_commit(&S.empty[stage]);
+          tc_commit(&S.sf_empty[sfb]);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++sfb == NSF) { sfb = 0; sf_phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(&S.acc_full[buf]);
+        tc_commit(&S.acc_full);
+        acc_phase ^= 1u;
       }
       if (!ok) {
         *abort_flag = 1;
         set_status(p.status, MINITE_ERR_TIMEOUT);
       }
       if (issued) {
-        // drain: all MMAs and scale copies of this thread complete before TMEM is freed
+        // drain: all MMAs of this thread complete before TMEM is freed
         tc_commit(&S.drain);
         volatile int no_abort = 0;
         mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
       }
     }
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------------------------------------ scale warps
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int stage = 0, sfb = 0;
+    uint32_t phase = 0, sf_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode_tile(t, n_tiles, tiles_prefix, p);
+      const int nrb = min(BN / 128, rb_per_expert - tl.nt * (BN / 128));
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag) ||
+            !mbar_wait(&S.full[stage], phase, budget, abort_flag))
+          ok = false;
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const int ks = min(4, KSTEPS - 4 * kt);
+        const uint8_t* sSFA = stages + stage * STAGE_BYTES + A_BYTES + B_BYTES;
+        const uint8_t* sSFB = sSFA + SFA_BYTES;
+        // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
+        uint32_t ra[16];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (s < ks) v = lds128(sSFA + s * SF_ATOM + lane * 16);
+          ra[4 * s] = v.x; ra[4 * s + 1] = v.y; ra[4 * s + 2] = v.z; ra[4 * s + 3] = v.w;
+        }
+        const uint32_t col = tmem + lane_base + SF_COL0 + sfb * SF_COLS;
+        tmem_st_16cols(col, ra);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          // k-steps 2h, 2h+1: columns 8s + 4rb of the B region
+          uint32_t rbv[16];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int s = 2 * h + j;
+#pragma unroll
+            for (int rb = 0; rb < 2; ++rb) {
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (s < ks && rb < nrb) v = lds128(sSFB + (rb * 4 + s) * SF_ATOM + lane * 16);
+              const int c = 8 * j + 4 * rb;
+              rbv[c] = v.x; rbv[c + 1] = v.y; rbv[c + 2] = v.z; rbv[c + 3] = v.w;
+            }
+          }
+          tmem_st_16cols(col + 16 + 16 * h, rbv);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.sf_full[sfb]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++sfb == NSF) { sfb = 0; sf_phase ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      set_status(p.status, MINITE_ERR_TIMEOUT);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int half = (warp - EPI_WARP0) >> 2;  // accumulator columns [128 half, 128 half + 128)
     const int r_in_tile = quarter * 32 + lane;
-    int local = 0;
+    uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
-      const int buf = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
-      if (!mbar_wait(&S.acc_full[buf], acc_phase, budget, abort_flag)) ok = false;
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile(t, n_tiles, tiles_prefix, p);
       const bool valid = r_in_tile < tl.rows;
       const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
       float scale = 0.0f;
       if (valid) scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * ACC_COLS;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(tbase + c * 32, r);
-        const int n = tl.nt * BN + c * 32;
-        if (valid && n < p.N) {
-          if (p.out_fp32) {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.N + n);
+      if (!mbar_wait(&S.acc_full, acc_phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      acc_phase ^= 1u;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+      const int n0 = tl.nt * BN + half * 128;
+      if (!p.out_fp32) {
+        // drain the whole 128-column slice into packed BF16 registers, release
+        // the accumulator to the next tile, then store
+        uint32_t pk[64];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), scale),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), scale),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), scale),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), scale));
-          } else {
-            uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.N + n);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(tbase + c * 32, r);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float lo = __fmul_rn(__uint_as_float(r[2 * j]), scale);
+            const float hi = __fmul_rn(__uint_as_float(r[2 * j + 1]), scale);
+            pk[16 * c + j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+                             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.acc_empty);
+        if (valid) {
+          uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.N + n0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (n0 + c * 32 < p.N) {
+              st_global_v8(orow + c * 32, pk[16 * c], pk[16 * c + 1], pk[16 * c + 2], pk[16 * c + 3],
+                           pk[16 * c + 4], pk[16 * c + 5], pk[16 * c + 6], pk[16 * c + 7]);
+              st_global_v8(orow + c * 32 + 16, pk[16 * c + 8], pk[16 * c + 9], pk[16 * c + 10],
+                           pk[16 * c + 11], pk[16 * c + 12], pk[16 * c + 13], pk[16 * c + 14],
+                           pk[16 * c + 15]);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(tbase + c * 32, r);
+          if (c == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty);
+          }
+          const int n = n0 + c * 32;
+          if (valid && n < p.N) {
+            float* o = static_cast<float*>(p.out) + row * p.N + n;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              uint32_t w[4];
+              uint32_t w[8];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float lo = __fmul_rn(__uint_as_float(r[8 * i + 2 * j]), scale);
-                const float hi = __fmul_rn(__uint_as_float(r[8 * i + 2 * j + 1]), scale);
-                w[j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-                       (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-              }
-              o[i] = make_uint4(w[0], w[1], w[2], w[3]);
+              for (int j = 0; j < 8; ++j)
+                w[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[8 * i + j]), scale));
+              st_global_v8(o + 8 * i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acc_empty[buf]);
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -420,7 +514,7 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
       K % 64 != 0 || E < 1 || E > 1024 || N * E >= (int64_t(1) << 31) || K > (1 << 20))
     return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(a_codes, 128) || !aligned(b_codes, 128) || !aligned(a_sf, 16) ||
-      !aligned(b_sf, 16) || !aligned(out, 16))
+      !aligned(b_sf, 16) || !aligned(out, 32))
     return MINITE_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
   if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, N * E, BN))
