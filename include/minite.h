@@ -57,7 +57,8 @@ typedef enum {
   MINITE_ERR_UNSUPPORTED_SHAPE = 2,/* a size rule below is violated */
   MINITE_ERR_CUDA = 3,             /* a CUDA launch or runtime call failed */
   MINITE_ERR_TIMEOUT = 4,          /* device: a pipeline wait gave up (status bit 1<<4) */
-  MINITE_ERR_BAD_ROUTING = 5       /* device: a routing id outside [0, E) (status bit 1<<5) */
+  MINITE_ERR_BAD_ROUTING = 5,      /* device: a routing id outside [0, E) (status bit 1<<5) */
+  MINITE_ERR_SCRATCH_LIMIT = 6     /* the problem needs more scratch than the built-in array */
 } minite_status_t;
 
 enum { MINITE_SCALE_PER_ROW = 0, MINITE_SCALE_PER_GROUP = 1 };
@@ -139,6 +140,33 @@ int minite_moe_permute_quant(const void* x, const int32_t* topk_ids, const float
                              int32_t* perm_src, int32_t* dest_row, float* perm_w,
                              void* workspace, size_t ws_bytes, int32_t* status,
                              minite_stream_t stream);
+
+/*
+ * minite_moe_permute_quant_noalloc -- minite_moe_permute_quant for callers
+ * that cannot allocate device memory. The paper has no counterpart to this
+ * entry point; it exists for deployment only.
+ *
+ * Same arguments, outputs and results as minite_moe_permute_quant, minus the
+ * workspace: the scratch lives in a 2 MiB array inside the library's device
+ * memory, held by every GPU that loads the library until the process exits.
+ * Use it where calling cudaMalloc is not possible: a fixed memory plan, a
+ * plugin that only receives its inputs and outputs, a loop that must not
+ * enter the allocator. It allocates nothing and calls no allocating routine.
+ *  - Limit: minite_workspace_bytes(MINITE_OP_PERMUTE_QUANT, T, H, E, k) must
+ *    not exceed 2 MiB (about T*E <= 8M at k = 8); larger problems return
+ *    MINITE_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls on a device share the array: calls that overlap on the GPU
+ *    (different streams with no ordering between them) race. Nothing needs
+ *    clearing between calls; every scratch word read is rewritten first.
+ */
+int minite_moe_permute_quant_noalloc(const void* x, const int32_t* topk_ids,
+                                     const float* topk_w, int64_t T, int64_t H, int32_t E,
+                                     int32_t k, uint8_t* codes, uint8_t* sf, float* row_g,
+                                     int32_t* expert_offsets, int32_t* sf_row_offsets,
+                                     int32_t* perm_src, int32_t* dest_row, float* perm_w,
+                                     int32_t* status, minite_stream_t stream);
 
 /*
  * minite_grouped_gemm_nvfp4 -- block-scaled FP4 x FP4 grouped GEMM over

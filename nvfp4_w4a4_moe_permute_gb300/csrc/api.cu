@@ -57,6 +57,7 @@ extern "C" const char* minite_status_string(int status) {
     case MINITE_ERR_CUDA: return "CUDA error";
     case MINITE_ERR_TIMEOUT: return "device pipeline wait timed out";
     case MINITE_ERR_BAD_ROUTING: return "routing id out of range";
+    case MINITE_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in array holds";
     default: return "unknown status";
   }
 }

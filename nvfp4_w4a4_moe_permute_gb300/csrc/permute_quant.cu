@@ -18,6 +18,8 @@
 //                         (token, slot) pair inside the chunk, then each token
 //                         is read once, quantized once in registers and its
 //                         codes / scales written to its k destination rows.
+#include <mutex>
+
 #include "common.cuh"
 #include "host_util.h"
 
@@ -283,4 +285,60 @@ extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
     default: return MINITE_ERR_UNSUPPORTED_SHAPE;
   }
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of minite_moe_permute_quant.
+//
+// Some callers cannot call cudaMalloc or hand out device memory at the point
+// where they run the permutation: a host application whose memory plan is
+// fixed before it starts, a plugin that receives only its input and output
+// buffers from the framework that loads it, or a latency-critical loop that
+// must not enter the allocator. For them this entry point takes the same
+// inputs and outputs but keeps its scratch (the per-chunk expert histogram
+// and the scan counter) in one fixed array in the library's own device
+// memory, so the call performs no allocation of any kind.
+//
+// The array is file-scope device memory: every GPU that loads the library
+// holds it until the process exits. Its device address is looked up once
+// per device (cudaGetSymbolAddress, under a mutex) on the first call made
+// while that device is current; make that first call before capturing a
+// stream. All calls on a device share the array, so two calls whose work
+// overlaps on the GPU (different streams, no ordering between them) race
+// and must not be issued. The kernels rewrite every scratch word they read
+// on each call (histogram entries and the counter), so nothing left by an
+// earlier call needs clearing.
+// ---------------------------------------------------------------------------
+
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(2) << 20;  // 2 MiB
+__device__ __align__(256) unsigned char g_permute_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[64] = {};
+}  // namespace
+
+extern "C" int minite_moe_permute_quant_noalloc(
+    const void* x, const int32_t* topk_ids, const float* topk_w, int64_t T, int64_t H,
+    int32_t E, int32_t k, uint8_t* codes, uint8_t* sf, float* row_g, int32_t* expert_offsets,
+    int32_t* sf_row_offsets, int32_t* perm_src, int32_t* dest_row, float* perm_w,
+    int32_t* status, minite_stream_t stream) {
+  if (T < 1 || E < 1 || E > 1024 || k < 1 || k > 32) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (perm_ws_bytes(T, E, k) > kStaticScratchBytes) return MINITE_ERR_SCRATCH_LIMIT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MINITE_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_permute_scratch) != cudaSuccess || !addr)
+        return MINITE_ERR_CUDA;
+      g_scratch_addr[dev] = addr;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  return minite_moe_permute_quant(x, topk_ids, topk_w, T, H, E, k, codes, sf, row_g,
+                                  expert_offsets, sf_row_offsets, perm_src, dest_row, perm_w,
+                                  scratch, kStaticScratchBytes, status, stream);
 }

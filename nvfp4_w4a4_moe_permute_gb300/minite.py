@@ -26,7 +26,7 @@ EXPORTS = [
     "minite_quantize_nvfp4", "minite_moe_permute_quant", "minite_grouped_gemm_nvfp4",
     "minite_swiglu_weighted_quant", "minite_moe_combine", "minite_workspace_bytes",
     "minite_status_string", "minite_version", "minite_test_convert",
-    "minite_set_wait_budget_ns",
+    "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc",
 ]
 
 
@@ -51,6 +51,8 @@ def load(path: str | None = None):
         "minite_quantize_nvfp4": [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp],
         "minite_moe_permute_quant": [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                      _vp, _vp, _vp, _vp, _sz, _vp, _vp],
+        "minite_moe_permute_quant_noalloc": [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp,
+                                             _vp, _vp, _vp, _vp, _vp, _vp, _vp],
         "minite_grouped_gemm_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                       _vp, _int, _vp, _vp],
         "minite_swiglu_weighted_quant": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -130,6 +132,20 @@ def minite_moe_permute_quant(x, topk_ids, topk_w, E, codes, sf, row_g, expert_of
                                          _p(perm_w), _p(workspace), ws_bytes, _p(status),
                                          _s(stream))
     _check(rc, "minite_moe_permute_quant")
+
+
+def minite_moe_permute_quant_noalloc(x, topk_ids, topk_w, E, codes, sf, row_g, expert_offsets,
+                                     sf_row_offsets, perm_src, dest_row, perm_w, status=None,
+                                     stream=None):
+    """As minite_moe_permute_quant, with the library's built-in scratch array
+    instead of a caller workspace (for callers that cannot allocate)."""
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    rc = load().minite_moe_permute_quant_noalloc(_p(x), _p(topk_ids), _p(topk_w), T, H, E, k,
+                                                 _p(codes), _p(sf), _p(row_g), _p(expert_offsets),
+                                                 _p(sf_row_offsets), _p(perm_src), _p(dest_row),
+                                                 _p(perm_w), _p(status), _s(stream))
+    _check(rc, "minite_moe_permute_quant_noalloc")
 
 
 def minite_grouped_gemm_nvfp4(a_codes, a_sf, a_g, b_codes, b_sf, b_g, expert_offsets,
