@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="minite", choices=["minite", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=["skewed", "mlp", "gate_up", "tiny"])
+    ap.add_argument("--gemm-variant", type=int, default=0,
+                    help="grouped-GEMM kernel: 0 automatic, 1 single-CTA, 2 CTA pair")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
@@ -254,6 +256,8 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     B.build()
+    from nvfp4_w4a4_moe_permute_gb300 import minite as M
+    M.minite_set_gemm_variant(args.gemm_variant)
     d = IN.make_moe_inputs(args.workload, seed=rank)
     step = Step(d, dev)
     stream = torch.cuda.current_stream(dev)

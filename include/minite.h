@@ -275,6 +275,15 @@ int minite_test_convert(const float* in, int64_t n, uint8_t* out_e2m1, uint8_t* 
  */
 void minite_set_wait_budget_ns(uint64_t ns);
 
+/*
+ * Test hook: which grouped-GEMM kernel minite_grouped_gemm_nvfp4 launches.
+ * 0 = automatic (currently the single-CTA kernel), 1 = single-CTA kernel
+ * (128 x 256 tiles), 2 = CTA-pair kernel (256 x 256 tiles on two SMs). Both
+ * give identical results.
+ * Process-wide; takes effect at the next call.
+ */
+void minite_set_gemm_variant(int variant);
+
 #ifdef __cplusplus
 }
 #endif

@@ -136,6 +136,70 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
+// One epilogue warp: drain 128 accumulator columns of its 32 TMEM lanes (row
+// `row` on each lane), call `release` on lane 0 once the accumulator slice is
+// in registers (the MMA may then overwrite it), then scale by `scale`,
+// convert and store the row's columns [n0, n0 + 128) that are below N.
+template <typename Release>
+__device__ __forceinline__ void epilogue_slice(const Params& p, uint32_t tbase, bool valid,
+                                               int64_t row, int n0, float scale, Release release) {
+  const int lane = threadIdx.x & 31;
+  if (!p.out_fp32) {
+    uint32_t pk[64];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      tmem_ld_32cols(tbase + c * 32, r);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float lo = __fmul_rn(__uint_as_float(r[2 * j]), scale);
+        const float hi = __fmul_rn(__uint_as_float(r[2 * j + 1]), scale);
+        pk[16 * c + j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+                         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) release();
+    if (valid) {
+      uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.N + n0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (n0 + c * 32 < p.N) {
+          st_global_v8(orow + c * 32, pk[16 * c], pk[16 * c + 1], pk[16 * c + 2], pk[16 * c + 3],
+                       pk[16 * c + 4], pk[16 * c + 5], pk[16 * c + 6], pk[16 * c + 7]);
+          st_global_v8(orow + c * 32 + 16, pk[16 * c + 8], pk[16 * c + 9], pk[16 * c + 10],
+                       pk[16 * c + 11], pk[16 * c + 12], pk[16 * c + 13], pk[16 * c + 14],
+                       pk[16 * c + 15]);
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      tmem_ld_32cols(tbase + c * 32, r);
+      if (c == 3) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release();
+      }
+      const int n = n0 + c * 32;
+      if (valid && n < p.N) {
+        float* o = static_cast<float*>(p.out) + row * p.N + n;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t w[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            w[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[8 * i + j]), scale));
+          st_global_v8(o + 8 * i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+        }
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -379,63 +443,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       acc_phase ^= 1u;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
-      const int n0 = tl.nt * BN + half * 128;
-      if (!p.out_fp32) {
-        // drain the whole 128-column slice into packed BF16 registers, release
-        // the accumulator to the next tile, then store
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld_32cols(tbase + c * 32, r);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float lo = __fmul_rn(__uint_as_float(r[2 * j]), scale);
-            const float hi = __fmul_rn(__uint_as_float(r[2 * j + 1]), scale);
-            pk[16 * c + j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-                             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.acc_empty);
-        if (valid) {
-          uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.N + n0;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (n0 + c * 32 < p.N) {
-              st_global_v8(orow + c * 32, pk[16 * c], pk[16 * c + 1], pk[16 * c + 2], pk[16 * c + 3],
-                           pk[16 * c + 4], pk[16 * c + 5], pk[16 * c + 6], pk[16 * c + 7]);
-              st_global_v8(orow + c * 32 + 16, pk[16 * c + 8], pk[16 * c + 9], pk[16 * c + 10],
-                           pk[16 * c + 11], pk[16 * c + 12], pk[16 * c + 13], pk[16 * c + 14],
-                           pk[16 * c + 15]);
-            }
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld_32cols(tbase + c * 32, r);
-          if (c == 3) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.acc_empty);
-          }
-          const int n = n0 + c * 32;
-          if (valid && n < p.N) {
-            float* o = static_cast<float*>(p.out) + row * p.N + n;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t w[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                w[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[8 * i + j]), scale));
-              st_global_v8(o + 8 * i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-            }
-          }
-        }
-      }
+      epilogue_slice(p, tbase, valid, row, tl.nt * BN + half * 128, scale,
+                     [&] { mbar_arrive(&S.acc_empty); });
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -449,6 +458,349 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ============================================================================
+// CTA-pair kernel (cta_group::2): a cluster of two CTAs on the two SMs of a
+// TPC computes a 256 x 256 output tile with tcgen05.mma.cta_group::2
+// (M = 256: each CTA holds 128 rows of A; N = 256: each CTA holds 128 rows of
+// B), so each SM stages half the B bytes of the single-CTA kernel for the same
+// MMA work and five stages fit in shared memory. Roles per CTA as in the
+// single-CTA kernel; the MMA thread of the even CTA issues for the pair and
+// its commits are multicast to both CTAs' barriers. Both CTAs' A/B TMA loads
+// count on the even CTA's full barrier; each CTA's scale atoms (A: its own
+// 128 rows, B: all 256 rows, which each SM's MMA half reads from its own
+// TMEM) arrive in its own stage on a local barrier. Scale warps copy them into
+// their CTA's TMEM ring and arrive on the even CTA's barrier.
+// ============================================================================
+
+constexpr int P_STAGES = 5;
+constexpr int P_A_BYTES = 128 * BK_BYTES;             // this CTA's 128 rows of A
+constexpr int P_B_BYTES = 128 * BK_BYTES;             // this CTA's 128 rows of B
+constexpr int P_SFA_BYTES = 4 * SF_ATOM;              // this CTA's A scales, 4 K-steps
+constexpr int P_SFB_BYTES = 8 * SF_ATOM;              // both 128-row blocks of B scales
+constexpr int P_AB_BYTES = P_A_BYTES + P_B_BYTES;     // counted on the even CTA's barrier
+constexpr int P_STAGE_BYTES = P_AB_BYTES + P_SFA_BYTES + P_SFB_BYTES;  // 38 KB
+constexpr int P_NSF = 5;
+constexpr uint32_t P_SF_COLS = 16 + 32;               // A: 4 x 4, B: 4 x 8 (256 rows)
+static_assert(P_STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+static_assert(SF_COL0 + P_NSF * P_SF_COLS <= TMEM_COLS, "TMEM budget");
+constexpr uint16_t kPairMask = 0x3;
+
+constexpr uint32_t make_idesc_pair() {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(256 >> 4) << 24);
+}
+
+struct PSmem {
+  uint64_t full[P_STAGES];
+  uint64_t sfdata[P_STAGES];
+  uint64_t empty[P_STAGES];
+  uint64_t sf_full[P_NSF];
+  uint64_t sf_empty[P_NSF];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_tiles;
+  int pad_;
+};
+
+struct PTile {
+  int e, nt;
+  int row0;      // first permuted row of the pair tile (the even CTA's first row)
+  int rows;      // valid rows from row0 (<= 256)
+  int sf_rb0;    // first 128-row scale block of the pair tile
+  int sf_rbs;    // scale blocks of the expert from sf_rb0 on
+};
+
+__device__ __forceinline__ PTile decode_pair_tile(int t, int n_tiles, const int32_t* tiles_prefix,
+                                                  const Params& p) {
+  PTile r;
+  const int mt = t / n_tiles;
+  r.nt = t - mt * n_tiles;
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tiles_prefix[mid] <= mt) lo = mid; else hi = mid;
+  }
+  r.e = lo;
+  const int ml = mt - tiles_prefix[lo];
+  const int off0 = __ldg(p.offsets + lo), off1 = __ldg(p.offsets + lo + 1);
+  r.row0 = off0 + ml * 256;
+  r.rows = min(256, off1 - r.row0);
+  const int s0 = __ldg(p.sf_offsets + lo), s1 = __ldg(p.sf_offsets + lo + 1);
+  r.sf_rb0 = s0 / 128 + 2 * ml;
+  r.sf_rbs = (s1 - s0) / 128 - 2 * ml;
+  return r;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PSmem& S = *reinterpret_cast<PSmem*>(stages + P_STAGES * P_STAGE_BYTES);
+  int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(num_clusters_x());
+  const int KT = (p.K + 255) / 256;
+  const int KSTEPS = p.K / 64;
+  const int atoms_per_rb = p.K / 64;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int rb_per_expert = (p.N + 127) / 128;
+  const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.sfdata[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int b = 0; b < P_NSF; ++b) {
+      mbar_init(&S.sf_full[b], 8);
+      mbar_init(&S.sf_empty[b], 1);
+    }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, 2 * NUM_EPI_WARPS);
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
+  if (warp == 2) {
+    int carry = 0;
+    bool bad = false;
+    if (lane == 0) tiles_prefix[0] = 0;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      int cnt = 0;
+      if (e < p.E) {
+        const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
+        const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
+        cnt = o1 - o0;
+        if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
+            (e == p.E - 1 && o1 > p.M))
+          bad = true;
+        cnt = cnt > 0 ? (cnt + 255) / 256 : 0;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (e < p.E) tiles_prefix[e + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      S.total_tiles = bad ? 0 : carry * n_tiles;
+      if (bad && blockIdx.x == 0) set_status(p.status, MINITE_ERR_INVALID_ARG);
+    }
+  }
+  // both CTAs' barriers exist and TMEM is allocated before any cross-CTA traffic
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+
+  const uint32_t tmem = S.tmem_base;
+  const int total = S.total_tiles;
+  volatile int* abort_flag = &S.abort_flag;
+  const uint32_t peer_abort = mapa_shared(smem_u32(&S.abort_flag), rank ^ 1u);
+  const uint32_t leader_full0 = mapa_shared(smem_u32(&S.full[0]), 0);
+  const uint32_t leader_sf_full0 = mapa_shared(smem_u32(&S.sf_full[0]), 0);
+  const uint32_t leader_acc_empty = mapa_shared(smem_u32(&S.acc_empty), 0);
+  const uint64_t budget = p.budget_ns;
+  constexpr uint64_t kDrainBudget = 200000000ull;
+  auto fail = [&](int code) {
+    *abort_flag = 1;
+    st_shared_cluster(peer_abort, 1u);
+    set_status(p.status, code);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t armed_mask = 0, armed_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, p);
+        const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;   // this CTA's A scale block exists
+        const int nrb = min(2, rb_per_expert - tl.nt * 2);      // B scale blocks inside the weight
+        const uint8_t* a_src = p.a_sf + static_cast<size_t>(tl.sf_rb0 + static_cast<int>(rank)) *
+                                            atoms_per_rb * SF_ATOM;
+        const uint8_t* b_src = p.b_sf + tl.e * sfb_expert +
+                               static_cast<size_t>(tl.nt * 2) * atoms_per_rb * SF_ATOM;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+          const int ks = min(4, KSTEPS - 4 * kt);
+          uint8_t* sA = stages + stage * P_STAGE_BYTES;
+          uint8_t* sB = sA + P_A_BYTES;
+          uint8_t* sSFA = sA + P_AB_BYTES;
+          uint8_t* sSFB = sSFA + P_SFA_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], 2 * P_AB_BYTES);
+          const uint32_t fb = leader_full0 + 8u * stage;
+          tma_load_2d_pair(sA, &tmap_a, fb, kt * BK_BYTES, tl.row0 + 128 * static_cast<int>(rank));
+          tma_load_2d_pair(sB, &tmap_b, fb, kt * BK_BYTES,
+                           tl.e * p.N + tl.nt * BN + 128 * static_cast<int>(rank));
+          mbar_arrive_expect_tx(&S.sfdata[stage],
+                                static_cast<uint32_t>(ks * ((a_ok ? 1 : 0) + nrb)) * SF_ATOM);
+          if (a_ok) bulk_load(sSFA, a_src + 4 * kt * SF_ATOM, ks * SF_ATOM, &S.sfdata[stage]);
+          for (int rb = 0; rb < nrb; ++rb)
+            bulk_load(sSFB + rb * 4 * SF_ATOM,
+                      b_src + (static_cast<size_t>(rb) * atoms_per_rb + 4 * kt) * SF_ATOM,
+                      ks * SF_ATOM, &S.sfdata[stage]);
+          armed_mask |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      volatile int no_abort = 0;
+      // this CTA's scale copies count on its own barriers
+      for (int s = 0; s < P_STAGES; ++s)
+        if (armed_mask & (1u << s))
+          mbar_wait(&S.sfdata[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
+      if (rank == 0) {
+        // both CTAs' A/B copies count on these barriers: all armed stages landed
+        for (int s = 0; s < P_STAGES; ++s)
+          if (armed_mask & (1u << s))
+            mbar_wait(&S.full[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
+      } else if (!ok) {
+        // this CTA's A/B copies count on the other CTA's barriers: give any
+        // copy still in flight time to land before the CTA can exit
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = make_idesc_pair();
+      const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t bdesc0 = smem_desc(smem_u32(stages + P_A_BYTES), 16, 1024, kLayoutSwizzle128B);
+      int stage = 0, sfb = 0;
+      uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int t = cid; t < total && ok; t += ncl) {
+        if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag) ||
+              !mbar_wait(&S.sf_full[sfb], sf_phase, budget, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const int ks = min(4, KSTEPS - 4 * kt);
+          const uint64_t soff = static_cast<uint64_t>(stage * P_STAGE_BYTES) >> 4;
+          const uint32_t sf_t = tmem + SF_COL0 + sfb * P_SF_COLS;
+          for (int s = 0; s < ks; ++s)
+            tc_mma_nvfp4_pair(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc,
+                              sf_t + 4 * s, sf_t + 16 + 8 * s, (kt | s) != 0);
+          issued = true;
+          tc_commit_pair_mc(&S.empty[stage], kPairMask);
+          tc_commit_pair_mc(&S.sf_empty[sfb], kPairMask);
+          if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+          if (++sfb == P_NSF) { sfb = 0; sf_phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&S.acc_full, kPairMask);
+        acc_phase ^= 1u;
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      if (issued) {
+        tc_commit_pair_mc(&S.drain, 0x1);
+        volatile int no_abort = 0;
+        mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
+      }
+    }
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------------------------------------ scale warps
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int stage = 0, sfb = 0;
+    uint32_t phase = 0, sf_phase = 0;
+    bool ok = true;
+    for (int t = cid; t < total && ok; t += ncl) {
+      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, p);
+      const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;
+      const int nrb = min(2, rb_per_expert - tl.nt * 2);
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag) ||
+            !mbar_wait(&S.sfdata[stage], phase, budget, abort_flag))
+          ok = false;
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const int ks = min(4, KSTEPS - 4 * kt);
+        const uint8_t* sSFA = stages + stage * P_STAGE_BYTES + P_AB_BYTES;
+        const uint8_t* sSFB = sSFA + P_SFA_BYTES;
+        // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
+        uint32_t ra[16], rbv[32];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (a_ok && s < ks) v = lds128(sSFA + s * SF_ATOM + lane * 16);
+          ra[4 * s] = v.x; ra[4 * s + 1] = v.y; ra[4 * s + 2] = v.z; ra[4 * s + 3] = v.w;
+#pragma unroll
+          for (int rb = 0; rb < 2; ++rb) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (rb < nrb && s < ks) w = lds128(sSFB + (rb * 4 + s) * SF_ATOM + lane * 16);
+            const int c = 8 * s + 4 * rb;
+            rbv[c] = w.x; rbv[c + 1] = w.y; rbv[c + 2] = w.z; rbv[c + 3] = w.w;
+          }
+        }
+        const uint32_t col = tmem + lane_base + SF_COL0 + sfb * P_SF_COLS;
+        tmem_st_16cols(col, ra);
+        tmem_st_16cols(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[0]));
+        tmem_st_16cols(col + 32, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[16]));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_sf_full0 + 8u * sfb);
+        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        if (++sfb == P_NSF) { sfb = 0; sf_phase ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int half = (warp - EPI_WARP0) >> 2;
+    const int r_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = cid; t < total; t += ncl) {
+      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, p);
+      const bool valid = r_in_tile < tl.rows;
+      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
+      float scale = 0.0f;
+      if (valid) scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
+      if (!mbar_wait(&S.acc_full, acc_phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      acc_phase ^= 1u;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+      epilogue_slice(p, tbase, valid, row, tl.nt * BN + half * 128, scale,
+                     [&] { mbar_arrive_cluster(leader_acc_empty); });
+    }
+    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  }
+
+  // no cross-CTA traffic may target a CTA that has left: both wait here, then
+  // free the pair's TMEM together
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
+}
+
 }  // namespace gemm
 
 // ---------------------------------------------------------------- host side
@@ -456,6 +808,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 namespace {
 
 std::atomic<uint64_t> g_budget_ns{0};
+std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -497,6 +850,10 @@ using namespace minite;
 
 extern "C" void minite_set_wait_budget_ns(uint64_t ns) { g_budget_ns.store(ns); }
 
+extern "C" void minite_set_gemm_variant(int variant) {
+  g_gemm_variant.store(variant == 1 || variant == 2 ? variant : 0);
+}
+
 extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
                                          const float* a_g, const uint8_t* b_codes,
                                          const uint8_t* b_sf, const float* b_g,
@@ -516,8 +873,12 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
   if (!aligned(a_codes, 128) || !aligned(b_codes, 128) || !aligned(a_sf, 16) ||
       !aligned(b_sf, 16) || !aligned(out, 32))
     return MINITE_ERR_INVALID_ARG;
+  // automatic choice: the single-CTA kernel (measured faster on every shape so far)
+  int variant = g_gemm_variant.load();
+  if (variant == 0) variant = 1;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, N * E, BN))
+  const uint32_t b_box = variant == 2 ? 128u : static_cast<uint32_t>(BN);
+  if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, N * E, b_box))
     return MINITE_ERR_CUDA;
   Params p;
   p.a_g = a_g;
@@ -534,19 +895,49 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
   p.E = E;
   p.out_fp32 = out_dtype == MINITE_OUT_FP32;
   p.budget_ns = wait_budget_ns();
-  const size_t smem = 1024 + STAGES * STAGE_BYTES + sizeof(Smem) + (E + 1) * sizeof(int32_t);
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-  });
-  if (attr_err != cudaSuccess || smem > 232448) return MINITE_ERR_CUDA;
-  // one CTA per SM, never more CTAs than the largest possible tile count
-  const int64_t max_tiles = (M_total / BM + E) * ((N + BN - 1) / BN);
-  int grid = num_sms();
-  if (max_tiles < grid) grid = static_cast<int>(max_tiles);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  grouped_gemm_kernel<<<grid, NUM_THREADS, smem, s>>>(ta, tb, p);
+  const int64_t n_tiles = (N + BN - 1) / BN;
+  if (variant == 1) {
+    const size_t smem = 1024 + STAGES * STAGE_BYTES + sizeof(Smem) + (E + 1) * sizeof(int32_t);
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+      attr_err = cudaFuncSetAttribute(grouped_gemm_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    });
+    if (attr_err != cudaSuccess || smem > 232448) return MINITE_ERR_CUDA;
+    // one CTA per SM, never more CTAs than the largest possible tile count
+    const int64_t max_tiles = (M_total / BM + E) * n_tiles;
+    int grid = num_sms();
+    if (max_tiles < grid) grid = static_cast<int>(max_tiles);
+    grouped_gemm_kernel<<<grid, NUM_THREADS, smem, s>>>(ta, tb, p);
+  } else {
+    const size_t smem = 1024 + P_STAGES * P_STAGE_BYTES + sizeof(PSmem) + (E + 1) * sizeof(int32_t);
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+      attr_err = cudaFuncSetAttribute(grouped_gemm_pair_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    });
+    if (attr_err != cudaSuccess || smem > 232448) return MINITE_ERR_CUDA;
+    // one CTA per SM in clusters of two, never more pairs than pair tiles
+    const int64_t max_pairs = (M_total / 256 + E) * n_tiles;
+    int pairs = num_sms() / 2;
+    if (max_pairs < pairs) pairs = static_cast<int>(max_pairs);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, ta, tb, p) != cudaSuccess)
+      return MINITE_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }

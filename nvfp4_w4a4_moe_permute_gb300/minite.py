@@ -26,7 +26,7 @@ EXPORTS = [
     "minite_quantize_nvfp4", "minite_moe_permute_quant", "minite_grouped_gemm_nvfp4",
     "minite_swiglu_weighted_quant", "minite_moe_combine", "minite_workspace_bytes",
     "minite_status_string", "minite_version", "minite_test_convert",
-    "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc",
+    "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc", "minite_set_gemm_variant",
 ]
 
 
@@ -71,6 +71,8 @@ def load(path: str | None = None):
     lib.minite_version.restype = ctypes.c_char_p
     lib.minite_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
     lib.minite_set_wait_budget_ns.restype = None
+    lib.minite_set_gemm_variant.argtypes = [_int]
+    lib.minite_set_gemm_variant.restype = None
     _LIB = lib
     return lib
 
@@ -107,6 +109,11 @@ def minite_workspace_bytes(op: int, a: int, b: int = 0, E: int = 0, k: int = 0) 
 
 def minite_set_wait_budget_ns(ns: int):
     load().minite_set_wait_budget_ns(int(ns))
+
+
+def minite_set_gemm_variant(variant: int):
+    """0 automatic, 1 single-CTA grouped-GEMM kernel, 2 CTA-pair kernel."""
+    load().minite_set_gemm_variant(int(variant))
 
 
 def minite_quantize_nvfp4(x, scale_mode, orientation, codes, sf, gscale_out, gscale_in=None,

@@ -30,6 +30,15 @@ def _lib():
     yield
 
 
+@pytest.fixture(autouse=True)
+def _automatic_gemm_variant():
+    yield
+    M.minite_set_gemm_variant(0)
+
+
+VARIANTS = [1, 2]  # single-CTA and CTA-pair grouped-GEMM kernels
+
+
 def _status():
     return torch.zeros(1, dtype=torch.int32, device="cuda")
 
@@ -257,7 +266,9 @@ GEMM_CASES = [
 
 @pytest.mark.parametrize("counts,N,K", GEMM_CASES)
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_grouped_gemm_small(counts, N, K, dtype):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_grouped_gemm_small(counts, N, K, dtype, variant):
+    M.minite_set_gemm_variant(variant)
     c = make_gemm_case(counts, N, K, seed=sum(counts) + N + K)
     out = run_gemm(c, dtype)
     check_gemm(c, out)
@@ -266,14 +277,18 @@ def test_grouped_gemm_small(counts, N, K, dtype):
         assert torch.isnan(out[c["Mu"]:].float()).all()
 
 
-def test_grouped_gemm_rows_beyond_used_are_untouched():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_grouped_gemm_rows_beyond_used_are_untouched(variant):
+    M.minite_set_gemm_variant(variant)
     c = make_gemm_case([10, 20], 128, 256, seed=3)
     out = run_gemm(c, torch.float32, M_total=100)
     check_gemm(c, out)
     assert torch.isnan(out[30:]).all()
 
 
-def test_grouped_gemm_one_hot_weights_reproduce_dequantized_activations():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_grouped_gemm_one_hot_weights_reproduce_dequantized_activations(variant):
+    M.minite_set_gemm_variant(variant)
     rng = np.random.default_rng(9)
     Mu, K, N = 200, 256, 32
     x = _rand_bf16(rng, (Mu, K))
@@ -293,7 +308,9 @@ def test_grouped_gemm_one_hot_weights_reproduce_dequantized_activations():
     assert np.allclose(out, ref, rtol=2.0 ** -22, atol=0)
 
 
-def test_grouped_gemm_dense_config_bf16_and_fp32():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_grouped_gemm_dense_config_bf16_and_fp32(variant):
+    M.minite_set_gemm_variant(variant)
     d = IN.make_dense_inputs()
     Mr, N, K = d["cfg"]["M"], d["cfg"]["N"], d["cfg"]["K"]
     codes, sf, g = O.quantize_per_row(O.bf16_to_f32(d["a"]))
@@ -313,9 +330,11 @@ def test_grouped_gemm_dense_config_bf16_and_fp32():
         check_gemm(c, out, rows=np.unique(rows))
 
 
-def test_grouped_gemm_batch_invariance():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_grouped_gemm_batch_invariance(variant):
     """A token's output row is bitwise identical whatever else is routed to its
     expert (more rows, fewer rows, other experts)."""
+    M.minite_set_gemm_variant(variant)
     base = make_gemm_case([70, 150, 33], 128, 512, seed=11)
     out0 = run_gemm(base, torch.float32).cpu().numpy()
     rng = np.random.default_rng(12)
@@ -344,7 +363,20 @@ def test_grouped_gemm_batch_invariance():
     assert np.array_equal(out2[:5].view(np.uint32), out0[70:75].view(np.uint32))
 
 
-def test_grouped_gemm_inconsistent_offsets_are_reported_not_executed():
+def test_grouped_gemm_kernels_agree_bitwise():
+    """The single-CTA and CTA-pair kernels use the same K order per row, so
+    their outputs are identical."""
+    c = make_gemm_case([300, 0, 1, 700, 129], 384, 1024, seed=31)
+    outs = []
+    for v in VARIANTS:
+        M.minite_set_gemm_variant(v)
+        outs.append(run_gemm(c, torch.float32).cpu().numpy().view(np.uint32))
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_grouped_gemm_inconsistent_offsets_are_reported_not_executed(variant):
+    M.minite_set_gemm_variant(variant)
     c = make_gemm_case([10, 20], 128, 256, seed=5)
     c["off"] = np.array([0, 25, 20], dtype=np.int32)  # decreasing
     Mt = 30
@@ -460,7 +492,9 @@ def test_mlp_forward_full_size_sampled_tokens_match_oracle_chain():
 
 # --------------------------------------------------------------------- failure detection
 
-def test_gemm_wait_timeout_sets_status_and_context_survives():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_gemm_wait_timeout_sets_status_and_context_survives(variant):
+    M.minite_set_gemm_variant(variant)
     c = make_gemm_case([600, 300], 256, 2048, seed=21)
     Mt = c["Mu"]
     args = [np_dev(c["codes"]), np_dev(np.concatenate([c["a_sw"], np.zeros(256 * 128, np.uint8)])),
