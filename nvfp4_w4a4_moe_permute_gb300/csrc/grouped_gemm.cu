@@ -112,9 +112,12 @@ struct Tile {
   int sf_rb;          // 128-row block of A's scales
 };
 
-// tile index -> (expert, m block, n block); tiles_prefix[e] = m blocks before e.
+// tile index -> (expert, m block, n block). tiles_prefix[e] = 128-row m blocks
+// before expert e; s_off = expert_offsets (both in shared memory). With
+// validated offsets the A scale block of m block `mt` is mt itself, since
+// sf_row_offsets[e] / 128 = sum of ceil(count / 128) = tiles_prefix[e].
 __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, const int32_t* tiles_prefix,
-                                            const Params& p) {
+                                            const int32_t* s_off, const Params& p) {
   Tile r;
   const int mt = t / n_tiles;
   r.nt = t - mt * n_tiles;
@@ -125,10 +128,9 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, const int32_t* t
   }
   r.e = lo;
   const int ml = mt - tiles_prefix[lo];
-  const int off0 = __ldg(p.offsets + lo), off1 = __ldg(p.offsets + lo + 1);
-  r.row0 = off0 + ml * BM;
-  r.rows = min(BM, off1 - r.row0);
-  r.sf_rb = __ldg(p.sf_offsets + lo) / 128 + ml;
+  r.row0 = s_off[lo] + ml * BM;
+  r.rows = min(BM, s_off[lo + 1] - r.row0);
+  r.sf_rb = mt;
   return r;
 }
 
@@ -208,6 +210,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Smem& S = *reinterpret_cast<Smem*>(stages + STAGES * STAGE_BYTES);
   int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
+  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -246,6 +249,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       if (e < p.E) {
         const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
         const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
+        s_off[e + 1] = o1;
+        if (e == 0) s_off[0] = o0;
         cnt = o1 - o0;
         if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
             (e == p.E - 1 && o1 > p.M))
@@ -286,7 +291,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       bool ok = true;
       const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(t, n_tiles, tiles_prefix, p);
+        const Tile tl = decode_tile(t, n_tiles, tiles_prefix, s_off, p);
         // the second 128-row scale block of B exists only inside the padded weight
         const int nrb = min(BN / 128, rb_per_expert - tl.nt * (BN / 128));
         for (int kt = 0; kt < KT; ++kt) {
@@ -376,7 +381,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint32_t phase = 0, sf_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode_tile(t, n_tiles, tiles_prefix, p);
+      const Tile tl = decode_tile(t, n_tiles, tiles_prefix, s_off, p);
       const int nrb = min(BN / 128, rb_per_expert - tl.nt * (BN / 128));
       for (int kt = 0; kt < KT; ++kt) {
         if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag) ||
@@ -433,7 +438,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile(t, n_tiles, tiles_prefix, p);
+      const Tile tl = decode_tile(t, n_tiles, tiles_prefix, s_off, p);
       const bool valid = r_in_tile < tl.rows;
       const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
       float scale = 0.0f;
@@ -463,26 +468,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // TPC computes a 256 x 256 output tile with tcgen05.mma.cta_group::2
 // (M = 256: each CTA holds 128 rows of A; N = 256: each CTA holds 128 rows of
 // B), so each SM stages half the B bytes of the single-CTA kernel for the same
-// MMA work and five stages fit in shared memory. Roles per CTA as in the
-// single-CTA kernel; the MMA thread of the even CTA issues for the pair and
-// its commits are multicast to both CTAs' barriers. Both CTAs' A/B TMA loads
-// count on the even CTA's full barrier; each CTA's scale atoms (A: its own
-// 128 rows, B: all 256 rows, which each SM's MMA half reads from its own
-// TMEM) arrive in its own stage on a local barrier. Scale warps copy them into
-// their CTA's TMEM ring and arrive on the even CTA's barrier.
+// MMA work. Roles per CTA as in the single-CTA kernel; the MMA thread of the
+// even CTA issues for the pair and its commits are multicast to both CTAs'
+// barriers. Both CTAs' A/B TMA loads count on the even CTA's full barrier.
+// Each CTA's scale atoms (A: its own 128 rows; B: all 256 rows, since each
+// SM's half of the MMA reads them from its own TMEM) go to a separate ring of
+// shared-memory slots, loaded P_LEAD k-tiles ahead of the A/B tiles, so the
+// scale warps have written them into their CTA's TMEM ring before the A/B
+// data lands and their latency stays off the MMA's critical path.
 // ============================================================================
 
-constexpr int P_STAGES = 5;
+constexpr int P_STAGES = 5;                           // A/B stages
 constexpr int P_A_BYTES = 128 * BK_BYTES;             // this CTA's 128 rows of A
 constexpr int P_B_BYTES = 128 * BK_BYTES;             // this CTA's 128 rows of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;  // 32 KB, counted on the even CTA's barrier
 constexpr int P_SFA_BYTES = 4 * SF_ATOM;              // this CTA's A scales, 4 K-steps
 constexpr int P_SFB_BYTES = 8 * SF_ATOM;              // both 128-row blocks of B scales
-constexpr int P_AB_BYTES = P_A_BYTES + P_B_BYTES;     // counted on the even CTA's barrier
-constexpr int P_STAGE_BYTES = P_AB_BYTES + P_SFA_BYTES + P_SFB_BYTES;  // 38 KB
-constexpr int P_NSF = 5;
+constexpr int P_SLOT_BYTES = P_SFA_BYTES + P_SFB_BYTES;  // 6 KB scale slot
+constexpr int P_SLOTS = 8;                            // scale slots in shared memory
+constexpr int P_LEAD = 3;                             // scale loads run this many k-tiles ahead
+constexpr int P_NSF = 5;                              // TMEM scale ring
 constexpr uint32_t P_SF_COLS = 16 + 32;               // A: 4 x 4, B: 4 x 8 (256 rows)
 static_assert(P_STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
 static_assert(SF_COL0 + P_NSF * P_SF_COLS <= TMEM_COLS, "TMEM budget");
+static_assert(P_LEAD < P_SLOTS, "scale lead");
 constexpr uint16_t kPairMask = 0x3;
 
 constexpr uint32_t make_idesc_pair() {
@@ -492,8 +501,9 @@ constexpr uint32_t make_idesc_pair() {
 
 struct PSmem {
   uint64_t full[P_STAGES];
-  uint64_t sfdata[P_STAGES];
   uint64_t empty[P_STAGES];
+  uint64_t sfdata[P_SLOTS];
+  uint64_t sfread[P_SLOTS];
   uint64_t sf_full[P_NSF];
   uint64_t sf_empty[P_NSF];
   uint64_t acc_full;
@@ -513,7 +523,10 @@ struct PTile {
   int sf_rbs;    // scale blocks of the expert from sf_rb0 on
 };
 
+// s_off = expert_offsets, s_sfb = sf_row_offsets / 128 (shared memory);
+// tiles_prefix[e] = 256-row m blocks before expert e.
 __device__ __forceinline__ PTile decode_pair_tile(int t, int n_tiles, const int32_t* tiles_prefix,
+                                                  const int32_t* s_off, const int32_t* s_sfb,
                                                   const Params& p) {
   PTile r;
   const int mt = t / n_tiles;
@@ -525,14 +538,35 @@ __device__ __forceinline__ PTile decode_pair_tile(int t, int n_tiles, const int3
   }
   r.e = lo;
   const int ml = mt - tiles_prefix[lo];
-  const int off0 = __ldg(p.offsets + lo), off1 = __ldg(p.offsets + lo + 1);
-  r.row0 = off0 + ml * 256;
-  r.rows = min(256, off1 - r.row0);
-  const int s0 = __ldg(p.sf_offsets + lo), s1 = __ldg(p.sf_offsets + lo + 1);
-  r.sf_rb0 = s0 / 128 + 2 * ml;
-  r.sf_rbs = (s1 - s0) / 128 - 2 * ml;
+  r.row0 = s_off[lo] + ml * 256;
+  r.rows = min(256, s_off[lo + 1] - r.row0);
+  r.sf_rb0 = s_sfb[lo] + 2 * ml;
+  r.sf_rbs = s_sfb[lo + 1] - r.sf_rb0;
   return r;
 }
+
+// Walks this cluster's k-tiles in order: tiles t = cid, cid + ncl, ...,
+// k-tiles 0..KT-1 of each.
+struct KIter {
+  int t, kt, ncl, total, KT, n_tiles;
+  PTile tl;
+  __device__ __forceinline__ bool valid() const { return t < total; }
+  const int32_t *prefix, *s_off, *s_sfb;
+  __device__ __forceinline__ void start(int cid, int ncl_, int total_, int KT_, int n_tiles_,
+                                        const int32_t* prefix_, const int32_t* s_off_,
+                                        const int32_t* s_sfb_, const Params& p) {
+    t = cid; kt = 0; ncl = ncl_; total = total_; KT = KT_; n_tiles = n_tiles_;
+    prefix = prefix_; s_off = s_off_; s_sfb = s_sfb_;
+    if (t < total) tl = decode_pair_tile(t, n_tiles, prefix, s_off, s_sfb, p);
+  }
+  __device__ __forceinline__ void advance(const Params& p) {
+    if (++kt == KT) {
+      kt = 0;
+      t += ncl;
+      if (t < total) tl = decode_pair_tile(t, n_tiles, prefix, s_off, s_sfb, p);
+    }
+  }
+};
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -540,8 +574,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  PSmem& S = *reinterpret_cast<PSmem*>(stages + P_STAGES * P_STAGE_BYTES);
+  uint8_t* slots = stages + P_STAGES * P_STAGE_BYTES;
+  PSmem& S = *reinterpret_cast<PSmem*>(slots + P_SLOTS * P_SLOT_BYTES);
   int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
+  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
+  int32_t* s_sfb = s_off + (p.E + 1);                           // [E+1] sf_row_offsets / 128
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -560,8 +597,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     tma_prefetch_desc(&tmap_b);
     for (int s = 0; s < P_STAGES; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.sfdata[s], 1);
       mbar_init(&S.empty[s], 1);
+    }
+    for (int s = 0; s < P_SLOTS; ++s) {
+      mbar_init(&S.sfdata[s], 1);
+      mbar_init(&S.sfread[s], 4);
     }
     for (int b = 0; b < P_NSF; ++b) {
       mbar_init(&S.sf_full[b], 8);
@@ -584,6 +624,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
       if (e < p.E) {
         const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
         const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
+        s_off[e + 1] = o1;
+        s_sfb[e + 1] = s1 / 128;
+        if (e == 0) { s_off[0] = o0; s_sfb[0] = s0 / 128; }
         cnt = o1 - o0;
         if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
             (e == p.E - 1 && o1 > p.M))
@@ -628,48 +671,69 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t armed_mask = 0, armed_parity = 0;
-      int stage = 0;
-      uint32_t phase = 0;
+      uint32_t armed_mask = 0, armed_parity = 0;            // A/B stages
+      uint32_t slot_mask = 0, slot_parity = 0;              // scale slots
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, slot_phase = 0;
       bool ok = true;
-      for (int t = cid; t < total && ok; t += ncl) {
-        const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, p);
-        const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;   // this CTA's A scale block exists
-        const int nrb = min(2, rb_per_expert - tl.nt * 2);      // B scale blocks inside the weight
-        const uint8_t* a_src = p.a_sf + static_cast<size_t>(tl.sf_rb0 + static_cast<int>(rank)) *
-                                            atoms_per_rb * SF_ATOM;
-        const uint8_t* b_src = p.b_sf + tl.e * sfb_expert +
-                               static_cast<size_t>(tl.nt * 2) * atoms_per_rb * SF_ATOM;
-        for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
-          const int ks = min(4, KSTEPS - 4 * kt);
-          uint8_t* sA = stages + stage * P_STAGE_BYTES;
-          uint8_t* sB = sA + P_A_BYTES;
-          uint8_t* sSFA = sA + P_AB_BYTES;
-          uint8_t* sSFB = sSFA + P_SFA_BYTES;
-          if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], 2 * P_AB_BYTES);
-          const uint32_t fb = leader_full0 + 8u * stage;
-          tma_load_2d_pair(sA, &tmap_a, fb, kt * BK_BYTES, tl.row0 + 128 * static_cast<int>(rank));
-          tma_load_2d_pair(sB, &tmap_b, fb, kt * BK_BYTES,
-                           tl.e * p.N + tl.nt * BN + 128 * static_cast<int>(rank));
-          mbar_arrive_expect_tx(&S.sfdata[stage],
-                                static_cast<uint32_t>(ks * ((a_ok ? 1 : 0) + nrb)) * SF_ATOM);
-          if (a_ok) bulk_load(sSFA, a_src + 4 * kt * SF_ATOM, ks * SF_ATOM, &S.sfdata[stage]);
-          for (int rb = 0; rb < nrb; ++rb)
-            bulk_load(sSFB + rb * 4 * SF_ATOM,
-                      b_src + (static_cast<size_t>(rb) * atoms_per_rb + 4 * kt) * SF_ATOM,
-                      ks * SF_ATOM, &S.sfdata[stage]);
-          armed_mask |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+      KIter ab, sf;
+      ab.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      sf.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      // scale atoms of k-tile `it` into the next slot, once the scale warps
+      // have read that slot's previous contents
+      auto issue_scales = [&](const KIter& it) -> bool {
+        if (!mbar_wait(&S.sfread[slot], slot_phase ^ 1u, budget, abort_flag)) return false;
+        const PTile& tl = it.tl;
+        const int ks = min(4, KSTEPS - 4 * it.kt);
+        const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;   // this CTA's A block exists
+        const int nrb = min(2, rb_per_expert - tl.nt * 2);      // B blocks inside the weight
+        uint8_t* sSFA = slots + slot * P_SLOT_BYTES;
+        uint8_t* sSFB = sSFA + P_SFA_BYTES;
+        mbar_arrive_expect_tx(&S.sfdata[slot],
+                              static_cast<uint32_t>(ks * ((a_ok ? 1 : 0) + nrb)) * SF_ATOM);
+        if (a_ok)
+          bulk_load(sSFA,
+                    p.a_sf + (static_cast<size_t>(tl.sf_rb0 + static_cast<int>(rank)) * atoms_per_rb +
+                              4 * it.kt) * SF_ATOM,
+                    ks * SF_ATOM, &S.sfdata[slot]);
+        for (int rb = 0; rb < nrb; ++rb)
+          bulk_load(sSFB + rb * 4 * SF_ATOM,
+                    p.b_sf + tl.e * sfb_expert +
+                        (static_cast<size_t>(tl.nt * 2 + rb) * atoms_per_rb + 4 * it.kt) * SF_ATOM,
+                    ks * SF_ATOM, &S.sfdata[slot]);
+        slot_mask |= 1u << slot;
+        slot_parity = (slot_parity & ~(1u << slot)) | (slot_phase << slot);
+        if (++slot == P_SLOTS) { slot = 0; slot_phase ^= 1u; }
+        return true;
+      };
+      for (int i = 0; i < P_LEAD && sf.valid() && ok; ++i) {
+        ok = issue_scales(sf);
+        sf.advance(p);
+      }
+      while (ab.valid() && ok) {
+        if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        uint8_t* sA = stages + stage * P_STAGE_BYTES;
+        uint8_t* sB = sA + P_A_BYTES;
+        if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], 2 * P_STAGE_BYTES);
+        const uint32_t fb = leader_full0 + 8u * stage;
+        tma_load_2d_pair(sA, &tmap_a, fb, ab.kt * BK_BYTES, ab.tl.row0 + 128 * static_cast<int>(rank));
+        tma_load_2d_pair(sB, &tmap_b, fb, ab.kt * BK_BYTES,
+                         ab.tl.e * p.N + ab.tl.nt * BN + 128 * static_cast<int>(rank));
+        armed_mask |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        ab.advance(p);
+        if (sf.valid()) {
+          if (!issue_scales(sf)) { ok = false; break; }
+          sf.advance(p);
         }
       }
       if (!ok) fail(MINITE_ERR_TIMEOUT);
       volatile int no_abort = 0;
       // this CTA's scale copies count on its own barriers
-      for (int s = 0; s < P_STAGES; ++s)
-        if (armed_mask & (1u << s))
-          mbar_wait(&S.sfdata[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
+      for (int s = 0; s < P_SLOTS; ++s)
+        if (slot_mask & (1u << s))
+          mbar_wait(&S.sfdata[s], (slot_parity >> s) & 1u, kDrainBudget, &no_abort);
       if (rank == 0) {
         // both CTAs' A/B copies count on these barriers: all armed stages landed
         for (int s = 0; s < P_STAGES; ++s)
@@ -726,47 +790,49 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ------------------------------------------------------------ scale warps
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    int stage = 0, sfb = 0;
-    uint32_t phase = 0, sf_phase = 0;
+    int slot = 0, sfb = 0;
+    uint32_t slot_phase = 0, sf_phase = 0;
     bool ok = true;
-    for (int t = cid; t < total && ok; t += ncl) {
-      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, p);
-      const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;
-      const int nrb = min(2, rb_per_expert - tl.nt * 2);
-      for (int kt = 0; kt < KT; ++kt) {
-        if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag) ||
-            !mbar_wait(&S.sfdata[stage], phase, budget, abort_flag))
-          ok = false;
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const int ks = min(4, KSTEPS - 4 * kt);
-        const uint8_t* sSFA = stages + stage * P_STAGE_BYTES + P_AB_BYTES;
-        const uint8_t* sSFB = sSFA + P_SFA_BYTES;
-        // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
-        uint32_t ra[16], rbv[32];
+    KIter it;
+    it.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
+    while (it.valid()) {
+      const bool a_ok = static_cast<int>(rank) < it.tl.sf_rbs;
+      const int nrb = min(2, rb_per_expert - it.tl.nt * 2);
+      const int ks = min(4, KSTEPS - 4 * it.kt);
+      if (!mbar_wait(&S.sfdata[slot], slot_phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const uint8_t* sSFA = slots + slot * P_SLOT_BYTES;
+      const uint8_t* sSFB = sSFA + P_SFA_BYTES;
+      // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
+      uint32_t ra[16], rbv[32];
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (a_ok && s < ks) v = lds128(sSFA + s * SF_ATOM + lane * 16);
-          ra[4 * s] = v.x; ra[4 * s + 1] = v.y; ra[4 * s + 2] = v.z; ra[4 * s + 3] = v.w;
+      for (int s = 0; s < 4; ++s) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (a_ok && s < ks) v = lds128(sSFA + s * SF_ATOM + lane * 16);
+        ra[4 * s] = v.x; ra[4 * s + 1] = v.y; ra[4 * s + 2] = v.z; ra[4 * s + 3] = v.w;
 #pragma unroll
-          for (int rb = 0; rb < 2; ++rb) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (rb < nrb && s < ks) w = lds128(sSFB + (rb * 4 + s) * SF_ATOM + lane * 16);
-            const int c = 8 * s + 4 * rb;
-            rbv[c] = w.x; rbv[c + 1] = w.y; rbv[c + 2] = w.z; rbv[c + 3] = w.w;
-          }
+        for (int rb = 0; rb < 2; ++rb) {
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (rb < nrb && s < ks) w = lds128(sSFB + (rb * 4 + s) * SF_ATOM + lane * 16);
+          const int c = 8 * s + 4 * rb;
+          rbv[c] = w.x; rbv[c + 1] = w.y; rbv[c + 2] = w.z; rbv[c + 3] = w.w;
         }
-        const uint32_t col = tmem + lane_base + SF_COL0 + sfb * P_SF_COLS;
-        tmem_st_16cols(col, ra);
-        tmem_st_16cols(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[0]));
-        tmem_st_16cols(col + 32, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[16]));
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(leader_sf_full0 + 8u * sfb);
-        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
-        if (++sfb == P_NSF) { sfb = 0; sf_phase ^= 1u; }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.sfread[slot]);
+      if (++slot == P_SLOTS) { slot = 0; slot_phase ^= 1u; }
+      if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const uint32_t col = tmem + lane_base + SF_COL0 + sfb * P_SF_COLS;
+      tmem_st_16cols(col, ra);
+      tmem_st_16cols(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[0]));
+      tmem_st_16cols(col + 32, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[16]));
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_sf_full0 + 8u * sfb);
+      if (++sfb == P_NSF) { sfb = 0; sf_phase ^= 1u; }
+      it.advance(p);
     }
     if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
   } else {
@@ -777,7 +843,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = cid; t < total; t += ncl) {
-      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, p);
+      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, s_off, s_sfb, p);
       const bool valid = r_in_tile < tl.rows;
       const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
       float scale = 0.0f;
@@ -898,7 +964,7 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t n_tiles = (N + BN - 1) / BN;
   if (variant == 1) {
-    const size_t smem = 1024 + STAGES * STAGE_BYTES + sizeof(Smem) + (E + 1) * sizeof(int32_t);
+    const size_t smem = 1024 + STAGES * STAGE_BYTES + sizeof(Smem) + 2 * (E + 1) * sizeof(int32_t);
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -912,7 +978,8 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     if (max_tiles < grid) grid = static_cast<int>(max_tiles);
     grouped_gemm_kernel<<<grid, NUM_THREADS, smem, s>>>(ta, tb, p);
   } else {
-    const size_t smem = 1024 + P_STAGES * P_STAGE_BYTES + sizeof(PSmem) + (E + 1) * sizeof(int32_t);
+    const size_t smem = 1024 + P_STAGES * P_STAGE_BYTES + P_SLOTS * P_SLOT_BYTES + sizeof(PSmem) +
+                        3 * (E + 1) * sizeof(int32_t);
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
