@@ -22,10 +22,11 @@
 //    the four 32-lane quarters (the layout a 32x128b.warpx4 copy produces).
 //    This keeps scale movement off the tensor pipe, where copies and MMAs
 //    would otherwise share issue bandwidth.
-//  * Warps 6..13 (epilogue): two warps per TMEM lane quarter, each draining
-//    128 of the 256 accumulator columns; the accumulator is released as soon
-//    as it is read, then rows are scaled by 1/(g_a[row] * g_w[e]), converted
-//    and stored for the rows of the tile's expert only.
+//  * Warps 6..21 (epilogue): four warps per TMEM lane quarter, each draining
+//    64 of the 256 accumulator columns (two 32-column loads) and releasing
+//    the accumulator right after the second; the next tile's MMAs then overlap
+//    the rest of the scaling by 1/(g_a[row] * g_w[e]), conversion and stores
+//    (rows of the tile's expert only).
 //  * TMEM: 256 accumulator columns + a 4-deep ring of 48 scale columns.
 //  * Static round-robin tile schedule over one CTA per SM; the tile list is
 //    derived on the device from expert_offsets.
@@ -57,9 +58,11 @@ constexpr int SF_ATOM = 512;                  // 128 rows x 4 scales (one K = 64
 constexpr int SFA_BYTES = 4 * SF_ATOM;        // 4 K-steps
 constexpr int SFB_BYTES = 4 * SF_ATOM * (BN / 128);
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-constexpr int NUM_WARPS = 14;
+constexpr int NUM_EPI_WARPS = 16;                 // four per TMEM lane quarter, 64 columns each
+constexpr int EPI_WARP0 = 6;
+constexpr int NUM_WARPS = EPI_WARP0 + NUM_EPI_WARPS;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
-constexpr int SF_WARP0 = 2, EPI_WARP0 = 6, NUM_EPI_WARPS = 8;
+constexpr int EPI_COLS = BN / (NUM_EPI_WARPS / 4);  // accumulator columns per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = BN;
 constexpr int NSF = 4;                                   // scale ring depth
@@ -138,20 +141,27 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
-// One epilogue warp: drain 128 accumulator columns of its 32 TMEM lanes (row
-// `row` on each lane), call `release` on lane 0 once the accumulator slice is
-// in registers (the MMA may then overwrite it), then scale by `scale`,
-// convert and store the row's columns [n0, n0 + 128) that are below N.
+// One epilogue warp: drain EPI_COLS (= 64) accumulator columns of its 32 TMEM
+// lanes (row `row` on each lane) as two 32-column loads, packing each to
+// BF16 (scaled by `scale`) as it arrives; call `release` on lane 0 as soon
+// as the second load has landed (the MMA may then overwrite the
+// accumulator), then store the row's columns [n0, n0 + 64) below N.
 template <typename Release>
 __device__ __forceinline__ void epilogue_slice(const Params& p, uint32_t tbase, bool valid,
                                                int64_t row, int n0, float scale, Release release) {
+  static_assert(EPI_COLS == 64, "two 32-column TMEM loads per epilogue warp");
   const int lane = threadIdx.x & 31;
   if (!p.out_fp32) {
-    uint32_t pk[64];
+    uint32_t pk[32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t r[32];
-      tmem_ld_32cols(tbase + c * 32, r);
+      tmem_ld_32cols(tbase + 32 * c, r);
+      if (c == 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release();
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float lo = __fmul_rn(__uint_as_float(r[2 * j]), scale);
@@ -160,35 +170,30 @@ __device__ __forceinline__ void epilogue_slice(const Params& p, uint32_t tbase, 
                          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
       }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) release();
-    if (valid) {
-      uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.N + n0;
+    if (!valid) return;
+    uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.N + n0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (n0 + c * 32 < p.N) {
-          st_global_v8(orow + c * 32, pk[16 * c], pk[16 * c + 1], pk[16 * c + 2], pk[16 * c + 3],
-                       pk[16 * c + 4], pk[16 * c + 5], pk[16 * c + 6], pk[16 * c + 7]);
-          st_global_v8(orow + c * 32 + 16, pk[16 * c + 8], pk[16 * c + 9], pk[16 * c + 10],
-                       pk[16 * c + 11], pk[16 * c + 12], pk[16 * c + 13], pk[16 * c + 14],
-                       pk[16 * c + 15]);
-        }
+    for (int c = 0; c < 2; ++c) {
+      if (n0 + c * 32 < p.N) {
+        st_global_v8(orow + c * 32, pk[16 * c], pk[16 * c + 1], pk[16 * c + 2], pk[16 * c + 3],
+                     pk[16 * c + 4], pk[16 * c + 5], pk[16 * c + 6], pk[16 * c + 7]);
+        st_global_v8(orow + c * 32 + 16, pk[16 * c + 8], pk[16 * c + 9], pk[16 * c + 10],
+                     pk[16 * c + 11], pk[16 * c + 12], pk[16 * c + 13], pk[16 * c + 14],
+                     pk[16 * c + 15]);
       }
     }
   } else {
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t r[32];
-      tmem_ld_32cols(tbase + c * 32, r);
-      if (c == 3) {
+      tmem_ld_32cols(tbase + 32 * c, r);
+      if (c == 1) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) release();
       }
-      const int n = n0 + c * 32;
-      if (valid && n < p.N) {
-        float* o = static_cast<float*>(p.out) + row * p.N + n;
+      if (valid && n0 + 32 * c < p.N) {
+        float* o = static_cast<float*>(p.out) + row * p.N + n0 + 32 * c;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint32_t w[8];
@@ -432,8 +437,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int half = (warp - EPI_WARP0) >> 2;  // accumulator columns [128 half, 128 half + 128)
+    const int quarter = warp & 3;                 // TMEM lanes this warp may access
+    const int cb = (warp - EPI_WARP0) >> 2;       // accumulator columns [64 cb, 64 cb + 64)
     const int r_in_tile = quarter * 32 + lane;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -447,8 +452,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       acc_phase ^= 1u;
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
-      epilogue_slice(p, tbase, valid, row, tl.nt * BN + half * 128, scale,
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * EPI_COLS;
+      epilogue_slice(p, tbase, valid, row, tl.nt * BN + cb * EPI_COLS, scale,
                      [&] { mbar_arrive(&S.acc_empty); });
     }
     if (!ok && lane == 0) {
@@ -838,7 +843,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
-    const int half = (warp - EPI_WARP0) >> 2;
+    const int cb = (warp - EPI_WARP0) >> 2;
     const int r_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -852,8 +857,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       acc_phase ^= 1u;
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
-      epilogue_slice(p, tbase, valid, row, tl.nt * BN + half * 128, scale,
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * EPI_COLS;
+      epilogue_slice(p, tbase, valid, row, tl.nt * BN + cb * EPI_COLS, scale,
                      [&] { mbar_arrive_cluster(leader_acc_empty); });
     }
     if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
