@@ -269,6 +269,15 @@ int minite_test_convert(const float* in, int64_t n, uint8_t* out_e2m1, uint8_t* 
                         float* out_exp, minite_stream_t stream);
 
 /*
+ * Test hook: the quantizers divide a block amax by 6 with an FMA-corrected
+ * division by a constant instead of an IEEE division. This adds, into the
+ * device counter *mismatches (caller zeroes it), the number of non-negative
+ * finite floats x for which that result differs from the IEEE quotient x / 6
+ * (expected: 0).
+ */
+int minite_test_div6_exhaustive(unsigned long long* mismatches, minite_stream_t stream);
+
+/*
  * Test hook for failure detection: sets the time budget of every bounded
  * pipeline wait in the GEMM (nanoseconds; 0 restores the default of 2 s).
  * Process-wide; takes effect at the next launch.

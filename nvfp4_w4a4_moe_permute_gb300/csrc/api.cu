@@ -33,6 +33,17 @@ __global__ void convert_test_kernel(const float* __restrict__ in, int64_t n,
   }
 }
 
+// Every non-negative finite float x: count x with div6_rn(x) != IEEE x / 6.
+__global__ void div6_exhaustive_kernel(unsigned long long* mismatches) {
+  unsigned long long bad = 0;
+  for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < 0x7F800000u;
+       b += gridDim.x * blockDim.x) {
+    const float x = __uint_as_float(b);
+    if (__float_as_uint(div6_rn(x)) != __float_as_uint(__fdiv_rn(x, 6.0f))) ++bad;
+  }
+  if (bad) atomicAdd(mismatches, bad);
+}
+
 }  // namespace minite
 
 using namespace minite;
@@ -73,5 +84,12 @@ extern "C" int minite_test_convert(const float* in, int64_t n, uint8_t* out_e2m1
   convert_test_kernel<<<static_cast<unsigned>(blocks), 256, 0,
                         reinterpret_cast<cudaStream_t>(stream)>>>(in, n, out_e2m1, out_e4m3,
                                                                   out_exp);
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
+extern "C" int minite_test_div6_exhaustive(unsigned long long* mismatches, minite_stream_t stream) {
+  if (!mismatches) return MINITE_ERR_INVALID_ARG;
+  div6_exhaustive_kernel<<<4 * num_sms(), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      mismatches);
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }

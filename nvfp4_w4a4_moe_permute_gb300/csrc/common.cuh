@@ -58,17 +58,54 @@ __device__ __forceinline__ float global_scale(float amax) {
   return fminf(__fdiv_rn(kGlobalNumerator, amax), kFltMax);
 }
 
+// x / 6 rounded to nearest for finite x >= 0, by Markstein's FMA-corrected
+// division by a constant (q0 = x * RN(1/6); r = x - 6 q0 exactly; q = q0 + r
+// RN(1/6)), with IEEE division kept for tiny x where the remainder could be
+// inexact. Equality with IEEE division over every non-negative finite float
+// is checked on the device by minite_test_div6_exhaustive.
+__device__ __forceinline__ float div6_rn(float x) {
+  constexpr float kSixth = 0.16666667163372039794921875f;  // RN(1/6)
+  if (x < 1.0e-30f) return __fdiv_rn(x, kE2M1Max);
+  const float q0 = __fmul_rn(x, kSixth);
+  const float r = __fmaf_rn(-kE2M1Max, q0, x);
+  return __fmaf_rn(r, kSixth, q0);
+}
+
+// Per-row table of encode factors: lane l holds RN(g / (1 + (l & 7) / 8)), g
+// divided by each of the 8 E4M3 significands. A block's factor RN(g / sf) is
+// the entry of sf's significand scaled by a power of two, which is exact
+// whenever the result is a normal float (checked; IEEE division otherwise).
+__device__ __forceinline__ float enc_table_entry(float g) {
+  return __fdiv_rn(g, 1.0f + 0.125f * static_cast<float>(threadIdx.x & 7));
+}
+
 // One 16-element block: scale code from its amax and the row's global scale,
 // and the factor that maps elements onto the E2M1 grid (0 when sf == 0).
+// s = (amax_b / 6) * g; sf = E4M3(s); enc = min(g / sf, FLT_MAX).
+// Warp-collective (one shuffle): every lane of the warp must call it.
 struct BlockScale {
   uint32_t sf;
   float enc;
 };
-__device__ __forceinline__ BlockScale block_scale(float amax_b, float g) {
+__device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float tk) {
   BlockScale r;
-  float s = __fmul_rn(__fdiv_rn(amax_b, kE2M1Max), g);
+  const float s = __fmul_rn(div6_rn(amax_b), g);
   r.sf = cvt_e4m3(s);
-  r.enc = r.sf ? fminf(__fdiv_rn(g, e4m3_value(r.sf)), kFltMax) : 0.0f;
+  const uint32_t e = (r.sf >> 3) & 15, m = r.sf & 7;
+  uint32_t idx;
+  int k;
+  if (e) {            // (1 + m/8) * 2^(e-7)
+    idx = m;
+    k = 7 - static_cast<int>(e);
+  } else {            // m * 2^-9 = (1 + idx/8) * 2^(j-9)
+    const int j = 31 - __clz(m | 1u);
+    idx = (m << (3 - j)) & 7u;
+    k = 9 - j;
+  }
+  const float t = __shfl_sync(0xffffffffu, tk, static_cast<int>(idx));
+  float enc = __fmul_rn(t, __uint_as_float(static_cast<uint32_t>(127 + k) << 23));
+  if (enc < 2.3509887016445750e-38f) enc = __fdiv_rn(g, e4m3_value(r.sf));  // below 2^-125
+  r.enc = r.sf ? fminf(enc, kFltMax) : 0.0f;
   return r;
 }
 
@@ -123,12 +160,13 @@ template <int NCH>
 __device__ __forceinline__ void quantize_row_warp(const float (&v)[NCH][8], int C, float g,
                                                   RowQuant<NCH>& out) {
   const int lane = threadIdx.x & 31;
+  const float tk = enc_table_entry(g);
 #pragma unroll
   for (int j = 0; j < NCH; ++j) {
     const bool valid = (256 * j + 8 * lane) < C;
     float am = amax8(v[j]);
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-    BlockScale bs = block_scale(am, g);
+    BlockScale bs = block_scale(am, g, tk);
     uint32_t sf = valid ? bs.sf : 0u;
     out.codes[j] = encode8(v[j], bs.enc, !valid || sf == 0);
     // gather the SF bytes of lanes 8a, 8a+2, 8a+4, 8a+6 into lane 8a

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(
   __syncthreads();
 
   const float g = g_in ? g_in[grp] : global_scale(__uint_as_float(amax_bits[grp]));
+  const float tk = enc_table_entry(g);
   const int lq = t / 2, half = t % 2;
   const int64_t q = c0 + lq;               // quantized row
   const int64_t e0 = r0 + 32 * half;       // first quantized column of this thread
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(
       am = fmaxf(am, fabsf(v[i]));
     }
     const bool valid = (e0 + 16 * b) < rows;
-    BlockScale bs = block_scale(am, g);
+    BlockScale bs = block_scale(am, g, tk);
     const uint32_t s = valid ? bs.sf : 0u;
     const bool zero = !valid || s == 0;
     float lo[8], hi[8];

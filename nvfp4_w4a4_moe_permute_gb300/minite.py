@@ -27,6 +27,7 @@ EXPORTS = [
     "minite_swiglu_weighted_quant", "minite_moe_combine", "minite_workspace_bytes",
     "minite_status_string", "minite_version", "minite_test_convert",
     "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc", "minite_set_gemm_variant",
+    "minite_test_div6_exhaustive",
 ]
 
 
@@ -58,6 +59,7 @@ def load(path: str | None = None):
         "minite_swiglu_weighted_quant": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
         "minite_moe_combine": [_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp],
         "minite_test_convert": [_vp, _i64, _vp, _vp, _vp, _vp],
+        "minite_test_div6_exhaustive": [_vp, _vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -187,6 +189,11 @@ def minite_test_convert(x, out_e2m1=None, out_e4m3=None, out_exp=None, stream=No
     rc = load().minite_test_convert(_p(x), x.numel(), _p(out_e2m1), _p(out_e4m3), _p(out_exp),
                                     _s(stream))
     _check(rc, "minite_test_convert")
+
+
+def minite_test_div6_exhaustive(counter, stream=None):
+    rc = load().minite_test_div6_exhaustive(_p(counter), _s(stream))
+    _check(rc, "minite_test_div6_exhaustive")
 
 
 # ---------------------------------------------------------------- allocation helpers

@@ -86,6 +86,13 @@ def test_converters_bit_exact_over_float32_sweep():
         assert np.array_equal(got, O.exp_spec(c).view(np.uint32)), "exp_spec"
 
 
+def test_division_by_six_is_exact_for_every_nonnegative_float():
+    counter = torch.zeros(1, dtype=torch.int64, device="cuda")
+    M.minite_test_div6_exhaustive(counter)
+    torch.cuda.synchronize()
+    assert int(counter.item()) == 0
+
+
 # --------------------------------------------------------------------- quantize
 
 @pytest.mark.parametrize("rows,cols", [(1, 16), (3, 48), (37, 80), (128, 256), (130, 2048),
