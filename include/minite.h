@@ -73,7 +73,8 @@ enum { MINITE_OP_QUANTIZE = 0, MINITE_OP_PERMUTE_QUANT = 1 };
  * path"); swizzled scale layout written by the quantizer itself ("Two
  * complementary interventions").
  *
- * x:           device, BF16 [groups, rows, cols].
+ * x:           device, BF16 [groups, rows, cols], 16-byte aligned (32-byte
+ *              aligned x is read with 32-byte loads).
  * scale_mode:  MINITE_SCALE_PER_ROW: one g per quantized row (activations);
  *              MINITE_SCALE_PER_GROUP: one g per group from the amax of the
  *              whole group (one expert's weight matrix).
@@ -87,13 +88,17 @@ enum { MINITE_OP_QUANTIZE = 0, MINITE_OP_PERMUTE_QUANT = 1 };
  * gscale_in:   device float [groups] or NULL. PER_GROUP only: use these g
  *              instead of computing the amax (re-quantizing a weight in the
  *              other orientation with the same global scale).
- * codes:       device, uint8 [groups, Rq, Cq/2].
- * sf:          device, uint8 [groups, roundup(Rq,128) * roundup(Cq/16,4)].
+ * codes:       device, uint8 [groups, Rq, Cq/2], 8-byte aligned.
+ * sf:          device, uint8 [groups, roundup(Rq,128) * roundup(Cq/16,4)],
+ *              4-byte aligned.
  * gscale_out:  device float, [groups*Rq] (PER_ROW) or [groups] (PER_GROUP).
  *              May equal gscale_in.
  * workspace:   device, >= minite_workspace_bytes(MINITE_OP_QUANTIZE, groups,
  *              0, 0, 0) bytes (PER_GROUP without gscale_in only; else NULL ok).
- * Shape rules: Cq % 16 == 0 (blocks), Rq % 2 == 0 when ALONG_ROWS, all > 0.
+ * Shape rules: Cq % 16 == 0 (blocks), cols % 8 == 0, all > 0; ALONG_COLS:
+ * cols <= 4096; ALONG_ROWS: PER_GROUP only; PER_GROUP: rows * cols / 16 <
+ * 2^32; groups * rows * cols < 2^40. Misaligned pointers: INVALID_ARG;
+ * other shapes: UNSUPPORTED_SHAPE (nothing enqueued in either case).
  */
 int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows, int64_t cols,
                           int scale_mode, int orientation, const float* gscale_in,
@@ -221,10 +226,12 @@ int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const
  * row exactly as minite_quantize_nvfp4 PER_ROW, with the SF written into the
  * per-expert padded regions given by sf_row_offsets.
  *
- * gate_up: device, BF16 [M, 2I].  perm_w: device float [M] or NULL.
- * codes:   device, uint8 [M, I/2].  sf: as for the permute output with I in
- *          place of H.  row_g: device, float [M].
- * Shape rules: I % 64 == 0, 1 <= E <= 1024.
+ * gate_up: device, BF16 [M, 2I], 32-byte aligned.  perm_w: device float [M]
+ *          or NULL.
+ * codes:   device, uint8 [M, I/2], 16-byte aligned.  sf: as for the permute
+ *          output with I in place of H, 16-byte aligned.  row_g: device,
+ *          float [M].
+ * Shape rules: I % 64 == 0, 64 <= I <= 2048, 1 <= E <= 1024, M < 2^31.
  */
 int minite_swiglu_weighted_quant(const void* gate_up, const float* perm_w,
                                  int64_t M, int64_t I, int32_t E,

@@ -195,6 +195,190 @@ __device__ __forceinline__ void store_row_warp(const RowQuant<NCH>& q, int C, ui
 }
 
 // ----------------------------------------------------------------------------
+// Lane-per-block quantizer core: one lane owns one whole 16-element block, so
+// the block amax needs no shuffle and the block scale is computed once per
+// block. A warp's 32 lanes cover 32 consecutive blocks (1 KB of BF16 input,
+// 256 bytes of codes).
+// ----------------------------------------------------------------------------
+
+// 16 BF16 values from a 32-byte aligned address, streaming (read once).
+__device__ __forceinline__ void ld_bf16x16(const uint16_t* p, uint32_t (&w)[8]) {
+  asm("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+
+// Same values from a 16-byte aligned address (two 16-byte loads).
+__device__ __forceinline__ void ld_bf16x16_a16(const uint16_t* p, uint32_t (&w)[8]) {
+  const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
+  const uint4 b = __ldcs(reinterpret_cast<const uint4*>(p) + 1);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+// max(|a|, |b|) per BF16 half, sign = sign(a) xor sign(b).
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// max |x| over 16 BF16 values (exact: the result is one of the inputs).
+__device__ __forceinline__ float amax_bf16x16(const uint32_t (&w)[8]) {
+  const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(w[0], w[1]),
+                                                   max_abs_bf16x2(w[2], w[3])),
+                                    max_abs_bf16x2(max_abs_bf16x2(w[4], w[5]),
+                                                   max_abs_bf16x2(w[6], w[7])));
+  return fmaxf(__uint_as_float((m & 0x7FFFu) << 16), __uint_as_float(m & 0x7FFF0000u));
+}
+
+__device__ __forceinline__ void unpack_bf16x16(const uint32_t (&w)[8], float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16lo(w[i]);
+    v[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ float amax_f32x16(const float (&v)[16]) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])),
+               fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+// Elementwise a * b (IEEE float products) on pairs of floats.
+__device__ __forceinline__ void mul_f32x2(float& a0, float& a1, float b0, float b1) {
+  uint64_t p, q;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(q) : "f"(b0), "f"(b1));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(p) : "l"(q));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(p));
+}
+
+// 8 values -> 4 code bytes: E2M1(v_i * enc) with each product an IEEE float
+// product (two per packed multiply); element 0 lands in the low nibble.
+__device__ __forceinline__ uint32_t encode8_packed(float v0, float v1, float v2, float v3,
+                                                   float v4, float v5, float v6, float v7,
+                                                   float enc) {
+  uint32_t out;
+  asm("{\n\t"
+      ".reg .b64 e2, p0, p1, p2, p3;\n\t"
+      ".reg .f32 b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
+      ".reg .b8 c0, c1, c2, c3;\n\t"
+      "mov.b64 e2, {%9, %9};\n\t"
+      "mov.b64 p0, {%1, %2};\n\t"
+      "mov.b64 p1, {%3, %4};\n\t"
+      "mov.b64 p2, {%5, %6};\n\t"
+      "mov.b64 p3, {%7, %8};\n\t"
+      "mul.rn.f32x2 p0, p0, e2;\n\t"
+      "mul.rn.f32x2 p1, p1, e2;\n\t"
+      "mul.rn.f32x2 p2, p2, e2;\n\t"
+      "mul.rn.f32x2 p3, p3, e2;\n\t"
+      "mov.b64 {b0, b1}, p0;\n\t"
+      "mov.b64 {b2, b3}, p1;\n\t"
+      "mov.b64 {b4, b5}, p2;\n\t"
+      "mov.b64 {b6, b7}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, b1, b0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, b3, b2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, b5, b4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, b7, b6;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t"
+      "}"
+      : "=r"(out)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7), "f"(enc));
+  return out;
+}
+
+// One block of 16 values -> 8 code bytes (all zero when `zero`).
+__device__ __forceinline__ uint2 encode16(const float (&v)[16], float enc, bool zero) {
+  const uint32_t lo = encode8_packed(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], enc);
+  const uint32_t hi = encode8_packed(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15], enc);
+  return zero ? make_uint2(0u, 0u) : make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ void st_u64(uint8_t* p, uint2 v) {
+  *reinterpret_cast<uint2*>(p) = v;
+}
+
+// One block: its scale code and 8 code bytes. Warp-collective (block_scale).
+struct QBlock {
+  uint2 codes;
+  uint32_t sf;
+};
+__device__ __forceinline__ QBlock quant_block(const float (&v)[16], float am, float g, float tk,
+                                              bool valid) {
+  const BlockScale bs = block_scale(am, g, tk);
+  QBlock r;
+  r.sf = valid ? bs.sf : 0u;
+  r.codes = encode16(v, bs.enc, r.sf == 0);
+  return r;
+}
+
+// A row of nb <= 32*NCH blocks held by one warp, lane l owning blocks 32j + l
+// as raw BF16 words. Loads return this lane's amax over its blocks.
+template <int NCH, bool A32>
+__device__ __forceinline__ float load_row_blocks(const uint16_t* row, int nb,
+                                                 uint32_t (&w)[NCH][8], float (&am)[NCH]) {
+  const int lane = threadIdx.x & 31;
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int c = 32 * j + lane;
+    if (c < nb) {
+      if (A32) ld_bf16x16(row + 16 * c, w[j]);
+      else ld_bf16x16_a16(row + 16 * c, w[j]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[j][i] = 0u;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    am[j] = amax_bf16x16(w[j]);
+    m = fmaxf(m, am[j]);
+  }
+  return m;
+}
+
+template <int NCH>
+__device__ __forceinline__ void quant_row_blocks(const uint32_t (&w)[NCH][8],
+                                                 const float (&am)[NCH], int nb, float g,
+                                                 QBlock (&q)[NCH]) {
+  const int lane = threadIdx.x & 31;
+  const float tk = enc_table_entry(g);
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    if (32 * j < nb) {  // warp-uniform
+      float v[16];
+      unpack_bf16x16(w[j], v);
+      q[j] = quant_block(v, am[j], g, tk, 32 * j + lane < nb);
+    } else {
+      q[j].codes = make_uint2(0u, 0u);
+      q[j].sf = 0u;
+    }
+  }
+}
+
+// Codes of the row at codes_row (8 bytes per block); one scale byte per SF
+// column (0 for the padding columns [nb, kc)) into the swizzled region sf_base
+// at local row r.
+template <int NCH>
+__device__ __forceinline__ void store_row_blocks(const QBlock (&q)[NCH], int nb,
+                                                 uint8_t* codes_row, uint8_t* sf_base,
+                                                 int64_t r, int kc) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int c = 32 * j + lane;
+    if (c < nb) st_u64(codes_row + 8 * c, q[j].codes);
+    if (c < kc) sf_base[sf_offset(r, c, kc)] = static_cast<uint8_t>(q[j].sf);
+  }
+}
+
+// ----------------------------------------------------------------------------
 // The specified exponential: Cody-Waite reduction with a two-part ln 2 and a
 // degree-7 Taylor polynomial, every step one IEEE float operation rounded to
 // nearest (no contraction), inputs clamped to [-87, 88].

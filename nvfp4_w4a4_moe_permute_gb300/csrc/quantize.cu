@@ -44,61 +44,123 @@ __global__ void group_amax_kernel(const uint16_t* __restrict__ x, int64_t elems_
   }
 }
 
-template <int NCH>
-__global__ void __launch_bounds__(256) quantize_rows_kernel(
-    const uint16_t* __restrict__ x, int64_t groups, int64_t rows, int cols, int per_group,
+// Per-group quantization along columns as one flat stream of blocks: the
+// blocks of group grp are numbered row-major, b = r * nb + c, and cut into
+// chunks of 32 (one per lane). Warp w owns a contiguous range of chunks and
+// keeps kU of them in flight; the group's g and encode table are refreshed
+// only when the group changes.
+constexpr int kU = 4;
+template <bool A32>
+__global__ void __launch_bounds__(256, 2) quantize_group_blocks_kernel(
+    const uint16_t* __restrict__ x, int64_t groups, int64_t rows, int nb, uint32_t nb_magic,
     const float* __restrict__ g_in, const uint32_t* __restrict__ amax_bits,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int kc = ((cols / 16) + 3) & ~3;
+  const int kc = (nb + 3) & ~3;
   const int64_t rows_pad = (rows + 127) & ~int64_t(127);
   const int64_t sf_group_bytes = rows_pad * kc;
-  const int64_t total = groups * rows;
-
-  for (int64_t row = warp; row < total; row += nwarps) {
-    const int64_t grp = row / rows;
-    const int64_t r = row - grp * rows;
-    const uint16_t* xr = x + row * cols;
-    float v[NCH][8];
-    float am = 0.0f;
+  const uint32_t bpg = static_cast<uint32_t>(rows * nb);  // blocks per group (< 2^32)
+  const int64_t cpg = (bpg + 31) / 32;
+  const int64_t total = groups * cpg;
+  const int64_t per = (total + nwarps - 1) / nwarps;
+  int64_t q = warp * per;
+  const int64_t q_end = q + per < total ? q + per : total;
+  int64_t grp = q / cpg;
+  int64_t qin = q - grp * cpg;
+  int64_t cur = -1;
+  float g = 1.0f, tk = 1.0f;
+  while (q < q_end) {
+    uint32_t w[kU][8];
+    int64_t gq[kU];
+    uint32_t bq[kU];
 #pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int e0 = 256 * j + 8 * lane;
-      if (e0 < cols) {
-        uint4 u = __ldcs(reinterpret_cast<const uint4*>(xr + e0));
-        unpack_bf16x8(u, v[j]);
+    for (int u = 0; u < kU; ++u) {
+      gq[u] = grp;
+      bq[u] = static_cast<uint32_t>(qin) * 32u + lane;
+      if (q + u < q_end && bq[u] < bpg) {
+        const uint16_t* src = x + (grp * bpg + bq[u]) * 16;
+        if (A32) ld_bf16x16(src, w[u]);
+        else ld_bf16x16_a16(src, w[u]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[j][i] = 0.0f;
+        for (int i = 0; i < 8; ++i) w[u][i] = 0u;
       }
-      am = fmaxf(am, amax8(v[j]));
+      if (++qin == cpg) { qin = 0; ++grp; }
     }
-    float g;
-    if (per_group) {
-      g = g_in ? g_in[grp] : global_scale(__uint_as_float(amax_bits[grp]));
-    } else {
-      g = global_scale(warp_max(am));
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (q + u >= q_end) break;  // warp-uniform
+      if (gq[u] != cur) {         // warp-uniform
+        cur = gq[u];
+        g = g_in ? g_in[cur] : global_scale(__uint_as_float(amax_bits[cur]));
+        tk = enc_table_entry(g);
+      }
+      const bool valid = bq[u] < bpg;
+      float v[16];
+      unpack_bf16x16(w[u], v);
+      const QBlock qb = quant_block(v, amax_bf16x16(w[u]), g, tk, valid);
+      if (valid) {
+        // r = bq / nb: nb_magic = floor(2^32 / nb) undershoots by at most one
+        uint32_t r = __umulhi(bq[u], nb_magic);
+        uint32_t c = bq[u] - r * static_cast<uint32_t>(nb);
+        if (c >= static_cast<uint32_t>(nb)) { c -= nb; ++r; }
+        st_u64(codes + (gq[u] * bpg + bq[u]) * 8, qb.codes);
+        sf[gq[u] * sf_group_bytes + sf_offset(r, c, kc)] = static_cast<uint8_t>(qb.sf);
+        if (c + 1 == static_cast<uint32_t>(nb)) {  // last block of the row: pad columns
+          for (int cc = nb; cc < kc; ++cc) sf[gq[u] * sf_group_bytes + sf_offset(r, cc, kc)] = 0;
+        }
+      }
     }
-    RowQuant<NCH> q;
-    quantize_row_warp<NCH>(v, cols, g, q);
-    store_row_warp<NCH>(q, cols, codes + row * (cols / 2), sf + grp * sf_group_bytes, r, kc);
-    if (!per_group && lane == 0) g_out[row] = g;
+    q += kU;
   }
 
   // zero the scale bytes of the padding rows [rows, rows_pad) of every group
   const int64_t pad_rows = rows_pad - rows;
   for (int64_t p = warp; p < groups * pad_rows; p += nwarps) {
-    const int64_t grp = p / pad_rows;
-    const int64_t r = rows + (p - grp * pad_rows);
+    const int64_t gp = p / pad_rows;
+    const int64_t r = rows + (p - gp * pad_rows);
     for (int a = lane; a < kc / 4; a += 32)
-      *reinterpret_cast<uint32_t*>(sf + grp * sf_group_bytes + sf_offset(r, 4 * a, kc)) = 0u;
+      *reinterpret_cast<uint32_t*>(sf + gp * sf_group_bytes + sf_offset(r, 4 * a, kc)) = 0u;
   }
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (t < groups) g_out[t] = g_in ? g_in[t] : global_scale(__uint_as_float(amax_bits[t]));
+}
 
-  if (per_group) {
-    const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (t < groups) g_out[t] = g_in ? g_in[t] : global_scale(__uint_as_float(amax_bits[t]));
+// Per-row (activation) quantization along columns: one warp per row, lane l
+// owning blocks 32j + l, the row held in registers between its amax and its
+// encoding.
+template <int NCH, bool A32>
+__global__ void __launch_bounds__(256) quantize_token_rows_kernel(
+    const uint16_t* __restrict__ x, int64_t groups, int64_t rows, int cols,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nb = cols / 16;
+  const int kc = (nb + 3) & ~3;
+  const int64_t rows_pad = (rows + 127) & ~int64_t(127);
+  const int64_t sf_group_bytes = rows_pad * kc;
+  const int64_t total = groups * rows;
+  for (int64_t row = warp; row < total; row += nwarps) {
+    const int64_t grp = row / rows;
+    const int64_t r = row - grp * rows;
+    uint32_t w[NCH][8];
+    float am[NCH];
+    const float m = load_row_blocks<NCH, A32>(x + row * cols, nb, w, am);
+    const float g = global_scale(warp_max(m));
+    QBlock qb[NCH];
+    quant_row_blocks<NCH>(w, am, nb, g, qb);
+    store_row_blocks<NCH>(qb, nb, codes + row * (cols / 2), sf + grp * sf_group_bytes, r, kc);
+    if (lane == 0) g_out[row] = g;
+  }
+  const int64_t pad_rows = rows_pad - rows;
+  for (int64_t p = warp; p < groups * pad_rows; p += nwarps) {
+    const int64_t gp = p / pad_rows;
+    const int64_t r = rows + (p - gp * pad_rows);
+    for (int a = lane; a < kc / 4; a += 32)
+      *reinterpret_cast<uint32_t*>(sf + gp * sf_group_bytes + sf_offset(r, 4 * a, kc)) = 0u;
   }
 }
 
@@ -181,16 +243,39 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(
 }
 
 template <int NCH>
-static void launch_rows(const uint16_t* x, int64_t groups, int64_t rows, int cols, int per_group,
-                        const float* g_in, const uint32_t* amax, uint8_t* codes, uint8_t* sf,
-                        float* g_out, cudaStream_t s) {
+static void launch_token_rows(const uint16_t* x, int64_t groups, int64_t rows, int cols, bool a32,
+                              uint8_t* codes, uint8_t* sf, float* g_out, cudaStream_t s) {
   const int64_t total = groups * ((rows + 127) & ~int64_t(127));
   int64_t blocks = (total + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
-  if (per_group && blocks * 256 < groups) blocks = (groups + 255) / 256;
-  quantize_rows_kernel<NCH><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      x, groups, rows, cols, per_group, g_in, amax, codes, sf, g_out);
+  if (a32)
+    quantize_token_rows_kernel<NCH, true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        x, groups, rows, cols, codes, sf, g_out);
+  else
+    quantize_token_rows_kernel<NCH, false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        x, groups, rows, cols, codes, sf, g_out);
+}
+
+static void launch_group_blocks(const uint16_t* x, int64_t groups, int64_t rows, int cols,
+                                bool a32, const float* g_in, const uint32_t* amax,
+                                uint8_t* codes, uint8_t* sf, float* g_out, cudaStream_t s) {
+  const int nb = cols / 16;
+  const uint32_t magic = nb == 1 ? 0xFFFFFFFFu
+                                 : static_cast<uint32_t>((uint64_t(1) << 32) / uint64_t(nb));
+  const int64_t chunks = groups * ((rows * nb + 31) / 32);
+  int64_t blocks = static_cast<int64_t>(num_sms()) * 2;
+  const int64_t need = (chunks + 8 * kU - 1) / (8 * kU);
+  if (blocks > need) blocks = need;
+  const int64_t min_blocks = (groups + 255) / 256;  // g_out is written by thread t < groups
+  if (blocks < min_blocks) blocks = min_blocks;
+  if (blocks < 1) blocks = 1;
+  if (a32)
+    quantize_group_blocks_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        x, groups, rows, nb, magic, g_in, amax, codes, sf, g_out);
+  else
+    quantize_group_blocks_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        x, groups, rows, nb, magic, g_in, amax, codes, sf, g_out);
 }
 
 }  // namespace minite
@@ -209,7 +294,7 @@ extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows
   if (orientation != MINITE_ALONG_COLS && orientation != MINITE_ALONG_ROWS)
     return MINITE_ERR_INVALID_ARG;
   if (groups <= 0 || rows <= 0 || cols <= 0) return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(x, 16) || !aligned(codes, 4) || !aligned(sf, 4)) return MINITE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(sf, 4)) return MINITE_ERR_INVALID_ARG;
   const bool per_group = scale_mode == MINITE_SCALE_PER_GROUP;
   if (gscale_in && !per_group) return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -219,6 +304,7 @@ extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows
   if (orientation == MINITE_ALONG_ROWS && !per_group) return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (orientation == MINITE_ALONG_COLS && cols > 4096) return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (groups * rows * cols >= (int64_t(1) << 40)) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (per_group && rows * (cols / 16) >= (int64_t(1) << 32)) return MINITE_ERR_UNSUPPORTED_SHAPE;
 
   uint32_t* amax = nullptr;
   if (per_group && !gscale_in) {
@@ -237,17 +323,19 @@ extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows
   }
 
   if (orientation == MINITE_ALONG_COLS) {
-    const int nch = static_cast<int>((cols + 255) / 256);
     const int c = static_cast<int>(cols);
-    const int pg = per_group ? 1 : 0;
-    switch (nch) {
+    const bool a32 = aligned(x, 32);
+    if (per_group) {
+      launch_group_blocks(xb, groups, rows, c, a32, gscale_in, amax, codes, sf, gscale_out, s);
+    } else {
+      switch ((cols / 16 + 31) / 32) {
 #define MINITE_CASE(N) \
-  case N: launch_rows<N>(xb, groups, rows, c, pg, gscale_in, amax, codes, sf, gscale_out, s); break;
-      MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
-      MINITE_CASE(7) MINITE_CASE(8) MINITE_CASE(9) MINITE_CASE(10) MINITE_CASE(11)
-      MINITE_CASE(12) MINITE_CASE(13) MINITE_CASE(14) MINITE_CASE(15) MINITE_CASE(16)
+  case N: launch_token_rows<N>(xb, groups, rows, c, a32, codes, sf, gscale_out, s); break;
+        MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5)
+        MINITE_CASE(6) MINITE_CASE(7) MINITE_CASE(8)
 #undef MINITE_CASE
-      default: return MINITE_ERR_UNSUPPORTED_SHAPE;
+        default: return MINITE_ERR_UNSUPPORTED_SHAPE;
+      }
     }
   } else {
     dim3 grid(static_cast<unsigned>((rows + kTR - 1) / kTR),

@@ -24,19 +24,71 @@ __device__ bool offsets_consistent(const int32_t* s_off, const int32_t* s_sfoff,
   return !__syncthreads_or(bad);
 }
 
+// silu(g) = g / (1 + exp_spec(-g)), every step an IEEE float operation.
+__device__ __forceinline__ float silu_spec(float g) {
+  return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));
+}
+
+// The gates are BF16, so silu takes at most 2^16 distinct inputs: each CTA
+// tabulates silu_spec in shared memory for |g| in [2^-24, 2^8) (32 binades,
+// both signs, 32 KB) and evaluates the formula only for gates outside it.
+// Entry index: (sign << 12) | (|g| bits - bits of 2^-24).
+constexpr uint32_t kLutLo = (127u - 24u) << 7;  // BF16 bits of 2^-24
+constexpr uint32_t kLutSpan = 32u << 7;          // 4096 magnitudes per sign
+constexpr int kLutEntries = 2 * static_cast<int>(kLutSpan);
+
+__device__ void build_silu_lut(float* lut) {
+  for (int i = threadIdx.x; i < kLutEntries; i += blockDim.x) {
+    const uint32_t bits = (static_cast<uint32_t>(i >> 12) << 15) | (kLutLo + (i & 4095));
+    lut[i] = silu_spec(__uint_as_float(bits << 16));
+  }
+}
+
+// h = (silu(g) * u) * w for the 16 gates and ups of one block.
+__device__ __forceinline__ void swiglu_block(const float* lut, const uint32_t (&wg)[8],
+                                             const uint32_t (&wu)[8], float w, float (&h)[16]) {
+  uint32_t miss = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t bits = (i & 1) ? (wg[i >> 1] >> 16) : (wg[i >> 1] & 0xFFFFu);
+    const uint32_t off = (bits & 0x7FFFu) - kLutLo;
+    miss |= static_cast<uint32_t>(off >= kLutSpan) << i;
+    h[i] = lut[(off & (kLutSpan - 1)) | ((bits >> 3) & kLutSpan)];
+  }
+  if (miss) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (miss & (1u << i)) {
+        const uint32_t bits = (i & 1) ? (wg[i >> 1] >> 16) : (wg[i >> 1] & 0xFFFFu);
+        h[i] = silu_spec(__uint_as_float(bits << 16));
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    mul_f32x2(h[2 * i], h[2 * i + 1], bf16lo(wu[i]), bf16hi(wu[i]));
+    mul_f32x2(h[2 * i], h[2 * i + 1], w, w);
+  }
+}
+
+// One CTA per SM, one warp per permuted row, lane l owning blocks 32j + l of
+// the row's intermediate (its gates at [0, I), its ups at [I, 2I)).
+constexpr int kSwigluThreads = 512;
 template <int NCH>
-__global__ void __launch_bounds__(256) swiglu_quant_kernel(
+__global__ void __launch_bounds__(kSwigluThreads, 1) swiglu_quant_kernel(
     const uint16_t* __restrict__ gu, const float* __restrict__ perm_w, int64_t M, int I, int E,
     const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ sf_row_offsets,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
     int32_t* status) {
-  extern __shared__ int32_t sm[];
-  int32_t* s_off = sm;
-  int32_t* s_sfoff = sm + (E + 1);
+  extern __shared__ float smf[];
+  float* lut = smf;
+  int32_t* s_off = reinterpret_cast<int32_t*>(smf + kLutEntries);
+  int32_t* s_sfoff = s_off + (E + 1);
   for (int i = threadIdx.x; i <= E; i += blockDim.x) {
     s_off[i] = expert_offsets[i];
     s_sfoff[i] = sf_row_offsets[i];
   }
+  build_silu_lut(lut);
   __syncthreads();
   if (!offsets_consistent(s_off, s_sfoff, E, M)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MINITE_ERR_INVALID_ARG);
@@ -46,9 +98,23 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int kc = ((I / 16) + 3) & ~3;
+  const int nb = I / 16;
+  const int kc = (nb + 3) & ~3;
   const int64_t used = s_off[E];
   for (int64_t m = warp; m < used; m += nwarps) {
+    const uint16_t* gr = gu + m * (2 * static_cast<int64_t>(I));
+    uint32_t wg[NCH][8], wu[NCH][8];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = 32 * j + lane;
+      if (c < nb) {
+        ld_bf16x16(gr + 16 * c, wg[j]);
+        ld_bf16x16(gr + I + 16 * c, wu[j]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wg[j][i] = wu[j][i] = 0u;
+      }
+    }
     // expert of row m: the last e with s_off[e] <= m
     int lo = 0, hi = E;
     while (hi - lo > 1) {
@@ -56,37 +122,34 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
       if (s_off[mid] <= m) lo = mid; else hi = mid;
     }
     const int e = lo;
-    const uint16_t* gr = gu + m * (2 * static_cast<int64_t>(I));
     const float w = perm_w ? perm_w[m] : 1.0f;
-    float h[NCH][8];
-    float am = 0.0f;
+    float h[NCH][16], am[NCH];
+    float rm = 0.0f;
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      const int e0 = 256 * j + 8 * lane;
-      if (e0 < I) {
-        const uint4 ug = __ldcs(reinterpret_cast<const uint4*>(gr + e0));
-        const uint4 uu = __ldcs(reinterpret_cast<const uint4*>(gr + I + e0));
-        float gv[8], uv[8];
-        unpack_bf16x8(ug, gv);
-        unpack_bf16x8(uu, uv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float silu = __fdiv_rn(gv[i], __fadd_rn(1.0f, exp_spec(-gv[i])));
-          float v = __fmul_rn(silu, uv[i]);
-          if (perm_w) v = __fmul_rn(v, w);
-          h[j][i] = v;
-        }
+      if (32 * j + lane < nb) {
+        swiglu_block(lut, wg[j], wu[j], w, h[j]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h[j][i] = 0.0f;
+        for (int i = 0; i < 16; ++i) h[j][i] = 0.0f;
       }
-      am = fmaxf(am, amax8(h[j]));
+      am[j] = amax_f32x16(h[j]);
+      rm = fmaxf(rm, am[j]);
     }
-    const float g = global_scale(warp_max(am));
-    RowQuant<NCH> q;
-    quantize_row_warp<NCH>(h, I, g, q);
+    const float g = global_scale(warp_max(rm));
+    const float tk = enc_table_entry(g);
+    QBlock qb[NCH];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      if (32 * j < nb) {  // warp-uniform
+        qb[j] = quant_block(h[j], am[j], g, tk, 32 * j + lane < nb);
+      } else {
+        qb[j].codes = make_uint2(0u, 0u);
+        qb[j].sf = 0u;
+      }
+    }
     const int64_t r = static_cast<int64_t>(s_sfoff[e]) + (m - s_off[e]);
-    store_row_warp<NCH>(q, I, codes + m * (I / 2), sf, r, kc);
+    store_row_blocks<NCH>(qb, nb, codes + m * (I / 2), sf, r, kc);
     if (lane == 0) row_g[m] = g;
   }
 
@@ -170,24 +233,26 @@ extern "C" int minite_swiglu_weighted_quant(const void* gate_up, const float* pe
   if (M < 1 || I < 64 || I % 64 != 0 || I > 2048 || E < 1 || E > 1024)
     return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (M >= (int64_t(1) << 31)) return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(gate_up, 16) || !aligned(codes, 16) || !aligned(sf, 16))
+  if (!aligned(gate_up, 32) || !aligned(codes, 16) || !aligned(sf, 16))
     return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int64_t blocks = (M + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  int64_t blocks = (M + kSwigluThreads / 32 - 1) / (kSwigluThreads / 32);
+  const int64_t cap = static_cast<int64_t>(num_sms());
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  const size_t smem = 2 * (E + 1) * sizeof(int32_t);
+  const size_t smem = kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
   const uint16_t* g = static_cast<const uint16_t*>(gate_up);
   const int i = static_cast<int>(I);
-  switch ((I + 255) / 256) {
+  switch ((I / 16 + 31) / 32) {
 #define MINITE_CASE(N)                                                                         \
   case N:                                                                                      \
-    swiglu_quant_kernel<N><<<static_cast<unsigned>(blocks), 256, smem, s>>>(                   \
+    if (cudaFuncSetAttribute(swiglu_quant_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             static_cast<int>(smem)) != cudaSuccess)                           \
+      return MINITE_ERR_CUDA;                                                                  \
+    swiglu_quant_kernel<N><<<static_cast<unsigned>(blocks), kSwigluThreads, smem, s>>>(        \
         g, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes, sf, row_g, status);         \
     break;
-    MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
-    MINITE_CASE(7) MINITE_CASE(8)
+    MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4)
 #undef MINITE_CASE
     default: return MINITE_ERR_UNSUPPORTED_SHAPE;
   }

@@ -410,6 +410,12 @@ def test_swiglu_weighted_quant_bit_exact(counts, I):
     Mt = Mu + 7
     gu = O.f32_to_bf16((rng.standard_normal((Mt, 2 * I)) * 3).astype(np.float32))
     gu[0, :I] = O.f32_to_bf16(np.linspace(-120, 120, I).astype(np.float32))  # clamp region
+    # gates on both sides of every tabulation edge: zeros, subnormals, |g| near
+    # 2^-24 and 2^8, large magnitudes
+    special = np.array([0.0, -0.0, 1e-40, -1e-40, 2.0 ** -25, -(2.0 ** -24), 2.0 ** -24,
+                        -(2.0 ** -25), 255.0, -255.0, 256.0, -256.0, 300.0, -300.0, 3e4, -3e4],
+                       dtype=np.float32)
+    gu[1 % Mt, :I] = O.f32_to_bf16(np.resize(special, I))
     pw = rng.random(Mt).astype(np.float32)
     for weights in (pw, None):
         ref = O.swiglu_weighted_quant(gu, weights, off, sfo)
