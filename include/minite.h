@@ -286,7 +286,10 @@ int minite_test_div6_exhaustive(unsigned long long* mismatches, minite_stream_t 
 
 /*
  * Test hook for failure detection: sets the time budget of every bounded
- * pipeline wait in the GEMM (nanoseconds; 0 restores the default of 2 s).
+ * pipeline wait (the GEMM and the streaming kernels that stage rows through
+ * shared memory with asynchronous copies; nanoseconds; 0 restores the
+ * default of 2 s). A wait that runs out sets status bit 1<<MINITE_ERR_TIMEOUT
+ * and the kernel returns after its in-flight copies have landed.
  * Process-wide; takes effect at the next launch.
  */
 void minite_set_wait_budget_ns(uint64_t ns);

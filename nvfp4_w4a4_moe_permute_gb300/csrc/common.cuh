@@ -82,12 +82,15 @@ __device__ __forceinline__ float enc_table_entry(float g) {
 // One 16-element block: scale code from its amax and the row's global scale,
 // and the factor that maps elements onto the E2M1 grid (0 when sf == 0).
 // s = (amax_b / 6) * g; sf = E4M3(s); enc = min(g / sf, FLT_MAX).
-// Warp-collective (one shuffle): every lane of the warp must call it.
+// Warp-collective (one shuffle): every lane of the warp must call it. `tk` is
+// the caller's table entry enc_table_entry(g); the table of this lane's row
+// sits in lanes tbase .. tbase + 7.
 struct BlockScale {
   uint32_t sf;
   float enc;
 };
-__device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float tk) {
+__device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float tk,
+                                                  int tbase = 0) {
   BlockScale r;
   const float s = __fmul_rn(div6_rn(amax_b), g);
   r.sf = cvt_e4m3(s);
@@ -102,7 +105,7 @@ __device__ __forceinline__ BlockScale block_scale(float amax_b, float g, float t
     idx = (m << (3 - j)) & 7u;
     k = 9 - j;
   }
-  const float t = __shfl_sync(0xffffffffu, tk, static_cast<int>(idx));
+  const float t = __shfl_sync(0xffffffffu, tk, tbase + static_cast<int>(idx));
   float enc = __fmul_rn(t, __uint_as_float(static_cast<uint32_t>(127 + k) << 23));
   if (enc < 2.3509887016445750e-38f) enc = __fdiv_rn(g, e4m3_value(r.sf));  // below 2^-125
   r.enc = r.sf ? fminf(enc, kFltMax) : 0.0f;
@@ -224,6 +227,13 @@ __device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// min(|a|, |b|) per BF16 half, sign = sign(a) xor sign(b).
+__device__ __forceinline__ uint32_t min_abs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // max |x| over 16 BF16 values (exact: the result is one of the inputs).
 __device__ __forceinline__ float amax_bf16x16(const uint32_t (&w)[8]) {
   const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(w[0], w[1]),
@@ -309,8 +319,8 @@ struct QBlock {
   uint32_t sf;
 };
 __device__ __forceinline__ QBlock quant_block(const float (&v)[16], float am, float g, float tk,
-                                              bool valid) {
-  const BlockScale bs = block_scale(am, g, tk);
+                                              bool valid, int tbase = 0) {
+  const BlockScale bs = block_scale(am, g, tk, tbase);
   QBlock r;
   r.sf = valid ? bs.sf : 0u;
   r.codes = encode16(v, bs.enc, r.sf == 0);

@@ -37,31 +37,43 @@ constexpr uint32_t kLutLo = (127u - 24u) << 7;  // BF16 bits of 2^-24
 constexpr uint32_t kLutSpan = 32u << 7;          // 4096 magnitudes per sign
 constexpr int kLutEntries = 2 * static_cast<int>(kLutSpan);
 
-__device__ void build_silu_lut(float* lut) {
-  for (int i = threadIdx.x; i < kLutEntries; i += blockDim.x) {
+__device__ void build_silu_lut_part(float* lut, int t, int nthreads) {
+  for (int i = t; i < kLutEntries; i += nthreads) {
     const uint32_t bits = (static_cast<uint32_t>(i >> 12) << 15) | (kLutLo + (i & 4095));
     lut[i] = silu_spec(__uint_as_float(bits << 16));
   }
 }
 
-// h = (silu(g) * u) * w for the 16 gates and ups of one block.
+// h = (silu(g) * u) * w for the 16 gates and ups of one block. Blocks whose
+// gates all lie inside the table take one lookup per gate; any other block
+// evaluates the formula for the gates outside it.
 __device__ __forceinline__ void swiglu_block(const float* lut, const uint32_t (&wg)[8],
                                              const uint32_t (&wu)[8], float w, float (&h)[16]) {
-  uint32_t miss = 0;
+  const uint32_t mx = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(wg[0], wg[1]),
+                                                    max_abs_bf16x2(wg[2], wg[3])),
+                                     max_abs_bf16x2(max_abs_bf16x2(wg[4], wg[5]),
+                                                    max_abs_bf16x2(wg[6], wg[7])));
+  const uint32_t mn = min_abs_bf16x2(min_abs_bf16x2(min_abs_bf16x2(wg[0], wg[1]),
+                                                    min_abs_bf16x2(wg[2], wg[3])),
+                                     min_abs_bf16x2(min_abs_bf16x2(wg[4], wg[5]),
+                                                    min_abs_bf16x2(wg[6], wg[7])));
+  // magnitudes as BF16 bit patterns compare like unsigned integers
+  const uint32_t hi_mag = max(mx & 0x7FFFu, (mx >> 16) & 0x7FFFu);
+  const uint32_t lo_mag = min(mn & 0x7FFFu, (mn >> 16) & 0x7FFFu);
+  if (lo_mag >= kLutLo && hi_mag < kLutLo + kLutSpan) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t bits = (i & 1) ? (wg[i >> 1] >> 16) : (wg[i >> 1] & 0xFFFFu);
-    const uint32_t off = (bits & 0x7FFFu) - kLutLo;
-    miss |= static_cast<uint32_t>(off >= kLutSpan) << i;
-    h[i] = lut[(off & (kLutSpan - 1)) | ((bits >> 3) & kLutSpan)];
-  }
-  if (miss) {
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t a = wg[i], b = wg[i] >> 16;
+      h[2 * i] = lut[((a - kLutLo) & (kLutSpan - 1)) | ((a >> 3) & kLutSpan)];
+      h[2 * i + 1] = lut[((b - kLutLo) & (kLutSpan - 1)) | ((b >> 3) & kLutSpan)];
+    }
+  } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      if (miss & (1u << i)) {
-        const uint32_t bits = (i & 1) ? (wg[i >> 1] >> 16) : (wg[i >> 1] & 0xFFFFu);
-        h[i] = silu_spec(__uint_as_float(bits << 16));
-      }
+      const uint32_t bits = (i & 1) ? (wg[i >> 1] >> 16) : (wg[i >> 1] & 0xFFFFu);
+      const uint32_t off = (bits & 0x7FFFu) - kLutLo;
+      h[i] = off < kLutSpan ? lut[off | ((bits >> 3) & kLutSpan)]
+                            : silu_spec(__uint_as_float(bits << 16));
     }
   }
 #pragma unroll
@@ -71,16 +83,26 @@ __device__ __forceinline__ void swiglu_block(const float* lut, const uint32_t (&
   }
 }
 
-// One CTA per SM, one warp per permuted row, lane l owning blocks 32j + l of
-// the row's intermediate (its gates at [0, I), its ups at [I, 2I)).
-constexpr int kSwigluThreads = 512;
-template <int NCH>
-__global__ void __launch_bounds__(kSwigluThreads, 1) swiglu_quant_kernel(
+// Max over the LPR lanes of one row group (LPR = 32 or 16).
+template <int LPR>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// One warp holds 32 / LPR permuted rows at a time, LPR lanes per row; lane l
+// of a row owns blocks l + LPR*j (j < NCH) of the row's intermediate, with
+// the gates at [0, I) and the ups at [I, 2I) of the gate_up row. Every row's
+// 4I input bytes are requested before any of them is used.
+constexpr int kSwThreads = 512;
+template <int LPR, int NCH>
+__global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
     const uint16_t* __restrict__ gu, const float* __restrict__ perm_w, int64_t M, int I, int E,
     const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ sf_row_offsets,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
     int32_t* status) {
-  extern __shared__ float smf[];
+  extern __shared__ __align__(16) float smf[];
   float* lut = smf;
   int32_t* s_off = reinterpret_cast<int32_t*>(smf + kLutEntries);
   int32_t* s_sfoff = s_off + (E + 1);
@@ -88,69 +110,78 @@ __global__ void __launch_bounds__(kSwigluThreads, 1) swiglu_quant_kernel(
     s_off[i] = expert_offsets[i];
     s_sfoff[i] = sf_row_offsets[i];
   }
-  build_silu_lut(lut);
+  build_silu_lut_part(lut, threadIdx.x, blockDim.x);
   __syncthreads();
   if (!offsets_consistent(s_off, s_sfoff, E, M)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MINITE_ERR_INVALID_ARG);
     return;
   }
 
+  constexpr int RPW = 32 / LPR;  // rows per warp
   const int lane = threadIdx.x & 31;
+  const int l = lane % LPR;
+  const int tbase = lane - l;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int nb = I / 16;
   const int kc = (nb + 3) & ~3;
   const int64_t used = s_off[E];
-  for (int64_t m = warp; m < used; m += nwarps) {
+  for (int64_t base = warp * RPW; base < used; base += nwarps * RPW) {
+    const int64_t m = base + lane / LPR;
+    const bool live = m < used;
     const uint16_t* gr = gu + m * (2 * static_cast<int64_t>(I));
     uint32_t wg[NCH][8], wu[NCH][8];
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      const int c = 32 * j + lane;
-      if (c < nb) {
+      const int c = l + LPR * j;
+      if (live && c < nb) {
         ld_bf16x16(gr + 16 * c, wg[j]);
         ld_bf16x16(gr + I + 16 * c, wu[j]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) wg[j][i] = wu[j][i] = 0u;
       }
     }
-    // expert of row m: the last e with s_off[e] <= m
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_off[mid] <= m) lo = mid; else hi = mid;
-    }
-    const int e = lo;
-    const float w = perm_w ? perm_w[m] : 1.0f;
+    const float w = live && perm_w ? perm_w[m] : 1.0f;
     float h[NCH][16], am[NCH];
     float rm = 0.0f;
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      if (32 * j + lane < nb) {
+      if (live && l + LPR * j < nb) {
         swiglu_block(lut, wg[j], wu[j], w, h[j]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) h[j][i] = 0.0f;
+        for (int t = 0; t < 16; ++t) h[j][t] = 0.0f;
       }
       am[j] = amax_f32x16(h[j]);
       rm = fmaxf(rm, am[j]);
     }
-    const float g = global_scale(warp_max(rm));
+    const float g = global_scale(group_max<LPR>(rm));
     const float tk = enc_table_entry(g);
     QBlock qb[NCH];
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      if (32 * j < nb) {  // warp-uniform
-        qb[j] = quant_block(h[j], am[j], g, tk, 32 * j + lane < nb);
+      if (LPR * j < nb) {  // warp-uniform
+        qb[j] = quant_block(h[j], am[j], g, tk, live && l + LPR * j < nb, tbase);
       } else {
         qb[j].codes = make_uint2(0u, 0u);
         qb[j].sf = 0u;
       }
     }
-    const int64_t r = static_cast<int64_t>(s_sfoff[e]) + (m - s_off[e]);
-    store_row_blocks<NCH>(qb, nb, codes + m * (I / 2), sf, r, kc);
-    if (lane == 0) row_g[m] = g;
+    if (live) {
+      // expert of row m: the last e with s_off[e] <= m
+      int lo = 0, hi = E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= m) lo = mid; else hi = mid;
+      }
+      const int64_t r = static_cast<int64_t>(s_sfoff[lo]) + (m - s_off[lo]);
+      uint8_t* crow = codes + m * (I / 2);
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int c = l + LPR * j;
+        if (c < nb) st_u64(crow + 8 * c, qb[j].codes);
+        if (c < kc) sf[sf_offset(r, c, kc)] = static_cast<uint8_t>(qb[j].sf);
+      }
+      if (l == 0) row_g[m] = g;
+    }
   }
 
   // zero the scale bytes of each expert's padding rows
@@ -163,6 +194,25 @@ __global__ void __launch_bounds__(kSwigluThreads, 1) swiglu_quant_kernel(
       *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * (i % words), kc)) = 0u;
     }
   }
+}
+
+template <int LPR, int NCH>
+static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int I, int E,
+                         const int32_t* off, const int32_t* sfoff, uint8_t* codes, uint8_t* sf,
+                         float* row_g, int32_t* status, cudaStream_t s) {
+  const size_t smem = kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
+  if (cudaFuncSetAttribute(swiglu_quant_kernel<LPR, NCH>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MINITE_ERR_CUDA;
+  constexpr int rows_per_cta = kSwThreads / 32 * (32 / LPR);
+  int64_t blocks = (M + rows_per_cta - 1) / rows_per_cta;
+  const int64_t cap = static_cast<int64_t>(num_sms());
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  swiglu_quant_kernel<LPR, NCH><<<static_cast<unsigned>(blocks), kSwThreads, smem, s>>>(
+      g, perm_w, M, I, E, off, sfoff, codes, sf, row_g, status);
+  return MINITE_OK;
 }
 
 // One warp per token; lane l owns columns [256c + 8l, 256c + 8l + 8) of chunk c.
@@ -236,26 +286,24 @@ extern "C" int minite_swiglu_weighted_quant(const void* gate_up, const float* pe
   if (!aligned(gate_up, 32) || !aligned(codes, 16) || !aligned(sf, 16))
     return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int64_t blocks = (M + kSwigluThreads / 32 - 1) / (kSwigluThreads / 32);
-  const int64_t cap = static_cast<int64_t>(num_sms());
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  const size_t smem = kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
   const uint16_t* g = static_cast<const uint16_t*>(gate_up);
   const int i = static_cast<int>(I);
-  switch ((I / 16 + 31) / 32) {
-#define MINITE_CASE(N)                                                                         \
-  case N:                                                                                      \
-    if (cudaFuncSetAttribute(swiglu_quant_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             static_cast<int>(smem)) != cudaSuccess)                           \
-      return MINITE_ERR_CUDA;                                                                  \
-    swiglu_quant_kernel<N><<<static_cast<unsigned>(blocks), kSwigluThreads, smem, s>>>(        \
-        g, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes, sf, row_g, status);         \
-    break;
-    MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4)
-#undef MINITE_CASE
-    default: return MINITE_ERR_UNSUPPORTED_SHAPE;
-  }
+  const int nb = i / 16;
+  int rc;
+  // 16 lanes per row when that leaves no lane idle or the row is short
+  if (nb <= 16) rc = launch_swiglu<16, 1>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets,
+                                           codes, sf, row_g, status, s);
+  else if (nb <= 32) rc = launch_swiglu<16, 2>(g, perm_w, M, i, E, expert_offsets,
+                                                sf_row_offsets, codes, sf, row_g, status, s);
+  else if (nb <= 48) rc = launch_swiglu<16, 3>(g, perm_w, M, i, E, expert_offsets,
+                                                sf_row_offsets, codes, sf, row_g, status, s);
+  else if (nb <= 64) rc = launch_swiglu<32, 2>(g, perm_w, M, i, E, expert_offsets,
+                                                sf_row_offsets, codes, sf, row_g, status, s);
+  else if (nb <= 96) rc = launch_swiglu<32, 3>(g, perm_w, M, i, E, expert_offsets,
+                                                sf_row_offsets, codes, sf, row_g, status, s);
+  else rc = launch_swiglu<32, 4>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes, sf,
+                                 row_g, status, s);
+  if (rc != MINITE_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
 

@@ -400,7 +400,8 @@ def test_grouped_gemm_inconsistent_offsets_are_reported_not_executed(variant):
 # --------------------------------------------------------------------- SwiGLU, combine
 
 @pytest.mark.parametrize("counts,I", [([3, 0, 130, 1], 64), ([256, 17], 768), ([1], 128),
-                                      ([100] * 5, 1536)])
+                                      ([100] * 5, 1536), ([5, 130], 512), ([33], 1024),
+                                      ([40, 0, 7], 2048)])
 def test_swiglu_weighted_quant_bit_exact(counts, I):
     rng = np.random.default_rng(len(counts) * 31 + I)
     E = len(counts)
