@@ -158,7 +158,7 @@ int minite_moe_permute_quant(const void* x, const int32_t* topk_ids, const float
  * plugin that only receives its inputs and outputs, a loop that must not
  * enter the allocator. It allocates nothing and calls no allocating routine.
  *  - Limit: minite_workspace_bytes(MINITE_OP_PERMUTE_QUANT, T, H, E, k) must
- *    not exceed 2 MiB (about T*E <= 8M at k = 8); larger problems return
+ *    not exceed 2 MiB (about T*E <= 32M at k = 8); larger problems return
  *    MINITE_ERR_SCRATCH_LIMIT before anything is enqueued.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.

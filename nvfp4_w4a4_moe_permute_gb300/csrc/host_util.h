@@ -17,9 +17,9 @@ int num_sms();
 // Budget of the GEMM's bounded pipeline waits, in nanoseconds.
 uint64_t wait_budget_ns();
 
-// Token-chunk size of the permutation for top-k = k (pairs per chunk <= 128).
+// Token-chunk size of the permutation for top-k = k (pairs per chunk <= 512).
 inline int permute_chunk_tokens(int k) {
-  int ct = 128 / (k > 0 ? k : 1);
+  int ct = 512 / (k > 0 ? k : 1);
   return ct < 1 ? 1 : ct;
 }
 

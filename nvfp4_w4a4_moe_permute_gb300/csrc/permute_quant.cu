@@ -9,15 +9,17 @@
 // execution path".
 //
 // Three launches, no host synchronization:
-//   permute_hist_kernel   per token-chunk expert histogram -> table[e][chunk]
-//                         (also resets the scan's completion counter).
+//   permute_rank_kernel   one warp per token chunk: stable in-chunk rank of
+//                         every (token, slot) pair (kept in dest_row) and the
+//                         chunk's expert histogram -> table[e][chunk]; also
+//                         resets the scan's completion counter.
 //   permute_scan_kernel   one block per expert: exclusive prefix of its
 //                         chunk counts; the last block to finish turns the
 //                         expert totals into expert_offsets / sf_row_offsets.
-//   permute_quant_kernel  one block per chunk: stable rank of every
-//                         (token, slot) pair inside the chunk, then each token
-//                         is read once, quantized once in registers and its
-//                         codes / scales written to its k destination rows.
+//   permute_quant_kernel  one warp per token: completes the token's k
+//                         permuted rows, reads the token once, quantizes it
+//                         once in registers and writes its codes / scales to
+//                         its k destination rows.
 #include <mutex>
 
 #include "common.cuh"
@@ -48,26 +50,44 @@ static PermWs perm_ws(void* ws, int E) {
   return w;
 }
 
-__global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(
+// One warp per chunk of ct tokens (ct * k <= 512 pairs): the stable rank of
+// every pair among the chunk's pairs with the same expert, in pair order, 32
+// pairs at a time. Lanes carrying the same expert find each other with a
+// match, take their order among themselves from the match mask and continue
+// a per-expert running count kept in shared memory; the final counts are the
+// chunk's histogram. The local rank goes to dest_row (completed later).
+constexpr int kRankWarps = 4;  // chunks per block
+__global__ void __launch_bounds__(32 * kRankWarps) permute_rank_kernel(
     const int32_t* __restrict__ ids, int64_t T, int k, int E, int ct, int nchunks,
-    int32_t* __restrict__ table, uint32_t* __restrict__ counter, int32_t* status) {
-  extern __shared__ int32_t hist[];
-  const int c = blockIdx.x;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  if (c == 0 && threadIdx.x == 0) *counter = 0u;
-  __syncthreads();
+    int32_t* __restrict__ table, int32_t* __restrict__ dest_row, uint32_t* __restrict__ counter,
+    int32_t* status) {
+  extern __shared__ int32_t cnt_all[];  // [kRankWarps][E]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int c = blockIdx.x * kRankWarps + wid;
+  int32_t* cnt = cnt_all + wid * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
+  __syncwarp();
+  if (c >= nchunks) return;
   const int64_t p0 = static_cast<int64_t>(c) * ct * k;
-  const int64_t p1 = min(static_cast<int64_t>(c + 1) * ct, T) * k;
+  const int npairs = static_cast<int>(min(static_cast<int64_t>(c + 1) * ct, T) * k - p0);
   bool bad = false;
-  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-    const int e = ids[p];
-    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
-    else bad = true;
+  for (int b = 0; b < npairs; b += 32) {
+    const int p = b + lane;
+    const int e = p < npairs ? ids[p0 + p] : -1;
+    const bool valid = e >= 0 && e < E;
+    if (p < npairs && !valid) bad = true;
+    const uint32_t mask = __match_any_sync(0xffffffffu, valid ? e : E + lane);
+    const int before = __popc(mask & ((1u << lane) - 1u));
+    const int run = valid ? cnt[e] : 0;
+    __syncwarp();
+    if (valid && before == 0) cnt[e] = run + __popc(mask);
+    __syncwarp();
+    if (p < npairs) dest_row[p0 + p] = valid ? run + before : -1;
   }
   if (bad) set_status(status, MINITE_ERR_BAD_ROUTING);
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    table[static_cast<int64_t>(e) * nchunks + c] = hist[e];
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) table[static_cast<int64_t>(e) * nchunks + c] = cnt[e];
 }
 
 // Exclusive scan of one value per thread over a 256-thread block; returns the
@@ -145,8 +165,13 @@ __global__ void __launch_bounds__(kPermThreads) permute_scan_kernel(
   }
 }
 
+// Quantize and scatter, one warp per token over a grid of resident blocks:
+// lane j < k completes pair j's permuted row (expert offset + the chunk's
+// base for the expert + the local rank) and writes the routing outputs; the
+// warp reads the token once (lane l owns blocks 32i + l), quantizes it once
+// in registers and writes its codes, scales and g to each destination row.
 template <int NCH>
-__global__ void __launch_bounds__(kPermThreads) permute_quant_kernel(
+__global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
     const float* __restrict__ topk_w, int64_t T, int H, int E, int k, int ct, int nchunks,
     const int32_t* __restrict__ table, const int32_t* __restrict__ expert_offsets,
@@ -154,78 +179,71 @@ __global__ void __launch_bounds__(kPermThreads) permute_quant_kernel(
     uint8_t* __restrict__ sf, float* __restrict__ row_g, int32_t* __restrict__ perm_src,
     int32_t* __restrict__ dest_row, float* __restrict__ perm_w) {
   extern __shared__ int32_t sm[];
-  int32_t* s_off = sm;                // [E+1]
-  int32_t* s_sfoff = sm + (E + 1);    // [E+1]
-  int32_t* s_id = sm + 2 * (E + 1);   // [ct*k]
-  int32_t* s_dest = s_id + ct * k;    // [ct*k]
-  const int c = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, wid = tid >> 5;
-  const int kc = ((H / 16) + 3) & ~3;
-  for (int i = tid; i <= E; i += blockDim.x) {
+  int32_t* s_off = sm;                 // [E+1]
+  int32_t* s_sfoff = s_off + (E + 1);  // [E+1]
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
     s_off[i] = expert_offsets[i];
     s_sfoff[i] = sf_row_offsets[i];
   }
-  const int64_t t0 = static_cast<int64_t>(c) * ct;
-  const int ntok = static_cast<int>(min(static_cast<int64_t>(ct), T - t0));
-  const int npairs = ntok * k;
-  for (int p = tid; p < npairs; p += blockDim.x) s_id[p] = ids[t0 * k + p];
   __syncthreads();
-
-  // stable rank of each pair among the chunk's pairs with the same expert
-  for (int p = tid; p < npairs; p += blockDim.x) {
-    const int e = s_id[p];
-    int dest = -1;
-    if (e >= 0 && e < E) {
-      int rank = 0;
-      for (int q = 0; q < p; ++q) rank += (s_id[q] == e);
-      dest = s_off[e] + table[static_cast<int64_t>(e) * nchunks + c] + rank;
-      const int64_t t = t0 + p / k;
-      perm_src[dest] = static_cast<int32_t>(t);
-      if (perm_w) perm_w[dest] = topk_w[t0 * k + p];
-    }
-    s_dest[p] = dest;
-    dest_row[t0 * k + p] = dest;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nb = H / 16;
+  const int kc = (nb + 3) & ~3;
+  int cpart[NCH];  // the column part of each owned block's scale offset
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int cc = 32 * j + lane;
+    cpart[j] = (cc >> 2) * 512 + (cc & 3);
   }
-  __syncthreads();
-
-  // each token: one read, one quantization, k scattered writes
-  const int nwarps = blockDim.x >> 5;
-  for (int tl = wid; tl < ntok; tl += nwarps) {
-    const uint16_t* xr = x + (t0 + tl) * H;
-    float v[NCH][8];
-    float am = 0.0f;
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int e0 = 256 * j + 8 * lane;
-      if (e0 < H) {
-        uint4 u = __ldcs(reinterpret_cast<const uint4*>(xr + e0));
-        unpack_bf16x8(u, v[j]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[j][i] = 0.0f;
+  const bool a32 = (reinterpret_cast<uintptr_t>(x) & 31) == 0;
+  for (int64_t t = warp; t < T; t += nwarps) {
+    // routing of pair (t, lane)
+    int dest = -1;
+    int64_t sfrow = 0;
+    if (lane < k) {
+      const int64_t p = t * k + lane;
+      const int e = ids[p];
+      if (e >= 0 && e < E) {
+        const int local = table[static_cast<int64_t>(e) * nchunks + t / ct] + dest_row[p];
+        dest = s_off[e] + local;
+        sfrow = static_cast<int64_t>(s_sfoff[e]) + local;
+        perm_src[dest] = static_cast<int32_t>(t);
+        if (perm_w) perm_w[dest] = topk_w[p];
       }
-      am = fmaxf(am, amax8(v[j]));
+      dest_row[p] = dest;
     }
-    const float g = global_scale(warp_max(am));
-    RowQuant<NCH> q;
-    quantize_row_warp<NCH>(v, H, g, q);
+    uint32_t w[NCH][8];
+    float am[NCH];
+    const uint16_t* xr = x + t * H;
+    const float m = a32 ? load_row_blocks<NCH, true>(xr, nb, w, am)
+                        : load_row_blocks<NCH, false>(xr, nb, w, am);
+    const float g = global_scale(warp_max(m));
+    QBlock qb[NCH];
+    quant_row_blocks<NCH>(w, am, nb, g, qb);
     for (int j = 0; j < k; ++j) {
-      const int d = s_dest[tl * k + j];
-      if (d < 0) continue;
-      const int e = s_id[tl * k + j];
-      const int64_t r = static_cast<int64_t>(s_sfoff[e]) + (d - s_off[e]);
-      store_row_warp<NCH>(q, H, codes + static_cast<int64_t>(d) * (H / 2), sf, r, kc);
+      const int d = __shfl_sync(0xffffffffu, dest, j);
+      const int64_t r = __shfl_sync(0xffffffffu, sfrow, j);
+      if (d < 0) continue;  // warp-uniform
+      uint8_t* srow = sf + ((r >> 7) * (kc >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+      uint8_t* crow = codes + static_cast<int64_t>(d) * (H / 2);
+#pragma unroll
+      for (int jj = 0; jj < NCH; ++jj) {
+        const int cc = 32 * jj + lane;
+        if (cc < nb) st_u64(crow + 8 * cc, qb[jj].codes);
+        if (cc < kc) srow[cpart[jj]] = static_cast<uint8_t>(qb[jj].sf);
+      }
       if (lane == 0) row_g[d] = g;
     }
   }
 
   // zero the scale bytes of each expert's padding rows
-  for (int e = c; e < E; e += gridDim.x) {
+  const int words = kc / 4;
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
     const int cnt = s_off[e + 1] - s_off[e];
     const int pad = ((cnt + 127) & ~127) - cnt;
-    const int words = kc / 4;
-    for (int i = tid; i < pad * words; i += blockDim.x) {
+    for (int i = threadIdx.x; i < pad * words; i += blockDim.x) {
       const int64_t r = static_cast<int64_t>(s_sfoff[e]) + cnt + i / words;
       *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * (i % words), kc)) = 0u;
     }
@@ -263,24 +281,28 @@ extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
   const int nchunks = static_cast<int>((T + ct - 1) / ct);
   PermWs w = perm_ws(workspace, E);
 
-  permute_hist_kernel<<<nchunks, kPermThreads, E * sizeof(int32_t), s>>>(
-      topk_ids, T, k, E, ct, nchunks, w.table, w.counter, status);
+  const int rank_blocks = (nchunks + kRankWarps - 1) / kRankWarps;
+  permute_rank_kernel<<<rank_blocks, 32 * kRankWarps, kRankWarps * E * sizeof(int32_t), s>>>(
+      topk_ids, T, k, E, ct, nchunks, w.table, dest_row, w.counter, status);
   permute_scan_kernel<<<E, kPermThreads, 0, s>>>(w.table, nchunks, E, w.counter, w.totals,
                                                  expert_offsets, sf_row_offsets);
-  const size_t smem = (2 * (E + 1) + 2 * ct * k) * sizeof(int32_t);
-  const int nch = static_cast<int>((H + 255) / 256);
+  const size_t smem = 2 * (E + 1) * sizeof(int32_t);
+  const int nch = static_cast<int>((H / 16 + 31) / 32);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   const int h = static_cast<int>(H);
+  const int per_sm = nch <= 5 ? 3 : 2;
+  int64_t qblocks = (T + kPermThreads / 32 - 1) / (kPermThreads / 32);
+  if (qblocks > static_cast<int64_t>(num_sms()) * per_sm) qblocks = num_sms() * per_sm;
+  if (qblocks < 1) qblocks = 1;
   switch (nch) {
 #define MINITE_CASE(N)                                                                     \
   case N:                                                                                  \
-    permute_quant_kernel<N><<<nchunks, kPermThreads, smem, s>>>(                           \
+    permute_quant_kernel<N><<<static_cast<unsigned>(qblocks), kPermThreads, smem, s>>>(    \
         xb, topk_ids, topk_w, T, h, E, k, ct, nchunks, w.table, expert_offsets,            \
         sf_row_offsets, codes, sf, row_g, perm_src, dest_row, perm_w);                     \
     break;
     MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
-    MINITE_CASE(7) MINITE_CASE(8) MINITE_CASE(9) MINITE_CASE(10) MINITE_CASE(11)
-    MINITE_CASE(12) MINITE_CASE(13) MINITE_CASE(14) MINITE_CASE(15) MINITE_CASE(16)
+    MINITE_CASE(7) MINITE_CASE(8)
 #undef MINITE_CASE
     default: return MINITE_ERR_UNSUPPORTED_SHAPE;
   }

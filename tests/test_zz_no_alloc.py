@@ -79,7 +79,7 @@ def test_noalloc_permute_matches_workspace_entry_point_on_consecutive_calls():
 def test_noalloc_rejects_problems_beyond_its_scratch():
     lib = M.load()
     fake = ctypes.c_void_p(4096)  # never dereferenced: the size check comes first
-    T, H, E, k = 16384, 2048, 1024, 8
+    T, H, E, k = 65536, 2048, 1024, 8
     assert M.minite_workspace_bytes(M.OP_PERMUTE_QUANT, T, H, E, k) > (2 << 20)
     rc = lib.minite_moe_permute_quant_noalloc(fake, fake, None, T, H, E, k, fake, fake, fake, fake,
                                               fake, fake, fake, None, None, None)
