@@ -8,7 +8,7 @@
 // quantization. Per-token scales follow its section "Follow the numerical
 // execution path".
 //
-// Three launches, no host synchronization:
+// Four launches, no host synchronization:
 //   permute_rank_kernel   one warp per token chunk: stable in-chunk rank of
 //                         every (token, slot) pair (kept in dest_row) and the
 //                         chunk's expert histogram -> table[e][chunk]; also
@@ -16,10 +16,12 @@
 //   permute_scan_kernel   one block per expert: exclusive prefix of its
 //                         chunk counts; the last block to finish turns the
 //                         expert totals into expert_offsets / sf_row_offsets.
-//   permute_quant_kernel  one warp per token: completes the token's k
-//                         permuted rows, reads the token once, quantizes it
-//                         once in registers and writes its codes / scales to
-//                         its k destination rows.
+//   permute_route_kernel  one thread per pair: the pair's permuted row
+//                         (offset + chunk base + local rank), perm_src and
+//                         perm_w.
+//   permute_quant_kernel  one warp per token: reads the token once,
+//                         quantizes it once in registers and writes its
+//                         codes / scales to its k destination rows.
 #include <mutex>
 
 #include "common.cuh"
@@ -165,19 +167,37 @@ __global__ void __launch_bounds__(kPermThreads) permute_scan_kernel(
   }
 }
 
+// Completes every pair's permuted row (expert offset + the chunk's base for
+// the expert + the local rank) and writes the routing outputs; one thread per
+// pair.
+__global__ void __launch_bounds__(kPermThreads) permute_route_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ topk_w, int64_t T, int E, int k,
+    int ct, int nchunks, const int32_t* __restrict__ table,
+    const int32_t* __restrict__ expert_offsets, int32_t* __restrict__ perm_src,
+    int32_t* __restrict__ dest_row, float* __restrict__ perm_w) {
+  const int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (p >= T * k) return;
+  const int e = ids[p];
+  if (e < 0 || e >= E) return;  // dest_row already -1
+  const int64_t t = p / k;
+  const int dest = expert_offsets[e] + table[static_cast<int64_t>(e) * nchunks + t / ct] +
+                   dest_row[p];
+  dest_row[p] = dest;
+  perm_src[dest] = static_cast<int32_t>(t);
+  if (perm_w) perm_w[dest] = topk_w[p];
+}
+
 // Quantize and scatter, one warp per token over a grid of resident blocks:
-// lane j < k completes pair j's permuted row (expert offset + the chunk's
-// base for the expert + the local rank) and writes the routing outputs; the
-// warp reads the token once (lane l owns blocks 32i + l), quantizes it once
-// in registers and writes its codes, scales and g to each destination row.
+// the warp reads the token once (lane l owns blocks 32i + l), quantizes it
+// once in registers and writes its codes, scales and g to each of its k
+// permuted rows. Each warp requests its next token (row and routing) before
+// it writes the current one.
 template <int NCH>
 __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_kernel(
-    const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
-    const float* __restrict__ topk_w, int64_t T, int H, int E, int k, int ct, int nchunks,
-    const int32_t* __restrict__ table, const int32_t* __restrict__ expert_offsets,
-    const int32_t* __restrict__ sf_row_offsets, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ sf, float* __restrict__ row_g, int32_t* __restrict__ perm_src,
-    int32_t* __restrict__ dest_row, float* __restrict__ perm_w) {
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int64_t T, int H, int E,
+    int k, const int32_t* __restrict__ expert_offsets,
+    const int32_t* __restrict__ sf_row_offsets, const int32_t* __restrict__ dest_row,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g) {
   extern __shared__ int32_t sm[];
   int32_t* s_off = sm;                 // [E+1]
   int32_t* s_sfoff = s_off + (E + 1);  // [E+1]
@@ -198,34 +218,33 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
     cpart[j] = (cc >> 2) * 512 + (cc & 3);
   }
   const bool a32 = (reinterpret_cast<uintptr_t>(x) & 31) == 0;
-  for (int64_t t = warp; t < T; t += nwarps) {
-    // routing of pair (t, lane)
-    int dest = -1;
-    int64_t sfrow = 0;
+  uint32_t w[NCH][8];
+  float am[NCH];
+  float m = 0.0f;
+  int dest = -1, e = -1;  // pair (t, lane)
+  auto fetch = [&](int64_t t) {
     if (lane < k) {
-      const int64_t p = t * k + lane;
-      const int e = ids[p];
-      if (e >= 0 && e < E) {
-        const int local = table[static_cast<int64_t>(e) * nchunks + t / ct] + dest_row[p];
-        dest = s_off[e] + local;
-        sfrow = static_cast<int64_t>(s_sfoff[e]) + local;
-        perm_src[dest] = static_cast<int32_t>(t);
-        if (perm_w) perm_w[dest] = topk_w[p];
-      }
-      dest_row[p] = dest;
+      dest = dest_row[t * k + lane];
+      e = ids[t * k + lane];
     }
-    uint32_t w[NCH][8];
-    float am[NCH];
     const uint16_t* xr = x + t * H;
-    const float m = a32 ? load_row_blocks<NCH, true>(xr, nb, w, am)
-                        : load_row_blocks<NCH, false>(xr, nb, w, am);
+    m = a32 ? load_row_blocks<NCH, true>(xr, nb, w, am)
+            : load_row_blocks<NCH, false>(xr, nb, w, am);
+  };
+  int64_t t = warp;
+  if (t < T) fetch(t);
+  while (t < T) {
     const float g = global_scale(warp_max(m));
     QBlock qb[NCH];
     quant_row_blocks<NCH>(w, am, nb, g, qb);
+    const int dcur = dest, ecur = e;
+    t += nwarps;
+    if (t < T) fetch(t);
     for (int j = 0; j < k; ++j) {
-      const int d = __shfl_sync(0xffffffffu, dest, j);
-      const int64_t r = __shfl_sync(0xffffffffu, sfrow, j);
+      const int d = __shfl_sync(0xffffffffu, dcur, j);
       if (d < 0) continue;  // warp-uniform
+      const int ej = __shfl_sync(0xffffffffu, ecur, j);
+      const int64_t r = static_cast<int64_t>(s_sfoff[ej]) + (d - s_off[ej]);
       uint8_t* srow = sf + ((r >> 7) * (kc >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
       uint8_t* crow = codes + static_cast<int64_t>(d) * (H / 2);
 #pragma unroll
@@ -286,6 +305,10 @@ extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
       topk_ids, T, k, E, ct, nchunks, w.table, dest_row, w.counter, status);
   permute_scan_kernel<<<E, kPermThreads, 0, s>>>(w.table, nchunks, E, w.counter, w.totals,
                                                  expert_offsets, sf_row_offsets);
+  const int64_t pairs = T * k;
+  permute_route_kernel<<<static_cast<unsigned>((pairs + kPermThreads - 1) / kPermThreads),
+                         kPermThreads, 0, s>>>(topk_ids, topk_w, T, E, k, ct, nchunks, w.table,
+                                               expert_offsets, perm_src, dest_row, perm_w);
   const size_t smem = 2 * (E + 1) * sizeof(int32_t);
   const int nch = static_cast<int>((H / 16 + 31) / 32);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
@@ -298,8 +321,8 @@ extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
 #define MINITE_CASE(N)                                                                     \
   case N:                                                                                  \
     permute_quant_kernel<N><<<static_cast<unsigned>(qblocks), kPermThreads, smem, s>>>(    \
-        xb, topk_ids, topk_w, T, h, E, k, ct, nchunks, w.table, expert_offsets,            \
-        sf_row_offsets, codes, sf, row_g, perm_src, dest_row, perm_w);                     \
+        xb, topk_ids, T, h, E, k, expert_offsets, sf_row_offsets, dest_row, codes, sf,     \
+        row_g);                                                                            \
     break;
     MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
     MINITE_CASE(7) MINITE_CASE(8)

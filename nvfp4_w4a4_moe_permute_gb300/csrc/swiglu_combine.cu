@@ -215,55 +215,78 @@ static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int 
   return MINITE_OK;
 }
 
-// One warp per token; lane l owns columns [256c + 8l, 256c + 8l + 8) of chunk c.
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ D,
-                                                      const int32_t* __restrict__ dest_row,
-                                                      int64_t T, int64_t M, int N, int k,
-                                                      uint16_t* __restrict__ y, int32_t* status) {
+// Work unit: (token t, column chunk of 512); lane l owns columns
+// [512 ch + 16 l, +16). For each slot j in order the lane adds the 16 BF16
+// values of row dest_row[t, j] into FP32 accumulators; up to 8 rows are in
+// flight at once, and each warp requests the next unit's routing before it
+// reads the current unit's rows.
+template <bool A32>
+__global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restrict__ D,
+                                                         const int32_t* __restrict__ dest_row,
+                                                         int64_t T, int64_t M, int N, int k,
+                                                         uint16_t* __restrict__ y,
+                                                         int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t t = warp; t < T; t += nwarps) {
-    int my = lane < k ? dest_row[t * k + lane] : -1;
+  const int upt = (N + 511) / 512;
+  const int64_t units = T * upt;
+  int64_t u = warp;
+  int nxt = -1;
+  if (u < units && lane < k) nxt = dest_row[(u / upt) * k + lane];
+  for (; u < units; u += nwarps) {
+    const int64_t t = u / upt;
+    const int ch = static_cast<int>(u - t * upt);
+    int my = nxt;
+    const int64_t un = u + nwarps;
+    if (un < units && lane < k) nxt = dest_row[(un / upt) * k + lane];
     if (my >= M) {
       set_status(status, MINITE_ERR_BAD_ROUTING);
       my = -1;
     }
-    for (int c0 = 0; c0 < N; c0 += 256) {
-      const int col = c0 + 8 * lane;
-      float acc[8];
+    const int col = 512 * ch + 16 * lane;
+    const int nv = col < N ? min(16, N - col) : 0;  // 0, 8 or 16 valid columns
+    float acc[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      for (int j0 = 0; j0 < k; j0 += 8) {
-        uint4 u[8];
+    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint32_t v[8][8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int d = __shfl_sync(0xffffffffu, my, (j0 + jj) & 31);
-          u[jj] = make_uint4(0, 0, 0, 0);
-          if (j0 + jj < k && d >= 0 && col < N)
-            u[jj] = __ldcs(reinterpret_cast<const uint4*>(D + static_cast<int64_t>(d) * N + col));
+      for (int jj = 0; jj < 8; ++jj) {
+        const int d = __shfl_sync(0xffffffffu, my, (j0 + jj) & 31);
+        const uint16_t* src = D + static_cast<int64_t>(d) * N + col;
+        if (j0 + jj < k && d >= 0 && nv == 16) {
+          if (A32) ld_bf16x16(src, v[jj]);
+          else ld_bf16x16_a16(src, v[jj]);
+        } else if (j0 + jj < k && d >= 0 && nv == 8) {
+          const uint4 a = __ldcs(reinterpret_cast<const uint4*>(src));
+          v[jj][0] = a.x; v[jj][1] = a.y; v[jj][2] = a.z; v[jj][3] = a.w;
+          v[jj][4] = v[jj][5] = v[jj][6] = v[jj][7] = 0u;
         }
+      }
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int d = __shfl_sync(0xffffffffu, my, (j0 + jj) & 31);
-          if (j0 + jj < k && d >= 0) {
-            float v[8];
-            unpack_bf16x8(u[jj], v);
+      for (int jj = 0; jj < 8; ++jj) {
+        const int d = __shfl_sync(0xffffffffu, my, (j0 + jj) & 31);
+        if (j0 + jj < k && d >= 0 && nv > 0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
+          for (int i = 0; i < 8; ++i) {
+            acc[2 * i] = __fadd_rn(acc[2 * i], bf16lo(v[jj][i]));
+            acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], bf16hi(v[jj][i]));
           }
         }
       }
-      if (col < N) {
-        uint32_t o[4];
+    }
+    if (nv > 0) {
+      uint32_t o[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i]));
-          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1]));
-          o[i] = lo | (hi << 16);
-        }
-        *reinterpret_cast<uint4*>(y + t * N + col) = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i]));
+        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1]));
+        o[i] = lo | (hi << 16);
       }
+      uint16_t* dst = y + t * N + col;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+      if (nv == 16) *reinterpret_cast<uint4*>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
 }
@@ -315,11 +338,18 @@ extern "C" int minite_moe_combine(const void* expert_out, const int32_t* dest_ro
     return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(expert_out, 16) || !aligned(y, 16)) return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int64_t blocks = (T + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  const int64_t units = T * ((N + 511) / 512);
+  int64_t blocks = (units + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 2;
   if (blocks > cap) blocks = cap;
-  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      static_cast<const uint16_t*>(expert_out), dest_row, T, M, static_cast<int>(N), k,
-      static_cast<uint16_t*>(y), status);
+  const uint16_t* d = static_cast<const uint16_t*>(expert_out);
+  uint16_t* yy = static_cast<uint16_t*>(y);
+  const int n = static_cast<int>(N);
+  if (N % 16 == 0 && aligned(expert_out, 32))
+    combine_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(d, dest_row, T, M, n, k,
+                                                                       yy, status);
+  else
+    combine_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(d, dest_row, T, M, n, k,
+                                                                        yy, status);
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
