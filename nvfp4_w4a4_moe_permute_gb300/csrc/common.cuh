@@ -421,6 +421,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count));
 }
@@ -481,6 +482,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_
       " [%0], [%1, {%3, %4}], [%2];"
       :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)),
          "r"(x), "r"(y)
+      : "memory");
+}
+
+// 3-D TMA load global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* desc, uint64_t* bar, int x,
+                                            int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)),
+         "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 
@@ -639,6 +651,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* desc, ui
       ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
       :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(desc)), "r"(mbar_cluster), "r"(x),
          "r"(y)
+      : "memory");
+}
+// 3-D TMA load into this CTA's shared memory, completion counted on an
+// mbarrier that may live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* desc, uint32_t mbar_cluster,
+                                                 int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(desc)), "r"(mbar_cluster), "r"(x),
+         "r"(y), "r"(z)
       : "memory");
 }
 // One warp in each CTA of the pair, collectively.

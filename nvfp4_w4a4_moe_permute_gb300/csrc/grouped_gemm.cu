@@ -35,6 +35,16 @@
 //  * Every mbarrier wait is bounded by a %globaltimer budget; on expiry the
 //    CTA records MINITE_ERR_TIMEOUT, drains its in-flight copies and MMAs,
 //    frees TMEM and exits.
+//
+// Kernels (all bit-identical; the automatic choice is the fourth where it
+// applies): grouped_gemm_kernel (above, one-chunk stages),
+// grouped_gemm_pair_kernel and grouped_gemm_pair2_kernel (256 x 256 tiles
+// with tcgen05.mma.cta_group::2 on the two SMs of a cluster, one- and
+// two-chunk stages), grouped_gemm_dc_kernel (128 x 256 tiles, two-chunk
+// stages loaded with one 3-D box per operand and scale atoms from a separate
+// producer warp). A copy instruction costs the issuing thread a roughly
+// fixed time whatever its size, so fewer, larger copies per tensor cycle
+// keep the producer ahead of the MMA.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -872,6 +882,719 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
+// ============================================================================
+// CTA-pair kernel with two-chunk stages. Each TMA copy instruction costs the
+// issuing thread a roughly fixed time, whatever its size, so a stage covers
+// two 128-byte K chunks (K = 512, eight pair MMAs, 1024 tensor cycles) and
+// is loaded with one 3-D box per operand: a box {128 bytes, 128 rows, 2
+// chunks} lands as two consecutive 128-byte-swizzled chunk tiles. Per stage
+// and CTA that is two A/B copies from warp 0 and three scale copies (A: 8
+// atoms of its 128 rows; B: 8 atoms of each of the two 128-row blocks, all
+// contiguous) from a separate scale-producer warp, into two 12 KB slots.
+// MMA, scale-warp and epilogue roles are those of the CTA-pair kernel, with
+// the scale warps walking a slot chunk by chunk into the per-chunk TMEM ring.
+// ============================================================================
+
+constexpr int Q_CH = 2;                                  // 128-byte K chunks per stage
+constexpr int Q_STAGES = 3;
+constexpr int Q_A_BYTES = Q_CH * 128 * BK_BYTES;         // 32 KB: this CTA's 128 rows of A
+constexpr int Q_B_BYTES = Q_CH * 128 * BK_BYTES;         // 32 KB: this CTA's 128 rows of B
+constexpr int Q_STAGE_BYTES = Q_A_BYTES + Q_B_BYTES;     // 64 KB, counted on the even CTA
+constexpr int Q_SFA_BYTES = 4 * Q_CH * SF_ATOM;          // 4 KB: 8 k-steps of this CTA's A scales
+constexpr int Q_SFB_BYTES = 2 * 4 * Q_CH * SF_ATOM;      // 8 KB: 8 k-steps of both B blocks
+constexpr int Q_SLOT_BYTES = Q_SFA_BYTES + Q_SFB_BYTES;  // 12 KB
+constexpr int Q_SLOTS = 2;
+constexpr int Q_NSF = 5;                                 // TMEM scale ring (per chunk)
+constexpr int Q_SF_WARP = NUM_WARPS;                     // the scale-slot producer warp
+constexpr int Q_THREADS = (NUM_WARPS + 1) * 32;
+static_assert(Q_STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+static_assert(SF_COL0 + Q_NSF * P_SF_COLS <= TMEM_COLS, "TMEM budget");
+
+struct QSmem {
+  uint64_t full[Q_STAGES];
+  uint64_t empty[Q_STAGES];
+  uint64_t sfdata[Q_SLOTS];
+  uint64_t sfread[Q_SLOTS];
+  uint64_t sf_full[Q_NSF];
+  uint64_t sf_empty[Q_NSF];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_tiles;
+  int pad_;
+};
+
+// 23 warps: 6 sit on some sub-partition, whose 16K registers then allow 85
+// per thread.
+__global__ void __maxnreg__(80)
+grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                          const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* slots = stages + Q_STAGES * Q_STAGE_BYTES;
+  QSmem& S = *reinterpret_cast<QSmem*>(slots + Q_SLOTS * Q_SLOT_BYTES);
+  int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
+  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
+  int32_t* s_sfb = s_off + (p.E + 1);                           // [E+1] sf_row_offsets / 128
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(num_clusters_x());
+  const int KT = (p.K + 255) / 256;        // 128-byte chunks per tile
+  const int KD = (KT + Q_CH - 1) / Q_CH;   // stages per tile
+  const int KSTEPS = p.K / 64;
+  const int atoms_per_rb = p.K / 64;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int rb_per_expert = (p.N + 127) / 128;
+  const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    for (int s = 0; s < Q_STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int s = 0; s < Q_SLOTS; ++s) {
+      mbar_init(&S.sfdata[s], 1);
+      mbar_init(&S.sfread[s], 4);
+    }
+    for (int b = 0; b < Q_NSF; ++b) {
+      mbar_init(&S.sf_full[b], 8);
+      mbar_init(&S.sf_empty[b], 1);
+    }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, 2 * NUM_EPI_WARPS);
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
+  if (warp == 2) {
+    int carry = 0;
+    bool bad = false;
+    if (lane == 0) tiles_prefix[0] = 0;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      int cnt = 0;
+      if (e < p.E) {
+        const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
+        const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
+        s_off[e + 1] = o1;
+        s_sfb[e + 1] = s1 / 128;
+        if (e == 0) { s_off[0] = o0; s_sfb[0] = s0 / 128; }
+        cnt = o1 - o0;
+        if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
+            (e == p.E - 1 && o1 > p.M))
+          bad = true;
+        cnt = cnt > 0 ? (cnt + 255) / 256 : 0;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (e < p.E) tiles_prefix[e + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      S.total_tiles = bad ? 0 : carry * n_tiles;
+      if (bad && blockIdx.x == 0) set_status(p.status, MINITE_ERR_INVALID_ARG);
+    }
+  }
+  // both CTAs' barriers exist and TMEM is allocated before any cross-CTA traffic
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+
+  const uint32_t tmem = S.tmem_base;
+  const int total = S.total_tiles;
+  volatile int* abort_flag = &S.abort_flag;
+  const uint32_t peer_abort = mapa_shared(smem_u32(&S.abort_flag), rank ^ 1u);
+  const uint32_t leader_full0 = mapa_shared(smem_u32(&S.full[0]), 0);
+  const uint32_t leader_sf_full0 = mapa_shared(smem_u32(&S.sf_full[0]), 0);
+  const uint32_t leader_acc_empty = mapa_shared(smem_u32(&S.acc_empty), 0);
+  const uint64_t budget = p.budget_ns;
+  constexpr uint64_t kDrainBudget = 200000000ull;
+  auto fail = [&](int code) {
+    *abort_flag = 1;
+    st_shared_cluster(peer_abort, 1u);
+    set_status(p.status, code);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ A/B producer
+    if (lane == 0) {
+      uint32_t armed_mask = 0, armed_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      KIter it;
+      it.start(cid, ncl, total, KD, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      while (it.valid()) {
+        if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        uint8_t* sA = stages + stage * Q_STAGE_BYTES;
+        uint8_t* sB = sA + Q_A_BYTES;
+        if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], 2 * Q_STAGE_BYTES);
+        const uint32_t fb = leader_full0 + 8u * stage;
+        tma_load_3d_pair(sA, &tmap_a, fb, 0, it.tl.row0 + 128 * static_cast<int>(rank),
+                         Q_CH * it.kt);
+        tma_load_3d_pair(sB, &tmap_b, fb, 0,
+                         it.tl.e * p.N + it.tl.nt * BN + 128 * static_cast<int>(rank),
+                         Q_CH * it.kt);
+        armed_mask |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == Q_STAGES) { stage = 0; phase ^= 1u; }
+        it.advance(p);
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      volatile int no_abort = 0;
+      if (rank == 0) {
+        // both CTAs' A/B copies count on these barriers: all armed stages landed
+        for (int s = 0; s < Q_STAGES; ++s)
+          if (armed_mask & (1u << s))
+            mbar_wait(&S.full[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
+      } else if (!ok) {
+        // this CTA's copies count on the other CTA's barriers: give any copy
+        // still in flight time to land before the CTA can exit
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {}
+      }
+    }
+  } else if (warp == Q_SF_WARP) {
+    // ------------------------------------------------------------ scale-slot producer
+    if (lane == 0) {
+      uint32_t slot_mask = 0, slot_parity = 0;
+      int slot = 0;
+      uint32_t slot_phase = 0;
+      bool ok = true;
+      KIter it;
+      it.start(cid, ncl, total, KD, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      while (it.valid()) {
+        if (!mbar_wait(&S.sfread[slot], slot_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        const PTile& tl = it.tl;
+        const int na = min(4 * Q_CH, KSTEPS - 4 * Q_CH * it.kt);   // atoms (k-steps) in this stage
+        const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;     // this CTA's A block exists
+        const int nrb = min(2, rb_per_expert - tl.nt * 2);        // B blocks inside the weight
+        uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
+        uint8_t* sSFB = sSFA + Q_SFA_BYTES;
+        mbar_arrive_expect_tx(&S.sfdata[slot],
+                              static_cast<uint32_t>(na * ((a_ok ? 1 : 0) + nrb)) * SF_ATOM);
+        if (a_ok)
+          bulk_load(sSFA,
+                    p.a_sf + (static_cast<size_t>(tl.sf_rb0 + static_cast<int>(rank)) * atoms_per_rb +
+                              4 * Q_CH * it.kt) * SF_ATOM,
+                    na * SF_ATOM, &S.sfdata[slot]);
+        for (int rb = 0; rb < nrb; ++rb)
+          bulk_load(sSFB + rb * 4 * Q_CH * SF_ATOM,
+                    p.b_sf + tl.e * sfb_expert +
+                        (static_cast<size_t>(tl.nt * 2 + rb) * atoms_per_rb + 4 * Q_CH * it.kt) *
+                            SF_ATOM,
+                    na * SF_ATOM, &S.sfdata[slot]);
+        slot_mask |= 1u << slot;
+        slot_parity = (slot_parity & ~(1u << slot)) | (slot_phase << slot);
+        if (++slot == Q_SLOTS) { slot = 0; slot_phase ^= 1u; }
+        it.advance(p);
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      // this CTA's scale copies count on its own barriers
+      volatile int no_abort = 0;
+      for (int s = 0; s < Q_SLOTS; ++s)
+        if (slot_mask & (1u << s))
+          mbar_wait(&S.sfdata[s], (slot_parity >> s) & 1u, kDrainBudget, &no_abort);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = make_idesc_pair();
+      const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t bdesc0 = smem_desc(smem_u32(stages + Q_A_BYTES), 16, 1024, kLayoutSwizzle128B);
+      int stage = 0, sfb = 0;
+      uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int t = cid; t < total && ok; t += ncl) {
+        if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int kd = 0; kd < KD && ok; ++kd) {
+          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag)) { ok = false; break; }
+          const int nch = min(Q_CH, KT - Q_CH * kd);
+          for (int c = 0; c < nch; ++c) {
+            if (!mbar_wait(&S.sf_full[sfb], sf_phase, budget, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const int kt = Q_CH * kd + c;
+            const int ks = min(4, KSTEPS - 4 * kt);
+            const uint64_t soff =
+                static_cast<uint64_t>(stage * Q_STAGE_BYTES + c * 128 * BK_BYTES) >> 4;
+            const uint32_t sf_t = tmem + SF_COL0 + sfb * P_SF_COLS;
+            for (int s = 0; s < ks; ++s)
+              tc_mma_nvfp4_pair(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc,
+                                sf_t + 4 * s, sf_t + 16 + 8 * s, (kt | s) != 0);
+            issued = true;
+            tc_commit_pair_mc(&S.sf_empty[sfb], kPairMask);
+            if (++sfb == Q_NSF) { sfb = 0; sf_phase ^= 1u; }
+          }
+          if (!ok) break;
+          tc_commit_pair_mc(&S.empty[stage], kPairMask);
+          if (++stage == Q_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&S.acc_full, kPairMask);
+        acc_phase ^= 1u;
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      if (issued) {
+        tc_commit_pair_mc(&S.drain, 0x1);
+        volatile int no_abort = 0;
+        mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
+      }
+    }
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------------------------------------ scale warps
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int slot = 0, sfb = 0;
+    uint32_t slot_phase = 0, sf_phase = 0;
+    bool ok = true;
+    KIter it;
+    it.start(cid, ncl, total, KD, n_tiles, tiles_prefix, s_off, s_sfb, p);
+    while (it.valid() && ok) {
+      const bool a_ok = static_cast<int>(rank) < it.tl.sf_rbs;
+      const int nrb = min(2, rb_per_expert - it.tl.nt * 2);
+      const int nch = min(Q_CH, KT - Q_CH * it.kt);
+      if (!mbar_wait(&S.sfdata[slot], slot_phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
+      const uint8_t* sSFB = sSFA + Q_SFA_BYTES;
+      for (int c = 0; c < nch; ++c) {
+        const int ks = min(4, KSTEPS - 4 * (Q_CH * it.kt + c));
+        // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
+        uint32_t ra[16], rbv[32];
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          const int a = 4 * c + st;   // atom index within the slot's 8
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (a_ok && st < ks) v = lds128(sSFA + a * SF_ATOM + lane * 16);
+          ra[4 * st] = v.x; ra[4 * st + 1] = v.y; ra[4 * st + 2] = v.z; ra[4 * st + 3] = v.w;
+#pragma unroll
+          for (int rb = 0; rb < 2; ++rb) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (rb < nrb && st < ks)
+              w = lds128(sSFB + (rb * 4 * Q_CH + a) * SF_ATOM + lane * 16);
+            const int cc = 8 * st + 4 * rb;
+            rbv[cc] = w.x; rbv[cc + 1] = w.y; rbv[cc + 2] = w.z; rbv[cc + 3] = w.w;
+          }
+        }
+        if (c == nch - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.sfread[slot]);
+        }
+        if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag)) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint32_t col = tmem + lane_base + SF_COL0 + sfb * P_SF_COLS;
+        tmem_st_16cols(col, ra);
+        tmem_st_16cols(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[0]));
+        tmem_st_16cols(col + 32, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[16]));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_sf_full0 + 8u * sfb);
+        if (++sfb == Q_NSF) { sfb = 0; sf_phase ^= 1u; }
+      }
+      if (++slot == Q_SLOTS) { slot = 0; slot_phase ^= 1u; }
+      it.advance(p);
+    }
+    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int cb = (warp - EPI_WARP0) >> 2;
+    const int r_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = cid; t < total; t += ncl) {
+      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      const bool valid = r_in_tile < tl.rows;
+      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
+      float scale = 0.0f;
+      if (valid) scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
+      if (!mbar_wait(&S.acc_full, acc_phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      acc_phase ^= 1u;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * EPI_COLS;
+      epilogue_slice(p, tbase, valid, row, tl.nt * BN + cb * EPI_COLS, scale,
+                     [&] { mbar_arrive_cluster(leader_acc_empty); });
+    }
+    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  }
+
+  // no cross-CTA traffic may target a CTA that has left: both wait here, then
+  // free the pair's TMEM together
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
+}
+
+// ============================================================================
+// Single-CTA kernel with two-chunk stages: the 128 x 256 tile of the
+// single-CTA kernel, with each stage covering two 128-byte K chunks (eight
+// MMAs, 1024 tensor cycles) loaded by one 3-D box per operand, so that the
+// producer spends two copy instructions per 1024 tensor cycles instead of
+// five per 512. Scale atoms come from a separate scale-producer warp, three
+// copies per stage (A: 8 atoms; B: 8 atoms of each 128-row block) into two
+// 12 KB slots, which the scale warps walk chunk by chunk into the TMEM ring.
+// ============================================================================
+
+constexpr int D_STAGES = 2;
+constexpr int D_A_BYTES = Q_CH * A_BYTES;                 // 32 KB
+constexpr int D_B_BYTES = Q_CH * B_BYTES;                 // 64 KB
+constexpr int D_STAGE_BYTES = D_A_BYTES + D_B_BYTES;      // 96 KB
+constexpr int D_SLOTS = 2;
+static_assert(D_STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+
+struct DSmem {
+  uint64_t full[D_STAGES];
+  uint64_t empty[D_STAGES];
+  uint64_t sfdata[D_SLOTS];
+  uint64_t sfread[D_SLOTS];
+  uint64_t sf_full[NSF];
+  uint64_t sf_empty[NSF];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_tiles;
+  int pad_;
+};
+
+// Walks this CTA's (tile, stage) pairs in order.
+struct DIter {
+  int t, kd, ncl, total, KD, n_tiles;
+  Tile tl;
+  const int32_t *prefix, *s_off;
+  __device__ __forceinline__ bool valid() const { return t < total; }
+  __device__ __forceinline__ void start(int t0, int ncl_, int total_, int KD_, int n_tiles_,
+                                        const int32_t* prefix_, const int32_t* s_off_,
+                                        const Params& p) {
+    t = t0; kd = 0; ncl = ncl_; total = total_; KD = KD_; n_tiles = n_tiles_;
+    prefix = prefix_; s_off = s_off_;
+    if (t < total) tl = decode_tile(t, n_tiles, prefix, s_off, p);
+  }
+  __device__ __forceinline__ void advance(const Params& p) {
+    if (++kd == KD) {
+      kd = 0;
+      t += ncl;
+      if (t < total) tl = decode_tile(t, n_tiles, prefix, s_off, p);
+    }
+  }
+};
+
+__global__ void __maxnreg__(80)
+grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                       const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* slots = stages + D_STAGES * D_STAGE_BYTES;
+  DSmem& S = *reinterpret_cast<DSmem*>(slots + D_SLOTS * Q_SLOT_BYTES);
+  int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
+  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KT = (p.K + 255) / 256;        // 128-byte chunks per tile
+  const int KD = (KT + Q_CH - 1) / Q_CH;   // stages per tile
+  const int KSTEPS = p.K / 64;
+  const int atoms_per_rb = p.K / 64;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int rb_per_expert = (p.N + 127) / 128;
+  const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    for (int s = 0; s < D_STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int s = 0; s < D_SLOTS; ++s) {
+      mbar_init(&S.sfdata[s], 1);
+      mbar_init(&S.sfread[s], 4);
+    }
+    for (int b = 0; b < NSF; ++b) {
+      mbar_init(&S.sf_full[b], 4);
+      mbar_init(&S.sf_empty[b], 1);
+    }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, NUM_EPI_WARPS);
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&S.tmem_base, TMEM_COLS);
+  if (warp == 2) {
+    // m-block prefix over experts, validating the device offsets on the way
+    int carry = 0;
+    bool bad = false;
+    if (lane == 0) tiles_prefix[0] = 0;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      int cnt = 0;
+      if (e < p.E) {
+        const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
+        const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
+        s_off[e + 1] = o1;
+        if (e == 0) s_off[0] = o0;
+        cnt = o1 - o0;
+        if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
+            (e == p.E - 1 && o1 > p.M))
+          bad = true;
+        cnt = cnt > 0 ? (cnt + BM - 1) / BM : 0;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (e < p.E) tiles_prefix[e + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      S.total_tiles = bad ? 0 : carry * n_tiles;
+      if (bad && blockIdx.x == 0) set_status(p.status, MINITE_ERR_INVALID_ARG);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = S.tmem_base;
+  const int total = S.total_tiles;
+  volatile int* abort_flag = &S.abort_flag;
+  const uint64_t budget = p.budget_ns;
+  constexpr uint64_t kDrainBudget = 200000000ull;
+  auto fail = [&](int code) {
+    *abort_flag = 1;
+    set_status(p.status, code);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ A/B producer
+    if (lane == 0) {
+      uint32_t armed_mask = 0, armed_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      DIter it;
+      it.start(blockIdx.x, gridDim.x, total, KD, n_tiles, tiles_prefix, s_off, p);
+      while (it.valid()) {
+        if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        uint8_t* sA = stages + stage * D_STAGE_BYTES;
+        uint8_t* sB = sA + D_A_BYTES;
+        mbar_arrive_expect_tx(&S.full[stage], D_STAGE_BYTES);
+        tma_load_3d(sA, &tmap_a, &S.full[stage], 0, it.tl.row0, Q_CH * it.kd);
+        tma_load_3d(sB, &tmap_b, &S.full[stage], 0, it.tl.e * p.N + it.tl.nt * BN, Q_CH * it.kd);
+        armed_mask |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == D_STAGES) { stage = 0; phase ^= 1u; }
+        it.advance(p);
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      volatile int no_abort = 0;
+      for (int s = 0; s < D_STAGES; ++s)
+        if (armed_mask & (1u << s))
+          mbar_wait(&S.full[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
+    }
+  } else if (warp == Q_SF_WARP) {
+    // ------------------------------------------------------------ scale-slot producer
+    if (lane == 0) {
+      uint32_t slot_mask = 0, slot_parity = 0;
+      int slot = 0;
+      uint32_t slot_phase = 0;
+      bool ok = true;
+      DIter it;
+      it.start(blockIdx.x, gridDim.x, total, KD, n_tiles, tiles_prefix, s_off, p);
+      while (it.valid()) {
+        if (!mbar_wait(&S.sfread[slot], slot_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        const Tile& tl = it.tl;
+        const int na = min(4 * Q_CH, KSTEPS - 4 * Q_CH * it.kd);   // atoms (k-steps) in this stage
+        const int nrb = min(BN / 128, rb_per_expert - tl.nt * (BN / 128));
+        uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
+        uint8_t* sSFB = sSFA + Q_SFA_BYTES;
+        mbar_arrive_expect_tx(&S.sfdata[slot], static_cast<uint32_t>(na * (1 + nrb)) * SF_ATOM);
+        bulk_load(sSFA,
+                  p.a_sf + (static_cast<size_t>(tl.sf_rb) * atoms_per_rb + 4 * Q_CH * it.kd) *
+                               SF_ATOM,
+                  na * SF_ATOM, &S.sfdata[slot]);
+        for (int rb = 0; rb < nrb; ++rb)
+          bulk_load(sSFB + rb * 4 * Q_CH * SF_ATOM,
+                    p.b_sf + tl.e * sfb_expert +
+                        (static_cast<size_t>(tl.nt * (BN / 128) + rb) * atoms_per_rb +
+                         4 * Q_CH * it.kd) * SF_ATOM,
+                    na * SF_ATOM, &S.sfdata[slot]);
+        slot_mask |= 1u << slot;
+        slot_parity = (slot_parity & ~(1u << slot)) | (slot_phase << slot);
+        if (++slot == D_SLOTS) { slot = 0; slot_phase ^= 1u; }
+        it.advance(p);
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      volatile int no_abort = 0;
+      for (int s = 0; s < D_SLOTS; ++s)
+        if (slot_mask & (1u << s))
+          mbar_wait(&S.sfdata[s], (slot_parity >> s) & 1u, kDrainBudget, &no_abort);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc();
+      const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t bdesc0 = smem_desc(smem_u32(stages + D_A_BYTES), 16, 1024, kLayoutSwizzle128B);
+      int stage = 0, sfb = 0;
+      uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int kd = 0; kd < KD && ok; ++kd) {
+          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag)) { ok = false; break; }
+          const int nch = min(Q_CH, KT - Q_CH * kd);
+          for (int c = 0; c < nch; ++c) {
+            if (!mbar_wait(&S.sf_full[sfb], sf_phase, budget, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const int kt = Q_CH * kd + c;
+            const int ks = min(4, KSTEPS - 4 * kt);
+            const uint64_t aoff = static_cast<uint64_t>(stage * D_STAGE_BYTES + c * A_BYTES) >> 4;
+            const uint64_t boff = static_cast<uint64_t>(stage * D_STAGE_BYTES + c * B_BYTES) >> 4;
+            const uint32_t sf_t = tmem + SF_COL0 + sfb * SF_COLS;
+            for (int s = 0; s < ks; ++s)
+              tc_mma_nvfp4(tmem, adesc0 + aoff + 2 * s, bdesc0 + boff + 2 * s, idesc, sf_t + 4 * s,
+                           sf_t + 16 + 4 * (BN / 128) * s, (kt | s) != 0);
+            issued = true;
+            tc_commit(&S.sf_empty[sfb]);
+            if (++sfb == NSF) { sfb = 0; sf_phase ^= 1u; }
+          }
+          if (!ok) break;
+          tc_commit(&S.empty[stage]);
+          if (++stage == D_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&S.acc_full);
+        acc_phase ^= 1u;
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      if (issued) {
+        // drain: all MMAs of this thread complete before TMEM is freed
+        tc_commit(&S.drain);
+        volatile int no_abort = 0;
+        mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
+      }
+    }
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------------------------------------ scale warps
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int slot = 0, sfb = 0;
+    uint32_t slot_phase = 0, sf_phase = 0;
+    bool ok = true;
+    DIter it;
+    it.start(blockIdx.x, gridDim.x, total, KD, n_tiles, tiles_prefix, s_off, p);
+    while (it.valid() && ok) {
+      const int nrb = min(BN / 128, rb_per_expert - it.tl.nt * (BN / 128));
+      const int nch = min(Q_CH, KT - Q_CH * it.kd);
+      if (!mbar_wait(&S.sfdata[slot], slot_phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
+      const uint8_t* sSFB = sSFA + Q_SFA_BYTES;
+      for (int c = 0; c < nch; ++c) {
+        const int ks = min(4, KSTEPS - 4 * (Q_CH * it.kd + c));
+        // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
+        uint32_t ra[16];
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (st < ks) v = lds128(sSFA + (4 * c + st) * SF_ATOM + lane * 16);
+          ra[4 * st] = v.x; ra[4 * st + 1] = v.y; ra[4 * st + 2] = v.z; ra[4 * st + 3] = v.w;
+        }
+        uint32_t rbv[2][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          // k-steps 2h, 2h+1: columns 8s + 4rb of the B region
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int st = 2 * h + j;
+#pragma unroll
+            for (int rb = 0; rb < 2; ++rb) {
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (st < ks && rb < nrb)
+                v = lds128(sSFB + (rb * 4 * Q_CH + 4 * c + st) * SF_ATOM + lane * 16);
+              const int cc = 8 * j + 4 * rb;
+              rbv[h][cc] = v.x; rbv[h][cc + 1] = v.y; rbv[h][cc + 2] = v.z; rbv[h][cc + 3] = v.w;
+            }
+          }
+        }
+        if (c == nch - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.sfread[slot]);
+        }
+        if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag)) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint32_t col = tmem + lane_base + SF_COL0 + sfb * SF_COLS;
+        tmem_st_16cols(col, ra);
+        tmem_st_16cols(col + 16, rbv[0]);
+        tmem_st_16cols(col + 32, rbv[1]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.sf_full[sfb]);
+        if (++sfb == NSF) { sfb = 0; sf_phase ^= 1u; }
+      }
+      if (++slot == D_SLOTS) { slot = 0; slot_phase ^= 1u; }
+      it.advance(p);
+    }
+    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;                 // TMEM lanes this warp may access
+    const int cb = (warp - EPI_WARP0) >> 2;       // accumulator columns [64 cb, 64 cb + 64)
+    const int r_in_tile = quarter * 32 + lane;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile(t, n_tiles, tiles_prefix, s_off, p);
+      const bool valid = r_in_tile < tl.rows;
+      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
+      float scale = 0.0f;
+      if (valid) scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
+      if (!mbar_wait(&S.acc_full, acc_phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      acc_phase ^= 1u;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * EPI_COLS;
+      epilogue_slice(p, tbase, valid, row, tl.nt * BN + cb * EPI_COLS, scale,
+                     [&] { mbar_arrive(&S.acc_empty); });
+    }
+    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
 }  // namespace gemm
 
 // ---------------------------------------------------------------- host side
@@ -879,7 +1602,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 namespace {
 
 std::atomic<uint64_t> g_budget_ns{0};
-std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel
+std::atomic<int> g_gemm_variant{0};  // 0 auto, 1 single-CTA, 2 CTA-pair, 4 pair two-chunk, 5 single two-chunk
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -908,6 +1631,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same operand as 3-D: {128 bytes of a K chunk, rows, K / 128 chunks} with
+// strides {row pitch, 128 bytes}; a box of 2 chunks lands as two consecutive
+// 128-byte-swizzled chunk tiles. Only for K a multiple of 256, so that no
+// chunk runs past the end of a row.
+bool make_map3(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
+               uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(gemm::BK_BYTES), rows, row_bytes / gemm::BK_BYTES};
+  cuuint64_t strides[2] = {row_bytes, static_cast<cuuint64_t>(gemm::BK_BYTES)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(gemm::BK_BYTES), box_rows,
+                       static_cast<cuuint32_t>(gemm::Q_CH)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 uint64_t wait_budget_ns() {
@@ -922,7 +1663,7 @@ using namespace minite;
 extern "C" void minite_set_wait_budget_ns(uint64_t ns) { g_budget_ns.store(ns); }
 
 extern "C" void minite_set_gemm_variant(int variant) {
-  g_gemm_variant.store(variant == 1 || variant == 2 ? variant : 0);
+  g_gemm_variant.store(variant >= 1 && variant <= 5 && variant != 3 ? variant : 0);
 }
 
 extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
@@ -945,12 +1686,29 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
       !aligned(b_sf, 16) || !aligned(out, 32))
     return MINITE_ERR_INVALID_ARG;
   // automatic choice: the single-CTA kernel (measured faster on every shape so far)
+  // automatic choice: the single-CTA kernel with two-chunk stages where it
+  // applies (measured fastest on the MoE shapes), else the single-CTA kernel
   int variant = g_gemm_variant.load();
-  if (variant == 0) variant = 1;
+  if (variant == 0) variant = 5;
+  const size_t q_smem = 1024 + Q_STAGES * Q_STAGE_BYTES + Q_SLOTS * Q_SLOT_BYTES + sizeof(QSmem) +
+                        3 * (E + 1) * sizeof(int32_t);
+  const size_t d_smem = 1024 + D_STAGES * D_STAGE_BYTES + D_SLOTS * Q_SLOT_BYTES + sizeof(DSmem) +
+                        2 * (E + 1) * sizeof(int32_t);
+  // the two-chunk kernels read whole 128-byte chunks of every row
+  if (variant == 4 && (K % 256 != 0 || q_smem > 232448)) variant = 1;
+  if (variant == 5 && (K % 256 != 0 || d_smem > 232448)) variant = 1;
   CUtensorMap ta, tb;
-  const uint32_t b_box = variant == 2 ? 128u : static_cast<uint32_t>(BN);
-  if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, N * E, b_box))
-    return MINITE_ERR_CUDA;
+  if (variant == 4) {
+    if (!make_map3(&ta, a_codes, K / 2, M_total, 128) || !make_map3(&tb, b_codes, K / 2, N * E, 128))
+      return MINITE_ERR_CUDA;
+  } else if (variant == 5) {
+    if (!make_map3(&ta, a_codes, K / 2, M_total, BM) || !make_map3(&tb, b_codes, K / 2, N * E, BN))
+      return MINITE_ERR_CUDA;
+  } else {
+    const uint32_t b_box = variant == 2 ? 128u : static_cast<uint32_t>(BN);
+    if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, N * E, b_box))
+      return MINITE_ERR_CUDA;
+  }
   Params p;
   p.a_g = a_g;
   p.b_g = b_g;
@@ -982,6 +1740,44 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     int grid = num_sms();
     if (max_tiles < grid) grid = static_cast<int>(max_tiles);
     grouped_gemm_kernel<<<grid, NUM_THREADS, smem, s>>>(ta, tb, p);
+  } else if (variant == 5) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+      attr_err = cudaFuncSetAttribute(grouped_gemm_dc_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    });
+    if (attr_err != cudaSuccess) return MINITE_ERR_CUDA;
+    const int64_t max_tiles = (M_total / BM + E) * n_tiles;
+    int grid = num_sms();
+    if (max_tiles < grid) grid = static_cast<int>(max_tiles);
+    grouped_gemm_dc_kernel<<<grid, Q_THREADS, d_smem, s>>>(ta, tb, p);
+  } else if (variant == 4) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+      attr_err = cudaFuncSetAttribute(grouped_gemm_pair2_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    });
+    if (attr_err != cudaSuccess) return MINITE_ERR_CUDA;
+    // one CTA per SM in clusters of two, never more pairs than pair tiles
+    const int64_t max_pairs = (M_total / 256 + E) * n_tiles;
+    int pairs = num_sms() / 2;
+    if (max_pairs < pairs) pairs = static_cast<int>(max_pairs);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(Q_THREADS);
+    cfg.dynamicSmemBytes = q_smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair2_kernel, ta, tb, p) != cudaSuccess)
+      return MINITE_ERR_CUDA;
   } else {
     const size_t smem = 1024 + P_STAGES * P_STAGE_BYTES + P_SLOTS * P_SLOT_BYTES + sizeof(PSmem) +
                         3 * (E + 1) * sizeof(int32_t);

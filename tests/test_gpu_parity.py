@@ -36,7 +36,7 @@ def _automatic_gemm_variant():
     M.minite_set_gemm_variant(0)
 
 
-VARIANTS = [1, 2]  # single-CTA and CTA-pair grouped-GEMM kernels
+VARIANTS = [1, 2, 4, 5]  # single-CTA, CTA-pair, and both with two-chunk stages
 
 
 def _status():
@@ -268,6 +268,7 @@ def check_gemm(c, out, rows=None):
 GEMM_CASES = [
     ([5], 32, 64), ([128], 128, 256), ([1, 0, 300, 17], 160, 320), ([0, 0, 0, 9], 384, 512),
     ([129, 127], 256, 2048), ([3, 200, 1, 0, 64], 96, 768), ([257], 128, 128), ([40] * 9, 64, 192),
+    ([70, 300], 256, 1280),
 ]
 
 
@@ -371,14 +372,15 @@ def test_grouped_gemm_batch_invariance(variant):
 
 
 def test_grouped_gemm_kernels_agree_bitwise():
-    """The single-CTA and CTA-pair kernels use the same K order per row, so
-    their outputs are identical."""
+    """All grouped-GEMM kernels use the same K order per row, so their
+    outputs are identical."""
     c = make_gemm_case([300, 0, 1, 700, 129], 384, 1024, seed=31)
     outs = []
     for v in VARIANTS:
         M.minite_set_gemm_variant(v)
         outs.append(run_gemm(c, torch.float32).cpu().numpy().view(np.uint32))
-    assert np.array_equal(outs[0], outs[1])
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
