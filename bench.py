@@ -127,8 +127,8 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rates
 class Step:
     """All device buffers of one step; ``run`` enqueues the whole path."""
 
-    STAGES = ["wq_gate_up", "wq_down", "permute_x", "gemm_gate_up", "swiglu", "gemm_down",
-              "combine", "requant_down_N", "permute_dy", "gemm_dgrad"]
+    STAGES = ["wq_gate_up", "wq_down_both", "permute_x", "gemm_gate_up", "swiglu", "gemm_down",
+              "combine", "permute_dy", "gemm_dgrad"]
 
     def __init__(self, d, dev):
         import torch
@@ -185,8 +185,9 @@ class Step:
         M.minite_quantize_nvfp4(self.wgu_bf, M.SCALE_PER_GROUP, M.ALONG_COLS, self.wgu["codes"],
                                 self.wgu["sf"], self.wgu["g"], None, self.ws_q, self.status, s)
         mark(1)
-        M.minite_quantize_nvfp4(self.wd_bf, M.SCALE_PER_GROUP, M.ALONG_COLS, self.wd["codes"],
-                                self.wd["sf"], self.wd["g"], None, self.ws_q, self.status, s)
+        # W_down in both orientations (forward K-major and the dgrad copy along N)
+        M.minite_quantize_nvfp4_dual(self.wd_bf, self.wd["codes"], self.wd["sf"], self.wdT["codes"],
+                                     self.wdT["sf"], self.wd["g"], self.ws_q, self.status, s)
         mark(2)
         mlp = self.mlp
         mlp.permute_quant(self.x, self.ids, self.w, s)
@@ -205,18 +206,17 @@ class Step:
         mark(6)
         M.minite_moe_combine(mlp.down, mlp.dest_row, mlp.y, self.status, s)
         mark(7)
-        M.minite_quantize_nvfp4(self.wd_bf, M.SCALE_PER_GROUP, M.ALONG_ROWS, self.wdT["codes"],
-                                self.wdT["sf"], self.wdT["g"], self.wd["g"], None, self.status, s)
-        mark(8)
         self.bwd.permute_quant(self.dy, self.ids, None, s)
-        mark(9)
+        mark(8)
         b = self.bwd
         M.minite_grouped_gemm_nvfp4(b.a_codes, b.a_sf, b.a_g, self.wdT["codes"], self.wdT["sf"],
-                                    self.wdT["g"], b.offsets, b.sf_offsets, self.dh, self.status, s)
-        mark(10)
+                                    self.wd["g"], b.offsets, b.sf_offsets, self.dh, self.status, s)
+        mark(9)
 
-    # kernels launched per step by the library (memsets not counted)
-    LAUNCHES = 2 + 2 + 3 + 1 + 1 + 1 + 1 + 1 + 3 + 1
+    # kernels launched per step by the library (memsets not counted): weight
+    # quantization 2 + 2, permutation 4, GEMM 1, SwiGLU 1, GEMM 1, combine 1,
+    # permutation of dY 4, GEMM 1
+    LAUNCHES = 2 + 2 + 4 + 1 + 1 + 1 + 1 + 4 + 1
 
     def flops(self):
         Mu = int(self.mlp.offsets[-1].item())
@@ -231,11 +231,10 @@ class Step:
         sfb = lambda r, c: r * c / 16  # noqa: E731  one scale byte per 16 values
         return dict(
             wq_gate_up=E * 2 * I * H * 2 + E * 2 * I * H / 2 + sfb(E * 2 * I, H),
-            wq_down=E * H * I * 2 + E * H * I / 2 + sfb(E * H, I),
+            wq_down_both=E * H * I * 2 + E * H * I + sfb(E * H, I) + sfb(E * I, H),
             permute_x=T * H * 2 + T * k * 8 + Mu * (H / 2 + H / 16 + 4 + 12),
             swiglu=Mu * 2 * I * 2 + Mu * (I / 2 + I / 16 + 4),
             combine=Mu * H * 2 + T * H * 2 + T * k * 4,
-            requant_down_N=E * H * I * 2 + E * H * I / 2 + sfb(E * I, H),
             permute_dy=T * H * 2 + T * k * 4 + Mu * (H / 2 + H / 16 + 4 + 8),
         )
 

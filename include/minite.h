@@ -107,6 +107,35 @@ int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows, int64_t c
                           minite_stream_t stream);
 
 /*
+ * minite_quantize_nvfp4_dual -- per-group (weight) NVFP4 quantization in both
+ * orientations from one read of x: the forward copy with blocks of 16 along
+ * cols and the dgrad copy (x[g] transposed) with blocks of 16 along rows,
+ * both with the group's global scale g = 2688 / amax(x[g]).
+ *
+ * Cites: the weight recipe of "Follow the numerical execution path"
+ * (per-tensor FP32 global scale, E4M3 block scales) and the fused scale
+ * layout of "Two complementary interventions". The pages do not describe a
+ * two-orientation pass; the results are exactly those of
+ * minite_quantize_nvfp4(PER_GROUP, ALONG_COLS) followed by
+ * minite_quantize_nvfp4(PER_GROUP, ALONG_ROWS, gscale_in = its g).
+ *
+ * x:          device, BF16 [groups, rows, cols], 16-byte aligned.
+ * codes_k:    device, uint8 [groups, rows, cols/2], 8-byte aligned.
+ * sf_k:       device, uint8 [groups, roundup(rows,128) * roundup(cols/16,4)].
+ * codes_n:    device, uint8 [groups, cols, rows/2], 8-byte aligned.
+ * sf_n:       device, uint8 [groups, roundup(cols,128) * roundup(rows/16,4)].
+ * gscale_out: device float [groups].
+ * workspace:  device, >= minite_workspace_bytes(MINITE_OP_QUANTIZE, groups,
+ *             0, 0, 0) bytes; contents on entry are ignored.
+ * Shape rules: rows % 16 == 0, cols % 16 == 0, rows, cols < 2^30,
+ * groups * rows * cols < 2^40.
+ */
+int minite_quantize_nvfp4_dual(const void* x, int64_t groups, int64_t rows, int64_t cols,
+                               uint8_t* codes_k, uint8_t* sf_k, uint8_t* codes_n,
+                               uint8_t* sf_n, float* gscale_out, void* workspace,
+                               size_t ws_bytes, int32_t* status, minite_stream_t stream);
+
+/*
  * minite_moe_permute_quant -- MoE permutation fused with per-token amax,
  * NVFP4 quantization and the SF swizzle, in one pass over x.
  *

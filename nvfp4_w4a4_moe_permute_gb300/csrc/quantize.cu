@@ -242,6 +242,168 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(
   if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) g_out[grp] = g;
 }
 
+// Both orientations of per-group quantization from one read of each weight:
+// 64 x 128 tiles of x[grp] are staged in shared memory (two buffers, the next
+// tile's per-thread asynchronous copies in flight while the current one is
+// quantized). Warps 0-3 take one tile column each (its 4 blocks along the
+// rows: 32 contiguous code bytes and 4 contiguous scale bytes of the
+// transposed copy); warps 4-7 take half a tile row each (4 blocks along the
+// columns: 32 contiguous code bytes and 4 contiguous scale bytes of the
+// forward copy). Both copies use the group's global scale.
+constexpr int kDR = 64, kDC = 128, kDPitch = kDC + 8;  // pitch in BF16, rows 16-byte aligned
+constexpr int kDTile = kDR * kDPitch;
+
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(256) quantize_dual_kernel(
+    const uint16_t* __restrict__ x, int64_t groups, int rows, int cols,
+    const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes_k,
+    uint8_t* __restrict__ sf_k, uint8_t* __restrict__ codes_n, uint8_t* __restrict__ sf_n,
+    float* __restrict__ g_out) {
+  __shared__ __align__(16) uint16_t tiles[2][kDTile];
+  const int t = threadIdx.x;
+  const int tr = (rows + kDR - 1) / kDR, tc = (cols + kDC - 1) / kDC;
+  const int64_t ntiles = groups * tr * tc;
+  const int nbk = cols / 16, nbn = rows / 16;              // blocks per quantized row
+  const int kck = (nbk + 3) & ~3, kcn = (nbn + 3) & ~3;     // SF columns
+  const int64_t rows_pad = (rows + 127) & ~127, cols_pad = (cols + 127) & ~127;
+  const int64_t sfk_group = rows_pad * kck, sfn_group = cols_pad * kcn;
+  // 32-byte code stores where every destination row starts 32-byte aligned
+  const bool v8k = (cols / 2) % 32 == 0 && (reinterpret_cast<uintptr_t>(codes_k) & 31) == 0;
+  const bool v8n = (rows / 2) % 32 == 0 && (reinterpret_cast<uintptr_t>(codes_n) & 31) == 0;
+
+  auto tile_pos = [&](int64_t ti, int64_t& grp, int& r0, int& c0) {
+    grp = ti / (tr * tc);
+    const int rem = static_cast<int>(ti - grp * tr * tc);
+    r0 = (rem / tc) * kDR;
+    c0 = (rem % tc) * kDC;
+  };
+  auto fetch = [&](int64_t ti, uint16_t* buf) {
+    if (ti < ntiles) {
+      int64_t grp;
+      int r0, c0;
+      tile_pos(ti, grp, r0, c0);
+      const uint16_t* xg = x + grp * static_cast<int64_t>(rows) * cols;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = t + 256 * i;  // 16-byte piece q of the tile: row q / 16, piece q % 16
+        const int lr = q >> 4, seg = q & 15;
+        const bool valid = r0 + lr < rows && c0 + 8 * seg < cols;
+        const uint16_t* src = valid ? xg + static_cast<int64_t>(r0 + lr) * cols + c0 + 8 * seg : x;
+        cp_async16_zfill(buf + lr * kDPitch + 8 * seg, src, valid);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+  int64_t ti = blockIdx.x;
+  fetch(ti, tiles[0]);
+  int cur = 0;
+  int64_t gcur = -1;
+  float g = 1.0f, tk = 1.0f;
+  for (; ti < ntiles; ti += gridDim.x, cur ^= 1) {
+    fetch(ti + gridDim.x, tiles[cur ^ 1]);
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+    int64_t grp;
+    int r0, c0;
+    tile_pos(ti, grp, r0, c0);
+    if (grp != gcur) {  // block-uniform
+      gcur = grp;
+      g = global_scale(__uint_as_float(amax_bits[grp]));
+      tk = enc_table_entry(g);
+    }
+    const uint16_t* tile = tiles[cur];
+    if (t < 128) {
+      // ---- one tile column, 4 blocks along the rows (transposed copy)
+      const int c = c0 + t;
+      uint2 code[4];
+      uint32_t sfw = 0;
+#pragma unroll
+      for (int rb = 0; rb < 4; ++rb) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j] = __uint_as_float(static_cast<uint32_t>(tile[(16 * rb + j) * kDPitch + t]) << 16);
+        const bool valid = c < cols && r0 / 16 + rb < nbn;
+        const QBlock q = quant_block(v, amax_f32x16(v), g, tk, valid);
+        code[rb] = q.codes;
+        sfw |= q.sf << (8 * rb);
+      }
+      if (c < cols) {
+        const int gr = r0 / 16;  // multiple of 4
+        uint8_t* dst = codes_n + (grp * cols + c) * static_cast<int64_t>(rows / 2) + 8 * gr;
+        if (v8n && gr + 4 <= nbn) {
+          st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
+                       code[3].x, code[3].y);
+        } else {
+#pragma unroll
+          for (int rb = 0; rb < 4; ++rb)
+            if (gr + rb < nbn) st_u64(dst + 8 * rb, code[rb]);
+        }
+        *reinterpret_cast<uint32_t*>(sf_n + grp * sfn_group + sf_offset(c, gr, kcn)) = sfw;
+      }
+    } else {
+      // ---- half a tile row, 4 blocks along the columns (forward copy)
+      const int u = t - 128;
+      const int lr = u >> 1, half = u & 1;
+      const int r = r0 + lr;
+      uint2 code[4];
+      uint32_t sfw = 0;
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(tile + lr * kDPitch + 64 * half + 16 * cb);
+        const uint4 a0 = src[0], a1 = src[1];
+        const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float v[16];
+        unpack_bf16x16(w, v);
+        const bool valid = r < rows && c0 / 16 + 4 * half + cb < nbk;
+        const QBlock q = quant_block(v, amax_bf16x16(w), g, tk, valid);
+        code[cb] = q.codes;
+        sfw |= q.sf << (8 * cb);
+      }
+      const int gc = c0 / 16 + 4 * half;  // multiple of 4
+      if (r < rows && gc < nbk) {
+        uint8_t* dst = codes_k + (grp * rows + r) * static_cast<int64_t>(cols / 2) + 8 * gc;
+        if (v8k && gc + 4 <= nbk) {
+          st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
+                       code[3].x, code[3].y);
+        } else {
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb)
+            if (gc + cb < nbk) st_u64(dst + 8 * cb, code[cb]);
+        }
+        *reinterpret_cast<uint32_t*>(sf_k + grp * sfk_group + sf_offset(r, gc, kck)) = sfw;
+      }
+    }
+    __syncthreads();  // the buffer is refilled two tiles from now
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+  // zero the scale bytes of the padding rows of both copies, and publish g
+  const int64_t gt = blockIdx.x * (int64_t)blockDim.x + t;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t pk = rows_pad - rows, pn = cols_pad - cols;
+  for (int64_t i = gt; i < groups * pk * (kck / 4); i += nthreads) {
+    const int64_t grp = i / (pk * (kck / 4));
+    const int64_t rem = i - grp * pk * (kck / 4);
+    *reinterpret_cast<uint32_t*>(sf_k + grp * sfk_group +
+                                 sf_offset(rows + rem / (kck / 4), 4 * (rem % (kck / 4)), kck)) = 0u;
+  }
+  for (int64_t i = gt; i < groups * pn * (kcn / 4); i += nthreads) {
+    const int64_t grp = i / (pn * (kcn / 4));
+    const int64_t rem = i - grp * pn * (kcn / 4);
+    *reinterpret_cast<uint32_t*>(sf_n + grp * sfn_group +
+                                 sf_offset(cols + rem / (kcn / 4), 4 * (rem % (kcn / 4)), kcn)) = 0u;
+  }
+  if (gt < groups) g_out[gt] = global_scale(__uint_as_float(amax_bits[gt]));
+}
+
 template <int NCH>
 static void launch_token_rows(const uint16_t* x, int64_t groups, int64_t rows, int cols, bool a32,
                               uint8_t* codes, uint8_t* sf, float* g_out, cudaStream_t s) {
@@ -278,9 +440,56 @@ static void launch_group_blocks(const uint16_t* x, int64_t groups, int64_t rows,
         x, groups, rows, nb, magic, g_in, amax, codes, sf, g_out);
 }
 
+// Per-group |x| maxima into amax (zeroed first), one grid over all groups.
+static int launch_group_amax(const uint16_t* x, int64_t groups, int64_t per_group,
+                             uint32_t* amax, cudaStream_t s) {
+  if (cudaMemsetAsync(amax, 0, groups * sizeof(uint32_t), s) != cudaSuccess)
+    return MINITE_ERR_CUDA;
+  int64_t bx = (per_group / 8 + 255) / 256;
+  const int64_t want = (num_sms() * 8 + groups - 1) / groups;
+  if (bx > want) bx = want;
+  if (bx < 1) bx = 1;
+  dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(groups));
+  group_amax_kernel<<<grid, 256, 0, s>>>(x, per_group, amax);
+  return MINITE_OK;
+}
+
 }  // namespace minite
 
 using namespace minite;
+
+extern "C" int minite_quantize_nvfp4_dual(const void* x, int64_t groups, int64_t rows,
+                                          int64_t cols, uint8_t* codes_k, uint8_t* sf_k,
+                                          uint8_t* codes_n, uint8_t* sf_n, float* gscale_out,
+                                          void* workspace, size_t ws_bytes, int32_t* status,
+                                          minite_stream_t stream) {
+  (void)status;
+  if (!x || !codes_k || !sf_k || !codes_n || !sf_n || !gscale_out || !workspace)
+    return MINITE_ERR_INVALID_ARG;
+  if (groups <= 0 || rows <= 0 || cols <= 0 || rows % 16 != 0 || cols % 16 != 0)
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (rows >= (int64_t(1) << 30) || cols >= (int64_t(1) << 30) ||
+      groups * rows * cols >= (int64_t(1) << 40))
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(codes_k, 8) || !aligned(codes_n, 8) || !aligned(sf_k, 4) ||
+      !aligned(sf_n, 4))
+    return MINITE_ERR_INVALID_ARG;
+  if (ws_bytes < minite_workspace_bytes(MINITE_OP_QUANTIZE, groups, 0, 0, 0))
+    return MINITE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  uint32_t* amax = static_cast<uint32_t*>(workspace);
+  const int rc = launch_group_amax(xb, groups, rows * cols, amax, s);
+  if (rc != MINITE_OK) return rc;
+  const int64_t tiles = groups * ((rows + kDR - 1) / kDR) * ((cols + kDC - 1) / kDC);
+  int64_t blocks = static_cast<int64_t>(num_sms()) * 6;
+  if (blocks > tiles) blocks = tiles;
+  if (blocks * 256 < groups) blocks = (groups + 255) / 256;
+  quantize_dual_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      xb, groups, static_cast<int>(rows), static_cast<int>(cols), amax, codes_k, sf_k, codes_n,
+      sf_n, gscale_out);
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
 
 extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows, int64_t cols,
                                      int scale_mode, int orientation, const float* gscale_in,
@@ -311,15 +520,8 @@ extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows
     if (!workspace || ws_bytes < minite_workspace_bytes(MINITE_OP_QUANTIZE, groups, 0, 0, 0))
       return MINITE_ERR_INVALID_ARG;
     amax = static_cast<uint32_t*>(workspace);
-    if (cudaMemsetAsync(amax, 0, groups * sizeof(uint32_t), s) != cudaSuccess)
-      return MINITE_ERR_CUDA;
-    const int64_t per = rows * cols;
-    int64_t bx = (per / 8 + 255) / 256;
-    const int64_t want = (num_sms() * 8 + groups - 1) / groups;
-    if (bx > want) bx = want;
-    if (bx < 1) bx = 1;
-    dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(groups));
-    group_amax_kernel<<<grid, 256, 0, s>>>(xb, per, amax);
+    const int rc = launch_group_amax(xb, groups, rows * cols, amax, s);
+    if (rc != MINITE_OK) return rc;
   }
 
   if (orientation == MINITE_ALONG_COLS) {

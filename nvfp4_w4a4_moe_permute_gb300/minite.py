@@ -27,7 +27,7 @@ EXPORTS = [
     "minite_swiglu_weighted_quant", "minite_moe_combine", "minite_workspace_bytes",
     "minite_status_string", "minite_version", "minite_test_convert",
     "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc", "minite_set_gemm_variant",
-    "minite_test_div6_exhaustive",
+    "minite_test_div6_exhaustive", "minite_quantize_nvfp4_dual",
 ]
 
 
@@ -50,6 +50,8 @@ def load(path: str | None = None):
     lib = ctypes.CDLL(path)
     sig = {
         "minite_quantize_nvfp4": [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp],
+        "minite_quantize_nvfp4_dual": [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                                       _vp],
         "minite_moe_permute_quant": [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                      _vp, _vp, _vp, _vp, _sz, _vp, _vp],
         "minite_moe_permute_quant_noalloc": [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp,
@@ -127,6 +129,38 @@ def minite_quantize_nvfp4(x, scale_mode, orientation, codes, sf, gscale_out, gsc
                                       _p(codes), _p(sf), _p(gscale_out), _p(workspace), ws_bytes,
                                       _p(status), _s(stream))
     _check(rc, "minite_quantize_nvfp4")
+
+
+def minite_quantize_nvfp4_dual(x, codes_k, sf_k, codes_n, sf_n, gscale_out, workspace,
+                               status=None, stream=None):
+    """x: bf16 [groups, rows, cols] (or [rows, cols] = one group); per-group scales."""
+    g, r, c = (1,) + tuple(x.shape) if x.dim() == 2 else tuple(x.shape)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().minite_quantize_nvfp4_dual(_p(x), g, r, c, _p(codes_k), _p(sf_k), _p(codes_n),
+                                           _p(sf_n), _p(gscale_out), _p(workspace), ws_bytes,
+                                           _p(status), _s(stream))
+    _check(rc, "minite_quantize_nvfp4_dual")
+
+
+def quantize_dual(x, stream=None):
+    """Weight x ([rows, cols] or [groups, rows, cols]) quantized per group in both
+    orientations; returns (forward dict, transposed dict) like quantize()."""
+    dev = x.device
+    g3 = x if x.dim() == 3 else x.unsqueeze(0)
+    G, R, C = g3.shape
+    fk = dict(codes=torch.empty((G, R, C // 2), dtype=torch.uint8, device=dev),
+              sf=torch.empty((G, sf_bytes((R + 127) // 128 * 128, C)), dtype=torch.uint8, device=dev))
+    fn = dict(codes=torch.empty((G, C, R // 2), dtype=torch.uint8, device=dev),
+              sf=torch.empty((G, sf_bytes((C + 127) // 128 * 128, R)), dtype=torch.uint8, device=dev))
+    g = torch.empty((G,), dtype=torch.float32, device=dev)
+    ws = torch.empty(minite_workspace_bytes(OP_QUANTIZE, G), dtype=torch.uint8, device=dev)
+    minite_quantize_nvfp4_dual(g3, fk["codes"], fk["sf"], fn["codes"], fn["sf"], g, ws, stream=stream)
+    fk["g"] = g
+    fn["g"] = g
+    if x.dim() == 2:
+        for d in (fk, fn):
+            d["codes"], d["sf"] = d["codes"][0], d["sf"][0]
+    return fk, fn
 
 
 def minite_moe_permute_quant(x, topk_ids, topk_w, E, codes, sf, row_g, expert_offsets,

@@ -70,6 +70,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.minite_quantize_nvfp4(fake, 1, 16, 64, 0, 1, None, fake, fake, fake, None, 0, None, None) == 2
     # per-group without gscale_in needs a workspace
     assert lib.minite_quantize_nvfp4(fake, 1, 16, 64, 1, 0, None, fake, fake, fake, None, 0, None, None) == 1
+    # two-orientation weight quantization: rows not a multiple of 16, no workspace
+    assert lib.minite_quantize_nvfp4_dual(fake, 1, 24, 64, fake, fake, fake, fake, fake, fake, 512,
+                                          None, None) == 2
+    assert lib.minite_quantize_nvfp4_dual(fake, 1, 32, 64, fake, fake, fake, fake, fake, None, 0,
+                                          None, None) == 1
     # permute: H not a multiple of 64, too many experts, misaligned x
     args = [fake, fake, None, 16, 96, 4, 2] + [fake] * 7 + [None, fake, 1 << 20, None, None]
     assert lib.minite_moe_permute_quant(*args) == 2

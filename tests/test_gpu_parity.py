@@ -140,6 +140,24 @@ def test_quantize_weights_along_rows_bit_exact(E, R, C):
         assert np.array_equal(q["g"].cpu().numpy().view(np.uint32), g.view(np.uint32))
 
 
+@pytest.mark.parametrize("E,R,C", [(1, 64, 128), (2, 96, 80), (3, 2048, 768), (1, 48, 208),
+                                   (2, 144, 1536), (4, 16, 16)])
+def test_quantize_weights_both_orientations_in_one_pass_bit_exact(E, R, C):
+    rng = np.random.default_rng(E * 77 + R + C)
+    w = O.f32_to_bf16((rng.standard_normal((E, R, C)) * 0.02).astype(np.float32))
+    w[0, 0, :] = 0  # a zero row in the forward copy, a zero element run in the transposed one
+    ck, _, swk, gk = O.quantize_weights(w)
+    cn, _, swn, gn = O.quantize_weights(w, along_rows=True)
+    fk, fn = M.quantize_dual(bf16_dev(w))
+    torch.cuda.synchronize()
+    assert np.array_equal(fk["codes"].cpu().numpy(), ck)
+    assert np.array_equal(fk["sf"].cpu().numpy(), swk)
+    assert np.array_equal(fn["codes"].cpu().numpy(), cn)
+    assert np.array_equal(fn["sf"].cpu().numpy(), swn)
+    assert np.array_equal(fk["g"].cpu().numpy().view(np.uint32), gk.view(np.uint32))
+    assert np.array_equal(gk.view(np.uint32), gn.view(np.uint32))
+
+
 # --------------------------------------------------------------------- permute
 
 def run_permute(x_u16, ids, w, E):
