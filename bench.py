@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--gemm-variant", type=int, default=0,
                     help="grouped-GEMM kernel: 0 automatic, 1 single-CTA, 2 CTA pair")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches only (default: the step replayed as one CUDA graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--cpu-sample-experts", type=int, default=2)
@@ -291,12 +293,34 @@ def run_gpu(args):
         step.run(stream, ev[i])
     t1.record(stream)
     barrier()
+    ms_eager = t0.elapsed_time(t1)
+    # the same step captured once as a CUDA graph and replayed: no launch gaps
+    ms_graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap):
+            step.run(torch.cuda.current_stream(dev))
+        stream.wait_stream(cap)
+        for _ in range(args.warmup):
+            graph.replay()
+        barrier()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        barrier()
+        ms_graph = g0.elapsed_time(g1)
+        assert int(step.status.item()) == 0, f"device status {int(step.status.item())}"
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
+    ms = ms_graph if ms_graph is not None else ms_eager
     if world > 1:
-        tt = torch.tensor([ms], device=dev)
+        tt = torch.tensor([ms, ms_eager], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms, ms_eager = float(tt[0].item()), float(tt[1].item())
     ms_per_step = ms / args.steps
     stage_ms = {s: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j, s in enumerate(Step.STAGES)}
@@ -388,6 +412,7 @@ def run_gpu(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
+        "ms_per_step_eager": ms_eager / args.steps,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -398,6 +423,7 @@ def run_gpu(args):
                            " + gate_up GEMM + SwiGLU+quant + down GEMM + combine + permute+quant dY"
                            " + dgrad GEMM",
                    "l2": "inputs larger than L2 (each step streams ~5 GB)",
+                   "launch": "eager" if args.no_graph else "CUDA graph of the step, replayed",
                    "parallelism": f"replicas{world}"},
         "gemm_gate_up_tflops": achieved,
         "gemm_gate_up_frac_fp4_peak": achieved / fp4_peak,

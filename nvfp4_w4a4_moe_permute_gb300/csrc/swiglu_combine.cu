@@ -201,10 +201,7 @@ static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int 
                          const int32_t* off, const int32_t* sfoff, uint8_t* codes, uint8_t* sf,
                          float* row_g, int32_t* status, cudaStream_t s) {
   const size_t smem = kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
-  if (cudaFuncSetAttribute(swiglu_quant_kernel<LPR, NCH>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return MINITE_ERR_CUDA;
+  // table (32 KB) + offsets stay under the default 48 KB of dynamic shared memory
   constexpr int rows_per_cta = kSwThreads / 32 * (32 / LPR);
   int64_t blocks = (M + rows_per_cta - 1) / rows_per_cta;
   const int64_t cap = static_cast<int64_t>(num_sms());
