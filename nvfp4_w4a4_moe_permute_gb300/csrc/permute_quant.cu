@@ -35,20 +35,41 @@ struct PermWs {
   uint32_t* counter;  // scan completion counter
   int32_t* totals;    // [E]
   int32_t* table;     // [E][nchunks]
+  uint8_t* sfc;       // [T][kc] each token's scale bytes, token order (or null)
+  float* gtok;        // [T] each token's global scale (or null)
 };
 
-static size_t perm_ws_bytes(int64_t T, int E, int k) {
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Scratch of the ranking and scan (the histogram table).
+static size_t perm_ws_base_bytes(int64_t T, int E, int k) {
   const int64_t ct = permute_chunk_tokens(k);
   const int64_t nchunks = (T + ct - 1) / ct;
-  return 256 + static_cast<size_t>(E) * 4 + 256 + static_cast<size_t>(E) * nchunks * 4;
+  return 256 + align256(static_cast<size_t>(E) * 4) + align256(static_cast<size_t>(E) * nchunks * 4);
 }
 
-static PermWs perm_ws(void* ws, int E) {
+// Plus the token-order scale bytes and global scales that the scale gather
+// turns into the swizzled layout.
+static size_t perm_ws_bytes(int64_t T, int64_t H, int E, int k) {
+  const size_t kc = static_cast<size_t>(((H / 16) + 3) & ~int64_t(3));
+  return perm_ws_base_bytes(T, E, k) + align256(static_cast<size_t>(T) * kc) +
+         align256(static_cast<size_t>(T) * 4);
+}
+
+static PermWs perm_ws(void* ws, int64_t T, int64_t H, int E, int k, bool compact) {
   PermWs w;
   char* p = static_cast<char*>(ws);
   w.counter = reinterpret_cast<uint32_t*>(p);
   w.totals = reinterpret_cast<int32_t*>(p + 256);
-  w.table = reinterpret_cast<int32_t*>(p + 256 + ((static_cast<size_t>(E) * 4 + 255) & ~size_t(255)));
+  w.table = reinterpret_cast<int32_t*>(p + 256 + align256(static_cast<size_t>(E) * 4));
+  w.sfc = nullptr;
+  w.gtok = nullptr;
+  if (compact) {
+    const size_t kc = static_cast<size_t>(((H / 16) + 3) & ~int64_t(3));
+    char* q = p + perm_ws_base_bytes(T, E, k);
+    w.sfc = reinterpret_cast<uint8_t*>(q);
+    w.gtok = reinterpret_cast<float*>(q + align256(static_cast<size_t>(T) * kc));
+  }
   return w;
 }
 
@@ -197,7 +218,8 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
     const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int64_t T, int H, int E,
     int k, const int32_t* __restrict__ expert_offsets,
     const int32_t* __restrict__ sf_row_offsets, const int32_t* __restrict__ dest_row,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g) {
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
+    uint8_t* __restrict__ sfc, float* __restrict__ gtok) {
   extern __shared__ int32_t sm[];
   int32_t* s_off = sm;                 // [E+1]
   int32_t* s_sfoff = s_off + (E + 1);  // [E+1]
@@ -238,8 +260,18 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
     QBlock qb[NCH];
     quant_row_blocks<NCH>(w, am, nb, g, qb);
     const int dcur = dest, ecur = e;
+    const int64_t tcur = t;
     t += nwarps;
     if (t < T) fetch(t);
+    if (sfc) {
+      // scales once per token, in token order; the scale gather places them
+#pragma unroll
+      for (int jj = 0; jj < NCH; ++jj) {
+        const int cc = 32 * jj + lane;
+        if (cc < kc) sfc[tcur * kc + cc] = static_cast<uint8_t>(qb[jj].sf);
+      }
+      if (lane == 0) gtok[tcur] = g;
+    }
     for (int j = 0; j < k; ++j) {
       const int d = __shfl_sync(0xffffffffu, dcur, j);
       if (d < 0) continue;  // warp-uniform
@@ -251,11 +283,12 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
       for (int jj = 0; jj < NCH; ++jj) {
         const int cc = 32 * jj + lane;
         if (cc < nb) st_u64(crow + 8 * cc, qb[jj].codes);
-        if (cc < kc) srow[cpart[jj]] = static_cast<uint8_t>(qb[jj].sf);
+        if (!sfc && cc < kc) srow[cpart[jj]] = static_cast<uint8_t>(qb[jj].sf);
       }
-      if (lane == 0) row_g[d] = g;
+      if (!sfc && lane == 0) row_g[d] = g;
     }
   }
+  if (sfc) return;  // the scale gather writes every scale row, padding included
 
   // zero the scale bytes of each expert's padding rows
   const int words = kc / 4;
@@ -269,21 +302,90 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
   }
 }
 
+// Scale gather: writes the swizzled scale layout one 128-row block (one row of
+// atoms, 128 x kc bytes) at a time, in order, from the token-order scales:
+// row r of an expert's region holds the scales of token perm_src[p] for its
+// permuted row p, or zeros past the expert's rows. Thread unit (line i of 32,
+// group of 4 atoms): reads 16 bytes of each of the rows i, i+32, i+64, i+96
+// and writes the 16-byte line i of each of the 4 atoms, so a warp writes
+// whole 512-byte atoms. Also row_g[p] = the token's g.
+__global__ void __launch_bounds__(kPermThreads) permute_sf_gather_kernel(
+    const uint8_t* __restrict__ sfc, const float* __restrict__ gtok,
+    const int32_t* __restrict__ perm_src, const int32_t* __restrict__ expert_offsets,
+    const int32_t* __restrict__ sf_row_offsets, int E, int kc, uint8_t* __restrict__ sf,
+    float* __restrict__ row_g) {
+  extern __shared__ int32_t sm[];
+  int32_t* s_off = sm;                 // [E+1]
+  int32_t* s_sfoff = s_off + (E + 1);  // [E+1]
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    s_off[i] = expert_offsets[i];
+    s_sfoff[i] = sf_row_offsets[i];
+  }
+  __syncthreads();
+  const int t = threadIdx.x;
+  const int natoms = kc / 4;
+  const int ngroups = (natoms + 3) / 4;
+  const int nblocks = s_sfoff[E] / 128;
+  for (int blk = blockIdx.x; blk < nblocks; blk += gridDim.x) {
+    // expert of the block: the last e with s_sfoff[e] <= 128 blk
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_sfoff[mid] <= 128 * blk) lo = mid; else hi = mid;
+    }
+    const int row0 = 128 * blk - s_sfoff[lo];  // local row of the block's first row
+    const int cnt = s_off[lo + 1] - s_off[lo];
+    const int p0 = s_off[lo] + row0;
+    if (t < 128 && row0 + t < cnt) row_g[p0 + t] = gtok[perm_src[p0 + t]];
+    for (int u = t; u < 32 * ngroups; u += blockDim.x) {
+      const int i = u & 31, ag = u >> 5;
+      int tok[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tok[q] = row0 + 32 * q + i < cnt ? perm_src[p0 + 32 * q + i] : -1;
+      uint32_t wv[4][4];  // [q][atom j]: 4 scale bytes of row 32q+i, columns 4(4ag+j) ..
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint8_t* src = sfc + static_cast<int64_t>(tok[q]) * kc + 16 * ag;
+        if (tok[q] >= 0 && 4 * ag + 4 <= natoms && kc % 16 == 0) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          wv[q][0] = v.x; wv[q][1] = v.y; wv[q][2] = v.z; wv[q][3] = v.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            wv[q][j] = (tok[q] >= 0 && 4 * ag + j < natoms)
+                           ? *reinterpret_cast<const uint32_t*>(src + 4 * j) : 0u;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int a = 4 * ag + j;
+        if (a < natoms)
+          *reinterpret_cast<uint4*>(sf + (static_cast<int64_t>(blk) * natoms + a) * 512 + 16 * i) =
+              make_uint4(wv[0][j], wv[1][j], wv[2][j], wv[3][j]);
+      }
+    }
+  }
+}
+
 }  // namespace minite
 
 using namespace minite;
 
 namespace minite {
-size_t permute_workspace_bytes(int64_t T, int32_t E, int32_t k) { return perm_ws_bytes(T, E, k); }
+size_t permute_workspace_bytes(int64_t T, int64_t H, int32_t E, int32_t k) {
+  return perm_ws_bytes(T, H, E, k);
+}
 }  // namespace minite
 
-extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
-                                        const float* topk_w, int64_t T, int64_t H, int32_t E,
-                                        int32_t k, uint8_t* codes, uint8_t* sf, float* row_g,
-                                        int32_t* expert_offsets, int32_t* sf_row_offsets,
-                                        int32_t* perm_src, int32_t* dest_row, float* perm_w,
-                                        void* workspace, size_t ws_bytes, int32_t* status,
-                                        minite_stream_t stream) {
+// compact = true: scales go to a token-order scratch and the scale gather
+// writes the swizzled layout with whole-atom stores (needs the full
+// workspace); false: each token's scales are scattered to its k rows.
+static int permute_quant_impl(const void* x, const int32_t* topk_ids, const float* topk_w,
+                              int64_t T, int64_t H, int32_t E, int32_t k, uint8_t* codes,
+                              uint8_t* sf, float* row_g, int32_t* expert_offsets,
+                              int32_t* sf_row_offsets, int32_t* perm_src, int32_t* dest_row,
+                              float* perm_w, void* workspace, size_t ws_bytes, bool compact,
+                              int32_t* status, minite_stream_t stream) {
   if (!x || !topk_ids || !codes || !sf || !row_g || !expert_offsets || !sf_row_offsets ||
       !perm_src || !dest_row || !workspace)
     return MINITE_ERR_INVALID_ARG;
@@ -294,11 +396,12 @@ extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
     return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(workspace, 256))
     return MINITE_ERR_INVALID_ARG;
-  if (ws_bytes < perm_ws_bytes(T, E, k)) return MINITE_ERR_INVALID_ARG;
+  if (ws_bytes < (compact ? perm_ws_bytes(T, H, E, k) : perm_ws_base_bytes(T, E, k)))
+    return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int ct = permute_chunk_tokens(k);
   const int nchunks = static_cast<int>((T + ct - 1) / ct);
-  PermWs w = perm_ws(workspace, E);
+  PermWs w = perm_ws(workspace, T, H, E, k, compact);
 
   const int rank_blocks = (nchunks + kRankWarps - 1) / kRankWarps;
   permute_rank_kernel<<<rank_blocks, 32 * kRankWarps, kRankWarps * E * sizeof(int32_t), s>>>(
@@ -322,14 +425,34 @@ extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
   case N:                                                                                  \
     permute_quant_kernel<N><<<static_cast<unsigned>(qblocks), kPermThreads, smem, s>>>(    \
         xb, topk_ids, T, h, E, k, expert_offsets, sf_row_offsets, dest_row, codes, sf,     \
-        row_g);                                                                            \
+        row_g, w.sfc, w.gtok);                                                             \
     break;
     MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
     MINITE_CASE(7) MINITE_CASE(8)
 #undef MINITE_CASE
     default: return MINITE_ERR_UNSUPPORTED_SHAPE;
   }
+  if (compact) {
+    const int kc = static_cast<int>(((H / 16) + 3) & ~int64_t(3));
+    int64_t gblocks = (T * k) / 128 + E;   // upper bound of the 128-row scale blocks
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+    if (gblocks > cap) gblocks = cap;
+    permute_sf_gather_kernel<<<static_cast<unsigned>(gblocks), kPermThreads, smem, s>>>(
+        w.sfc, w.gtok, perm_src, expert_offsets, sf_row_offsets, E, kc, sf, row_g);
+  }
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
+extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
+                                        const float* topk_w, int64_t T, int64_t H, int32_t E,
+                                        int32_t k, uint8_t* codes, uint8_t* sf, float* row_g,
+                                        int32_t* expert_offsets, int32_t* sf_row_offsets,
+                                        int32_t* perm_src, int32_t* dest_row, float* perm_w,
+                                        void* workspace, size_t ws_bytes, int32_t* status,
+                                        minite_stream_t stream) {
+  return permute_quant_impl(x, topk_ids, topk_w, T, H, E, k, codes, sf, row_g, expert_offsets,
+                            sf_row_offsets, perm_src, dest_row, perm_w, workspace, ws_bytes,
+                            true, status, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -351,8 +474,10 @@ extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
 // stream. All calls on a device share the array, so two calls whose work
 // overlaps on the GPU (different streams, no ordering between them) race
 // and must not be issued. The kernels rewrite every scratch word they read
-// on each call (histogram entries and the counter), so nothing left by an
-// earlier call needs clearing.
+// on each call (histogram entries, the counter and, when they fit, the
+// token-order scales), so nothing left by an earlier call needs clearing.
+// When the token-order scales do not fit, each token's scales are scattered
+// straight to its k rows instead (same results).
 // ---------------------------------------------------------------------------
 
 namespace {
@@ -368,8 +493,11 @@ extern "C" int minite_moe_permute_quant_noalloc(
     int32_t E, int32_t k, uint8_t* codes, uint8_t* sf, float* row_g, int32_t* expert_offsets,
     int32_t* sf_row_offsets, int32_t* perm_src, int32_t* dest_row, float* perm_w,
     int32_t* status, minite_stream_t stream) {
-  if (T < 1 || E < 1 || E > 1024 || k < 1 || k > 32) return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (perm_ws_bytes(T, E, k) > kStaticScratchBytes) return MINITE_ERR_SCRATCH_LIMIT;
+  if (T < 1 || E < 1 || E > 1024 || k < 1 || k > 32 || H < 64 || H > 4096)
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (perm_ws_base_bytes(T, E, k) > kStaticScratchBytes) return MINITE_ERR_SCRATCH_LIMIT;
+  // token-order scale staging when it fits in the array as well
+  const bool compact = perm_ws_bytes(T, H, E, k) <= kStaticScratchBytes;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MINITE_ERR_CUDA;
   void* scratch = nullptr;
@@ -383,7 +511,7 @@ extern "C" int minite_moe_permute_quant_noalloc(
     }
     scratch = g_scratch_addr[dev];
   }
-  return minite_moe_permute_quant(x, topk_ids, topk_w, T, H, E, k, codes, sf, row_g,
-                                  expert_offsets, sf_row_offsets, perm_src, dest_row, perm_w,
-                                  scratch, kStaticScratchBytes, status, stream);
+  return permute_quant_impl(x, topk_ids, topk_w, T, H, E, k, codes, sf, row_g, expert_offsets,
+                            sf_row_offsets, perm_src, dest_row, perm_w, scratch,
+                            kStaticScratchBytes, compact, status, stream);
 }

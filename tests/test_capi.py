@@ -50,6 +50,8 @@ def test_workspace_sizes(lib):
     a = M.minite_workspace_bytes(M.OP_PERMUTE_QUANT, 4096, 2048, 128, 8)
     b = M.minite_workspace_bytes(M.OP_PERMUTE_QUANT, 8192, 2048, 128, 8)
     assert 0 < a < b
+    # the token-order scale staging grows with H
+    assert M.minite_workspace_bytes(M.OP_PERMUTE_QUANT, 4096, 4096, 128, 8) > a
     assert M.minite_workspace_bytes(99, 1) == 0
 
 

@@ -76,6 +76,30 @@ def test_noalloc_permute_matches_workspace_entry_point_on_consecutive_calls():
         assert int(got["status"].item()) == 0
 
 
+def test_noalloc_scatters_scales_directly_when_token_order_staging_does_not_fit():
+    """T * (H/16 + 4) bytes of token-order scales exceed the 2 MiB array here,
+    so the allocation-free entry writes each token's scales straight to its
+    rows; the results must still equal the workspace entry point's."""
+    dev = torch.device("cuda:0")
+    T, H, E, k = 20000, 2048, 8, 2
+    rng = np.random.default_rng(5)
+    xf = rng.standard_normal((T, H)).astype(np.float32)
+    x = torch.from_numpy(xf).to(dev).to(torch.bfloat16)
+    ids = torch.from_numpy(np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)).to(dev)
+    w = torch.from_numpy(rng.random((T, k)).astype(np.float32)).to(dev)
+    assert M.minite_workspace_bytes(M.OP_PERMUTE_QUANT, T, H, E, k) > (2 << 20)
+    ref = _outputs(T, H, E, k, dev)
+    ws = torch.empty(M.minite_workspace_bytes(M.OP_PERMUTE_QUANT, T, H, E, k),
+                     dtype=torch.uint8, device=dev)
+    _run("ws", x, ids, w, E, ref, ws)
+    got = _outputs(T, H, E, k, dev)
+    _run("noalloc", x, ids, w, E, got)
+    torch.cuda.synchronize()
+    for key in ref:
+        assert torch.equal(ref[key], got[key]), f"{key} differs"
+    assert int(got["status"].item()) == 0
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     lib = M.load()
     fake = ctypes.c_void_p(4096)  # never dereferenced: the size check comes first
