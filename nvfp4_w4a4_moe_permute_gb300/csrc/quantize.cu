@@ -49,9 +49,9 @@ __global__ void group_amax_kernel(const uint16_t* __restrict__ x, int64_t elems_
 // chunks of 32 (one per lane). Warp w owns a contiguous range of chunks and
 // keeps kU of them in flight; the group's g and encode table are refreshed
 // only when the group changes.
-constexpr int kU = 4;
+constexpr int kU = 2;
 template <bool A32>
-__global__ void __launch_bounds__(256, 2) quantize_group_blocks_kernel(
+__global__ void __launch_bounds__(256, 4) quantize_group_blocks_kernel(
     const uint16_t* __restrict__ x, int64_t groups, int64_t rows, int nb, uint32_t nb_magic,
     const float* __restrict__ g_in, const uint32_t* __restrict__ amax_bits,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out) {
@@ -426,7 +426,7 @@ static void launch_group_blocks(const uint16_t* x, int64_t groups, int64_t rows,
   const uint32_t magic = nb == 1 ? 0xFFFFFFFFu
                                  : static_cast<uint32_t>((uint64_t(1) << 32) / uint64_t(nb));
   const int64_t chunks = groups * ((rows * nb + 31) / 32);
-  int64_t blocks = static_cast<int64_t>(num_sms()) * 2;
+  int64_t blocks = static_cast<int64_t>(num_sms()) * 4;
   const int64_t need = (chunks + 8 * kU - 1) / (8 * kU);
   if (blocks > need) blocks = need;
   const int64_t min_blocks = (groups + 255) / 256;  // g_out is written by thread t < groups
