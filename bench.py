@@ -124,6 +124,24 @@ def measured_peaks():
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rates
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` (floats) over all ranks of the default
+    process group (NCCL on GPUs, gloo in the CPU tests); identity when there
+    is no process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def workload_name(name, cfg):
+    """The `config.workload` string of both arms."""
+    return f"{name}: T={cfg['T']} H={cfg['H']} E={cfg['E']} top{cfg['k']} I={cfg['I']}"
+
+
 # ----------------------------------------------------------------------------- GPU step
 
 class Step:
@@ -317,10 +335,7 @@ def run_gpu(args):
         assert int(step.status.item()) == 0, f"device status {int(step.status.item())}"
     clk = clocks.stop()
     ms = ms_graph if ms_graph is not None else ms_eager
-    if world > 1:
-        tt = torch.tensor([ms, ms_eager], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, ms_eager = float(tt[0].item()), float(tt[1].item())
+    ms, ms_eager = max_over_ranks([ms, ms_eager], dev)
     ms_per_step = ms / args.steps
     stage_ms = {s: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j, s in enumerate(Step.STAGES)}
@@ -380,11 +395,7 @@ def run_gpu(args):
         e1.record(stream)
         barrier()
         step.bind(bufs[0], ys[0])
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([ems], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = max_over_ranks([e0.elapsed_time(e1)], dev)[0]
         e2e = {"value": step.T * world / (ems / args.steps / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": ems / args.steps}
@@ -418,7 +429,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "nvfp4(e2m1+e4m3)xnvfp4->fp32 acc; bf16 io",
         "data": "synthetic (seeded numpy; Qwen3-30B-A3B shapes, random weights)",
-        "config": {"workload": f"{args.workload}: T={step.T} H={step.H} E={step.E} top{step.k} I={step.I}",
+        "config": {"workload": workload_name(args.workload, d["cfg"]),
                    "step": "wq(gate_up along K; down along K and along N in one pass) + permute+quant"
                            " + gate_up GEMM + SwiGLU+quant + down GEMM + combine + permute+quant dY"
                            " + dgrad GEMM",
@@ -545,7 +556,8 @@ def run_reference(args):
            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "fp32 quantization / fp64 GEMM (numpy)",
            "data": "synthetic (seeded numpy)", "impl": "reference",
-           "config": {"workload": args.workload, "parallelism": "host cpu"},
+           "config": {"workload": workload_name(args.workload, smp.d["cfg"]),
+                      "parallelism": "host cpu"},
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
