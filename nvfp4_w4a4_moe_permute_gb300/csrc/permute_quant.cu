@@ -95,9 +95,19 @@ __global__ void __launch_bounds__(32 * kRankWarps) permute_rank_kernel(
   const int64_t p0 = static_cast<int64_t>(c) * ct * k;
   const int npairs = static_cast<int>(min(static_cast<int64_t>(c + 1) * ct, T) * k - p0);
   bool bad = false;
-  for (int b = 0; b < npairs; b += 32) {
+  // all of the chunk's ids requested at once (at most 16 per lane)
+  int ids_r[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int p = 32 * r + lane;
+    ids_r[r] = p < npairs ? ids[p0 + p] : -1;
+  }
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int b = 32 * r;
+    if (b >= npairs) break;  // warp-uniform
     const int p = b + lane;
-    const int e = p < npairs ? ids[p0 + p] : -1;
+    const int e = ids_r[r];
     const bool valid = e >= 0 && e < E;
     if (p < npairs && !valid) bad = true;
     const uint32_t mask = __match_any_sync(0xffffffffu, valid ? e : E + lane);
