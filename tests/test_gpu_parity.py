@@ -158,6 +158,29 @@ def test_quantize_weights_both_orientations_in_one_pass_bit_exact(E, R, C):
     assert np.array_equal(gk.view(np.uint32), gn.view(np.uint32))
 
 
+def test_tensor_wide_policy_depends_on_the_batch_and_per_token_does_not():
+    """The comparison policy (one global scale over the whole activation
+    tensor, PER_GROUP on a single group) matches the oracle's negative
+    control bit-exactly and changes a token's codes when an outlier token
+    joins the batch; per-token scaling leaves them unchanged."""
+    rng = np.random.default_rng(41)
+    x = _rand_bf16(rng, (32, 512))
+    other = O.f32_to_bf16((rng.standard_normal((8, 512)) * 50).astype(np.float32))
+    both = np.concatenate([other, x])
+    tw_alone = M.quantize(bf16_dev(x), per_group=True)
+    tw_both = M.quantize(bf16_dev(both), per_group=True)
+    pt_alone = M.quantize(bf16_dev(x))
+    pt_both = M.quantize(bf16_dev(both))
+    torch.cuda.synchronize()
+    ref_c, ref_s, _ = O.quantize_tensor_wide_activations(O.bf16_to_f32(x))
+    assert np.array_equal(tw_alone["codes"].cpu().numpy(), ref_c)
+    assert np.array_equal(tw_alone["sf"].cpu().numpy(), O.swizzle_sf(ref_s))
+    assert not np.array_equal(tw_both["codes"].cpu().numpy()[8:], tw_alone["codes"].cpu().numpy())
+    assert np.array_equal(pt_both["codes"].cpu().numpy()[8:], pt_alone["codes"].cpu().numpy())
+    assert np.array_equal(pt_both["g"].cpu().numpy()[8:].view(np.uint32),
+                          pt_alone["g"].cpu().numpy().view(np.uint32))
+
+
 # --------------------------------------------------------------------- permute
 
 def run_permute(x_u16, ids, w, E):
