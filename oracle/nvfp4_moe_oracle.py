@@ -548,6 +548,51 @@ def swiglu_weighted_quant(gate_up_bf16: np.ndarray, perm_w, expert_offsets, sf_r
                 sf_swizzled=place_sf_per_expert(sf, expert_offsets, sf_row_offsets))
 
 
+def swiglu_backward(gate_up: np.ndarray, dh: np.ndarray, perm_w) -> np.ndarray:
+    """Gradient of h = (silu(g) * u) * w with respect to gate_up = [g | u],
+    given the gradient dh of h (float32 [M, I]); the routing weight w is a
+    constant here. With d = 1 + exp_spec(-g), the sigmoid s = 1 / d and
+    silu = g / d (as in the forward), the chain rule gives
+        silu'(g) = s * (1 + g * (1 - s))
+        dg = ((dh * u) * w) * silu'(g)
+        du = (dh * silu) * w
+    every step one float32 IEEE operation rounded to nearest, in this order.
+    Returns float32 [M, 2I] = [dg | du].
+
+    Pins: the float64 derivative of the forward formula (central differences
+    of swiglu_weighted and the closed form), g = 0 (silu' = 1/2, du = 0),
+    large |g| (silu' -> 1 or 0)."""
+    gu = np.asarray(gate_up, dtype=F32)
+    I = gu.shape[1] // 2
+    g, u = gu[:, :I], gu[:, I:]
+    dh = np.asarray(dh, dtype=F32)
+    w = F32(1.0) if perm_w is None else np.asarray(perm_w, dtype=F32)[:, None]
+    d = (F32(1.0) + exp_spec(-g)).astype(F32)
+    sig = (F32(1.0) / d).astype(F32)
+    silu = (g / d).astype(F32)
+    dsilu = (sig * (F32(1.0) + (g * (F32(1.0) - sig).astype(F32)).astype(F32)).astype(F32)).astype(F32)
+    dg = ((((dh * u).astype(F32)) * w).astype(F32) * dsilu).astype(F32)
+    du = (((dh * silu).astype(F32)) * w).astype(F32)
+    return np.concatenate([dg, du], axis=1)
+
+
+def swiglu_backward_quant(gate_up_bf16: np.ndarray, dh_bf16: np.ndarray, perm_w,
+                          expert_offsets, sf_row_offsets):
+    """The SwiGLU backward step: [dg | du] per permuted row, then per-row NVFP4
+    over its 2I values, scales placed per expert like every permuted
+    activation (input of the gate_up dgrad GEMM). Rows at or beyond
+    expert_offsets[E] are not produced. Returns dict codes [M, I] (2I/2
+    bytes), sf [M, 2I/16], sf_swizzled, row_g [M], dgu."""
+    M = int(np.asarray(expert_offsets)[-1])
+    gu = bf16_to_f32(gate_up_bf16[:M])
+    dh = bf16_to_f32(dh_bf16[:M])
+    w = None if perm_w is None else np.asarray(perm_w)[:M]
+    dgu = swiglu_backward(gu, dh, w)
+    codes, sf, g = quantize_per_row(dgu)
+    return dict(codes=codes, sf=sf, row_g=g, dgu=dgu,
+                sf_swizzled=place_sf_per_expert(sf, expert_offsets, sf_row_offsets))
+
+
 # --------------------------------------------------------------------------
 # Combine (unpermute)
 # --------------------------------------------------------------------------

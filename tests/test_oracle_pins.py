@@ -401,6 +401,40 @@ def test_swiglu_matches_float64_formula():
     assert np.max(_ulp_err_f32(h, ref)) <= 6.0
 
 
+def test_swiglu_backward_is_the_derivative_of_the_forward():
+    """Central differences of the float64 forward h = g/(1+e^-g) * u * w
+    (independent of the closed form typed in the oracle) against dg, and the
+    float64 silu against du."""
+    rng = np.random.default_rng(23)
+    M, I = 48, 64
+    gu = (rng.standard_normal((M, 2 * I)) * 3).astype(np.float32)
+    dh = rng.standard_normal((M, I)).astype(np.float32)
+    w = rng.uniform(0.1, 1, M).astype(np.float32)
+    out = O.swiglu_backward(gu, dh, w)
+    g, u = gu[:, :I].astype(np.float64), gu[:, I:].astype(np.float64)
+    wd = w.astype(np.float64)[:, None]
+    f = lambda gg: gg / (1 + np.exp(-gg)) * u * wd  # noqa: E731
+    eps = 1e-6 * np.maximum(1.0, np.abs(g))
+    dg_fd = dh.astype(np.float64) * (f(g + eps) - f(g - eps)) / (2 * eps)
+    scale = np.abs(dh.astype(np.float64) * u * wd) + 1e-30
+    assert np.max(np.abs(out[:, :I] - dg_fd) / scale) < 2e-5
+    du_ref = dh.astype(np.float64) * (g / (1 + np.exp(-g))) * wd
+    assert np.max(_ulp_err_f32(out[:, I:], du_ref)) <= 8.0
+
+
+def test_swiglu_backward_special_gates():
+    """g = 0: silu' = 1/2 exactly and du = 0; g = +-30: silu' -> 1 and -> 0."""
+    I = 4
+    g = np.array([[0.0, 0.0, 30.0, -30.0]], dtype=np.float32)
+    u = np.array([[1.5, -2.0, 1.0, 1.0]], dtype=np.float32)
+    dh = np.array([[1.0, 3.0, 2.0, 2.0]], dtype=np.float32)
+    out = O.swiglu_backward(np.concatenate([g, u], axis=1), dh, None)
+    assert out[0, 0] == np.float32(0.75) and out[0, 1] == np.float32(-3.0)
+    assert out[0, I] == 0.0 and out[0, I + 1] == 0.0
+    assert abs(out[0, 2] - 2.0) < 1e-5 and abs(out[0, 3]) < 1e-9
+    assert abs(out[0, I + 2] - 60.0) < 1e-4 and abs(out[0, I + 3]) < 1e-9
+
+
 # ---------------------------------------------------------------- combine
 
 def test_combine_exact_cases():
