@@ -269,6 +269,47 @@ int minite_swiglu_weighted_quant(const void* gate_up, const float* perm_w,
                                  int32_t* status, minite_stream_t stream);
 
 /*
+ * minite_swiglu_backward_quant -- gradient of the routing-weighted SwiGLU
+ * with respect to its gate and up inputs, with per-row NVFP4 requantization
+ * of the result fused into the same pass (the A operand of the gate_up
+ * dgrad GEMM).
+ *
+ * Cites: miniTE report summary, "Two complementary interventions" (amax
+ * computed inside the SwiGLU pass, fused scale layout) and "Respect the
+ * timing boundaries" (the backward of the learner's expert MLP; the pages
+ * run it in BF16, this entry point is the NVFP4 variant of that step).
+ *
+ * For each used row m (< expert_offsets[E]), with g = gate_up[m, 0:I],
+ * u = gate_up[m, I:2I], w = perm_w[m] (1 if perm_w is NULL) and the
+ * gradient dh[m, 0:I] of h = (silu(g) * u) * w:
+ *   d = 1 + exp(-g), s = 1 / d, silu = g / d, silu' = s * (1 + g * (1 - s))
+ *   dg = ((dh * u) * w) * silu',  du = (dh * silu) * w
+ * every step one FP32 operation rounded to nearest, in this order, with the
+ * exponential of minite_swiglu_weighted_quant. The row [dg | du] (2I values)
+ * is then quantized per row exactly as minite_quantize_nvfp4 PER_ROW, the SF
+ * written into the per-expert padded regions given by sf_row_offsets; the
+ * SF bytes of each expert's padding rows are set to 0.
+ *
+ * gate_up: device, BF16 [M, 2I], 32-byte aligned (the forward's gate_up
+ *          GEMM output).  dh: device, BF16 [M, I], 32-byte aligned.
+ * perm_w:  device float [M] or NULL.
+ * codes:   device, uint8 [M, I] (2I E2M1 codes per row), 16-byte aligned.
+ * sf:      device, uint8 [(M + 128 E) * (2I/16)] at most, 16-byte aligned,
+ *          rows per expert as sf_row_offsets says.  row_g: device, float [M].
+ * Rows at or beyond expert_offsets[E] are not written. Inconsistent offsets
+ * make the kernel write nothing and store MINITE_ERR_INVALID_ARG in *status.
+ * A row whose dg or du overflows FP32 (or holds NaN) has no finite amax;
+ * its codes, scales and global scale are unspecified.
+ * All buffers are owned by the caller; the call is asynchronous on stream.
+ * Shape rules: I % 64 == 0, 64 <= I <= 2048, 1 <= E <= 1024, M < 2^31.
+ */
+int minite_swiglu_backward_quant(const void* gate_up, const void* dh, const float* perm_w,
+                                 int64_t M, int64_t I, int32_t E,
+                                 const int32_t* expert_offsets, const int32_t* sf_row_offsets,
+                                 uint8_t* codes, uint8_t* sf, float* row_g,
+                                 int32_t* status, minite_stream_t stream);
+
+/*
  * minite_moe_combine -- unpermute: y[t] = BF16(sum_{j<k} D[dest_row[t,j]]),
  * summed in FP32 in slot order starting from 0; dropped pairs (dest_row < 0)
  * are skipped. The routing weight is already inside D (applied in the

@@ -4,6 +4,8 @@
 // writes NVFP4 codes plus swizzled scales directly (miniTE report summary,
 // section "Two complementary interventions"); the combine sums each token's
 // k expert rows back into token order.
+#include <mutex>
+
 #include "common.cuh"
 #include "host_util.h"
 
@@ -212,6 +214,211 @@ static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int 
   return MINITE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// SwiGLU backward: [dg | du] = d h / d [g | u] times dh, per permuted row, with
+// d = 1 + exp(-g), s = 1/d, silu = g/d, silu' = s (1 + g (1 - s)),
+// dg = ((dh u) w) silu', du = (dh silu) w, then per-row NVFP4 over the 2I
+// values. silu and silu' of a BF16 gate come from per-CTA tables over the
+// same 32 binades as the forward's (gates outside them take the formulas).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void silu_dsilu_spec(float g, float& silu, float& dsilu) {
+  const float d = __fadd_rn(1.0f, exp_spec(-g));
+  const float sig = __fdiv_rn(1.0f, d);
+  silu = __fdiv_rn(g, d);
+  dsilu = __fmul_rn(sig, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, sig))));
+}
+
+__device__ void build_silu_bwd_luts(float* lut_s, float* lut_d, int t, int nthreads) {
+  for (int i = t; i < kLutEntries; i += nthreads) {
+    const uint32_t bits = (static_cast<uint32_t>(i >> 12) << 15) | (kLutLo + (i & 4095));
+    silu_dsilu_spec(__uint_as_float(bits << 16), lut_s[i], lut_d[i]);
+  }
+}
+
+// dg and du of one 16-element block from its gates, ups and dh (raw BF16).
+__device__ __forceinline__ void swiglu_bwd_block(const float* lut_s, const float* lut_d,
+                                                 const uint32_t (&wg)[8], const uint32_t (&wu)[8],
+                                                 const uint32_t (&wd)[8], float w,
+                                                 float (&dg)[16], float (&du)[16]) {
+  const uint32_t mx = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(wg[0], wg[1]),
+                                                    max_abs_bf16x2(wg[2], wg[3])),
+                                     max_abs_bf16x2(max_abs_bf16x2(wg[4], wg[5]),
+                                                    max_abs_bf16x2(wg[6], wg[7])));
+  const uint32_t mn = min_abs_bf16x2(min_abs_bf16x2(min_abs_bf16x2(wg[0], wg[1]),
+                                                    min_abs_bf16x2(wg[2], wg[3])),
+                                     min_abs_bf16x2(min_abs_bf16x2(wg[4], wg[5]),
+                                                    min_abs_bf16x2(wg[6], wg[7])));
+  const uint32_t hi_mag = max(mx & 0x7FFFu, (mx >> 16) & 0x7FFFu);
+  const uint32_t lo_mag = min(mn & 0x7FFFu, (mn >> 16) & 0x7FFFu);
+  float sl[16], ds[16];
+  if (lo_mag >= kLutLo && hi_mag < kLutLo + kLutSpan) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t b = (i & 1) ? (wg[i >> 1] >> 16) : wg[i >> 1];
+      const uint32_t idx = ((b - kLutLo) & (kLutSpan - 1)) | ((b >> 3) & kLutSpan);
+      sl[i] = lut_s[idx];
+      ds[i] = lut_d[idx];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t bits = (i & 1) ? (wg[i >> 1] >> 16) : (wg[i >> 1] & 0xFFFFu);
+      const uint32_t off = (bits & 0x7FFFu) - kLutLo;
+      if (off < kLutSpan) {
+        const uint32_t idx = off | ((bits >> 3) & kLutSpan);
+        sl[i] = lut_s[idx];
+        ds[i] = lut_d[idx];
+      } else {
+        silu_dsilu_spec(__uint_as_float(bits << 16), sl[i], ds[i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float d0 = bf16lo(wd[i]), d1 = bf16hi(wd[i]);
+    float a0 = d0, a1 = d1;
+    mul_f32x2(a0, a1, bf16lo(wu[i]), bf16hi(wu[i]));   // dh * u
+    mul_f32x2(a0, a1, w, w);                           // * w
+    mul_f32x2(a0, a1, ds[2 * i], ds[2 * i + 1]);       // * silu'
+    dg[2 * i] = a0;
+    dg[2 * i + 1] = a1;
+    mul_f32x2(d0, d1, sl[2 * i], sl[2 * i + 1]);       // dh * silu
+    mul_f32x2(d0, d1, w, w);                           // * w
+    du[2 * i] = d0;
+    du[2 * i + 1] = d1;
+  }
+}
+
+// One warp per permuted row; lane l owns input blocks 32j + l (gates, ups and
+// dh), which give output blocks 32j + l (dg) and I/16 + 32j + l (du). Rows of
+// more than 64 blocks keep 2 x 16 x NCH values per lane live, so those
+// variants run half as many threads per CTA to get the registers.
+template <int NCH>
+constexpr int bwd_threads() { return NCH <= 2 ? 512 : 256; }
+
+template <int NCH>
+__global__ void __launch_bounds__(bwd_threads<NCH>(), 1) swiglu_bwd_quant_kernel(
+    const uint16_t* __restrict__ gu, const uint16_t* __restrict__ dh,
+    const float* __restrict__ perm_w, int64_t M, int I, int E,
+    const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ sf_row_offsets,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
+    int32_t* status) {
+  extern __shared__ __align__(16) float smf[];
+  float* lut_s = smf;
+  float* lut_d = smf + kLutEntries;
+  int32_t* s_off = reinterpret_cast<int32_t*>(smf + 2 * kLutEntries);
+  int32_t* s_sfoff = s_off + (E + 1);
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    s_off[i] = expert_offsets[i];
+    s_sfoff[i] = sf_row_offsets[i];
+  }
+  build_silu_bwd_luts(lut_s, lut_d, threadIdx.x, blockDim.x);
+  __syncthreads();
+  if (!offsets_consistent(s_off, s_sfoff, E, M)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MINITE_ERR_INVALID_ARG);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nb = I / 16;              // input blocks per row
+  const int kc = (2 * nb + 3) & ~3;   // SF columns of the 2I-wide output
+  const int64_t used = s_off[E];
+  for (int64_t m = warp; m < used; m += nwarps) {
+    const uint16_t* gr = gu + m * (2 * static_cast<int64_t>(I));
+    const uint16_t* dr = dh + m * static_cast<int64_t>(I);
+    const float w = perm_w ? perm_w[m] : 1.0f;
+    float dgv[NCH][16], duv[NCH][16], amg[NCH], amu[NCH];
+    float rm = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = 32 * j + lane;
+      if (c < nb) {
+        uint32_t wg[8], wu[8], wd[8];
+        ld_bf16x16(gr + 16 * c, wg);
+        ld_bf16x16(gr + I + 16 * c, wu);
+        ld_bf16x16(dr + 16 * c, wd);
+        swiglu_bwd_block(lut_s, lut_d, wg, wu, wd, w, dgv[j], duv[j]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) dgv[j][t] = duv[j][t] = 0.0f;
+      }
+      amg[j] = amax_f32x16(dgv[j]);
+      amu[j] = amax_f32x16(duv[j]);
+      rm = fmaxf(rm, fmaxf(amg[j], amu[j]));
+    }
+    const float g = global_scale(warp_max(rm));
+    const float tk = enc_table_entry(g);
+    QBlock qg[NCH], qu[NCH];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      if (32 * j < nb) {  // warp-uniform
+        const bool valid = 32 * j + lane < nb;
+        qg[j] = quant_block(dgv[j], amg[j], g, tk, valid);
+        qu[j] = quant_block(duv[j], amu[j], g, tk, valid);
+      } else {
+        qg[j].codes = qu[j].codes = make_uint2(0u, 0u);
+        qg[j].sf = qu[j].sf = 0u;
+      }
+    }
+    // expert of row m: the last e with s_off[e] <= m
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= m) lo = mid; else hi = mid;
+    }
+    const int64_t r = static_cast<int64_t>(s_sfoff[lo]) + (m - s_off[lo]);
+    uint8_t* crow = codes + m * static_cast<int64_t>(I);  // 2I codes = I bytes
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = 32 * j + lane;
+      if (c < nb) {
+        st_u64(crow + 8 * c, qg[j].codes);
+        st_u64(crow + 8 * (nb + c), qu[j].codes);
+        sf[sf_offset(r, c, kc)] = static_cast<uint8_t>(qg[j].sf);
+        sf[sf_offset(r, nb + c, kc)] = static_cast<uint8_t>(qu[j].sf);
+      }
+    }
+    if (lane == 0) row_g[m] = g;
+  }
+
+  // zero the scale bytes of each expert's padding rows
+  const int words = kc / 4;
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int cnt = s_off[e + 1] - s_off[e];
+    const int pad = ((cnt + 127) & ~127) - cnt;
+    for (int i = threadIdx.x; i < pad * words; i += blockDim.x) {
+      const int64_t r = static_cast<int64_t>(s_sfoff[e]) + cnt + i / words;
+      *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * (i % words), kc)) = 0u;
+    }
+  }
+}
+
+template <int NCH>
+static int launch_swiglu_bwd(const uint16_t* g, const uint16_t* dh, const float* perm_w,
+                             int64_t M, int I, int E, const int32_t* off, const int32_t* sfoff,
+                             uint8_t* codes, uint8_t* sf, float* row_g, int32_t* status,
+                             cudaStream_t s) {
+  const size_t smem = 2 * kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(swiglu_bwd_quant_kernel<NCH>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(2 * kLutEntries * sizeof(float) + 2 * 1025 * 4));
+  });
+  if (attr != cudaSuccess) return MINITE_ERR_CUDA;
+  constexpr int threads = bwd_threads<NCH>();
+  int64_t blocks = (M + threads / 32 - 1) / (threads / 32);
+  const int64_t cap = static_cast<int64_t>(num_sms());
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  swiglu_bwd_quant_kernel<NCH><<<static_cast<unsigned>(blocks), threads, smem, s>>>(
+      g, dh, perm_w, M, I, E, off, sfoff, codes, sf, row_g, status);
+  return MINITE_OK;
+}
+
 // Work unit: (token t, column chunk of 512); lane l owns columns
 // [512 ch + 16 l, +16). For each slot j in order the lane adds the 16 BF16
 // values of row dest_row[t, j] into FP32 accumulators; up to 8 rows are in
@@ -323,6 +530,37 @@ extern "C" int minite_swiglu_weighted_quant(const void* gate_up, const float* pe
                                                 sf_row_offsets, codes, sf, row_g, status, s);
   else rc = launch_swiglu<32, 4>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes, sf,
                                  row_g, status, s);
+  if (rc != MINITE_OK) return rc;
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
+extern "C" int minite_swiglu_backward_quant(const void* gate_up, const void* dh,
+                                            const float* perm_w, int64_t M, int64_t I, int32_t E,
+                                            const int32_t* expert_offsets,
+                                            const int32_t* sf_row_offsets, uint8_t* codes,
+                                            uint8_t* sf, float* row_g, int32_t* status,
+                                            minite_stream_t stream) {
+  if (!gate_up || !dh || !expert_offsets || !sf_row_offsets || !codes || !sf || !row_g)
+    return MINITE_ERR_INVALID_ARG;
+  if (M < 1 || I < 64 || I % 64 != 0 || I > 2048 || E < 1 || E > 1024)
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (M >= (int64_t(1) << 31)) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(gate_up, 32) || !aligned(dh, 32) || !aligned(codes, 16) || !aligned(sf, 16))
+    return MINITE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t* g = static_cast<const uint16_t*>(gate_up);
+  const uint16_t* d = static_cast<const uint16_t*>(dh);
+  const int i = static_cast<int>(I);
+  const int nb = i / 16;
+  int rc;
+  if (nb <= 32) rc = launch_swiglu_bwd<1>(g, d, perm_w, M, i, E, expert_offsets, sf_row_offsets,
+                                          codes, sf, row_g, status, s);
+  else if (nb <= 64) rc = launch_swiglu_bwd<2>(g, d, perm_w, M, i, E, expert_offsets,
+                                               sf_row_offsets, codes, sf, row_g, status, s);
+  else if (nb <= 96) rc = launch_swiglu_bwd<3>(g, d, perm_w, M, i, E, expert_offsets,
+                                               sf_row_offsets, codes, sf, row_g, status, s);
+  else rc = launch_swiglu_bwd<4>(g, d, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes,
+                                 sf, row_g, status, s);
   if (rc != MINITE_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }

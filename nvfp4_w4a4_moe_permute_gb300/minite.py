@@ -24,7 +24,8 @@ ERR_TIMEOUT, ERR_BAD_ROUTING = 4, 5
 
 EXPORTS = [
     "minite_quantize_nvfp4", "minite_moe_permute_quant", "minite_grouped_gemm_nvfp4",
-    "minite_swiglu_weighted_quant", "minite_moe_combine", "minite_workspace_bytes",
+    "minite_swiglu_weighted_quant", "minite_swiglu_backward_quant", "minite_moe_combine",
+    "minite_workspace_bytes",
     "minite_status_string", "minite_version", "minite_test_convert",
     "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc", "minite_set_gemm_variant",
     "minite_test_div6_exhaustive", "minite_quantize_nvfp4_dual",
@@ -59,6 +60,8 @@ def load(path: str | None = None):
         "minite_grouped_gemm_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                       _vp, _int, _vp, _vp],
         "minite_swiglu_weighted_quant": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+        "minite_swiglu_backward_quant": [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _vp],
         "minite_moe_combine": [_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp],
         "minite_test_convert": [_vp, _i64, _vp, _vp, _vp, _vp],
         "minite_test_div6_exhaustive": [_vp, _vp],
@@ -209,6 +212,15 @@ def minite_swiglu_weighted_quant(gate_up, perm_w, E, expert_offsets, sf_row_offs
                                              _p(expert_offsets), _p(sf_row_offsets), _p(codes),
                                              _p(sf), _p(row_g), _p(status), _s(stream))
     _check(rc, "minite_swiglu_weighted_quant")
+
+
+def minite_swiglu_backward_quant(gate_up, dh, perm_w, E, expert_offsets, sf_row_offsets, codes,
+                                 sf, row_g, status=None, stream=None):
+    M, I2 = gate_up.shape
+    rc = load().minite_swiglu_backward_quant(_p(gate_up), _p(dh), _p(perm_w), M, I2 // 2, E,
+                                             _p(expert_offsets), _p(sf_row_offsets), _p(codes),
+                                             _p(sf), _p(row_g), _p(status), _s(stream))
+    _check(rc, "minite_swiglu_backward_quant")
 
 
 def minite_moe_combine(expert_out, dest_row, y, status=None, stream=None):

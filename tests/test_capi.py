@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_path_entry_points():
     names = declared_functions()
     for n in ["minite_quantize_nvfp4", "minite_moe_permute_quant", "minite_grouped_gemm_nvfp4",
-              "minite_swiglu_weighted_quant", "minite_moe_combine"]:
+              "minite_swiglu_weighted_quant", "minite_swiglu_backward_quant",
+              "minite_moe_combine"]:
         assert n in names
 
 
@@ -95,6 +96,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.minite_grouped_gemm_nvfp4(*g, 128, 128, 128, 1, None, 0, None, None) == 1
     # swiglu: I not a multiple of 64
     assert lib.minite_swiglu_weighted_quant(fake, None, 16, 96, 1, fake, fake, fake, fake, fake, None, None) == 2
+    # swiglu backward: I too large, dh missing, misaligned dh
+    assert lib.minite_swiglu_backward_quant(fake, fake, None, 16, 4096, 1, fake, fake, fake, fake,
+                                            fake, None, None) == 2
+    assert lib.minite_swiglu_backward_quant(fake, None, None, 16, 128, 1, fake, fake, fake, fake,
+                                            fake, None, None) == 1
+    assert lib.minite_swiglu_backward_quant(fake, vp(4112), None, 16, 128, 1, fake, fake, fake,
+                                            fake, fake, None, None) == 1
     # combine: N not a multiple of 8, k too large
     assert lib.minite_moe_combine(fake, fake, 4, 8, 12, 2, fake, None, None) == 2
     assert lib.minite_moe_combine(fake, fake, 4, 8, 16, 64, fake, None, None) == 2

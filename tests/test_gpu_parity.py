@@ -165,7 +165,9 @@ def test_tensor_wide_policy_depends_on_the_batch_and_per_token_does_not():
     joins the batch; per-token scaling leaves them unchanged."""
     rng = np.random.default_rng(41)
     x = _rand_bf16(rng, (32, 512))
-    other = O.f32_to_bf16((rng.standard_normal((8, 512)) * 50).astype(np.float32))
+    # outliers well above every row of x (whose rows carry scales up to 2^6)
+    other = O.f32_to_bf16((rng.standard_normal((8, 512)) * 1e5).astype(np.float32))
+    assert np.abs(O.bf16_to_f32(other)).max() > 100 * np.abs(O.bf16_to_f32(x)).max()
     both = np.concatenate([other, x])
     tw_alone = M.quantize(bf16_dev(x), per_group=True)
     tw_both = M.quantize(bf16_dev(both), per_group=True)
@@ -474,6 +476,59 @@ def test_swiglu_weighted_quant_bit_exact(counts, I):
         assert np.array_equal(codes.cpu().numpy()[:Mu], ref["codes"])
         assert np.array_equal(sf.cpu().numpy()[:ref["sf_swizzled"].size], ref["sf_swizzled"])
         assert np.array_equal(g.cpu().numpy()[:Mu].view(np.uint32), ref["row_g"].view(np.uint32))
+
+
+@pytest.mark.parametrize("counts,I", [([3, 0, 130, 1], 64), ([256, 17], 768), ([1], 128),
+                                      ([100] * 5, 1536), ([5, 130], 512), ([33], 1024),
+                                      ([40, 0, 7], 2048), ([300, 212], 768)])
+def test_swiglu_backward_quant_bit_exact(counts, I):
+    rng = np.random.default_rng(len(counts) * 37 + I + 1)
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    sfo = np.concatenate([[0], np.cumsum((np.array(counts) + 127) // 128 * 128)]).astype(np.int32)
+    Mu = int(off[-1])
+    Mt = Mu + 5
+    gu = O.f32_to_bf16((rng.standard_normal((Mt, 2 * I)) * 3).astype(np.float32))
+    dh = _rand_bf16(rng, (Mt, I), scale_spread=10)
+    gu[0, :I] = O.f32_to_bf16(np.linspace(-120, 120, I).astype(np.float32))  # clamp region
+    special = np.array([0.0, -0.0, 1e-40, -1e-40, 2.0 ** -25, -(2.0 ** -24), 2.0 ** -24,
+                        -(2.0 ** -25), 255.0, -255.0, 256.0, -256.0, 300.0, -300.0, 3e4, -3e4],
+                       dtype=np.float32)
+    gu[1 % Mt, :I] = O.f32_to_bf16(np.resize(special, I))
+    dh[2 % Mt] = 0  # zero gradient row: global scale 1, all codes and scales 0
+    dh[3 % Mt, ::7] = O.f32_to_bf16(np.array([1.0e30], dtype=np.float32))[0]  # huge, finite
+    pw = rng.random(Mt).astype(np.float32)
+    for weights in (pw, None):
+        ref = O.swiglu_backward_quant(gu, dh, weights, off, sfo)
+        codes = torch.zeros((Mt, I), dtype=torch.uint8, device="cuda")
+        sf = torch.full(((Mt + 128 * E) * (2 * I // 16),), 0xAB, dtype=torch.uint8, device="cuda")
+        g = torch.zeros(Mt, dtype=torch.float32, device="cuda")
+        st = _status()
+        M.minite_swiglu_backward_quant(bf16_dev(gu), bf16_dev(dh),
+                                       None if weights is None else np_dev(weights),
+                                       E, np_dev(off), np_dev(sfo), codes, sf, g, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert np.array_equal(codes.cpu().numpy()[:Mu], ref["codes"])
+        assert np.array_equal(sf.cpu().numpy()[:ref["sf_swizzled"].size], ref["sf_swizzled"])
+        assert np.array_equal(g.cpu().numpy()[:Mu].view(np.uint32), ref["row_g"].view(np.uint32))
+        assert (codes.cpu().numpy()[Mu:] == 0).all()  # rows past the last expert untouched
+
+
+def test_swiglu_backward_inconsistent_offsets_are_reported_not_executed():
+    I, E = 128, 2
+    gu = torch.zeros((40, 2 * I), dtype=torch.bfloat16, device="cuda")
+    dh = torch.ones((40, I), dtype=torch.bfloat16, device="cuda")
+    off = np.array([0, 30, 20], dtype=np.int32)  # decreasing
+    sfo = np.array([0, 128, 128], dtype=np.int32)
+    codes = torch.full((40, I), 7, dtype=torch.uint8, device="cuda")
+    sf = torch.full((512 * 16,), 7, dtype=torch.uint8, device="cuda")
+    g = torch.zeros(40, dtype=torch.float32, device="cuda")
+    st = _status()
+    M.minite_swiglu_backward_quant(gu, dh, None, E, np_dev(off), np_dev(sfo), codes, sf, g, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1 << 1
+    assert (codes == 7).all() and (sf == 7).all()
 
 
 @pytest.mark.parametrize("T,k,N", [(1, 1, 8), (64, 2, 64), (300, 8, 2048), (33, 5, 136)])
