@@ -259,6 +259,142 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
                : "memory");
 }
 
+// Shape constants of the two-orientation quantization of one weight shape.
+struct DualGeom {
+  int rows, cols, tr, tc;        // tiles per group: tr x tc
+  int nbk, nbn, kck, kcn;        // blocks per quantized row, SF columns (forward, transposed)
+  int64_t sfk_group, sfn_group;  // SF bytes per group
+  bool v8k, v8n;                 // 32-byte code stores allowed
+};
+
+__device__ __forceinline__ DualGeom dual_geom(int rows, int cols, const uint8_t* codes_k,
+                                              const uint8_t* codes_n) {
+  DualGeom G;
+  G.rows = rows; G.cols = cols;
+  G.tr = (rows + kDR - 1) / kDR; G.tc = (cols + kDC - 1) / kDC;
+  G.nbk = cols / 16; G.nbn = rows / 16;
+  G.kck = (G.nbk + 3) & ~3; G.kcn = (G.nbn + 3) & ~3;
+  G.sfk_group = static_cast<int64_t>((rows + 127) & ~127) * G.kck;
+  G.sfn_group = static_cast<int64_t>((cols + 127) & ~127) * G.kcn;
+  // 32-byte code stores where every destination row starts 32-byte aligned
+  G.v8k = (cols / 2) % 32 == 0 && (reinterpret_cast<uintptr_t>(codes_k) & 31) == 0;
+  G.v8n = (rows / 2) % 32 == 0 && (reinterpret_cast<uintptr_t>(codes_n) & 31) == 0;
+  return G;
+}
+
+// Every thread of the block: per-thread asynchronous copies of the 64 x 128
+// tile (r0, c0) of group xg into buf (zero-filled outside the matrix), as
+// one commit group.
+__device__ __forceinline__ void dual_fetch(const uint16_t* xg, const DualGeom& G, int r0, int c0,
+                                           uint16_t* buf, const uint16_t* any_valid) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = t + 256 * i;  // 16-byte piece q of the tile: row q / 16, piece q % 16
+    const int lr = q >> 4, seg = q & 15;
+    const bool valid = r0 + lr < G.rows && c0 + 8 * seg < G.cols;
+    const uint16_t* src =
+        valid ? xg + static_cast<int64_t>(r0 + lr) * G.cols + c0 + 8 * seg : any_valid;
+    cp_async16_zfill(buf + lr * kDPitch + 8 * seg, src, valid);
+  }
+}
+
+// Every thread of the block (256): quantize the staged tile (r0, c0) of
+// group grp in both orientations with the group's global scale g.
+__device__ __forceinline__ void dual_tile_quant(const uint16_t* tile, const DualGeom& G,
+                                                int64_t grp, int r0, int c0, float g, float tk,
+                                                uint8_t* __restrict__ codes_k,
+                                                uint8_t* __restrict__ sf_k,
+                                                uint8_t* __restrict__ codes_n,
+                                                uint8_t* __restrict__ sf_n) {
+  const int t = threadIdx.x;
+  if (t < 128) {
+    // ---- one tile column, 4 blocks along the rows (transposed copy)
+    const int c = c0 + t;
+    uint2 code[4];
+    uint32_t sfw = 0;
+#pragma unroll
+    for (int rb = 0; rb < 4; ++rb) {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j] = __uint_as_float(static_cast<uint32_t>(tile[(16 * rb + j) * kDPitch + t]) << 16);
+      const bool valid = c < G.cols && r0 / 16 + rb < G.nbn;
+      const QBlock q = quant_block(v, amax_f32x16(v), g, tk, valid);
+      code[rb] = q.codes;
+      sfw |= q.sf << (8 * rb);
+    }
+    if (c < G.cols) {
+      const int gr = r0 / 16;  // multiple of 4
+      uint8_t* dst = codes_n + (grp * G.cols + c) * static_cast<int64_t>(G.rows / 2) + 8 * gr;
+      if (G.v8n && gr + 4 <= G.nbn) {
+        st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
+                     code[3].x, code[3].y);
+      } else {
+#pragma unroll
+        for (int rb = 0; rb < 4; ++rb)
+          if (gr + rb < G.nbn) st_u64(dst + 8 * rb, code[rb]);
+      }
+      *reinterpret_cast<uint32_t*>(sf_n + grp * G.sfn_group + sf_offset(c, gr, G.kcn)) = sfw;
+    }
+  } else {
+    // ---- half a tile row, 4 blocks along the columns (forward copy)
+    const int u = t - 128;
+    const int lr = u >> 1, half = u & 1;
+    const int r = r0 + lr;
+    uint2 code[4];
+    uint32_t sfw = 0;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(tile + lr * kDPitch + 64 * half + 16 * cb);
+      const uint4 a0 = src[0], a1 = src[1];
+      const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      float v[16];
+      unpack_bf16x16(w, v);
+      const bool valid = r < G.rows && c0 / 16 + 4 * half + cb < G.nbk;
+      const QBlock q = quant_block(v, amax_bf16x16(w), g, tk, valid);
+      code[cb] = q.codes;
+      sfw |= q.sf << (8 * cb);
+    }
+    const int gc = c0 / 16 + 4 * half;  // multiple of 4
+    if (r < G.rows && gc < G.nbk) {
+      uint8_t* dst = codes_k + (grp * G.rows + r) * static_cast<int64_t>(G.cols / 2) + 8 * gc;
+      if (G.v8k && gc + 4 <= G.nbk) {
+        st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
+                     code[3].x, code[3].y);
+      } else {
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb)
+          if (gc + cb < G.nbk) st_u64(dst + 8 * cb, code[cb]);
+      }
+      *reinterpret_cast<uint32_t*>(sf_k + grp * G.sfk_group + sf_offset(r, gc, G.kck)) = sfw;
+    }
+  }
+}
+
+// Scale bytes of the padding rows of both copies of groups [g0, g1), split
+// over `nthreads` threads numbered from `gt`.
+__device__ __forceinline__ void dual_zero_padding(const DualGeom& G, int64_t g0, int64_t g1,
+                                                  int64_t gt, int64_t nthreads,
+                                                  uint8_t* __restrict__ sf_k,
+                                                  uint8_t* __restrict__ sf_n) {
+  const int64_t pk = ((G.rows + 127) & ~127) - G.rows, pn = ((G.cols + 127) & ~127) - G.cols;
+  const int wk = G.kck / 4, wn = G.kcn / 4;
+  for (int64_t i = gt; i < (g1 - g0) * pk * wk; i += nthreads) {
+    const int64_t grp = g0 + i / (pk * wk);
+    const int64_t rem = i % (pk * wk);
+    *reinterpret_cast<uint32_t*>(sf_k + grp * G.sfk_group +
+                                 sf_offset(G.rows + rem / wk, 4 * (rem % wk), G.kck)) = 0u;
+  }
+  for (int64_t i = gt; i < (g1 - g0) * pn * wn; i += nthreads) {
+    const int64_t grp = g0 + i / (pn * wn);
+    const int64_t rem = i % (pn * wn);
+    *reinterpret_cast<uint32_t*>(sf_n + grp * G.sfn_group +
+                                 sf_offset(G.cols + rem / wn, 4 * (rem % wn), G.kcn)) = 0u;
+  }
+}
+
 __global__ void __launch_bounds__(256) quantize_dual_kernel(
     const uint16_t* __restrict__ x, int64_t groups, int rows, int cols,
     const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes_k,
@@ -266,36 +402,15 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
     float* __restrict__ g_out) {
   __shared__ __align__(16) uint16_t tiles[2][kDTile];
   const int t = threadIdx.x;
-  const int tr = (rows + kDR - 1) / kDR, tc = (cols + kDC - 1) / kDC;
-  const int64_t ntiles = groups * tr * tc;
-  const int nbk = cols / 16, nbn = rows / 16;              // blocks per quantized row
-  const int kck = (nbk + 3) & ~3, kcn = (nbn + 3) & ~3;     // SF columns
-  const int64_t rows_pad = (rows + 127) & ~127, cols_pad = (cols + 127) & ~127;
-  const int64_t sfk_group = rows_pad * kck, sfn_group = cols_pad * kcn;
-  // 32-byte code stores where every destination row starts 32-byte aligned
-  const bool v8k = (cols / 2) % 32 == 0 && (reinterpret_cast<uintptr_t>(codes_k) & 31) == 0;
-  const bool v8n = (rows / 2) % 32 == 0 && (reinterpret_cast<uintptr_t>(codes_n) & 31) == 0;
-
-  auto tile_pos = [&](int64_t ti, int64_t& grp, int& r0, int& c0) {
-    grp = ti / (tr * tc);
-    const int rem = static_cast<int>(ti - grp * tr * tc);
-    r0 = (rem / tc) * kDR;
-    c0 = (rem % tc) * kDC;
-  };
+  const DualGeom G = dual_geom(rows, cols, codes_k, codes_n);
+  const int64_t per_group = static_cast<int64_t>(G.tr) * G.tc;
+  const int64_t ntiles = groups * per_group;
   auto fetch = [&](int64_t ti, uint16_t* buf) {
     if (ti < ntiles) {
-      int64_t grp;
-      int r0, c0;
-      tile_pos(ti, grp, r0, c0);
-      const uint16_t* xg = x + grp * static_cast<int64_t>(rows) * cols;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int q = t + 256 * i;  // 16-byte piece q of the tile: row q / 16, piece q % 16
-        const int lr = q >> 4, seg = q & 15;
-        const bool valid = r0 + lr < rows && c0 + 8 * seg < cols;
-        const uint16_t* src = valid ? xg + static_cast<int64_t>(r0 + lr) * cols + c0 + 8 * seg : x;
-        cp_async16_zfill(buf + lr * kDPitch + 8 * seg, src, valid);
-      }
+      const int64_t grp = ti / per_group;
+      const int rem = static_cast<int>(ti - grp * per_group);
+      dual_fetch(x + grp * static_cast<int64_t>(rows) * cols, G, (rem / G.tc) * kDR,
+                 (rem % G.tc) * kDC, buf, x);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
@@ -309,98 +424,22 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
     fetch(ti + gridDim.x, tiles[cur ^ 1]);
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncthreads();
-    int64_t grp;
-    int r0, c0;
-    tile_pos(ti, grp, r0, c0);
+    const int64_t grp = ti / per_group;
+    const int rem = static_cast<int>(ti - grp * per_group);
     if (grp != gcur) {  // block-uniform
       gcur = grp;
       g = global_scale(__uint_as_float(amax_bits[grp]));
       tk = enc_table_entry(g);
     }
-    const uint16_t* tile = tiles[cur];
-    if (t < 128) {
-      // ---- one tile column, 4 blocks along the rows (transposed copy)
-      const int c = c0 + t;
-      uint2 code[4];
-      uint32_t sfw = 0;
-#pragma unroll
-      for (int rb = 0; rb < 4; ++rb) {
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          v[j] = __uint_as_float(static_cast<uint32_t>(tile[(16 * rb + j) * kDPitch + t]) << 16);
-        const bool valid = c < cols && r0 / 16 + rb < nbn;
-        const QBlock q = quant_block(v, amax_f32x16(v), g, tk, valid);
-        code[rb] = q.codes;
-        sfw |= q.sf << (8 * rb);
-      }
-      if (c < cols) {
-        const int gr = r0 / 16;  // multiple of 4
-        uint8_t* dst = codes_n + (grp * cols + c) * static_cast<int64_t>(rows / 2) + 8 * gr;
-        if (v8n && gr + 4 <= nbn) {
-          st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
-                       code[3].x, code[3].y);
-        } else {
-#pragma unroll
-          for (int rb = 0; rb < 4; ++rb)
-            if (gr + rb < nbn) st_u64(dst + 8 * rb, code[rb]);
-        }
-        *reinterpret_cast<uint32_t*>(sf_n + grp * sfn_group + sf_offset(c, gr, kcn)) = sfw;
-      }
-    } else {
-      // ---- half a tile row, 4 blocks along the columns (forward copy)
-      const int u = t - 128;
-      const int lr = u >> 1, half = u & 1;
-      const int r = r0 + lr;
-      uint2 code[4];
-      uint32_t sfw = 0;
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(tile + lr * kDPitch + 64 * half + 16 * cb);
-        const uint4 a0 = src[0], a1 = src[1];
-        const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        float v[16];
-        unpack_bf16x16(w, v);
-        const bool valid = r < rows && c0 / 16 + 4 * half + cb < nbk;
-        const QBlock q = quant_block(v, amax_bf16x16(w), g, tk, valid);
-        code[cb] = q.codes;
-        sfw |= q.sf << (8 * cb);
-      }
-      const int gc = c0 / 16 + 4 * half;  // multiple of 4
-      if (r < rows && gc < nbk) {
-        uint8_t* dst = codes_k + (grp * rows + r) * static_cast<int64_t>(cols / 2) + 8 * gc;
-        if (v8k && gc + 4 <= nbk) {
-          st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
-                       code[3].x, code[3].y);
-        } else {
-#pragma unroll
-          for (int cb = 0; cb < 4; ++cb)
-            if (gc + cb < nbk) st_u64(dst + 8 * cb, code[cb]);
-        }
-        *reinterpret_cast<uint32_t*>(sf_k + grp * sfk_group + sf_offset(r, gc, kck)) = sfw;
-      }
-    }
+    dual_tile_quant(tiles[cur], G, grp, (rem / G.tc) * kDR, (rem % G.tc) * kDC, g, tk, codes_k,
+                    sf_k, codes_n, sf_n);
     __syncthreads();  // the buffer is refilled two tiles from now
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 
   // zero the scale bytes of the padding rows of both copies, and publish g
   const int64_t gt = blockIdx.x * (int64_t)blockDim.x + t;
-  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-  const int64_t pk = rows_pad - rows, pn = cols_pad - cols;
-  for (int64_t i = gt; i < groups * pk * (kck / 4); i += nthreads) {
-    const int64_t grp = i / (pk * (kck / 4));
-    const int64_t rem = i - grp * pk * (kck / 4);
-    *reinterpret_cast<uint32_t*>(sf_k + grp * sfk_group +
-                                 sf_offset(rows + rem / (kck / 4), 4 * (rem % (kck / 4)), kck)) = 0u;
-  }
-  for (int64_t i = gt; i < groups * pn * (kcn / 4); i += nthreads) {
-    const int64_t grp = i / (pn * (kcn / 4));
-    const int64_t rem = i - grp * pn * (kcn / 4);
-    *reinterpret_cast<uint32_t*>(sf_n + grp * sfn_group +
-                                 sf_offset(cols + rem / (kcn / 4), 4 * (rem % (kcn / 4)), kcn)) = 0u;
-  }
+  dual_zero_padding(G, 0, groups, gt, (int64_t)gridDim.x * blockDim.x, sf_k, sf_n);
   if (gt < groups) g_out[gt] = global_scale(__uint_as_float(amax_bits[gt]));
 }
 
