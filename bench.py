@@ -43,8 +43,11 @@ def parse():
     ap.add_argument("--impl", default="minite", choices=["minite", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=["skewed", "mlp", "gate_up", "tiny"])
     ap.add_argument("--gemm-variant", type=int, default=0,
-                    help="grouped-GEMM kernel: 0 automatic, 1 single-CTA, 2 CTA pair")
+                    help="grouped-GEMM kernel: 0 automatic, 1 single-CTA one-chunk stages,"
+                         " 2 CTA pair, 4 CTA pair two-chunk stages, 5 single-CTA two-chunk stages")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip timing the rest of the NVFP4 backward beside the step")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches only (default: the step replayed as one CUDA graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -240,6 +243,50 @@ class Step:
                                     self.wd["g"], b.offsets, b.sf_offsets, self.dh, self.status, s)
         mark(9)
 
+    # The rest of the NVFP4 backward of the expert MLP, timed beside the step:
+    # W_gate_up in both orientations (one pass), SwiGLU backward with its
+    # per-row requantization, the gate_up dgrad GEMM (K = 2I, N = H) and the
+    # combine of dX back into token order.
+    BWD_STAGES = ["wq_gate_up_dual", "swiglu_bwd", "gemm_dgrad_gate_up", "combine_dx"]
+    BWD_LAUNCHES = 2 + 1 + 1 + 1
+
+    def init_backward(self):
+        import torch
+        T, H, E, k, I = self.T, self.H, self.E, self.k, self.I
+        dev, u8, f32 = self.dev, torch.uint8, torch.float32
+        M_ = T * k
+        self.wguT = dict(codes=torch.empty((E, H, I), dtype=u8, device=dev),
+                         sf=torch.empty((E, self.M.sf_bytes((H + 127) // 128 * 128, 2 * I)),
+                                        dtype=u8, device=dev))
+        self.dgu = dict(codes=torch.empty((M_, I), dtype=u8, device=dev),
+                        sf=torch.empty(self.M.sf_bytes(M_ + 128 * E, 2 * I), dtype=u8, device=dev),
+                        g=torch.empty(M_, dtype=f32, device=dev))
+        self.dx_perm = torch.empty((M_, H), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def run_backward(self, stream, events=None):
+        M, s, mlp = self.M, stream, self.mlp
+
+        def mark(i):
+            if events is not None:
+                events[i].record(s)
+
+        mark(0)
+        M.minite_quantize_nvfp4_dual(self.wgu_bf, self.wgu["codes"], self.wgu["sf"],
+                                     self.wguT["codes"], self.wguT["sf"], self.wgu["g"], self.ws_q,
+                                     self.status, s)
+        mark(1)
+        M.minite_swiglu_backward_quant(mlp.gate_up, self.dh, mlp.perm_w, self.E, mlp.offsets,
+                                       mlp.sf_offsets, self.dgu["codes"], self.dgu["sf"],
+                                       self.dgu["g"], self.status, s)
+        mark(2)
+        M.minite_grouped_gemm_nvfp4(self.dgu["codes"], self.dgu["sf"], self.dgu["g"],
+                                    self.wguT["codes"], self.wguT["sf"], self.wgu["g"],
+                                    mlp.offsets, mlp.sf_offsets, self.dx_perm, self.status, s)
+        mark(3)
+        M.minite_moe_combine(self.dx_perm, mlp.dest_row, self.dx, self.status, s)
+        mark(4)
+
     # kernels launched per step by the library (memsets not counted): weight
     # quantization 2 + 2, permutation 4, GEMM 1, SwiGLU 1, GEMM 1, combine 1,
     # permutation of dY 4, GEMM 1
@@ -250,6 +297,17 @@ class Step:
         H, I = self.H, self.I
         return dict(gemm_gate_up=2.0 * Mu * 2 * I * H, gemm_down=2.0 * Mu * H * I,
                     gemm_dgrad=2.0 * Mu * I * H, used_rows=Mu)
+
+    def backward_algorithmic_bytes(self):
+        """Bytes each backward stage must move at minimum (read once + write once)."""
+        T, H, E, k, I = self.T, self.H, self.E, self.k, self.I
+        Mu = int(self.mlp.offsets[-1].item())
+        sfb = lambda r, c: r * c / 16  # noqa: E731
+        return dict(
+            wq_gate_up_dual=E * 2 * I * H * 2 + 2 * (E * 2 * I * H / 2 + sfb(E * 2 * I, H)),
+            swiglu_bwd=Mu * (2 * I * 2 + I * 2 + 4) + Mu * (I + 2 * I / 16 + 4),
+            combine_dx=Mu * H * 2 + T * H * 2 + T * k * 4,
+        )
 
     def algorithmic_bytes(self):
         """Bytes each stage must move at minimum (read once + write once)."""
@@ -339,6 +397,37 @@ def run_gpu(args):
     ms_per_step = ms / args.steps
     stage_ms = {s: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j, s in enumerate(Step.STAGES)}
+
+    # the rest of the NVFP4 backward, eager, after the forward step's buffers
+    # hold one step's results
+    backward = None
+    if not args.no_backward:
+        step.init_backward()
+        for _ in range(args.warmup):
+            step.run_backward(stream)
+        barrier()
+        nb = len(Step.BWD_STAGES)
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)]
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            step.run_backward(stream, bev[i])
+        barrier()
+        assert int(step.status.item()) == 0, f"device status {int(step.status.item())}"
+        bst = {s: statistics.mean(bev[i][j].elapsed_time(bev[i][j + 1])
+                                  for i in range(args.steps))
+               for j, s in enumerate(Step.BWD_STAGES)}
+        bab = step.backward_algorithmic_bytes()
+        Mu = int(step.mlp.offsets[-1].item())
+        dg_fl = 2.0 * Mu * 2 * step.I * step.H
+        backward = {
+            "stages": "W_gate_up quantization in both orientations (one pass) + SwiGLU backward"
+                      " with per-row requant + gate_up dgrad GEMM (K=2I, N=H) + combine of dX",
+            "ms": round(sum(bst.values()), 4),
+            "stages_ms": {k_: round(v, 4) for k_, v in bst.items()},
+            "stages_hbm_gbs": {k_: round(bab[k_] / (bst[k_] / 1e3) / 1e9, 1) for k_ in bab},
+            "gemm_dgrad_gate_up_tflops": dg_fl / (bst["gemm_dgrad_gate_up"] / 1e3) / 1e12,
+            "gpu_launches": Step.BWD_LAUNCHES * args.steps,
+        }
 
     # end to end: every step copies its inputs in from pinned host memory and
     # its result y out to pinned host memory. Inputs and y are double-buffered
@@ -446,6 +535,7 @@ def run_gpu(args):
                      "peak_source": f"{peaks['source']} bf16 sustained x {FP4_OVER_BF16:g} (nominal FP4/BF16)"},
         "clocks": clk,
         "gpu_launches": Step.LAUNCHES * args.steps,
+        "backward": backward,
         "e2e": e2e,
         "cpu_baseline": None,
     }

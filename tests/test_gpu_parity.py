@@ -602,6 +602,64 @@ def test_mlp_forward_full_size_sampled_tokens_match_oracle_chain():
     assert same > 0.9, same
 
 
+@pytest.mark.parametrize("name,T", [("tiny", None), ("mlp", 256)])
+def test_backward_chain_stagewise(name, T):
+    """The NVFP4 backward of the expert MLP, stage by stage: permute+quant of
+    dY, down dgrad GEMM (W_down quantized along N), SwiGLU backward with
+    per-row requantization, gate_up dgrad GEMM (W_gate_up quantized along N),
+    combine of dX. Each stage is checked against the oracle fed with the
+    GPU's inputs to that stage: codes, scales and the combine bit-exact, GEMM
+    outputs within one BF16 ulp of the exact result."""
+    d = IN.make_moe_inputs(name, T=T)
+    c = d["cfg"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    rng = np.random.default_rng(9)
+    dy = O.f32_to_bf16(rng.standard_normal((T, H)).astype(np.float32))
+    ids, w = np_dev(d["topk_ids"]), np_dev(d["topk_w"])
+    wgu, wd = _weights(d)
+    _, wdT = M.quantize_dual(bf16_dev(d["w_down"]))
+    _, wguT = M.quantize_dual(bf16_dev(d["w_gate_up"]))
+    mlp = M.MoEMLP(T, H, I, E, k)
+    mlp.forward(bf16_dev(d["x"]), ids, w, wgu, wd)
+    bwd = M.MoEMLP(T, H, I, E, k)
+    bwd.permute_quant(bf16_dev(dy), ids, None)
+    Mt = T * k
+    st = _status()
+    dh = torch.empty((Mt, I), dtype=torch.bfloat16, device="cuda")
+    M.minite_grouped_gemm_nvfp4(bwd.a_codes, bwd.a_sf, bwd.a_g, wdT["codes"], wdT["sf"], wdT["g"],
+                                bwd.offsets, bwd.sf_offsets, dh, st)
+    dgu_codes = torch.zeros((Mt, I), dtype=torch.uint8, device="cuda")
+    dgu_sf = torch.full((M.sf_bytes(Mt + 128 * E, 2 * I),), 0xAB, dtype=torch.uint8, device="cuda")
+    dgu_g = torch.zeros(Mt, dtype=torch.float32, device="cuda")
+    M.minite_swiglu_backward_quant(mlp.gate_up, dh, mlp.perm_w, E, mlp.offsets, mlp.sf_offsets,
+                                   dgu_codes, dgu_sf, dgu_g, st)
+    dx_perm = torch.empty((Mt, H), dtype=torch.bfloat16, device="cuda")
+    M.minite_grouped_gemm_nvfp4(dgu_codes, dgu_sf, dgu_g, wguT["codes"], wguT["sf"], wguT["g"],
+                                mlp.offsets, mlp.sf_offsets, dx_perm, st)
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    M.minite_moe_combine(dx_perm, mlp.dest_row, dx, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(mlp.status.item()) == 0 and int(bwd.status.item()) == 0
+
+    p = O.moe_permute_quant(dy, d["topk_ids"], None, E)
+    check_permute(bwd, p, H)
+    off, sfo = p["expert_offsets"], p["sf_row_offsets"]
+    Mu = int(off[-1])
+    qdT = O.quantize_weights(d["w_down"], along_rows=True)
+    dh_exact, _ = O.grouped_gemm_exact(p["codes"], p["sf"], p["row_g"], qdT[0], qdT[1], qdT[3], off)
+    assert_bf16_within_one_ulp(u16(dh)[:Mu], dh_exact, "dh")
+    perm_w = mlp.perm_w.cpu().numpy()
+    sb = O.swiglu_backward_quant(u16(mlp.gate_up), u16(dh), perm_w, off, sfo)
+    assert np.array_equal(dgu_codes.cpu().numpy()[:Mu], sb["codes"])
+    assert np.array_equal(dgu_sf.cpu().numpy()[:sb["sf_swizzled"].size], sb["sf_swizzled"])
+    assert np.array_equal(dgu_g.cpu().numpy()[:Mu].view(np.uint32), sb["row_g"].view(np.uint32))
+    qguT = O.quantize_weights(d["w_gate_up"], along_rows=True)
+    dx_exact, _ = O.grouped_gemm_exact(sb["codes"], sb["sf"], sb["row_g"], qguT[0], qguT[1],
+                                       qguT[3], off)
+    assert_bf16_within_one_ulp(u16(dx_perm)[:Mu], dx_exact, "dx_perm")
+    assert np.array_equal(u16(dx), O.moe_combine(u16(dx_perm), mlp.dest_row.cpu().numpy()))
+
+
 # --------------------------------------------------------------------- failure detection
 
 @pytest.mark.parametrize("variant", VARIANTS)
