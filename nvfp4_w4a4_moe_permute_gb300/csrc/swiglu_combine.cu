@@ -34,16 +34,36 @@ __device__ __forceinline__ float silu_spec(float g) {
 // The gates are BF16, so silu takes at most 2^16 distinct inputs: each CTA
 // tabulates silu_spec in shared memory for |g| in [2^-24, 2^8) (32 binades,
 // both signs, 32 KB) and evaluates the formula only for gates outside it.
-// Entry index: (sign << 12) | (|g| bits - bits of 2^-24).
+// Entry index: 2 * (|g| bits - bits of 2^-24) + sign.
 constexpr uint32_t kLutLo = (127u - 24u) << 7;  // BF16 bits of 2^-24
 constexpr uint32_t kLutSpan = 32u << 7;          // 4096 magnitudes per sign
 constexpr int kLutEntries = 2 * static_cast<int>(kLutSpan);
 
+__device__ __forceinline__ uint32_t lut_gate_bits(int i) {
+  return (static_cast<uint32_t>(i & 1) << 15) | (kLutLo + static_cast<uint32_t>(i >> 1));
+}
+
 __device__ void build_silu_lut_part(float* lut, int t, int nthreads) {
-  for (int i = t; i < kLutEntries; i += nthreads) {
-    const uint32_t bits = (static_cast<uint32_t>(i >> 12) << 15) | (kLutLo + (i & 4095));
-    lut[i] = silu_spec(__uint_as_float(bits << 16));
-  }
+  for (int i = t; i < kLutEntries; i += nthreads)
+    lut[i] = silu_spec(__uint_as_float(lut_gate_bits(i) << 16));
+}
+
+// Byte offsets into a table of the two gates of a packed BF16 pair whose
+// magnitudes both lie in [2^-24, 2^8): per 16-bit half h, t = h - bits of
+// 2^-24 leaves the sign in bit 15 and the magnitude offset in bits 0..11
+// (bits 12..14 clear); the offset moves to bits 3..14 and the sign to bit 2,
+// i.e. 4 * (2 * offset + sign). No borrow crosses the halves since both are
+// at least the subtrahend.
+__device__ __forceinline__ void lut_offsets(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  constexpr uint32_t kMask = 0x7FF87FF8u;
+  const uint32_t t = w - (kLutLo | (kLutLo << 16));
+  const uint32_t r = ((t << 3) & kMask) | ((t >> 13) & ~kMask);
+  lo = r & 0xFFFFu;
+  hi = r >> 16;
+}
+
+__device__ __forceinline__ float lut_at(const float* lut, uint32_t byte_off) {
+  return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(lut) + byte_off);
 }
 
 // h = (silu(g) * u) * w for the 16 gates and ups of one block. Blocks whose
@@ -65,16 +85,17 @@ __device__ __forceinline__ void swiglu_block(const float* lut, const uint32_t (&
   if (lo_mag >= kLutLo && hi_mag < kLutLo + kLutSpan) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t a = wg[i], b = wg[i] >> 16;
-      h[2 * i] = lut[((a - kLutLo) & (kLutSpan - 1)) | ((a >> 3) & kLutSpan)];
-      h[2 * i + 1] = lut[((b - kLutLo) & (kLutSpan - 1)) | ((b >> 3) & kLutSpan)];
+      uint32_t a, b;
+      lut_offsets(wg[i], a, b);
+      h[2 * i] = lut_at(lut, a);
+      h[2 * i + 1] = lut_at(lut, b);
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t bits = (i & 1) ? (wg[i >> 1] >> 16) : (wg[i >> 1] & 0xFFFFu);
       const uint32_t off = (bits & 0x7FFFu) - kLutLo;
-      h[i] = off < kLutSpan ? lut[off | ((bits >> 3) & kLutSpan)]
+      h[i] = off < kLutSpan ? lut[2 * off + (bits >> 15)]
                             : silu_spec(__uint_as_float(bits << 16));
     }
   }
@@ -230,10 +251,8 @@ __device__ __forceinline__ void silu_dsilu_spec(float g, float& silu, float& dsi
 }
 
 __device__ void build_silu_bwd_luts(float* lut_s, float* lut_d, int t, int nthreads) {
-  for (int i = t; i < kLutEntries; i += nthreads) {
-    const uint32_t bits = (static_cast<uint32_t>(i >> 12) << 15) | (kLutLo + (i & 4095));
-    silu_dsilu_spec(__uint_as_float(bits << 16), lut_s[i], lut_d[i]);
-  }
+  for (int i = t; i < kLutEntries; i += nthreads)
+    silu_dsilu_spec(__uint_as_float(lut_gate_bits(i) << 16), lut_s[i], lut_d[i]);
 }
 
 // dg and du of one 16-element block from its gates, ups and dh (raw BF16).
@@ -254,11 +273,13 @@ __device__ __forceinline__ void swiglu_bwd_block(const float* lut_s, const float
   float sl[16], ds[16];
   if (lo_mag >= kLutLo && hi_mag < kLutLo + kLutSpan) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t b = (i & 1) ? (wg[i >> 1] >> 16) : wg[i >> 1];
-      const uint32_t idx = ((b - kLutLo) & (kLutSpan - 1)) | ((b >> 3) & kLutSpan);
-      sl[i] = lut_s[idx];
-      ds[i] = lut_d[idx];
+    for (int i = 0; i < 8; ++i) {
+      uint32_t a, b;
+      lut_offsets(wg[i], a, b);
+      sl[2 * i] = lut_at(lut_s, a);
+      ds[2 * i] = lut_at(lut_d, a);
+      sl[2 * i + 1] = lut_at(lut_s, b);
+      ds[2 * i + 1] = lut_at(lut_d, b);
     }
   } else {
 #pragma unroll
@@ -266,7 +287,7 @@ __device__ __forceinline__ void swiglu_bwd_block(const float* lut_s, const float
       const uint32_t bits = (i & 1) ? (wg[i >> 1] >> 16) : (wg[i >> 1] & 0xFFFFu);
       const uint32_t off = (bits & 0x7FFFu) - kLutLo;
       if (off < kLutSpan) {
-        const uint32_t idx = off | ((bits >> 3) & kLutSpan);
+        const uint32_t idx = 2 * off + (bits >> 15);
         sl[i] = lut_s[idx];
         ds[i] = lut_d[idx];
       } else {
