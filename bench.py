@@ -151,7 +151,7 @@ class Step:
     """All device buffers of one step; ``run`` enqueues the whole path."""
 
     STAGES = ["wq_gate_up", "wq_down_both", "permute_x", "gemm_gate_up", "swiglu", "gemm_down",
-              "combine", "permute_dy", "gemm_dgrad"]
+              "combine", "combine_bwd_quant_dy", "gemm_dgrad"]
 
     def __init__(self, d, dev):
         import torch
@@ -192,6 +192,8 @@ class Step:
         self.ws_q = torch.empty(M.minite_workspace_bytes(M.OP_QUANTIZE, E), dtype=u8, device=dev)
         self.mlp = M.MoEMLP(T, H, I, E, k, dev)
         self.bwd = M.MoEMLP(T, H, I, E, k, dev)  # permuted dY buffers (same routing)
+        self.ws_cb = torch.empty(M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, T, H),
+                                 dtype=u8, device=dev)
         self.dh = torch.empty((T * k, I), dtype=bf, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.mlp.status = self.status
@@ -236,11 +238,15 @@ class Step:
         mark(6)
         M.minite_moe_combine(mlp.down, mlp.dest_row, mlp.y, self.status, s)
         mark(7)
-        self.bwd.permute_quant(self.dy, self.ids, None, s)
-        mark(8)
+        # backward of the combine: dY to the forward's permuted rows, quantized
         b = self.bwd
+        M.minite_moe_combine_backward_quant(self.dy, self.E, mlp.dest_row, mlp.offsets,
+                                            mlp.sf_offsets, mlp.perm_src, b.a_codes, b.a_sf,
+                                            b.a_g, self.ws_cb, self.status, s)
+        mark(8)
         M.minite_grouped_gemm_nvfp4(b.a_codes, b.a_sf, b.a_g, self.wdT["codes"], self.wdT["sf"],
-                                    self.wd["g"], b.offsets, b.sf_offsets, self.dh, self.status, s)
+                                    self.wd["g"], mlp.offsets, mlp.sf_offsets, self.dh,
+                                    self.status, s)
         mark(9)
 
     # The rest of the NVFP4 backward of the expert MLP, timed beside the step:
@@ -288,9 +294,9 @@ class Step:
         mark(4)
 
     # kernels launched per step by the library (memsets not counted): weight
-    # quantization 2 + 2, permutation 4, GEMM 1, SwiGLU 1, GEMM 1, combine 1,
-    # permutation of dY 4, GEMM 1
-    LAUNCHES = 2 + 2 + 4 + 1 + 1 + 1 + 1 + 4 + 1
+    # quantization 2 + 2, permutation 5, GEMM 1, SwiGLU 1, GEMM 1, combine 1,
+    # combine backward with dY quantization 2, GEMM 1
+    LAUNCHES = 2 + 2 + 5 + 1 + 1 + 1 + 1 + 2 + 1
 
     def flops(self):
         Mu = int(self.mlp.offsets[-1].item())
@@ -320,7 +326,7 @@ class Step:
             permute_x=T * H * 2 + T * k * 8 + Mu * (H / 2 + H / 16 + 4 + 12),
             swiglu=Mu * 2 * I * 2 + Mu * (I / 2 + I / 16 + 4),
             combine=Mu * H * 2 + T * H * 2 + T * k * 4,
-            permute_dy=T * H * 2 + T * k * 4 + Mu * (H / 2 + H / 16 + 4 + 8),
+            combine_bwd_quant_dy=T * H * 2 + T * k * 4 + Mu * (H / 2 + H / 16 + 4 + 4),
         )
 
 
@@ -520,8 +526,8 @@ def run_gpu(args):
         "data": "synthetic (seeded numpy; Qwen3-30B-A3B shapes, random weights)",
         "config": {"workload": workload_name(args.workload, d["cfg"]),
                    "step": "wq(gate_up along K; down along K and along N in one pass) + permute+quant"
-                           " + gate_up GEMM + SwiGLU+quant + down GEMM + combine + permute+quant dY"
-                           " + dgrad GEMM",
+                           " + gate_up GEMM + SwiGLU+quant + down GEMM + combine + combine backward"
+                           " with dY quant (forward routing) + dgrad GEMM",
                    "l2": "inputs larger than L2 (each step streams ~5 GB)",
                    "launch": "eager" if args.no_graph else "CUDA graph of the step, replayed",
                    "parallelism": f"replicas{world}"},

@@ -64,7 +64,7 @@ typedef enum {
 enum { MINITE_SCALE_PER_ROW = 0, MINITE_SCALE_PER_GROUP = 1 };
 enum { MINITE_ALONG_COLS = 0, MINITE_ALONG_ROWS = 1 };
 enum { MINITE_OUT_BF16 = 0, MINITE_OUT_FP32 = 1 };
-enum { MINITE_OP_QUANTIZE = 0, MINITE_OP_PERMUTE_QUANT = 1 };
+enum { MINITE_OP_QUANTIZE = 0, MINITE_OP_PERMUTE_QUANT = 1, MINITE_OP_COMBINE_BACKWARD_QUANT = 2 };
 
 /*
  * minite_quantize_nvfp4 -- NVFP4 quantization of `groups` BF16 matrices.
@@ -325,8 +325,43 @@ int minite_moe_combine(const void* expert_out, const int32_t* dest_row,
                        int64_t T, int64_t M, int64_t N, int32_t k, void* y,
                        int32_t* status, minite_stream_t stream);
 
+/*
+ * minite_moe_combine_backward_quant -- the backward of the combine with the
+ * NVFP4 quantization of its result fused in: dD[dest_row[t, j]] = dY[t] for
+ * every routed pair (t, j), i.e. dY laid out like the forward's permuted
+ * activations, quantized per token exactly as minite_moe_permute_quant
+ * quantizes x (same codes, scales, layout and row_g), reusing the forward
+ * permutation's routing instead of ranking the routing ids again. The
+ * result is the A operand of the down-projection dgrad GEMM.
+ *
+ * Cites: miniTE report summary, "Follow the numerical execution path"
+ * (per-token scaling) and "Two complementary interventions" (contiguous
+ * expert buffers, device-side metadata, fused scale layout), applied to the
+ * backward; the pages run the backward in BF16 ("Respect the timing
+ * boundaries"), so this NVFP4 variant is a reading.
+ *
+ * dy:        device, BF16 [T, H], 16-byte aligned.
+ * dest_row, expert_offsets, sf_row_offsets, perm_src: device, the forward
+ *            permutation's outputs for the same routing (unchanged).
+ * codes, sf, row_g: device outputs as for minite_moe_permute_quant.
+ * workspace: device, >= minite_workspace_bytes(MINITE_OP_COMBINE_BACKWARD_QUANT,
+ *            T, H, 0, 0) bytes, 256-byte aligned, caller-owned scratch.
+ * The routing is checked on the device: inconsistent offsets make the
+ * kernels write nothing; a dest_row past expert_offsets[E] or a perm_src
+ * outside [0, T) is skipped; each sets bit 1<<MINITE_ERR_INVALID_ARG in
+ * *status. The call is asynchronous on stream.
+ * Shape rules: as minite_moe_permute_quant.
+ */
+int minite_moe_combine_backward_quant(const void* dy, int64_t T, int64_t H, int32_t E, int32_t k,
+                                      const int32_t* dest_row, const int32_t* expert_offsets,
+                                      const int32_t* sf_row_offsets, const int32_t* perm_src,
+                                      uint8_t* codes, uint8_t* sf, float* row_g,
+                                      void* workspace, size_t ws_bytes, int32_t* status,
+                                      minite_stream_t stream);
+
 /* Workspace bytes needed by `op` (MINITE_OP_QUANTIZE: a = groups;
- * MINITE_OP_PERMUTE_QUANT: a = T, b = H, E, k). 0 means none needed. */
+ * MINITE_OP_PERMUTE_QUANT: a = T, b = H, E, k; MINITE_OP_COMBINE_BACKWARD_QUANT:
+ * a = T, b = H). 0 means none needed. */
 size_t minite_workspace_bytes(int op, int64_t a, int64_t b, int32_t E, int32_t k);
 
 /* Static description of a status code. */

@@ -8,6 +8,7 @@
 namespace minite {
 
 size_t permute_workspace_bytes(int64_t T, int64_t H, int32_t E, int32_t k);
+size_t combine_backward_workspace_bytes(int64_t T, int64_t H);
 
 int num_sms() {
   static std::atomic<int> cache[64];
@@ -55,6 +56,8 @@ extern "C" size_t minite_workspace_bytes(int op, int64_t a, int64_t b, int32_t E
       return a > 0 ? static_cast<size_t>(a) * sizeof(uint32_t) : 0;
     case MINITE_OP_PERMUTE_QUANT:
       return (a > 0 && b > 0 && E > 0 && k > 0) ? permute_workspace_bytes(a, b, E, k) : 0;
+    case MINITE_OP_COMBINE_BACKWARD_QUANT:
+      return (a > 0 && b > 0) ? combine_backward_workspace_bytes(a, b) : 0;
     default:
       return 0;
   }

@@ -140,6 +140,21 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Offsets produced by the permutation must start at 0, be non-decreasing,
+// end at most at `rows`, and the padded offsets must match the counts. A
+// kernel that finds a violation skips all work and reports INVALID_ARG.
+// Block-wide: every thread of the block must call it.
+__device__ inline bool offsets_consistent(const int32_t* s_off, const int32_t* s_sfoff, int E,
+                                   int64_t rows) {
+  bool bad = false;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int cnt = s_off[e + 1] - s_off[e];
+    if (cnt < 0 || s_sfoff[e + 1] - s_sfoff[e] != ((cnt + 127) & ~127)) bad = true;
+  }
+  if (threadIdx.x == 0 && (s_off[0] != 0 || s_sfoff[0] != 0 || s_off[E] > rows)) bad = true;
+  return !__syncthreads_or(bad);
+}
+
 // Byte offset of the scale of (row r, SF column c) in a region with kc SF
 // columns: 128-row x 4-column atoms of 512 bytes.
 __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t kc) {

@@ -223,13 +223,16 @@ __global__ void __launch_bounds__(kPermThreads) permute_route_kernel(
 // once in registers and writes its codes, scales and g to each of its k
 // permuted rows. Each warp requests its next token (row and routing) before
 // it writes the current one.
+// ids == nullptr: the routing comes from the caller (dest_row and offsets of
+// an earlier permutation), which is then checked on the device; only the
+// token-order scale mode (sfc != nullptr) is used this way.
 template <int NCH>
 __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int64_t T, int H, int E,
     int k, const int32_t* __restrict__ expert_offsets,
     const int32_t* __restrict__ sf_row_offsets, const int32_t* __restrict__ dest_row,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
-    uint8_t* __restrict__ sfc, float* __restrict__ gtok) {
+    uint8_t* __restrict__ sfc, float* __restrict__ gtok, int32_t* status) {
   extern __shared__ int32_t sm[];
   int32_t* s_off = sm;                 // [E+1]
   int32_t* s_sfoff = s_off + (E + 1);  // [E+1]
@@ -238,6 +241,11 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
     s_sfoff[i] = sf_row_offsets[i];
   }
   __syncthreads();
+  if (ids == nullptr && !offsets_consistent(s_off, s_sfoff, E, T * k)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MINITE_ERR_INVALID_ARG);
+    return;
+  }
+  const int used = s_off[E];
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -257,7 +265,7 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
   auto fetch = [&](int64_t t) {
     if (lane < k) {
       dest = dest_row[t * k + lane];
-      e = ids[t * k + lane];
+      e = ids ? ids[t * k + lane] : 0;
     }
     const uint16_t* xr = x + t * H;
     m = a32 ? load_row_blocks<NCH, true>(xr, nb, w, am)
@@ -285,6 +293,10 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
     for (int j = 0; j < k; ++j) {
       const int d = __shfl_sync(0xffffffffu, dcur, j);
       if (d < 0) continue;  // warp-uniform
+      if (d >= used) {      // only a caller-given routing can point past the used rows
+        if (lane == 0) set_status(status, MINITE_ERR_INVALID_ARG);
+        continue;
+      }
       const int ej = __shfl_sync(0xffffffffu, ecur, j);
       const int64_t r = static_cast<int64_t>(s_sfoff[ej]) + (d - s_off[ej]);
       uint8_t* srow = sf + ((r >> 7) * (kc >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
@@ -322,8 +334,8 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
 __global__ void __launch_bounds__(kPermThreads) permute_sf_gather_kernel(
     const uint8_t* __restrict__ sfc, const float* __restrict__ gtok,
     const int32_t* __restrict__ perm_src, const int32_t* __restrict__ expert_offsets,
-    const int32_t* __restrict__ sf_row_offsets, int E, int kc, uint8_t* __restrict__ sf,
-    float* __restrict__ row_g) {
+    const int32_t* __restrict__ sf_row_offsets, int64_t T, int k, int E, int kc,
+    uint8_t* __restrict__ sf, float* __restrict__ row_g, int32_t* status) {
   extern __shared__ int32_t sm[];
   int32_t* s_off = sm;                 // [E+1]
   int32_t* s_sfoff = s_off + (E + 1);  // [E+1]
@@ -332,6 +344,19 @@ __global__ void __launch_bounds__(kPermThreads) permute_sf_gather_kernel(
     s_sfoff[i] = sf_row_offsets[i];
   }
   __syncthreads();
+  if (!offsets_consistent(s_off, s_sfoff, E, T * k)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MINITE_ERR_INVALID_ARG);
+    return;
+  }
+  // a permuted row's source token, or -1 (with the error bit) if out of range
+  auto source = [&](int p) {
+    const int tk = perm_src[p];
+    if (tk < 0 || tk >= T) {
+      set_status(status, MINITE_ERR_INVALID_ARG);
+      return -1;
+    }
+    return tk;
+  };
   const int t = threadIdx.x;
   const int natoms = kc / 4;
   const int ngroups = (natoms + 3) / 4;
@@ -346,12 +371,15 @@ __global__ void __launch_bounds__(kPermThreads) permute_sf_gather_kernel(
     const int row0 = 128 * blk - s_sfoff[lo];  // local row of the block's first row
     const int cnt = s_off[lo + 1] - s_off[lo];
     const int p0 = s_off[lo] + row0;
-    if (t < 128 && row0 + t < cnt) row_g[p0 + t] = gtok[perm_src[p0 + t]];
+    if (t < 128 && row0 + t < cnt) {
+      const int tk = source(p0 + t);
+      row_g[p0 + t] = tk >= 0 ? gtok[tk] : 0.0f;
+    }
     for (int u = t; u < 32 * ngroups; u += blockDim.x) {
       const int i = u & 31, ag = u >> 5;
       int tok[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tok[q] = row0 + 32 * q + i < cnt ? perm_src[p0 + 32 * q + i] : -1;
+      for (int q = 0; q < 4; ++q) tok[q] = row0 + 32 * q + i < cnt ? source(p0 + 32 * q + i) : -1;
       uint32_t wv[4][4];  // [q][atom j]: 4 scale bytes of row 32q+i, columns 4(4ag+j) ..
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -385,7 +413,52 @@ namespace minite {
 size_t permute_workspace_bytes(int64_t T, int64_t H, int32_t E, int32_t k) {
   return perm_ws_bytes(T, H, E, k);
 }
+// The combine backward keeps only the token-order scales and global scales.
+size_t combine_backward_workspace_bytes(int64_t T, int64_t H) {
+  const size_t kc = static_cast<size_t>(((H / 16) + 3) & ~int64_t(3));
+  return align256(static_cast<size_t>(T) * kc) + align256(static_cast<size_t>(T) * 4);
+}
 }  // namespace minite
+
+// The per-token quantization (codes to every destination row; scales to the
+// token-order scratch when compact, else straight to the rows) and, when
+// compact, the scale gather. ids == nullptr: caller-given routing.
+static int launch_quant_gather(const void* x, const int32_t* topk_ids, int64_t T, int64_t H,
+                               int32_t E, int32_t k, const int32_t* expert_offsets,
+                               const int32_t* sf_row_offsets, const int32_t* perm_src,
+                               const int32_t* dest_row, uint8_t* codes, uint8_t* sf,
+                               float* row_g, const PermWs& w, bool compact, int32_t* status,
+                               cudaStream_t s) {
+  const size_t smem = 2 * (E + 1) * sizeof(int32_t);
+  const int nch = static_cast<int>((H / 16 + 31) / 32);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  const int h = static_cast<int>(H);
+  const int per_sm = nch <= 5 ? 3 : 2;
+  int64_t qblocks = (T + kPermThreads / 32 - 1) / (kPermThreads / 32);
+  if (qblocks > static_cast<int64_t>(num_sms()) * per_sm) qblocks = num_sms() * per_sm;
+  if (qblocks < 1) qblocks = 1;
+  switch (nch) {
+#define MINITE_CASE(N)                                                                     \
+  case N:                                                                                  \
+    permute_quant_kernel<N><<<static_cast<unsigned>(qblocks), kPermThreads, smem, s>>>(    \
+        xb, topk_ids, T, h, E, k, expert_offsets, sf_row_offsets, dest_row, codes, sf,     \
+        row_g, w.sfc, w.gtok, status);                                                     \
+    break;
+    MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
+    MINITE_CASE(7) MINITE_CASE(8)
+#undef MINITE_CASE
+    default: return MINITE_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (compact) {
+    const int kc = static_cast<int>(((H / 16) + 3) & ~int64_t(3));
+    int64_t gblocks = (T * k) / 128 + E;   // upper bound of the 128-row scale blocks
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+    if (gblocks > cap) gblocks = cap;
+    permute_sf_gather_kernel<<<static_cast<unsigned>(gblocks), kPermThreads, smem, s>>>(
+        w.sfc, w.gtok, perm_src, expert_offsets, sf_row_offsets, T, k, E, kc, sf, row_g, status);
+  }
+  return MINITE_OK;
+}
 
 // compact = true: scales go to a token-order scratch and the scale gather
 // writes the swizzled layout with whole-atom stores (needs the full
@@ -422,34 +495,9 @@ static int permute_quant_impl(const void* x, const int32_t* topk_ids, const floa
   permute_route_kernel<<<static_cast<unsigned>((pairs + kPermThreads - 1) / kPermThreads),
                          kPermThreads, 0, s>>>(topk_ids, topk_w, T, E, k, ct, nchunks, w.table,
                                                expert_offsets, perm_src, dest_row, perm_w);
-  const size_t smem = 2 * (E + 1) * sizeof(int32_t);
-  const int nch = static_cast<int>((H / 16 + 31) / 32);
-  const uint16_t* xb = static_cast<const uint16_t*>(x);
-  const int h = static_cast<int>(H);
-  const int per_sm = nch <= 5 ? 3 : 2;
-  int64_t qblocks = (T + kPermThreads / 32 - 1) / (kPermThreads / 32);
-  if (qblocks > static_cast<int64_t>(num_sms()) * per_sm) qblocks = num_sms() * per_sm;
-  if (qblocks < 1) qblocks = 1;
-  switch (nch) {
-#define MINITE_CASE(N)                                                                     \
-  case N:                                                                                  \
-    permute_quant_kernel<N><<<static_cast<unsigned>(qblocks), kPermThreads, smem, s>>>(    \
-        xb, topk_ids, T, h, E, k, expert_offsets, sf_row_offsets, dest_row, codes, sf,     \
-        row_g, w.sfc, w.gtok);                                                             \
-    break;
-    MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
-    MINITE_CASE(7) MINITE_CASE(8)
-#undef MINITE_CASE
-    default: return MINITE_ERR_UNSUPPORTED_SHAPE;
-  }
-  if (compact) {
-    const int kc = static_cast<int>(((H / 16) + 3) & ~int64_t(3));
-    int64_t gblocks = (T * k) / 128 + E;   // upper bound of the 128-row scale blocks
-    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
-    if (gblocks > cap) gblocks = cap;
-    permute_sf_gather_kernel<<<static_cast<unsigned>(gblocks), kPermThreads, smem, s>>>(
-        w.sfc, w.gtok, perm_src, expert_offsets, sf_row_offsets, E, kc, sf, row_g);
-  }
+  const int rc = launch_quant_gather(x, topk_ids, T, H, E, k, expert_offsets, sf_row_offsets,
+                                     perm_src, dest_row, codes, sf, row_g, w, compact, status, s);
+  if (rc != MINITE_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
 
@@ -463,6 +511,38 @@ extern "C" int minite_moe_permute_quant(const void* x, const int32_t* topk_ids,
   return permute_quant_impl(x, topk_ids, topk_w, T, H, E, k, codes, sf, row_g, expert_offsets,
                             sf_row_offsets, perm_src, dest_row, perm_w, workspace, ws_bytes,
                             true, status, stream);
+}
+
+// The backward of the combine: dD[dest_row[t, j]] = dY[t] for every routed
+// pair, i.e. dY laid out like the forward's permuted activations. Each token
+// of dY is quantized once (per-token NVFP4) and its codes written to its k
+// rows, reusing the forward permutation's routing instead of ranking the
+// routing ids again.
+extern "C" int minite_moe_combine_backward_quant(
+    const void* dy, int64_t T, int64_t H, int32_t E, int32_t k, const int32_t* dest_row,
+    const int32_t* expert_offsets, const int32_t* sf_row_offsets, const int32_t* perm_src,
+    uint8_t* codes, uint8_t* sf, float* row_g, void* workspace, size_t ws_bytes,
+    int32_t* status, minite_stream_t stream) {
+  if (!dy || !dest_row || !expert_offsets || !sf_row_offsets || !perm_src || !codes || !sf ||
+      !row_g || !workspace)
+    return MINITE_ERR_INVALID_ARG;
+  if (T < 1 || H < 64 || H % 64 != 0 || H > 4096 || E < 1 || E > 1024 || k < 1 || k > 32)
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (T * k >= (int64_t(1) << 31) ||
+      (T * k + 128 * int64_t(E)) * ((H / 16 + 3) & ~3) >= (int64_t(1) << 40))
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(dy, 16) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(workspace, 256))
+    return MINITE_ERR_INVALID_ARG;
+  if (ws_bytes < combine_backward_workspace_bytes(T, H)) return MINITE_ERR_INVALID_ARG;
+  PermWs w = {};
+  const size_t kc = static_cast<size_t>(((H / 16) + 3) & ~int64_t(3));
+  w.sfc = static_cast<uint8_t*>(workspace);
+  w.gtok = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(T * kc));
+  const int rc = launch_quant_gather(dy, nullptr, T, H, E, k, expert_offsets, sf_row_offsets,
+                                     perm_src, dest_row, codes, sf, row_g, w, true, status,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  if (rc != MINITE_OK) return rc;
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------

@@ -11,21 +11,6 @@
 
 namespace minite {
 
-// Offsets produced by the permutation must start at 0, be non-decreasing,
-// end at most at `rows`, and the padded offsets must match the counts. Any
-// violation makes the kernels below skip all work and report INVALID_ARG.
-// Block-wide: every thread of the block must call it.
-__device__ bool offsets_consistent(const int32_t* s_off, const int32_t* s_sfoff, int E,
-                                   int64_t rows) {
-  bool bad = false;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int cnt = s_off[e + 1] - s_off[e];
-    if (cnt < 0 || s_sfoff[e + 1] - s_sfoff[e] != ((cnt + 127) & ~127)) bad = true;
-  }
-  if (threadIdx.x == 0 && (s_off[0] != 0 || s_sfoff[0] != 0 || s_off[E] > rows)) bad = true;
-  return !__syncthreads_or(bad);
-}
-
 // silu(g) = g / (1 + exp_spec(-g)), every step an IEEE float operation.
 __device__ __forceinline__ float silu_spec(float g) {
   return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));

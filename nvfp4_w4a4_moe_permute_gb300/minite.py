@@ -19,7 +19,7 @@ from . import build as _build
 SCALE_PER_ROW, SCALE_PER_GROUP = 0, 1
 ALONG_COLS, ALONG_ROWS = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-OP_QUANTIZE, OP_PERMUTE_QUANT = 0, 1
+OP_QUANTIZE, OP_PERMUTE_QUANT, OP_COMBINE_BACKWARD_QUANT = 0, 1, 2
 ERR_TIMEOUT, ERR_BAD_ROUTING = 4, 5
 
 EXPORTS = [
@@ -29,6 +29,7 @@ EXPORTS = [
     "minite_status_string", "minite_version", "minite_test_convert",
     "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc", "minite_set_gemm_variant",
     "minite_test_div6_exhaustive", "minite_quantize_nvfp4_dual",
+    "minite_moe_combine_backward_quant",
 ]
 
 
@@ -57,6 +58,8 @@ def load(path: str | None = None):
                                      _vp, _vp, _vp, _vp, _sz, _vp, _vp],
         "minite_moe_permute_quant_noalloc": [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp,
                                              _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+        "minite_moe_combine_backward_quant": [_vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                              _vp, _vp, _vp, _sz, _vp, _vp],
         "minite_grouped_gemm_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                       _vp, _int, _vp, _vp],
         "minite_swiglu_weighted_quant": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -221,6 +224,18 @@ def minite_swiglu_backward_quant(gate_up, dh, perm_w, E, expert_offsets, sf_row_
                                              _p(expert_offsets), _p(sf_row_offsets), _p(codes),
                                              _p(sf), _p(row_g), _p(status), _s(stream))
     _check(rc, "minite_swiglu_backward_quant")
+
+
+def minite_moe_combine_backward_quant(dy, E, dest_row, expert_offsets, sf_row_offsets, perm_src,
+                                      codes, sf, row_g, workspace, status=None, stream=None):
+    T, H = dy.shape
+    k = dest_row.shape[1]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().minite_moe_combine_backward_quant(_p(dy), T, H, E, k, _p(dest_row),
+                                                  _p(expert_offsets), _p(sf_row_offsets),
+                                                  _p(perm_src), _p(codes), _p(sf), _p(row_g),
+                                                  _p(workspace), ws_bytes, _p(status), _s(stream))
+    _check(rc, "minite_moe_combine_backward_quant")
 
 
 def minite_moe_combine(expert_out, dest_row, y, status=None, stream=None):

@@ -54,6 +54,9 @@ def test_workspace_sizes(lib):
     # the token-order scale staging grows with H
     assert M.minite_workspace_bytes(M.OP_PERMUTE_QUANT, 4096, 4096, 128, 8) > a
     assert M.minite_workspace_bytes(99, 1) == 0
+    # token-order scales (T x H/16 bytes) and global scales (T floats)
+    assert M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, 4096, 2048) == 4096 * 128 + 4096 * 4
+    assert M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, 0, 2048) == 0
 
 
 def _c(lib, name):
@@ -103,6 +106,12 @@ def test_host_validation_rejects_bad_arguments(lib):
                                             fake, None, None) == 1
     assert lib.minite_swiglu_backward_quant(fake, vp(4112), None, 16, 128, 1, fake, fake, fake,
                                             fake, fake, None, None) == 1
+    # combine backward: H not a multiple of 64, no workspace, workspace too small
+    cb = lambda T, H, E, k, ws, n: lib.minite_moe_combine_backward_quant(  # noqa: E731
+        fake, T, H, E, k, fake, fake, fake, fake, fake, fake, fake, ws, n, None, None)
+    assert cb(16, 96, 2, 2, fake, 1 << 20) == 2
+    assert cb(16, 128, 2, 2, None, 1 << 20) == 1
+    assert cb(16, 128, 2, 2, fake, 8) == 1
     # combine: N not a multiple of 8, k too large
     assert lib.minite_moe_combine(fake, fake, 4, 8, 12, 2, fake, None, None) == 2
     assert lib.minite_moe_combine(fake, fake, 4, 8, 16, 64, fake, None, None) == 2

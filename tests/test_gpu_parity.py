@@ -221,6 +221,72 @@ def test_permute_tiny_config():
     check_permute(mlp, O.moe_permute_quant(d["x"], d["topk_ids"], d["topk_w"], E), d["cfg"]["H"])
 
 
+@pytest.mark.parametrize("name,T", [("tiny", None), ("skewed", 1500), ("mlp", 300)])
+def test_combine_backward_quant_equals_the_permutation_of_dy(name, T):
+    """The combine backward with fused quantization, given the forward's
+    routing, produces exactly what a fresh permutation of dY produces (codes,
+    scales, row_g) and matches the oracle's permutation of dY bit for bit."""
+    d = IN.make_moe_inputs(name, T=T, with_weights=False)
+    c = d["cfg"]
+    T, H, E, k = c["T"], c["H"], c["E"], c["k"]
+    rng = np.random.default_rng(17)
+    dy = _rand_bf16(rng, (T, H))
+    dy[0] = 0
+    ids, w = np_dev(d["topk_ids"]), np_dev(d["topk_w"])
+    fwd = M.MoEMLP(T, H, 64, E, k)
+    fwd.permute_quant(bf16_dev(d["x"]), ids, w)
+    ref = M.MoEMLP(T, H, 64, E, k)
+    ref.permute_quant(bf16_dev(dy), ids, None)
+    Mt = T * k
+    codes = torch.zeros((Mt, H // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.full((M.sf_bytes(Mt + 128 * E, H),), 0xAB, dtype=torch.uint8, device="cuda")
+    g = torch.zeros(Mt, dtype=torch.float32, device="cuda")
+    ws = torch.empty(M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, T, H), dtype=torch.uint8,
+                     device="cuda")
+    st = _status()
+    M.minite_moe_combine_backward_quant(bf16_dev(dy), E, fwd.dest_row, fwd.offsets, fwd.sf_offsets,
+                                        fwd.perm_src, codes, sf, g, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    Mu = int(fwd.offsets[-1].item())
+    assert torch.equal(codes[:Mu], ref.a_codes[:Mu])
+    assert torch.equal(g[:Mu], ref.a_g[:Mu])
+    p = O.moe_permute_quant(dy, d["topk_ids"], None, E)
+    assert np.array_equal(codes.cpu().numpy()[:Mu], p["codes"])
+    assert np.array_equal(g.cpu().numpy()[:Mu].view(np.uint32), p["row_g"].view(np.uint32))
+    assert np.array_equal(sf.cpu().numpy()[:p["sf_swizzled"].size], p["sf_swizzled"])
+
+
+def test_combine_backward_quant_rejects_inconsistent_routing_on_the_device():
+    T, H, E, k = 64, 128, 2, 2
+    rng = np.random.default_rng(3)
+    dy = bf16_dev(_rand_bf16(rng, (T, H)))
+    dest = torch.arange(T * k, dtype=torch.int32, device="cuda").view(T, k)
+    perm_src = (torch.arange(T * k, dtype=torch.int32, device="cuda") // k).contiguous()
+    codes = torch.full((T * k, H // 2), 7, dtype=torch.uint8, device="cuda")
+    sf = torch.full((M.sf_bytes(T * k + 128 * E, H),), 7, dtype=torch.uint8, device="cuda")
+    g = torch.zeros(T * k, dtype=torch.float32, device="cuda")
+    ws = torch.empty(M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, T, H), dtype=torch.uint8,
+                     device="cuda")
+    # offsets that decrease: nothing is written
+    st = _status()
+    M.minite_moe_combine_backward_quant(dy, E, dest, np_dev(np.array([0, 100, 90], np.int32)),
+                                        np_dev(np.array([0, 128, 256], np.int32)), perm_src, codes,
+                                        sf, g, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1 << 1
+    assert (codes == 7).all() and (sf == 7).all()
+    # consistent offsets covering only 100 rows: the pairs routed past them are skipped
+    st.zero_()
+    M.minite_moe_combine_backward_quant(dy, E, dest, np_dev(np.array([0, 60, 100], np.int32)),
+                                        np_dev(np.array([0, 128, 256], np.int32)), perm_src, codes,
+                                        sf, g, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1 << 1
+    assert (codes[100:] == 7).all()
+    assert not (codes[:100] == 7).all()
+
+
 def test_permute_random_shapes_edge_cases():
     rng = np.random.default_rng(42)
     for trial in range(25):
