@@ -594,6 +594,92 @@ def swiglu_backward_quant(gate_up_bf16: np.ndarray, dh_bf16: np.ndarray, perm_w,
 
 
 # --------------------------------------------------------------------------
+# Weight gradient: operands quantized along tokens, K ragged per expert
+# --------------------------------------------------------------------------
+
+WGRAD_K_ALIGN = 256  # tokens: each expert's K range is padded to a multiple of this
+
+
+def wgrad_token_offsets(expert_offsets) -> np.ndarray:
+    """K layout of the token-axis operands of a weight-gradient GEMM: expert
+    e's tokens occupy columns [kofs[e], kofs[e] + count_e) of a [C, kofs[E]]
+    matrix, kofs being the prefix of the counts rounded up to 256 (reading:
+    the pages do not describe the backward's layout; 256 tokens is one
+    128-byte chunk of E2M1 codes). Columns past an expert's count are 0."""
+    off = np.asarray(expert_offsets, dtype=np.int64)
+    counts = off[1:] - off[:-1]
+    padded = (counts + WGRAD_K_ALIGN - 1) // WGRAD_K_ALIGN * WGRAD_K_ALIGN
+    return np.concatenate([[0], np.cumsum(padded)]).astype(np.int32)
+
+
+def quantize_tokens_per_expert(rows: np.ndarray, expert_offsets):
+    """One operand of a weight-gradient GEMM. rows: float32 [M, C], the
+    permuted rows (expert-contiguous, expert_offsets). For each expert e the
+    rows X_e [count_e, C] are transposed to [C, count_e], zero-padded to the
+    expert's K range, and quantized with one global scale per expert (from
+    the amax of X_e; 1 for an empty expert) and blocks of 16 consecutive
+    tokens (reading: the gradient sums over the expert's tokens, so the
+    scale cannot vary along them; one scale per expert, as for weights).
+    Returns dict codes [C, K/2], sf [C, K/16] row-major, sf_swizzled
+    (roundup(C, 128) x K/16 atoms), g [E], kofs [E+1] (K = kofs[E]).
+
+    Pins: per expert, equal to the per-expert weight quantization of the
+    padded block along its rows; exact round trip of grid values; the
+    dequantization error bound."""
+    x = np.asarray(rows, dtype=F32)
+    off = np.asarray(expert_offsets, dtype=np.int64)
+    kofs = wgrad_token_offsets(off)
+    E = len(off) - 1
+    C = x.shape[1]
+    K = int(kofs[E])
+    codes = np.zeros((C, K // 2), dtype=np.uint8)
+    sf = np.zeros((C, K // BLOCK), dtype=np.uint8)
+    g = np.ones(E, dtype=F32)
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b == a:
+            continue
+        k0, k1 = int(kofs[e]), int(kofs[e + 1])
+        xt = np.zeros((C, k1 - k0), dtype=F32)
+        xt[:, :b - a] = x[a:b].T
+        ce, se, ge = quantize_per_tensor(xt)
+        codes[:, k0 // 2:k1 // 2] = ce
+        sf[:, k0 // BLOCK:k1 // BLOCK] = se
+        g[e] = ge
+    return dict(codes=codes, sf=sf, sf_swizzled=swizzle_sf(sf) if K else np.zeros(0, np.uint8),
+                g=g, kofs=kofs)
+
+
+def wgrad_exact(a, b):
+    """Weight gradient per expert from two token-axis operands (dicts of
+    ``quantize_tokens_per_expert`` over the same routing):
+        out[e, n, i] = sum_{k in expert e's K range} ahat[n, k] * bhat[i, k]
+    with xhat = val * sf / g_e, in float64 (val*sf exact; the only roundings
+    are the float64 sums and the final division by g_a[e] * g_b[e]). Returns
+    (out [E, Ca, Cb] float64, abs_sum [E, Ca, Cb], the tolerance scale).
+
+    Pins: rational brute force on tiny operands; equality with the matmul of
+    the dequantized per-expert operands."""
+    kofs = np.asarray(a["kofs"], dtype=np.int64)
+    E = len(kofs) - 1
+    va = e2m1_decode(unpack_codes(a["codes"])) * np.repeat(
+        e4m3_decode(a["sf"]).astype(np.float64), BLOCK, axis=1)
+    vb = e2m1_decode(unpack_codes(b["codes"])) * np.repeat(
+        e4m3_decode(b["sf"]).astype(np.float64), BLOCK, axis=1)
+    Ca, Cb = va.shape[0], vb.shape[0]
+    out = np.zeros((E, Ca, Cb))
+    bound = np.zeros((E, Ca, Cb))
+    for e in range(E):
+        k0, k1 = int(kofs[e]), int(kofs[e + 1])
+        if k1 == k0:
+            continue
+        denom = np.float64(a["g"][e]) * np.float64(b["g"][e])
+        out[e] = (va[:, k0:k1] @ vb[:, k0:k1].T) / denom
+        bound[e] = (np.abs(va[:, k0:k1]) @ np.abs(vb[:, k0:k1]).T) / denom
+    return out, bound
+
+
+# --------------------------------------------------------------------------
 # Combine (unpermute)
 # --------------------------------------------------------------------------
 

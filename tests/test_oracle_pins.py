@@ -342,6 +342,129 @@ def test_grouped_gemm_brute_force_rational():
         assert np.all(bound >= np.abs(y))
 
 
+# ---------------------------------------------------------------- weight gradient
+
+def _token_operand_case(rng, counts, C, spread=True):
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = rng.standard_normal((int(off[-1]), C)).astype(np.float32)
+    if spread:  # experts far apart in magnitude: a scale applied to the wrong range shows
+        for e in range(len(counts)):
+            x[off[e]:off[e + 1]] *= np.float32(2.0 ** (6 * e - 6))
+    return O.bf16_to_f32(O.f32_to_bf16(x)), off  # BF16 values, as the operands are
+
+
+def test_token_operand_equals_weight_quantization_of_each_padded_expert_block():
+    rng = np.random.default_rng(41)
+    x, off = _token_operand_case(rng, [3, 0, 260, 17], 48)
+    q = O.quantize_tokens_per_expert(x, off)
+    kofs = q["kofs"]
+    assert list(kofs) == [0, 256, 256, 768, 1024]
+    for e in range(4):
+        a, b, k0, k1 = int(off[e]), int(off[e + 1]), int(kofs[e]), int(kofs[e + 1])
+        if b == a:
+            assert q["g"][e] == 1.0
+            continue
+        blk = np.zeros((k1 - k0, 48), dtype=np.float32)
+        blk[:b - a] = x[a:b]
+        wc, ws, _, wg = O.quantize_weights(_as_bf16_exact(blk)[None], along_rows=True)
+        assert np.array_equal(q["codes"][:, k0 // 2:k1 // 2], wc[0])
+        assert np.array_equal(q["sf"][:, k0 // 16:k1 // 16], ws[0])
+        assert q["g"][e] == wg[0]
+    # padding columns hold code 0 and scale 0
+    assert np.all(q["codes"][:, (3 + 1) // 2:128] == 0) and np.all(q["sf"][:, 1:16] == 0)
+
+
+def _as_bf16_exact(x):
+    """BF16 bits of float32 values that are already BF16-representable."""
+    b = O.f32_to_bf16(x)
+    assert np.array_equal(O.bf16_to_f32(b), x)
+    return b
+
+
+def test_token_operand_round_trip_of_scaled_grid_values():
+    rng = np.random.default_rng(42)
+    mags = np.array(FMT["e2m1_magnitudes"])
+    counts = [32, 0, 48, 16]
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M, C = int(off[-1]), 40
+    v = rng.choice(mags, size=(M, C)) * rng.choice([-1.0, 1.0], size=(M, C))
+    x = np.zeros((M, C))
+    for e, j in enumerate([-9, 0, 4, 13]):
+        a, b = off[e], off[e + 1]
+        blk = v[a:b].copy()
+        # every 16-token block of every channel holds a +-6, so every block scale is 448
+        for t0 in range(0, b - a, 16):
+            blk[t0 + 5, :] = 6.0 * rng.choice([-1.0, 1.0], size=C)
+        x[a:b] = blk * 2.0 ** j
+    x = x.astype(np.float32)
+    q = O.quantize_tokens_per_expert(x, off)
+    kofs = q["kofs"]
+    for e in range(4):
+        a, b, k0 = int(off[e]), int(off[e + 1]), int(kofs[e])
+        if b == a:
+            continue
+        xh = O.dequantize(q["codes"][:, k0 // 2:(k0 + b - a) // 2], q["sf"][:, k0 // 16:(k0 + b - a) // 16],
+                          np.full(C, q["g"][e]))
+        assert np.array_equal(xh, x[a:b].T.astype(np.float64))
+
+
+def _wgrad_rational(a, b, e, n, i):
+    mags = [Fraction(v).limit_denominator(4) for v in FMT["e2m1_magnitudes"]]
+
+    def val(c):
+        v = mags[int(c) & 7]
+        return -v if int(c) & 8 else v
+    k0, k1 = int(a["kofs"][e]), int(a["kofs"][e + 1])
+    qa = O.unpack_codes(a["codes"][n:n + 1])[0]
+    qb = O.unpack_codes(b["codes"][i:i + 1])[0]
+    tot = Fraction(0)
+    for kk in range(k0, k1):
+        sa = Fraction(float(O.e4m3_decode(a["sf"][n, kk // 16])))
+        sb = Fraction(float(O.e4m3_decode(b["sf"][i, kk // 16])))
+        tot += val(qa[kk]) * sa * val(qb[kk]) * sb
+    return tot / (Fraction(float(a["g"][e])) * Fraction(float(b["g"][e])))
+
+
+def test_wgrad_brute_force_rational():
+    rng = np.random.default_rng(43)
+    xa, off = _token_operand_case(rng, [5, 0, 20], 3)
+    xb = rng.standard_normal((int(off[-1]), 4)).astype(np.float32) * 0.1
+    qa = O.quantize_tokens_per_expert(xa, off)
+    qb = O.quantize_tokens_per_expert(xb, off)
+    out, bound = O.wgrad_exact(qa, qb)
+    assert out.shape == (3, 3, 4)
+    assert np.all(out[1] == 0)
+    for e in (0, 2):
+        for n in range(3):
+            for i in range(4):
+                ex = _wgrad_rational(qa, qb, e, n, i)
+                assert abs(Fraction(out[e, n, i]) - ex) <= abs(ex) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 200)
+    assert np.all(bound >= np.abs(out))
+
+
+def test_wgrad_equals_matmul_of_dequantized_tokens():
+    """Each expert's gradient is the product of its dequantized rows, the
+    definition of dW = sum over the expert's tokens of a_t (x) b_t."""
+    rng = np.random.default_rng(44)
+    xa, off = _token_operand_case(rng, [70, 300, 1], 32)
+    xb = rng.standard_normal((int(off[-1]), 24)).astype(np.float32)
+    qa = O.quantize_tokens_per_expert(xa, off)
+    qb = O.quantize_tokens_per_expert(xb, off)
+    out, _ = O.wgrad_exact(qa, qb)
+    kofs = qa["kofs"]
+    for e in range(3):
+        a, b, k0 = int(off[e]), int(off[e + 1]), int(kofs[e])
+        da = O.dequantize(qa["codes"][:, k0 // 2:(k0 + 256 * ((b - a + 255) // 256)) // 2],
+                          qa["sf"][:, k0 // 16:(k0 + 256 * ((b - a + 255) // 256)) // 16], np.full(32, qa["g"][e]))
+        db = O.dequantize(qb["codes"][:, k0 // 2:(k0 + 256 * ((b - a + 255) // 256)) // 2],
+                          qb["sf"][:, k0 // 16:(k0 + 256 * ((b - a + 255) // 256)) // 16], np.full(24, qb["g"][e]))
+        ref = da @ db.T
+        assert np.allclose(out[e], ref, rtol=1e-12, atol=1e-300)
+        # and the quantized gradient is close to the unquantized one
+        exact = xa[a:b].astype(np.float64).T @ xb[a:b].astype(np.float64)
+        assert np.linalg.norm(out[e] - exact) <= 0.25 * np.linalg.norm(exact)
+
+
 def test_grouped_gemm_one_hot_weights_gather():
     """One-hot weight rows (each row selects column c with value 6 on a grid-exact
     quantization) make row n of the output equal xhat[:, c]."""
