@@ -64,7 +64,12 @@ typedef enum {
 enum { MINITE_SCALE_PER_ROW = 0, MINITE_SCALE_PER_GROUP = 1 };
 enum { MINITE_ALONG_COLS = 0, MINITE_ALONG_ROWS = 1 };
 enum { MINITE_OUT_BF16 = 0, MINITE_OUT_FP32 = 1 };
-enum { MINITE_OP_QUANTIZE = 0, MINITE_OP_PERMUTE_QUANT = 1, MINITE_OP_COMBINE_BACKWARD_QUANT = 2 };
+enum {
+  MINITE_OP_QUANTIZE = 0,
+  MINITE_OP_PERMUTE_QUANT = 1,
+  MINITE_OP_COMBINE_BACKWARD_QUANT = 2,
+  MINITE_OP_QUANTIZE_TOKENS = 3
+};
 
 /*
  * minite_quantize_nvfp4 -- NVFP4 quantization of `groups` BF16 matrices.
@@ -241,6 +246,37 @@ int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const
                               minite_stream_t stream);
 
 /*
+ * minite_grouped_gemm_wgrad_nvfp4 -- weight gradient of a grouped
+ * projection, one launch for all experts, from two token-axis operands of
+ * minite_quantize_tokens_nvfp4 over the same routing (same kofs):
+ *   out[e, m, n] = sum_{k in [kofs[e], kofs[e+1])} (a(m,k) sfa(m,k/16))
+ *                  * (b(n,k) sfb(n,k/16)) / (a_g[e] * b_g[e])
+ * accumulated in FP32 on the tensor cores in a fixed K order (no split-K).
+ * Experts without tokens are not written.
+ *
+ * Cites: "Diagnostic, alignement et noyaux rapides" (grouped GEMMs over
+ * experts) and miniTE report summary, "Two complementary interventions"
+ * (device-side per-expert metadata); the pages' backward is BF16, so this
+ * NVFP4 weight gradient is a reading.
+ *
+ * a_codes: device, uint8 [M, k_cap/2], 128-byte aligned; a_sf: its scales
+ *          (k_cap/16 scale columns), 16-byte aligned; a_g: device float [E].
+ * b_codes, b_sf, b_g: the same for the N-channel operand.
+ * kofs:    device, int32 [E+1]: 0, non-decreasing, multiples of 256, at most
+ *          k_cap; otherwise nothing is written and bit 1<<MINITE_ERR_INVALID_ARG
+ *          is set in *status.
+ * out:     device, [E, M, N] BF16 or FP32 (out_dtype), 32-byte aligned.
+ * Shape rules: 1 <= M <= 65536, N % 32 == 0, 32 <= N <= 65536,
+ * k_cap % 256 == 0, 1 <= E <= 1024. Waits are bounded as in
+ * minite_grouped_gemm_nvfp4.
+ */
+int minite_grouped_gemm_wgrad_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_g,
+                                    const uint8_t* b_codes, const uint8_t* b_sf, const float* b_g,
+                                    const int32_t* kofs, int32_t E, int64_t M, int64_t N,
+                                    int64_t k_cap, void* out, int out_dtype, int32_t* status,
+                                    minite_stream_t stream);
+
+/*
  * minite_swiglu_weighted_quant -- routing-weighted SwiGLU with the per-row
  * amax and NVFP4 requantization fused into the same pass.
  *
@@ -267,6 +303,21 @@ int minite_swiglu_weighted_quant(const void* gate_up, const float* perm_w,
                                  const int32_t* expert_offsets, const int32_t* sf_row_offsets,
                                  uint8_t* codes, uint8_t* sf, float* row_g,
                                  int32_t* status, minite_stream_t stream);
+
+/*
+ * minite_swiglu_weighted_quant_keep_h -- minite_swiglu_weighted_quant that
+ * also stores h (the FP32 values it quantizes, each rounded to BF16 to
+ * nearest even) in h_out, device BF16 [M, I], 32-byte aligned, rows in
+ * permuted order; rows at or beyond expert_offsets[E] are not written. h is
+ * what the down projection's weight gradient needs from the forward (see
+ * minite_quantize_tokens_nvfp4). Same arguments, rules and errors otherwise;
+ * h_out may not be NULL.
+ */
+int minite_swiglu_weighted_quant_keep_h(const void* gate_up, const float* perm_w, int64_t M,
+                                        int64_t I, int32_t E, const int32_t* expert_offsets,
+                                        const int32_t* sf_row_offsets, uint8_t* codes,
+                                        uint8_t* sf, float* row_g, void* h_out, int32_t* status,
+                                        minite_stream_t stream);
 
 /*
  * minite_swiglu_backward_quant -- gradient of the routing-weighted SwiGLU
@@ -359,9 +410,54 @@ int minite_moe_combine_backward_quant(const void* dy, int64_t T, int64_t H, int3
                                       void* workspace, size_t ws_bytes, int32_t* status,
                                       minite_stream_t stream);
 
+/*
+ * minite_quantize_tokens_nvfp4 -- one operand of a weight-gradient GEMM:
+ * each expert's permuted rows transposed to [channels, tokens] and quantized
+ * in blocks of 16 consecutive tokens, one FP32 global scale per expert.
+ *
+ * Cites: miniTE report summary, "Two complementary interventions"
+ * (contiguous expert buffers, device-side metadata, scale layout written by
+ * the quantizer) and "Respect the timing boundaries" (the pages' backward is
+ * BF16; quantizing the weight gradient's operands along tokens is a reading:
+ * the gradient sums over the expert's tokens, so no scale may vary along
+ * them).
+ *
+ * Permuted row m (expert e of the offsets) holds x[row_src[m]] (or x[m] when
+ * row_src is NULL). For expert e with c_e rows, K range [kofs[e], kofs[e+1])
+ * where kofs is the prefix of c_e rounded up to 256 (written to kofs_out):
+ *   g[e] = min(2688 / amax(rows of e), FLT_MAX), 1 for amax 0;
+ *   column kofs[e] + j of channel row c holds x_e[j, c] for j < c_e, 0 after,
+ *   quantized as in minite_quantize_nvfp4 with blocks along the columns.
+ *
+ * x:         device, BF16 [x_rows, C], 16-byte aligned.
+ * row_src:   device, int32 [m_cap] (e.g. perm_src of the permutation), or
+ *            NULL (then rows are x's own and m_cap <= x_rows).
+ * m_cap:     permuted rows available (>= expert_offsets[E]).
+ * expert_offsets: device, int32 [E+1] (the permutation's).
+ * k_cap:     token columns allocated, a multiple of 256 and >= kofs[E]
+ *            (M + 256 E always suffices).
+ * codes:     device, uint8 [C, k_cap / 2] (row pitch k_cap / 2), 32-byte
+ *            aligned. sf: device, [roundup(C, 128) * k_cap / 16] bytes,
+ *            128-row x 4-column atoms with k_cap / 16 scale columns; rows past
+ *            C are zeroed up to column kofs[E] / 16.
+ * g_out:     device, float [E]. kofs_out: device, int32 [E+1].
+ * workspace: device, >= minite_workspace_bytes(MINITE_OP_QUANTIZE_TOKENS, E),
+ *            4-byte aligned.
+ * Device checks: offsets that do not start at 0, decrease or pass m_cap,
+ * and kofs[E] > k_cap make the kernels write nothing; a row_src entry
+ * outside [0, x_rows) reads as zeros; each sets bit 1<<MINITE_ERR_INVALID_ARG.
+ * Shape rules: C % 16 == 0, 16 <= C <= 65536, 1 <= E <= 1024,
+ * x_rows, m_cap < 2^31.
+ */
+int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const int32_t* row_src,
+                                 int64_t m_cap, int64_t C, int32_t E,
+                                 const int32_t* expert_offsets, int64_t k_cap, uint8_t* codes,
+                                 uint8_t* sf, float* g_out, int32_t* kofs_out, void* workspace,
+                                 size_t ws_bytes, int32_t* status, minite_stream_t stream);
+
 /* Workspace bytes needed by `op` (MINITE_OP_QUANTIZE: a = groups;
  * MINITE_OP_PERMUTE_QUANT: a = T, b = H, E, k; MINITE_OP_COMBINE_BACKWARD_QUANT:
- * a = T, b = H). 0 means none needed. */
+ * a = T, b = H; MINITE_OP_QUANTIZE_TOKENS: a = E). 0 means none needed. */
 size_t minite_workspace_bytes(int op, int64_t a, int64_t b, int32_t E, int32_t k);
 
 /* Static description of a status code. */

@@ -112,17 +112,19 @@ struct Params {
   const int32_t* sf_offsets;
   void* out;
   int32_t* status;
-  int64_t M;          // rows of A / out
-  int N, K, E;
+  int64_t M;          // rows of A / out (weight gradient: rows of A, i.e. channels)
+  int N, K, E;        // weight gradient: K = token columns allocated per operand row
   int out_fp32;
   uint64_t budget_ns;
 };
 
 struct Tile {
   int e, nt;
-  int row0;           // first permuted row of the tile
+  int row0;           // first permuted row of the tile (weight gradient: first A row)
   int rows;           // valid rows (<= 128)
   int sf_rb;          // 128-row block of A's scales
+  int kz0;            // first 128-byte K chunk (0 for the forward GEMMs)
+  int kt;             // K chunks of the tile
 };
 
 // tile index -> (expert, m block, n block). tiles_prefix[e] = 128-row m blocks
@@ -144,7 +146,40 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, const int32_t* t
   r.row0 = s_off[lo] + ml * BM;
   r.rows = min(BM, s_off[lo + 1] - r.row0);
   r.sf_rb = mt;
+  r.kz0 = 0;
+  r.kt = (p.K + 255) / 256;
   return r;
+}
+
+// Weight-gradient tile index -> (expert, A row block, B column block):
+// tiles_prefix[e] = A row blocks of the experts before e that have tokens;
+// s_kofs = the operands' token offsets (multiples of 256). Expert e's K range
+// is [s_kofs[e], s_kofs[e + 1]).
+__device__ __forceinline__ Tile decode_tile_wg(int t, int n_tiles, const int32_t* tiles_prefix,
+                                               const int32_t* s_kofs, const Params& p) {
+  Tile r;
+  const int mt = t / n_tiles;
+  r.nt = t - mt * n_tiles;
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tiles_prefix[mid] <= mt) lo = mid; else hi = mid;
+  }
+  r.e = lo;
+  const int ml = mt - tiles_prefix[lo];
+  r.row0 = ml * BM;
+  r.rows = min(BM, static_cast<int>(p.M) - r.row0);
+  r.sf_rb = ml;
+  r.kz0 = s_kofs[lo] / 256;
+  r.kt = (s_kofs[lo + 1] - s_kofs[lo]) / 256;
+  return r;
+}
+
+template <bool WG>
+__device__ __forceinline__ Tile decode_any(int t, int n_tiles, const int32_t* tiles_prefix,
+                                           const int32_t* s_off, const Params& p) {
+  if constexpr (WG) return decode_tile_wg(t, n_tiles, tiles_prefix, s_off, p);
+  else return decode_tile(t, n_tiles, tiles_prefix, s_off, p);
 }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -1277,28 +1312,37 @@ struct DSmem {
   int pad_;
 };
 
-// Walks this CTA's (tile, stage) pairs in order.
+// Walks this CTA's (tile, stage) pairs in order; a tile has
+// ceil(tl.kt / Q_CH) stages.
+template <bool WG>
 struct DIter {
-  int t, kd, ncl, total, KD, n_tiles;
+  int t, kd, ncl, total, n_tiles;
   Tile tl;
   const int32_t *prefix, *s_off;
   __device__ __forceinline__ bool valid() const { return t < total; }
-  __device__ __forceinline__ void start(int t0, int ncl_, int total_, int KD_, int n_tiles_,
+  __device__ __forceinline__ int stages() const { return (tl.kt + Q_CH - 1) / Q_CH; }
+  __device__ __forceinline__ void start(int t0, int ncl_, int total_, int n_tiles_,
                                         const int32_t* prefix_, const int32_t* s_off_,
                                         const Params& p) {
-    t = t0; kd = 0; ncl = ncl_; total = total_; KD = KD_; n_tiles = n_tiles_;
+    t = t0; kd = 0; ncl = ncl_; total = total_; n_tiles = n_tiles_;
     prefix = prefix_; s_off = s_off_;
-    if (t < total) tl = decode_tile(t, n_tiles, prefix, s_off, p);
+    if (t < total) tl = decode_any<WG>(t, n_tiles, prefix, s_off, p);
   }
   __device__ __forceinline__ void advance(const Params& p) {
-    if (++kd == KD) {
+    if (++kd == stages()) {
       kd = 0;
       t += ncl;
-      if (t < total) tl = decode_tile(t, n_tiles, prefix, s_off, p);
+      if (t < total) tl = decode_any<WG>(t, n_tiles, prefix, s_off, p);
     }
   }
 };
 
+// WG: weight-gradient mode. A [M channels, K tokens] and B [N channels, K
+// tokens] are token-axis operands whose expert e occupies token columns
+// [kofs[e], kofs[e + 1]) (p.offsets = kofs); the tile (e, A rows, B columns)
+// sums over that range and is written to out[e]; the scale is
+// 1 / (a_g[e] * b_g[e]).
+template <bool WG>
 __global__ void __maxnreg__(80)
 grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -1308,14 +1352,11 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint8_t* slots = stages + D_STAGES * D_STAGE_BYTES;
   DSmem& S = *reinterpret_cast<DSmem*>(slots + D_SLOTS * Q_SLOT_BYTES);
   int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
-  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
+  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets (WG: kofs)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int KT = (p.K + 255) / 256;        // 128-byte chunks per tile
-  const int KD = (KT + Q_CH - 1) / Q_CH;   // stages per tile
-  const int KSTEPS = p.K / 64;
-  const int atoms_per_rb = p.K / 64;
+  const int atoms_per_rb = p.K / 64;       // scale atoms per 128-row block of A or B
   const int n_tiles = (p.N + BN - 1) / BN;
   const int rb_per_expert = (p.N + 127) / 128;
   const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
@@ -1352,14 +1393,21 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
       int cnt = 0;
       if (e < p.E) {
         const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
-        const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
         s_off[e + 1] = o1;
         if (e == 0) s_off[0] = o0;
         cnt = o1 - o0;
-        if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
-            (e == p.E - 1 && o1 > p.M))
-          bad = true;
-        cnt = cnt > 0 ? (cnt + BM - 1) / BM : 0;
+        if constexpr (WG) {
+          // token ranges: from 0, multiples of 256, within the K columns
+          if (cnt < 0 || cnt % 256 != 0 || (e == 0 && o0 != 0) || (e == p.E - 1 && o1 > p.K))
+            bad = true;
+          cnt = cnt > 0 ? static_cast<int>((p.M + BM - 1) / BM) : 0;
+        } else {
+          const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
+          if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
+              (e == p.E - 1 && o1 > p.M))
+            bad = true;
+          cnt = cnt > 0 ? (cnt + BM - 1) / BM : 0;
+        }
       }
       int incl = cnt;
 #pragma unroll
@@ -1397,15 +1445,19 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      DIter it;
-      it.start(blockIdx.x, gridDim.x, total, KD, n_tiles, tiles_prefix, s_off, p);
+      DIter<WG> it;
+      it.start(blockIdx.x, gridDim.x, total, n_tiles, tiles_prefix, s_off, p);
       while (it.valid()) {
         if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
         uint8_t* sA = stages + stage * D_STAGE_BYTES;
         uint8_t* sB = sA + D_A_BYTES;
+        const int z = it.tl.kz0 + Q_CH * it.kd;
+        // a tile's last stage may hold one chunk: its second box lies in the
+        // next expert's range (or past the columns, zero-filled) and is unused
         mbar_arrive_expect_tx(&S.full[stage], D_STAGE_BYTES);
-        tma_load_3d(sA, &tmap_a, &S.full[stage], 0, it.tl.row0, Q_CH * it.kd);
-        tma_load_3d(sB, &tmap_b, &S.full[stage], 0, it.tl.e * p.N + it.tl.nt * BN, Q_CH * it.kd);
+        tma_load_3d(sA, &tmap_a, &S.full[stage], 0, it.tl.row0, z);
+        tma_load_3d(sB, &tmap_b, &S.full[stage], 0,
+                    (WG ? 0 : it.tl.e * p.N) + it.tl.nt * BN, z);
         armed_mask |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == D_STAGES) { stage = 0; phase ^= 1u; }
@@ -1424,25 +1476,24 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
       int slot = 0;
       uint32_t slot_phase = 0;
       bool ok = true;
-      DIter it;
-      it.start(blockIdx.x, gridDim.x, total, KD, n_tiles, tiles_prefix, s_off, p);
+      DIter<WG> it;
+      it.start(blockIdx.x, gridDim.x, total, n_tiles, tiles_prefix, s_off, p);
       while (it.valid()) {
         if (!mbar_wait(&S.sfread[slot], slot_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
         const Tile& tl = it.tl;
-        const int na = min(4 * Q_CH, KSTEPS - 4 * Q_CH * it.kd);   // atoms (k-steps) in this stage
+        const int na = min(4 * Q_CH, 4 * tl.kt - 4 * Q_CH * it.kd);  // atoms (k-steps) in this stage
+        const int a0 = 4 * tl.kz0 + 4 * Q_CH * it.kd;               // first atom of the stage
         const int nrb = min(BN / 128, rb_per_expert - tl.nt * (BN / 128));
         uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
         uint8_t* sSFB = sSFA + Q_SFA_BYTES;
         mbar_arrive_expect_tx(&S.sfdata[slot], static_cast<uint32_t>(na * (1 + nrb)) * SF_ATOM);
-        bulk_load(sSFA,
-                  p.a_sf + (static_cast<size_t>(tl.sf_rb) * atoms_per_rb + 4 * Q_CH * it.kd) *
-                               SF_ATOM,
+        bulk_load(sSFA, p.a_sf + (static_cast<size_t>(tl.sf_rb) * atoms_per_rb + a0) * SF_ATOM,
                   na * SF_ATOM, &S.sfdata[slot]);
         for (int rb = 0; rb < nrb; ++rb)
           bulk_load(sSFB + rb * 4 * Q_CH * SF_ATOM,
-                    p.b_sf + tl.e * sfb_expert +
-                        (static_cast<size_t>(tl.nt * (BN / 128) + rb) * atoms_per_rb +
-                         4 * Q_CH * it.kd) * SF_ATOM,
+                    p.b_sf + (WG ? 0 : tl.e * sfb_expert) +
+                        (static_cast<size_t>(tl.nt * (BN / 128) + rb) * atoms_per_rb + a0) *
+                            SF_ATOM,
                     na * SF_ATOM, &S.sfdata[slot]);
         slot_mask |= 1u << slot;
         slot_parity = (slot_parity & ~(1u << slot)) | (slot_phase << slot);
@@ -1466,6 +1517,8 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
       bool ok = true;
       bool issued = false;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_any<WG>(t, n_tiles, tiles_prefix, s_off, p);
+        const int KT = tl.kt, KD = (tl.kt + Q_CH - 1) / Q_CH, KSTEPS = 4 * tl.kt;
         if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
         tc_fence_after();
         for (int kd = 0; kd < KD && ok; ++kd) {
@@ -1509,11 +1562,12 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     int slot = 0, sfb = 0;
     uint32_t slot_phase = 0, sf_phase = 0;
     bool ok = true;
-    DIter it;
-    it.start(blockIdx.x, gridDim.x, total, KD, n_tiles, tiles_prefix, s_off, p);
+    DIter<WG> it;
+    it.start(blockIdx.x, gridDim.x, total, n_tiles, tiles_prefix, s_off, p);
     while (it.valid() && ok) {
       const int nrb = min(BN / 128, rb_per_expert - it.tl.nt * (BN / 128));
-      const int nch = min(Q_CH, KT - Q_CH * it.kd);
+      const int nch = min(Q_CH, it.tl.kt - Q_CH * it.kd);
+      const int KSTEPS = 4 * it.tl.kt;
       if (!mbar_wait(&S.sfdata[slot], slot_phase, budget, abort_flag)) ok = false;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       const uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
@@ -1573,11 +1627,13 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile(t, n_tiles, tiles_prefix, s_off, p);
+      const Tile tl = decode_any<WG>(t, n_tiles, tiles_prefix, s_off, p);
       const bool valid = r_in_tile < tl.rows;
-      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
+      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile +
+                          (WG ? static_cast<int64_t>(tl.e) * p.M : 0);  // output row
       float scale = 0.0f;
-      if (valid) scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
+      if (valid)
+        scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + (WG ? tl.e : row)), __ldg(p.b_g + tl.e)));
       if (!mbar_wait(&S.acc_full, acc_phase, budget, abort_flag)) ok = false;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       acc_phase ^= 1u;
@@ -1744,14 +1800,14 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-      attr_err = cudaFuncSetAttribute(grouped_gemm_dc_kernel,
+      attr_err = cudaFuncSetAttribute(grouped_gemm_dc_kernel<false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     });
     if (attr_err != cudaSuccess) return MINITE_ERR_CUDA;
     const int64_t max_tiles = (M_total / BM + E) * n_tiles;
     int grid = num_sms();
     if (max_tiles < grid) grid = static_cast<int>(max_tiles);
-    grouped_gemm_dc_kernel<<<grid, Q_THREADS, d_smem, s>>>(ta, tb, p);
+    grouped_gemm_dc_kernel<false><<<grid, Q_THREADS, d_smem, s>>>(ta, tb, p);
   } else if (variant == 4) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1807,5 +1863,59 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, ta, tb, p) != cudaSuccess)
       return MINITE_ERR_CUDA;
   }
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
+extern "C" int minite_grouped_gemm_wgrad_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
+                                               const float* a_g, const uint8_t* b_codes,
+                                               const uint8_t* b_sf, const float* b_g,
+                                               const int32_t* kofs, int32_t E, int64_t M,
+                                               int64_t N, int64_t k_cap, void* out,
+                                               int out_dtype, int32_t* status,
+                                               minite_stream_t stream) {
+  using namespace gemm;
+  if (!a_codes || !a_sf || !a_g || !b_codes || !b_sf || !b_g || !kofs || !out)
+    return MINITE_ERR_INVALID_ARG;
+  if (out_dtype != MINITE_OUT_BF16 && out_dtype != MINITE_OUT_FP32) return MINITE_ERR_INVALID_ARG;
+  if (M < 1 || M > 65536 || N < 32 || N % 32 != 0 || N > 65536 || E < 1 || E > 1024 ||
+      k_cap < 256 || k_cap % 256 != 0 || k_cap >= (int64_t(1) << 31) ||
+      int64_t(E) * M * N >= (int64_t(1) << 40))
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(a_codes, 128) || !aligned(b_codes, 128) || !aligned(a_sf, 16) ||
+      !aligned(b_sf, 16) || !aligned(out, 32))
+    return MINITE_ERR_INVALID_ARG;
+  const size_t d_smem = 1024 + D_STAGES * D_STAGE_BYTES + D_SLOTS * Q_SLOT_BYTES + sizeof(DSmem) +
+                        2 * (E + 1) * sizeof(int32_t);
+  if (d_smem > 232448) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap ta, tb;
+  if (!make_map3(&ta, a_codes, k_cap / 2, M, BM) || !make_map3(&tb, b_codes, k_cap / 2, N, BN))
+    return MINITE_ERR_CUDA;
+  Params p;
+  p.a_g = a_g;
+  p.b_g = b_g;
+  p.a_sf = a_sf;
+  p.b_sf = b_sf;
+  p.offsets = kofs;
+  p.sf_offsets = kofs;
+  p.out = out;
+  p.status = status;
+  p.M = M;
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(k_cap);
+  p.E = E;
+  p.out_fp32 = out_dtype == MINITE_OUT_FP32;
+  p.budget_ns = wait_budget_ns();
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_dc_kernel<true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  });
+  if (attr_err != cudaSuccess) return MINITE_ERR_CUDA;
+  const int64_t max_tiles = int64_t(E) * ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  int grid = num_sms();
+  if (max_tiles < grid) grid = static_cast<int>(max_tiles);
+  grouped_gemm_dc_kernel<true><<<grid, Q_THREADS, d_smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+      ta, tb, p);
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }

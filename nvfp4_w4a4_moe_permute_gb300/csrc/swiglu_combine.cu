@@ -103,13 +103,25 @@ __device__ __forceinline__ float group_max(float v) {
 // of a row owns blocks l + LPR*j (j < NCH) of the row's intermediate, with
 // the gates at [0, I) and the ups at [I, 2I) of the gate_up row. Every row's
 // 4I input bytes are requested before any of them is used.
+// KEEP_H: h is also stored as BF16 (round to nearest even) in h_out [M, I].
 constexpr int kSwThreads = 512;
-template <int LPR, int NCH>
+
+__device__ __forceinline__ void st_bf16x16(uint16_t* p, const float (&v)[16]) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  st_global_v8(p, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+}
+
+template <int LPR, int NCH, bool KEEP_H>
 __global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
     const uint16_t* __restrict__ gu, const float* __restrict__ perm_w, int64_t M, int I, int E,
     const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ sf_row_offsets,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
-    int32_t* status) {
+    uint16_t* __restrict__ h_out, int32_t* status) {
   extern __shared__ __align__(16) float smf[];
   float* lut = smf;
   int32_t* s_off = reinterpret_cast<int32_t*>(smf + kLutEntries);
@@ -154,6 +166,7 @@ __global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
     for (int j = 0; j < NCH; ++j) {
       if (live && l + LPR * j < nb) {
         swiglu_block(lut, wg[j], wu[j], w, h[j]);
+        if (KEEP_H) st_bf16x16(h_out + m * static_cast<int64_t>(I) + 16 * (l + LPR * j), h[j]);
       } else {
 #pragma unroll
         for (int t = 0; t < 16; ++t) h[j][t] = 0.0f;
@@ -207,7 +220,7 @@ __global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
 template <int LPR, int NCH>
 static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int I, int E,
                          const int32_t* off, const int32_t* sfoff, uint8_t* codes, uint8_t* sf,
-                         float* row_g, int32_t* status, cudaStream_t s) {
+                         float* row_g, uint16_t* h_out, int32_t* status, cudaStream_t s) {
   const size_t smem = kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
   // table (32 KB) + offsets stay under the default 48 KB of dynamic shared memory
   constexpr int rows_per_cta = kSwThreads / 32 * (32 / LPR);
@@ -215,8 +228,12 @@ static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int 
   const int64_t cap = static_cast<int64_t>(num_sms());
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  swiglu_quant_kernel<LPR, NCH><<<static_cast<unsigned>(blocks), kSwThreads, smem, s>>>(
-      g, perm_w, M, I, E, off, sfoff, codes, sf, row_g, status);
+  if (h_out)
+    swiglu_quant_kernel<LPR, NCH, true><<<static_cast<unsigned>(blocks), kSwThreads, smem, s>>>(
+        g, perm_w, M, I, E, off, sfoff, codes, sf, row_g, h_out, status);
+  else
+    swiglu_quant_kernel<LPR, NCH, false><<<static_cast<unsigned>(blocks), kSwThreads, smem, s>>>(
+        g, perm_w, M, I, E, off, sfoff, codes, sf, row_g, nullptr, status);
   return MINITE_OK;
 }
 
@@ -505,39 +522,58 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
 
 using namespace minite;
 
+static int swiglu_weighted_quant_impl(const void* gate_up, const float* perm_w, int64_t M,
+                                      int64_t I, int32_t E, const int32_t* expert_offsets,
+                                      const int32_t* sf_row_offsets, uint8_t* codes, uint8_t* sf,
+                                      float* row_g, void* h_out, int32_t* status,
+                                      minite_stream_t stream) {
+  if (!gate_up || !expert_offsets || !sf_row_offsets || !codes || !sf || !row_g)
+    return MINITE_ERR_INVALID_ARG;
+  if (M < 1 || I < 64 || I % 64 != 0 || I > 2048 || E < 1 || E > 1024)
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (M >= (int64_t(1) << 31)) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(gate_up, 32) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(h_out, 32))
+    return MINITE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t* g = static_cast<const uint16_t*>(gate_up);
+  uint16_t* h = static_cast<uint16_t*>(h_out);
+  const int i = static_cast<int>(I);
+  const int nb = i / 16;
+  int rc;
+  // 16 lanes per row when that leaves no lane idle or the row is short
+  if (nb <= 16) rc = launch_swiglu<16, 1>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets,
+                                           codes, sf, row_g, h, status, s);
+  else if (nb <= 32) rc = launch_swiglu<16, 2>(g, perm_w, M, i, E, expert_offsets,
+                                                sf_row_offsets, codes, sf, row_g, h, status, s);
+  else if (nb <= 48) rc = launch_swiglu<16, 3>(g, perm_w, M, i, E, expert_offsets,
+                                                sf_row_offsets, codes, sf, row_g, h, status, s);
+  else if (nb <= 64) rc = launch_swiglu<32, 2>(g, perm_w, M, i, E, expert_offsets,
+                                                sf_row_offsets, codes, sf, row_g, h, status, s);
+  else if (nb <= 96) rc = launch_swiglu<32, 3>(g, perm_w, M, i, E, expert_offsets,
+                                                sf_row_offsets, codes, sf, row_g, h, status, s);
+  else rc = launch_swiglu<32, 4>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes, sf,
+                                 row_g, h, status, s);
+  if (rc != MINITE_OK) return rc;
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
 extern "C" int minite_swiglu_weighted_quant(const void* gate_up, const float* perm_w, int64_t M,
                                             int64_t I, int32_t E,
                                             const int32_t* expert_offsets,
                                             const int32_t* sf_row_offsets, uint8_t* codes,
                                             uint8_t* sf, float* row_g, int32_t* status,
                                             minite_stream_t stream) {
-  if (!gate_up || !expert_offsets || !sf_row_offsets || !codes || !sf || !row_g)
-    return MINITE_ERR_INVALID_ARG;
-  if (M < 1 || I < 64 || I % 64 != 0 || I > 2048 || E < 1 || E > 1024)
-    return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (M >= (int64_t(1) << 31)) return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(gate_up, 32) || !aligned(codes, 16) || !aligned(sf, 16))
-    return MINITE_ERR_INVALID_ARG;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const uint16_t* g = static_cast<const uint16_t*>(gate_up);
-  const int i = static_cast<int>(I);
-  const int nb = i / 16;
-  int rc;
-  // 16 lanes per row when that leaves no lane idle or the row is short
-  if (nb <= 16) rc = launch_swiglu<16, 1>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets,
-                                           codes, sf, row_g, status, s);
-  else if (nb <= 32) rc = launch_swiglu<16, 2>(g, perm_w, M, i, E, expert_offsets,
-                                                sf_row_offsets, codes, sf, row_g, status, s);
-  else if (nb <= 48) rc = launch_swiglu<16, 3>(g, perm_w, M, i, E, expert_offsets,
-                                                sf_row_offsets, codes, sf, row_g, status, s);
-  else if (nb <= 64) rc = launch_swiglu<32, 2>(g, perm_w, M, i, E, expert_offsets,
-                                                sf_row_offsets, codes, sf, row_g, status, s);
-  else if (nb <= 96) rc = launch_swiglu<32, 3>(g, perm_w, M, i, E, expert_offsets,
-                                                sf_row_offsets, codes, sf, row_g, status, s);
-  else rc = launch_swiglu<32, 4>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes, sf,
-                                 row_g, status, s);
-  if (rc != MINITE_OK) return rc;
-  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+  return swiglu_weighted_quant_impl(gate_up, perm_w, M, I, E, expert_offsets, sf_row_offsets,
+                                    codes, sf, row_g, nullptr, status, stream);
+}
+
+extern "C" int minite_swiglu_weighted_quant_keep_h(
+    const void* gate_up, const float* perm_w, int64_t M, int64_t I, int32_t E,
+    const int32_t* expert_offsets, const int32_t* sf_row_offsets, uint8_t* codes, uint8_t* sf,
+    float* row_g, void* h_out, int32_t* status, minite_stream_t stream) {
+  if (!h_out) return MINITE_ERR_INVALID_ARG;
+  return swiglu_weighted_quant_impl(gate_up, perm_w, M, I, E, expert_offsets, sf_row_offsets,
+                                    codes, sf, row_g, h_out, status, stream);
 }
 
 extern "C" int minite_swiglu_backward_quant(const void* gate_up, const void* dh,

@@ -19,7 +19,7 @@ from . import build as _build
 SCALE_PER_ROW, SCALE_PER_GROUP = 0, 1
 ALONG_COLS, ALONG_ROWS = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-OP_QUANTIZE, OP_PERMUTE_QUANT, OP_COMBINE_BACKWARD_QUANT = 0, 1, 2
+OP_QUANTIZE, OP_PERMUTE_QUANT, OP_COMBINE_BACKWARD_QUANT, OP_QUANTIZE_TOKENS = 0, 1, 2, 3
 ERR_TIMEOUT, ERR_BAD_ROUTING = 4, 5
 
 EXPORTS = [
@@ -29,7 +29,8 @@ EXPORTS = [
     "minite_status_string", "minite_version", "minite_test_convert",
     "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc", "minite_set_gemm_variant",
     "minite_test_div6_exhaustive", "minite_quantize_nvfp4_dual",
-    "minite_moe_combine_backward_quant",
+    "minite_moe_combine_backward_quant", "minite_quantize_tokens_nvfp4",
+    "minite_swiglu_weighted_quant_keep_h", "minite_grouped_gemm_wgrad_nvfp4",
 ]
 
 
@@ -60,9 +61,15 @@ def load(path: str | None = None):
                                              _vp, _vp, _vp, _vp, _vp, _vp, _vp],
         "minite_moe_combine_backward_quant": [_vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                               _vp, _vp, _vp, _sz, _vp, _vp],
+        "minite_quantize_tokens_nvfp4": [_vp, _i64, _vp, _i64, _i64, _i32, _vp, _i64, _vp, _vp, _vp,
+                                         _vp, _vp, _sz, _vp, _vp],
+        "minite_grouped_gemm_wgrad_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64,
+                                            _vp, _int, _vp, _vp],
         "minite_grouped_gemm_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                       _vp, _int, _vp, _vp],
         "minite_swiglu_weighted_quant": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+        "minite_swiglu_weighted_quant_keep_h": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp,
+                                                _vp, _vp, _vp],
         "minite_swiglu_backward_quant": [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp],
         "minite_moe_combine": [_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp],
@@ -217,6 +224,16 @@ def minite_swiglu_weighted_quant(gate_up, perm_w, E, expert_offsets, sf_row_offs
     _check(rc, "minite_swiglu_weighted_quant")
 
 
+def minite_swiglu_weighted_quant_keep_h(gate_up, perm_w, E, expert_offsets, sf_row_offsets, codes,
+                                        sf, row_g, h_out, status=None, stream=None):
+    M, I2 = gate_up.shape
+    rc = load().minite_swiglu_weighted_quant_keep_h(_p(gate_up), _p(perm_w), M, I2 // 2, E,
+                                                    _p(expert_offsets), _p(sf_row_offsets),
+                                                    _p(codes), _p(sf), _p(row_g), _p(h_out),
+                                                    _p(status), _s(stream))
+    _check(rc, "minite_swiglu_weighted_quant_keep_h")
+
+
 def minite_swiglu_backward_quant(gate_up, dh, perm_w, E, expert_offsets, sf_row_offsets, codes,
                                  sf, row_g, status=None, stream=None):
     M, I2 = gate_up.shape
@@ -236,6 +253,49 @@ def minite_moe_combine_backward_quant(dy, E, dest_row, expert_offsets, sf_row_of
                                                   _p(perm_src), _p(codes), _p(sf), _p(row_g),
                                                   _p(workspace), ws_bytes, _p(status), _s(stream))
     _check(rc, "minite_moe_combine_backward_quant")
+
+
+def minite_quantize_tokens_nvfp4(x, row_src, m_cap, E, expert_offsets, k_cap, codes, sf, g, kofs,
+                                 workspace, status=None, stream=None):
+    x_rows, C = x.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().minite_quantize_tokens_nvfp4(_p(x), x_rows, _p(row_src), m_cap, C, E,
+                                             _p(expert_offsets), k_cap, _p(codes), _p(sf), _p(g),
+                                             _p(kofs), _p(workspace), ws_bytes, _p(status),
+                                             _s(stream))
+    _check(rc, "minite_quantize_tokens_nvfp4")
+
+
+def minite_grouped_gemm_wgrad_nvfp4(a, b, out, status=None, stream=None):
+    """a, b: ``quantize_tokens`` results over the same routing; out [E, Ma, Nb]."""
+    E, M, N = out.shape
+    if a["k_cap"] != b["k_cap"]:
+        raise MiniteError("minite_grouped_gemm_wgrad_nvfp4: operands with different token capacity")
+    out_dtype = OUT_FP32 if out.dtype == torch.float32 else OUT_BF16
+    rc = load().minite_grouped_gemm_wgrad_nvfp4(_p(a["codes"]), _p(a["sf"]), _p(a["g"]),
+                                                _p(b["codes"]), _p(b["sf"]), _p(b["g"]),
+                                                _p(a["kofs"]), E, M, N, a["k_cap"], _p(out),
+                                                out_dtype, _p(status), _s(stream))
+    _check(rc, "minite_grouped_gemm_wgrad_nvfp4")
+
+
+def quantize_tokens(x, expert_offsets, E, row_src=None, m_cap=None, stream=None):
+    """Weight-gradient operand of x's permuted rows (x[row_src[m]] or x[m]):
+    dict(codes [C, k_cap/2], sf, g [E], kofs [E+1], k_cap) with
+    k_cap = m_cap + 256 E rounded up to 256."""
+    dev = x.device
+    x_rows, C = x.shape
+    m_cap = (row_src.numel() if row_src is not None else x_rows) if m_cap is None else m_cap
+    k_cap = (m_cap + 256 * E + 255) // 256 * 256
+    out = dict(codes=torch.empty((C, k_cap // 2), dtype=torch.uint8, device=dev),
+               sf=torch.empty(((C + 127) // 128 * 128) * (k_cap // 16), dtype=torch.uint8, device=dev),
+               g=torch.empty(E, dtype=torch.float32, device=dev),
+               kofs=torch.empty(E + 1, dtype=torch.int32, device=dev), k_cap=k_cap)
+    ws = torch.empty(max(4, minite_workspace_bytes(OP_QUANTIZE_TOKENS, E)), dtype=torch.uint8,
+                     device=dev)
+    minite_quantize_tokens_nvfp4(x, row_src, m_cap, E, expert_offsets, k_cap, out["codes"],
+                                 out["sf"], out["g"], out["kofs"], ws, stream=stream)
+    return out
 
 
 def minite_moe_combine(expert_out, dest_row, y, status=None, stream=None):

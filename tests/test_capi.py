@@ -57,6 +57,8 @@ def test_workspace_sizes(lib):
     # token-order scales (T x H/16 bytes) and global scales (T floats)
     assert M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, 4096, 2048) == 4096 * 128 + 4096 * 4
     assert M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, 0, 2048) == 0
+    assert M.minite_workspace_bytes(M.OP_QUANTIZE_TOKENS, 128) == 512
+    assert M.minite_workspace_bytes(M.OP_QUANTIZE_TOKENS, 2000) == 0
 
 
 def _c(lib, name):
@@ -112,6 +114,20 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert cb(16, 96, 2, 2, fake, 1 << 20) == 2
     assert cb(16, 128, 2, 2, None, 1 << 20) == 1
     assert cb(16, 128, 2, 2, fake, 8) == 1
+    # token-axis quantizer: C not a multiple of 16, k_cap not a multiple of 256, misaligned codes
+    qt = lambda C, kcap, codes: lib.minite_quantize_tokens_nvfp4(  # noqa: E731
+        fake, 64, None, 64, C, 2, fake, kcap, codes, fake, fake, fake, fake, 1024, None, None)
+    assert qt(40, 1024, fake) == 2
+    assert qt(64, 1000, fake) == 2
+    assert qt(64, 1024, vp(4112)) == 1
+    # weight-gradient GEMM: N not a multiple of 32, bad out dtype
+    wg = lambda N, dt: lib.minite_grouped_gemm_wgrad_nvfp4(  # noqa: E731
+        fake, fake, fake, fake, fake, fake, fake, 2, 128, N, 1024, fake, dt, None, None)
+    assert wg(100, 0) == 2
+    assert wg(128, 7) == 1
+    # SwiGLU keeping h: h_out missing
+    assert lib.minite_swiglu_weighted_quant_keep_h(fake, None, 16, 128, 1, fake, fake, fake, fake,
+                                                   fake, None, None, None) == 1
     # combine: N not a multiple of 8, k too large
     assert lib.minite_moe_combine(fake, fake, 4, 8, 12, 2, fake, None, None) == 2
     assert lib.minite_moe_combine(fake, fake, 4, 8, 16, 64, fake, None, None) == 2

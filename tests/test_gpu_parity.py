@@ -726,6 +726,128 @@ def test_backward_chain_stagewise(name, T):
     assert np.array_equal(u16(dx), O.moe_combine(u16(dx_perm), mlp.dest_row.cpu().numpy()))
 
 
+# --------------------------------------------------------------------- weight gradient
+
+def _tok_sf_rows(q, C):
+    """Row-major [C, kofs[E]/16] scales of a GPU token-axis operand."""
+    K = int(q["kofs"][-1].item())
+    full = O.unswizzle_sf(q["sf"].cpu().numpy(), (C + 127) // 128 * 128, q["k_cap"] // 16)
+    return full[:C, :K // 16], full[C:, :K // 16]
+
+
+def check_token_operand(q, ref, C):
+    K = int(ref["kofs"][-1])
+    assert np.array_equal(q["kofs"].cpu().numpy(), ref["kofs"])
+    assert np.array_equal(q["codes"].cpu().numpy()[:, :K // 2], ref["codes"])
+    rows, pad = _tok_sf_rows(q, C)
+    assert np.array_equal(rows, ref["sf"])
+    assert (pad == 0).all()
+    assert np.array_equal(q["g"].cpu().numpy().view(np.uint32), ref["g"].view(np.uint32))
+
+
+@pytest.mark.parametrize("counts,C,gather", [([3, 0, 260, 17], 48, True), ([1], 16, False),
+                                              ([700, 5, 0, 0, 129], 256, True),
+                                              ([64, 64], 2048, False), ([300, 1000], 768, True)])
+def test_quantize_tokens_bit_exact(counts, C, gather):
+    rng = np.random.default_rng(sum(counts) + C)
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    Mu = int(off[-1])
+    if gather:  # permuted row m is source row src[m] of a smaller matrix
+        T = max(1, Mu // 3)
+        x = _rand_bf16(rng, (T, C))
+        src = rng.integers(0, T, Mu + 5).astype(np.int32)
+        rows = O.bf16_to_f32(x)[src[:Mu]]
+        q = M.quantize_tokens(bf16_dev(x), np_dev(off), E, row_src=np_dev(src))
+    else:
+        x = _rand_bf16(rng, (Mu + 7, C))
+        x[:, 3] = 0  # a zero channel
+        rows = O.bf16_to_f32(x)[:Mu]
+        q = M.quantize_tokens(bf16_dev(x), np_dev(off), E)
+    torch.cuda.synchronize()
+    check_token_operand(q, O.quantize_tokens_per_expert(rows, off), C)
+
+
+@pytest.mark.parametrize("counts,Ma,Nb", [([3, 0, 260, 17], 128, 256), ([1000, 40], 256, 96),
+                                          ([600], 2048, 768), ([5, 300, 2, 0, 90, 1], 160, 32)])
+def test_wgrad_gemm_within_bound(counts, Ma, Nb):
+    rng = np.random.default_rng(7 * sum(counts) + Ma)
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    Mu = int(off[-1])
+    xa = _rand_bf16(rng, (Mu, Ma))
+    xb = _rand_bf16(rng, (Mu, Nb))
+    qa = M.quantize_tokens(bf16_dev(xa), np_dev(off), E)
+    qb = M.quantize_tokens(bf16_dev(xb), np_dev(off), E)
+    outs = {}
+    for dt in (torch.float32, torch.bfloat16):
+        out = torch.full((E, Ma, Nb), float("nan"), dtype=dt, device="cuda")
+        st = _status()
+        M.minite_grouped_gemm_wgrad_nvfp4(qa, qb, out, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        outs[dt] = out
+    ra = O.quantize_tokens_per_expert(O.bf16_to_f32(xa), off)
+    rb = O.quantize_tokens_per_expert(O.bf16_to_f32(xb), off)
+    check_token_operand(qa, ra, Ma)
+    check_token_operand(qb, rb, Nb)
+    y, bound = O.wgrad_exact(ra, rb)
+    for e in range(E):
+        if counts[e] == 0:
+            assert torch.isnan(outs[torch.float32][e]).all()  # experts without tokens: untouched
+            continue
+        assert_fp32_within_bound(outs[torch.float32][e].cpu().numpy(), y[e], bound[e], f"dW[{e}]")
+        assert_bf16_within_one_ulp(u16(outs[torch.bfloat16][e]), y[e], f"dW[{e}] bf16")
+
+
+def test_wgrad_gemm_rejects_bad_token_offsets():
+    rng = np.random.default_rng(8)
+    off = np.array([0, 100, 300], np.int32)
+    xa = _rand_bf16(rng, (300, 128))
+    qa = M.quantize_tokens(bf16_dev(xa), np_dev(off), 2)
+    qa["kofs"] = np_dev(np.array([0, 200, 512], np.int32))  # 200: not a multiple of 256
+    out = torch.full((2, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    st = _status()
+    M.minite_grouped_gemm_wgrad_nvfp4(qa, qa, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1 << 1
+    assert torch.isnan(out).all()
+
+
+@pytest.mark.parametrize("I", [64, 768, 2048])
+def test_swiglu_keep_h_stores_rounded_h_and_the_same_codes(I):
+    rng = np.random.default_rng(I)
+    counts = [5, 130, 0, 40]
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    sfo = np.concatenate([[0], np.cumsum((np.array(counts) + 127) // 128 * 128)]).astype(np.int32)
+    Mu = int(off[-1])
+    Mt = Mu + 3
+    gu = O.f32_to_bf16((rng.standard_normal((Mt, 2 * I)) * 3).astype(np.float32))
+    pw = rng.random(Mt).astype(np.float32)
+    res = []
+    for keep in (False, True):
+        codes = torch.zeros((Mt, I // 2), dtype=torch.uint8, device="cuda")
+        sf = torch.zeros(((Mt + 128 * E) * (I // 16),), dtype=torch.uint8, device="cuda")
+        g = torch.zeros(Mt, dtype=torch.float32, device="cuda")
+        h = torch.zeros((Mt, I), dtype=torch.bfloat16, device="cuda")
+        st = _status()
+        if keep:
+            M.minite_swiglu_weighted_quant_keep_h(bf16_dev(gu), np_dev(pw), E, np_dev(off),
+                                                  np_dev(sfo), codes, sf, g, h, st)
+        else:
+            M.minite_swiglu_weighted_quant(bf16_dev(gu), np_dev(pw), E, np_dev(off), np_dev(sfo),
+                                           codes, sf, g, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        res.append((codes, sf, g, h))
+    for a, b in zip(res[0][:3], res[1][:3]):
+        assert torch.equal(a, b)
+    ref = O.f32_to_bf16(O.swiglu_weighted(O.bf16_to_f32(gu[:Mu]), pw[:Mu]))
+    assert np.array_equal(u16(res[1][3])[:Mu], ref)
+    assert (u16(res[1][3])[Mu:] == 0).all()
+
+
 # --------------------------------------------------------------------- failure detection
 
 @pytest.mark.parametrize("variant", VARIANTS)
