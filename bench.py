@@ -253,8 +253,10 @@ class Step:
     # W_gate_up in both orientations (one pass), SwiGLU backward with its
     # per-row requantization, the gate_up dgrad GEMM (K = 2I, N = H) and the
     # combine of dX back into token order.
-    BWD_STAGES = ["wq_gate_up_dual", "swiglu_bwd", "gemm_dgrad_gate_up", "combine_dx"]
-    BWD_LAUNCHES = 2 + 1 + 1 + 1
+    BWD_STAGES = ["wq_gate_up_dual", "swiglu_keep_h", "swiglu_bwd_keep", "gemm_dgrad_gate_up",
+                  "combine_dx", "quant_tokens", "gemm_wgrad_down", "gemm_wgrad_gate_up"]
+    # dual 2, SwiGLU 1, SwiGLU backward 1, GEMM 1, combine 1, 4 token-axis operands x 2, 2 GEMMs
+    BWD_LAUNCHES = 2 + 1 + 1 + 1 + 1 + 8 + 2
 
     def init_backward(self):
         import torch
@@ -269,6 +271,19 @@ class Step:
                         g=torch.empty(M_, dtype=f32, device=dev))
         self.dx_perm = torch.empty((M_, H), dtype=torch.bfloat16, device=dev)
         self.dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        # weight gradients: BF16 h and [dg | du] kept, their token-axis operands
+        self.h_bf = torch.zeros((M_, I), dtype=torch.bfloat16, device=dev)
+        self.dgu_bf = torch.zeros((M_, 2 * I), dtype=torch.bfloat16, device=dev)
+        mlp = self.mlp
+        self.tok = {}
+        for name, src, rs in (("dy", self.dy, mlp.perm_src), ("h", self.h_bf, None),
+                              ("dgu", self.dgu_bf, None), ("x", self.x, mlp.perm_src)):
+            self.tok[name] = (src, rs, self.M.quantize_tokens(src, mlp.offsets, E, row_src=rs,
+                                                              m_cap=M_))
+        self.ws_tok = torch.empty(max(4, self.M.minite_workspace_bytes(self.M.OP_QUANTIZE_TOKENS, E)),
+                                  dtype=u8, device=dev)
+        self.dWd = torch.empty((E, H, I), dtype=f32, device=dev)
+        self.dWgu = torch.empty((E, 2 * I, H), dtype=f32, device=dev)
 
     def run_backward(self, stream, events=None):
         M, s, mlp = self.M, stream, self.mlp
@@ -282,16 +297,32 @@ class Step:
                                      self.wguT["codes"], self.wguT["sf"], self.wgu["g"], self.ws_q,
                                      self.status, s)
         mark(1)
-        M.minite_swiglu_backward_quant(mlp.gate_up, self.dh, mlp.perm_w, self.E, mlp.offsets,
-                                       mlp.sf_offsets, self.dgu["codes"], self.dgu["sf"],
-                                       self.dgu["g"], self.status, s)
+        # the forward's SwiGLU keeping BF16 h for the down projection's weight gradient
+        M.minite_swiglu_weighted_quant_keep_h(mlp.gate_up, mlp.perm_w, self.E, mlp.offsets,
+                                              mlp.sf_offsets, mlp.h_codes, mlp.h_sf, mlp.h_g,
+                                              self.h_bf, self.status, s)
         mark(2)
+        M.minite_swiglu_backward_quant_keep(mlp.gate_up, self.dh, mlp.perm_w, self.E, mlp.offsets,
+                                            mlp.sf_offsets, self.dgu["codes"], self.dgu["sf"],
+                                            self.dgu["g"], self.dgu_bf, self.status, s)
+        mark(3)
         M.minite_grouped_gemm_nvfp4(self.dgu["codes"], self.dgu["sf"], self.dgu["g"],
                                     self.wguT["codes"], self.wguT["sf"], self.wgu["g"],
                                     mlp.offsets, mlp.sf_offsets, self.dx_perm, self.status, s)
-        mark(3)
-        M.minite_moe_combine(self.dx_perm, mlp.dest_row, self.dx, self.status, s)
         mark(4)
+        M.minite_moe_combine(self.dx_perm, mlp.dest_row, self.dx, self.status, s)
+        mark(5)
+        M_ = self.T * self.k
+        for src, rs, q in self.tok.values():
+            M.minite_quantize_tokens_nvfp4(src, rs, M_, self.E, mlp.offsets, q["k_cap"], q["codes"],
+                                           q["sf"], q["g"], q["kofs"], self.ws_tok, self.status, s)
+        mark(6)
+        M.minite_grouped_gemm_wgrad_nvfp4(self.tok["dy"][2], self.tok["h"][2], self.dWd,
+                                          self.status, s)
+        mark(7)
+        M.minite_grouped_gemm_wgrad_nvfp4(self.tok["dgu"][2], self.tok["x"][2], self.dWgu,
+                                          self.status, s)
+        mark(8)
 
     # kernels launched per step by the library (memsets not counted): weight
     # quantization 2 + 2, permutation 5, GEMM 1, SwiGLU 1, GEMM 1, combine 1,
@@ -311,8 +342,11 @@ class Step:
         sfb = lambda r, c: r * c / 16  # noqa: E731
         return dict(
             wq_gate_up_dual=E * 2 * I * H * 2 + 2 * (E * 2 * I * H / 2 + sfb(E * 2 * I, H)),
-            swiglu_bwd=Mu * (2 * I * 2 + I * 2 + 4) + Mu * (I + 2 * I / 16 + 4),
+            swiglu_keep_h=Mu * 2 * I * 2 + Mu * (I / 2 + I / 16 + 4) + Mu * I * 2,
+            swiglu_bwd_keep=Mu * (2 * I * 2 + I * 2 + 4) + Mu * (I + 2 * I / 16 + 4) + Mu * 2 * I * 2,
             combine_dx=Mu * H * 2 + T * H * 2 + T * k * 4,
+            # four operands: each reads its rows twice (amax, encode) and writes codes + scales
+            quant_tokens=sum(2 * Mu * C * 2 + Mu * C / 2 + Mu * C / 16 for C in (H, I, 2 * I, H)),
         )
 
     def algorithmic_bytes(self):
@@ -426,12 +460,17 @@ def run_gpu(args):
         Mu = int(step.mlp.offsets[-1].item())
         dg_fl = 2.0 * Mu * 2 * step.I * step.H
         backward = {
-            "stages": "W_gate_up quantization in both orientations (one pass) + SwiGLU backward"
-                      " with per-row requant + gate_up dgrad GEMM (K=2I, N=H) + combine of dX",
+            "stages": "W_gate_up quantization in both orientations (one pass) + forward SwiGLU"
+                      " keeping BF16 h + SwiGLU backward with per-row requant keeping BF16 dGU"
+                      " + gate_up dgrad GEMM (K=2I, N=H) + combine of dX + token-axis NVFP4"
+                      " operands (dY, h, dGU, x) + weight-gradient GEMMs of both projections",
             "ms": round(sum(bst.values()), 4),
             "stages_ms": {k_: round(v, 4) for k_, v in bst.items()},
             "stages_hbm_gbs": {k_: round(bab[k_] / (bst[k_] / 1e3) / 1e9, 1) for k_ in bab},
             "gemm_dgrad_gate_up_tflops": dg_fl / (bst["gemm_dgrad_gate_up"] / 1e3) / 1e12,
+            "gemm_wgrad_down_tflops": 2.0 * Mu * step.H * step.I / (bst["gemm_wgrad_down"] / 1e3) / 1e12,
+            "gemm_wgrad_gate_up_tflops": 2.0 * Mu * 2 * step.I * step.H
+                                         / (bst["gemm_wgrad_gate_up"] / 1e3) / 1e12,
             "gpu_launches": Step.BWD_LAUNCHES * args.steps,
         }
 

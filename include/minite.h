@@ -361,6 +361,21 @@ int minite_swiglu_backward_quant(const void* gate_up, const void* dh, const floa
                                  int32_t* status, minite_stream_t stream);
 
 /*
+ * minite_swiglu_backward_quant_keep -- minite_swiglu_backward_quant that also
+ * stores [dg | du] (the FP32 values it quantizes, each rounded to BF16 to
+ * nearest even) in dgu_out, device BF16 [M, 2I], 32-byte aligned, rows in
+ * permuted order; rows at or beyond expert_offsets[E] are not written. The
+ * gate_up projection's weight gradient takes its token-axis operand from it
+ * (see minite_quantize_tokens_nvfp4). Same arguments, rules and errors
+ * otherwise; dgu_out may not be NULL.
+ */
+int minite_swiglu_backward_quant_keep(const void* gate_up, const void* dh, const float* perm_w,
+                                      int64_t M, int64_t I, int32_t E,
+                                      const int32_t* expert_offsets, const int32_t* sf_row_offsets,
+                                      uint8_t* codes, uint8_t* sf, float* row_g, void* dgu_out,
+                                      int32_t* status, minite_stream_t stream);
+
+/*
  * minite_moe_combine -- unpermute: y[t] = BF16(sum_{j<k} D[dest_row[t,j]]),
  * summed in FP32 in slot order starting from 0; dropped pairs (dest_row < 0)
  * are skipped. The routing weight is already inside D (applied in the

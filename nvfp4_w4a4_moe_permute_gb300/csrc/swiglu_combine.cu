@@ -320,13 +320,14 @@ __device__ __forceinline__ void swiglu_bwd_block(const float* lut_s, const float
 template <int NCH>
 constexpr int bwd_threads() { return NCH <= 2 ? 512 : 256; }
 
-template <int NCH>
+// KEEP: [dg | du] is also stored as BF16 in dgu_out [M, 2I].
+template <int NCH, bool KEEP>
 __global__ void __launch_bounds__(bwd_threads<NCH>(), 1) swiglu_bwd_quant_kernel(
     const uint16_t* __restrict__ gu, const uint16_t* __restrict__ dh,
     const float* __restrict__ perm_w, int64_t M, int I, int E,
     const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ sf_row_offsets,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
-    int32_t* status) {
+    uint16_t* __restrict__ dgu_out, int32_t* status) {
   extern __shared__ __align__(16) float smf[];
   float* lut_s = smf;
   float* lut_d = smf + kLutEntries;
@@ -363,6 +364,11 @@ __global__ void __launch_bounds__(bwd_threads<NCH>(), 1) swiglu_bwd_quant_kernel
         ld_bf16x16(gr + I + 16 * c, wu);
         ld_bf16x16(dr + 16 * c, wd);
         swiglu_bwd_block(lut_s, lut_d, wg, wu, wd, w, dgv[j], duv[j]);
+        if (KEEP) {
+          uint16_t* o = dgu_out + m * (2 * static_cast<int64_t>(I)) + 16 * c;
+          st_bf16x16(o, dgv[j]);
+          st_bf16x16(o + I, duv[j]);
+        }
       } else {
 #pragma unroll
         for (int t = 0; t < 16; ++t) dgv[j][t] = duv[j][t] = 0.0f;
@@ -418,27 +424,37 @@ __global__ void __launch_bounds__(bwd_threads<NCH>(), 1) swiglu_bwd_quant_kernel
   }
 }
 
-template <int NCH>
-static int launch_swiglu_bwd(const uint16_t* g, const uint16_t* dh, const float* perm_w,
-                             int64_t M, int I, int E, const int32_t* off, const int32_t* sfoff,
-                             uint8_t* codes, uint8_t* sf, float* row_g, int32_t* status,
-                             cudaStream_t s) {
-  const size_t smem = 2 * kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
+template <int NCH, bool KEEP>
+static cudaError_t bwd_smem_attr() {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(swiglu_bwd_quant_kernel<NCH>,
+    attr = cudaFuncSetAttribute(swiglu_bwd_quant_kernel<NCH, KEEP>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(2 * kLutEntries * sizeof(float) + 2 * 1025 * 4));
   });
-  if (attr != cudaSuccess) return MINITE_ERR_CUDA;
+  return attr;
+}
+
+template <int NCH>
+static int launch_swiglu_bwd(const uint16_t* g, const uint16_t* dh, const float* perm_w,
+                             int64_t M, int I, int E, const int32_t* off, const int32_t* sfoff,
+                             uint8_t* codes, uint8_t* sf, float* row_g, uint16_t* dgu_out,
+                             int32_t* status, cudaStream_t s) {
+  const size_t smem = 2 * kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
+  if ((dgu_out ? bwd_smem_attr<NCH, true>() : bwd_smem_attr<NCH, false>()) != cudaSuccess)
+    return MINITE_ERR_CUDA;
   constexpr int threads = bwd_threads<NCH>();
   int64_t blocks = (M + threads / 32 - 1) / (threads / 32);
   const int64_t cap = static_cast<int64_t>(num_sms());
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  swiglu_bwd_quant_kernel<NCH><<<static_cast<unsigned>(blocks), threads, smem, s>>>(
-      g, dh, perm_w, M, I, E, off, sfoff, codes, sf, row_g, status);
+  if (dgu_out)
+    swiglu_bwd_quant_kernel<NCH, true><<<static_cast<unsigned>(blocks), threads, smem, s>>>(
+        g, dh, perm_w, M, I, E, off, sfoff, codes, sf, row_g, dgu_out, status);
+  else
+    swiglu_bwd_quant_kernel<NCH, false><<<static_cast<unsigned>(blocks), threads, smem, s>>>(
+        g, dh, perm_w, M, I, E, off, sfoff, codes, sf, row_g, nullptr, status);
   return MINITE_OK;
 }
 
@@ -576,35 +592,58 @@ extern "C" int minite_swiglu_weighted_quant_keep_h(
                                     codes, sf, row_g, h_out, status, stream);
 }
 
+static int swiglu_backward_quant_impl(const void* gate_up, const void* dh, const float* perm_w,
+                                      int64_t M, int64_t I, int32_t E,
+                                      const int32_t* expert_offsets,
+                                      const int32_t* sf_row_offsets, uint8_t* codes, uint8_t* sf,
+                                      float* row_g, void* dgu_out, int32_t* status,
+                                      minite_stream_t stream) {
+  if (!gate_up || !dh || !expert_offsets || !sf_row_offsets || !codes || !sf || !row_g)
+    return MINITE_ERR_INVALID_ARG;
+  if (M < 1 || I < 64 || I % 64 != 0 || I > 2048 || E < 1 || E > 1024)
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (M >= (int64_t(1) << 31)) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(gate_up, 32) || !aligned(dh, 32) || !aligned(codes, 16) || !aligned(sf, 16) ||
+      !aligned(dgu_out, 32))
+    return MINITE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t* g = static_cast<const uint16_t*>(gate_up);
+  const uint16_t* d = static_cast<const uint16_t*>(dh);
+  uint16_t* k = static_cast<uint16_t*>(dgu_out);
+  const int i = static_cast<int>(I);
+  const int nb = i / 16;
+  int rc;
+  if (nb <= 32) rc = launch_swiglu_bwd<1>(g, d, perm_w, M, i, E, expert_offsets, sf_row_offsets,
+                                          codes, sf, row_g, k, status, s);
+  else if (nb <= 64) rc = launch_swiglu_bwd<2>(g, d, perm_w, M, i, E, expert_offsets,
+                                               sf_row_offsets, codes, sf, row_g, k, status, s);
+  else if (nb <= 96) rc = launch_swiglu_bwd<3>(g, d, perm_w, M, i, E, expert_offsets,
+                                               sf_row_offsets, codes, sf, row_g, k, status, s);
+  else rc = launch_swiglu_bwd<4>(g, d, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes,
+                                 sf, row_g, k, status, s);
+  if (rc != MINITE_OK) return rc;
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
 extern "C" int minite_swiglu_backward_quant(const void* gate_up, const void* dh,
                                             const float* perm_w, int64_t M, int64_t I, int32_t E,
                                             const int32_t* expert_offsets,
                                             const int32_t* sf_row_offsets, uint8_t* codes,
                                             uint8_t* sf, float* row_g, int32_t* status,
                                             minite_stream_t stream) {
-  if (!gate_up || !dh || !expert_offsets || !sf_row_offsets || !codes || !sf || !row_g)
-    return MINITE_ERR_INVALID_ARG;
-  if (M < 1 || I < 64 || I % 64 != 0 || I > 2048 || E < 1 || E > 1024)
-    return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (M >= (int64_t(1) << 31)) return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(gate_up, 32) || !aligned(dh, 32) || !aligned(codes, 16) || !aligned(sf, 16))
-    return MINITE_ERR_INVALID_ARG;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const uint16_t* g = static_cast<const uint16_t*>(gate_up);
-  const uint16_t* d = static_cast<const uint16_t*>(dh);
-  const int i = static_cast<int>(I);
-  const int nb = i / 16;
-  int rc;
-  if (nb <= 32) rc = launch_swiglu_bwd<1>(g, d, perm_w, M, i, E, expert_offsets, sf_row_offsets,
-                                          codes, sf, row_g, status, s);
-  else if (nb <= 64) rc = launch_swiglu_bwd<2>(g, d, perm_w, M, i, E, expert_offsets,
-                                               sf_row_offsets, codes, sf, row_g, status, s);
-  else if (nb <= 96) rc = launch_swiglu_bwd<3>(g, d, perm_w, M, i, E, expert_offsets,
-                                               sf_row_offsets, codes, sf, row_g, status, s);
-  else rc = launch_swiglu_bwd<4>(g, d, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes,
-                                 sf, row_g, status, s);
-  if (rc != MINITE_OK) return rc;
-  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+  return swiglu_backward_quant_impl(gate_up, dh, perm_w, M, I, E, expert_offsets, sf_row_offsets,
+                                    codes, sf, row_g, nullptr, status, stream);
+}
+
+extern "C" int minite_swiglu_backward_quant_keep(const void* gate_up, const void* dh,
+                                                 const float* perm_w, int64_t M, int64_t I,
+                                                 int32_t E, const int32_t* expert_offsets,
+                                                 const int32_t* sf_row_offsets, uint8_t* codes,
+                                                 uint8_t* sf, float* row_g, void* dgu_out,
+                                                 int32_t* status, minite_stream_t stream) {
+  if (!dgu_out) return MINITE_ERR_INVALID_ARG;
+  return swiglu_backward_quant_impl(gate_up, dh, perm_w, M, I, E, expert_offsets, sf_row_offsets,
+                                    codes, sf, row_g, dgu_out, status, stream);
 }
 
 extern "C" int minite_moe_combine(const void* expert_out, const int32_t* dest_row, int64_t T,

@@ -31,6 +31,7 @@ EXPORTS = [
     "minite_test_div6_exhaustive", "minite_quantize_nvfp4_dual",
     "minite_moe_combine_backward_quant", "minite_quantize_tokens_nvfp4",
     "minite_swiglu_weighted_quant_keep_h", "minite_grouped_gemm_wgrad_nvfp4",
+    "minite_swiglu_backward_quant_keep",
 ]
 
 
@@ -72,6 +73,8 @@ def load(path: str | None = None):
                                                 _vp, _vp, _vp],
         "minite_swiglu_backward_quant": [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp],
+        "minite_swiglu_backward_quant_keep": [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp,
+                                              _vp, _vp, _vp, _vp],
         "minite_moe_combine": [_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp],
         "minite_test_convert": [_vp, _i64, _vp, _vp, _vp, _vp],
         "minite_test_div6_exhaustive": [_vp, _vp],
@@ -241,6 +244,16 @@ def minite_swiglu_backward_quant(gate_up, dh, perm_w, E, expert_offsets, sf_row_
                                              _p(expert_offsets), _p(sf_row_offsets), _p(codes),
                                              _p(sf), _p(row_g), _p(status), _s(stream))
     _check(rc, "minite_swiglu_backward_quant")
+
+
+def minite_swiglu_backward_quant_keep(gate_up, dh, perm_w, E, expert_offsets, sf_row_offsets,
+                                      codes, sf, row_g, dgu_out, status=None, stream=None):
+    M, I2 = gate_up.shape
+    rc = load().minite_swiglu_backward_quant_keep(_p(gate_up), _p(dh), _p(perm_w), M, I2 // 2, E,
+                                                  _p(expert_offsets), _p(sf_row_offsets),
+                                                  _p(codes), _p(sf), _p(row_g), _p(dgu_out),
+                                                  _p(status), _s(stream))
+    _check(rc, "minite_swiglu_backward_quant_keep")
 
 
 def minite_moe_combine_backward_quant(dy, E, dest_row, expert_offsets, sf_row_offsets, perm_src,

@@ -800,6 +800,87 @@ def test_wgrad_gemm_within_bound(counts, Ma, Nb):
         assert_bf16_within_one_ulp(u16(outs[torch.bfloat16][e]), y[e], f"dW[{e}] bf16")
 
 
+def _small_moe(seed, T, H, I, E, k):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((T, E))
+    ids = np.argsort(-logits, axis=1)[:, :k].astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    return dict(x=O.f32_to_bf16(rng.standard_normal((T, H)).astype(np.float32)), ids=ids, w=w,
+                wgu=O.f32_to_bf16((rng.standard_normal((E, 2 * I, H)) * 0.02).astype(np.float32)),
+                wd=O.f32_to_bf16((rng.standard_normal((E, H, I)) * 0.02).astype(np.float32)),
+                dy=O.f32_to_bf16(rng.standard_normal((T, H)).astype(np.float32)))
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(64, 64, 64, 4, 2), (600, 256, 128, 4, 2),
+                                       (900, 128, 64, 8, 3)])
+def test_weight_gradients_stagewise(T, H, I, E, k):
+    """Both weight gradients of the expert MLP, stage by stage: the forward
+    keeps BF16 h, the SwiGLU backward keeps BF16 [dg | du]; dW_down sums
+    dY x h and dW_gate_up sums [dg | du] x x over each expert's tokens, from
+    token-axis NVFP4 operands. Operands bit-exact, gradients within
+    2^-20 sum|ab| of the exact result."""
+    d = _small_moe(T + H, T, H, I, E, k)
+    dev = "cuda"
+    x, ids, w, dy = bf16_dev(d["x"]), np_dev(d["ids"]), np_dev(d["w"]), bf16_dev(d["dy"])
+    wgu = M.quantize(bf16_dev(d["wgu"]), per_group=True)
+    _, wdT = M.quantize_dual(bf16_dev(d["wd"]))
+    mlp = M.MoEMLP(T, H, I, E, k)
+    Mt = T * k
+    st = _status()
+    mlp.permute_quant(x, ids, w)
+    M.minite_grouped_gemm_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"], wgu["sf"], wgu["g"],
+                                mlp.offsets, mlp.sf_offsets, mlp.gate_up, st)
+    h = torch.zeros((Mt, I), dtype=torch.bfloat16, device=dev)
+    M.minite_swiglu_weighted_quant_keep_h(mlp.gate_up, mlp.perm_w, E, mlp.offsets, mlp.sf_offsets,
+                                          mlp.h_codes, mlp.h_sf, mlp.h_g, h, st)
+    bwd = M.MoEMLP(T, H, I, E, k)
+    ws = torch.empty(M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, T, H), dtype=torch.uint8,
+                     device=dev)
+    M.minite_moe_combine_backward_quant(dy, E, mlp.dest_row, mlp.offsets, mlp.sf_offsets,
+                                        mlp.perm_src, bwd.a_codes, bwd.a_sf, bwd.a_g, ws, st)
+    dh = torch.empty((Mt, I), dtype=torch.bfloat16, device=dev)
+    M.minite_grouped_gemm_nvfp4(bwd.a_codes, bwd.a_sf, bwd.a_g, wdT["codes"], wdT["sf"], wdT["g"],
+                                mlp.offsets, mlp.sf_offsets, dh, st)
+    dgu_codes = torch.empty((Mt, I), dtype=torch.uint8, device=dev)
+    dgu_sf = torch.empty((M.sf_bytes(Mt + 128 * E, 2 * I),), dtype=torch.uint8, device=dev)
+    dgu_g = torch.empty(Mt, dtype=torch.float32, device=dev)
+    dgu = torch.zeros((Mt, 2 * I), dtype=torch.bfloat16, device=dev)
+    M.minite_swiglu_backward_quant_keep(mlp.gate_up, dh, mlp.perm_w, E, mlp.offsets,
+                                        mlp.sf_offsets, dgu_codes, dgu_sf, dgu_g, dgu, st)
+    q_dy = M.quantize_tokens(dy, mlp.offsets, E, row_src=mlp.perm_src, m_cap=Mt)
+    q_h = M.quantize_tokens(h, mlp.offsets, E, m_cap=Mt)
+    q_dgu = M.quantize_tokens(dgu, mlp.offsets, E, m_cap=Mt)
+    q_x = M.quantize_tokens(x, mlp.offsets, E, row_src=mlp.perm_src, m_cap=Mt)
+    dWd = torch.full((E, H, I), float("nan"), dtype=torch.float32, device=dev)
+    dWgu = torch.full((E, 2 * I, H), float("nan"), dtype=torch.float32, device=dev)
+    M.minite_grouped_gemm_wgrad_nvfp4(q_dy, q_h, dWd, st)
+    M.minite_grouped_gemm_wgrad_nvfp4(q_dgu, q_x, dWgu, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(mlp.status.item()) == 0
+
+    off = mlp.offsets.cpu().numpy()
+    Mu = int(off[-1])
+    src = mlp.perm_src.cpu().numpy()[:Mu]
+    perm_w = mlp.perm_w.cpu().numpy()[:Mu]
+    # the kept BF16 tensors are the roundings of what the stages quantize
+    assert np.array_equal(u16(h)[:Mu], O.f32_to_bf16(O.swiglu_weighted(O.bf16_to_f32(u16(mlp.gate_up)[:Mu]), perm_w)))
+    assert np.array_equal(u16(dgu)[:Mu], O.f32_to_bf16(O.swiglu_backward(
+        O.bf16_to_f32(u16(mlp.gate_up)[:Mu]), O.bf16_to_f32(u16(dh)[:Mu]), perm_w)))
+    r_dy = O.quantize_tokens_per_expert(O.bf16_to_f32(d["dy"])[src], off)
+    r_h = O.quantize_tokens_per_expert(O.bf16_to_f32(u16(h)[:Mu]), off)
+    r_dgu = O.quantize_tokens_per_expert(O.bf16_to_f32(u16(dgu)[:Mu]), off)
+    r_x = O.quantize_tokens_per_expert(O.bf16_to_f32(d["x"])[src], off)
+    for q, r, C in ((q_dy, r_dy, H), (q_h, r_h, I), (q_dgu, r_dgu, 2 * I), (q_x, r_x, H)):
+        check_token_operand(q, r, C)
+    for out, ra, rb in ((dWd, r_dy, r_h), (dWgu, r_dgu, r_x)):
+        y, bound = O.wgrad_exact(ra, rb)
+        got = out.cpu().numpy()
+        for e in range(E):
+            if off[e + 1] == off[e]:
+                continue
+            assert_fp32_within_bound(got[e], y[e], bound[e], f"dW[{e}]")
+
+
 def test_wgrad_gemm_rejects_bad_token_offsets():
     rng = np.random.default_rng(8)
     off = np.array([0, 100, 300], np.int32)
