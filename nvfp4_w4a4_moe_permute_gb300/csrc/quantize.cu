@@ -20,19 +20,39 @@
 
 namespace minite {
 
-__global__ void group_amax_kernel(const uint16_t* __restrict__ x, int64_t elems_per_group,
-                                  uint32_t* __restrict__ amax_bits) {
+// Each thread keeps kAmaxU 32-byte loads in flight and takes maxima on packed
+// BF16 pairs (|x| compares like the unsigned magnitude bits).
+constexpr int kAmaxU = 4;
+__global__ void __launch_bounds__(256) group_amax_kernel(const uint16_t* __restrict__ x,
+                                                         int64_t elems_per_group,
+                                                         uint32_t* __restrict__ amax_bits) {
   const int64_t grp = blockIdx.y;
-  const uint4* base = reinterpret_cast<const uint4*>(x + grp * elems_per_group);
-  const int64_t nvec = elems_per_group / 8;
+  const uint16_t* base = x + grp * elems_per_group;
+  const int64_t nvec = elems_per_group / 16;                    // 32-byte vectors
+  const bool a32 = (reinterpret_cast<uintptr_t>(base) & 31) == 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   float m = 0.0f;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nvec;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    uint4 u = __ldcs(base + i);
-    float v[8];
-    unpack_bf16x8(u, v);
-    m = fmaxf(m, amax8(v));
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nvec;
+       i += kAmaxU * stride) {
+    uint32_t w[kAmaxU][8];
+#pragma unroll
+    for (int u = 0; u < kAmaxU; ++u) {
+      const int64_t v = i + u * stride;
+      if (v < nvec) {
+        if (a32) ld_bf16x16(base + 16 * v, w[u]);
+        else ld_bf16x16_a16(base + 16 * v, w[u]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[u][j] = 0u;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAmaxU; ++u) m = fmaxf(m, amax_bf16x16(w[u]));
   }
+  // the tail of a group whose size is not a multiple of 16 elements
+  for (int64_t e = nvec * 16 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       e < elems_per_group; e += stride)
+    m = fmaxf(m, fabsf(bf16lo(base[e])));
   m = warp_max(m);
   __shared__ float red[32];
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -484,7 +504,7 @@ static int launch_group_amax(const uint16_t* x, int64_t groups, int64_t per_grou
                              uint32_t* amax, cudaStream_t s) {
   if (cudaMemsetAsync(amax, 0, groups * sizeof(uint32_t), s) != cudaSuccess)
     return MINITE_ERR_CUDA;
-  int64_t bx = (per_group / 8 + 255) / 256;
+  int64_t bx = (per_group / 16 + 256 * kAmaxU - 1) / (256 * kAmaxU);
   const int64_t want = (num_sms() * 8 + groups - 1) / groups;
   if (bx > want) bx = want;
   if (bx < 1) bx = 1;
