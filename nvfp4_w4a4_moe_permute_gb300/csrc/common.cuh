@@ -20,6 +20,16 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) {
   if (status) atomicOr(status, 1 << code);
 }
 
+// Programmatic dependent launch: pdl_wait blocks the calling thread until the
+// kernel launched before this one on the stream has completed and its writes
+// are visible (it returns at once when this kernel was launched without the
+// programmatic attribute). A kernel calls it before its first global memory
+// access, so only prologue work that touches no global memory (barrier
+// setup, TMEM allocation, tables in shared memory) overlaps the previous
+// kernel's last CTAs. No kernel triggers its dependents early: measured on
+// the CUDA-graph step, an early trigger slowed the step down.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------
 // BF16 / scalar format conversions
 // ----------------------------------------------------------------------------

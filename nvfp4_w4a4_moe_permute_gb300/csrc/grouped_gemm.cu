@@ -1383,6 +1383,8 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&S.tmem_base, TMEM_COLS);
+  // everything above touches only this CTA's shared memory and TMEM
+  pdl_wait();
   if (warp == 2) {
     // m-block prefix over experts, validating the device offsets on the way
     int carry = 0;
@@ -1807,7 +1809,9 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     const int64_t max_tiles = (M_total / BM + E) * n_tiles;
     int grid = num_sms();
     if (max_tiles < grid) grid = static_cast<int>(max_tiles);
-    grouped_gemm_dc_kernel<false><<<grid, Q_THREADS, d_smem, s>>>(ta, tb, p);
+    if (launch_pdl(grouped_gemm_dc_kernel<false>, dim3(grid), dim3(Q_THREADS), d_smem, s, ta, tb,
+                   p) != cudaSuccess)
+      return MINITE_ERR_CUDA;
   } else if (variant == 4) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1915,7 +1919,8 @@ extern "C" int minite_grouped_gemm_wgrad_nvfp4(const uint8_t* a_codes, const uin
   const int64_t max_tiles = int64_t(E) * ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   int grid = num_sms();
   if (max_tiles < grid) grid = static_cast<int>(max_tiles);
-  grouped_gemm_dc_kernel<true><<<grid, Q_THREADS, d_smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-      ta, tb, p);
+  if (launch_pdl(grouped_gemm_dc_kernel<true>, dim3(grid), dim3(Q_THREADS), d_smem,
+                 reinterpret_cast<cudaStream_t>(stream), ta, tb, p) != cudaSuccess)
+    return MINITE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }

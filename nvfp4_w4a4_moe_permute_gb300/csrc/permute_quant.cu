@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(32 * kRankWarps) permute_rank_kernel(
     const int32_t* __restrict__ ids, int64_t T, int k, int E, int ct, int nchunks,
     int32_t* __restrict__ table, int32_t* __restrict__ dest_row, uint32_t* __restrict__ counter,
     int32_t* status) {
+  pdl_wait();
   extern __shared__ int32_t cnt_all[];  // [kRankWarps][E]
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int c = blockIdx.x * kRankWarps + wid;
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_scan_kernel(
     int32_t* __restrict__ table, int nchunks, int E, uint32_t* __restrict__ counter,
     int32_t* __restrict__ totals, int32_t* __restrict__ expert_offsets,
     int32_t* __restrict__ sf_row_offsets) {
+  pdl_wait();
   __shared__ int warp_sums[33];
   __shared__ int is_last;
   const int e = blockIdx.x;
@@ -206,6 +208,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_route_kernel(
     int ct, int nchunks, const int32_t* __restrict__ table,
     const int32_t* __restrict__ expert_offsets, int32_t* __restrict__ perm_src,
     int32_t* __restrict__ dest_row, float* __restrict__ perm_w) {
+  pdl_wait();
   const int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (p >= T * k) return;
   const int e = ids[p];
@@ -233,6 +236,7 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
     const int32_t* __restrict__ sf_row_offsets, const int32_t* __restrict__ dest_row,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
     uint8_t* __restrict__ sfc, float* __restrict__ gtok, int32_t* status) {
+  pdl_wait();
   extern __shared__ int32_t sm[];
   int32_t* s_off = sm;                 // [E+1]
   int32_t* s_sfoff = s_off + (E + 1);  // [E+1]
@@ -336,6 +340,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_sf_gather_kernel(
     const int32_t* __restrict__ perm_src, const int32_t* __restrict__ expert_offsets,
     const int32_t* __restrict__ sf_row_offsets, int64_t T, int k, int E, int kc,
     uint8_t* __restrict__ sf, float* __restrict__ row_g, int32_t* status) {
+  pdl_wait();
   extern __shared__ int32_t sm[];
   int32_t* s_off = sm;                 // [E+1]
   int32_t* s_sfoff = s_off + (E + 1);  // [E+1]
@@ -440,9 +445,9 @@ static int launch_quant_gather(const void* x, const int32_t* topk_ids, int64_t T
   switch (nch) {
 #define MINITE_CASE(N)                                                                     \
   case N:                                                                                  \
-    permute_quant_kernel<N><<<static_cast<unsigned>(qblocks), kPermThreads, smem, s>>>(    \
-        xb, topk_ids, T, h, E, k, expert_offsets, sf_row_offsets, dest_row, codes, sf,     \
-        row_g, w.sfc, w.gtok, status);                                                     \
+    launch_pdl(permute_quant_kernel<N>, dim3(static_cast<unsigned>(qblocks)),              \
+               dim3(kPermThreads), smem, s, xb, topk_ids, T, h, E, k, expert_offsets,      \
+               sf_row_offsets, dest_row, codes, sf, row_g, w.sfc, w.gtok, status);         \
     break;
     MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
     MINITE_CASE(7) MINITE_CASE(8)
@@ -454,8 +459,10 @@ static int launch_quant_gather(const void* x, const int32_t* topk_ids, int64_t T
     int64_t gblocks = (T * k) / 128 + E;   // upper bound of the 128-row scale blocks
     const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
     if (gblocks > cap) gblocks = cap;
-    permute_sf_gather_kernel<<<static_cast<unsigned>(gblocks), kPermThreads, smem, s>>>(
-        w.sfc, w.gtok, perm_src, expert_offsets, sf_row_offsets, T, k, E, kc, sf, row_g, status);
+    launch_pdl(permute_sf_gather_kernel, dim3(static_cast<unsigned>(gblocks)), dim3(kPermThreads),
+               smem, s, static_cast<const uint8_t*>(w.sfc), static_cast<const float*>(w.gtok),
+               perm_src, expert_offsets, sf_row_offsets, T, static_cast<int>(k),
+               static_cast<int>(E), kc, sf, row_g, status);
   }
   return MINITE_OK;
 }
@@ -487,14 +494,16 @@ static int permute_quant_impl(const void* x, const int32_t* topk_ids, const floa
   PermWs w = perm_ws(workspace, T, H, E, k, compact);
 
   const int rank_blocks = (nchunks + kRankWarps - 1) / kRankWarps;
-  permute_rank_kernel<<<rank_blocks, 32 * kRankWarps, kRankWarps * E * sizeof(int32_t), s>>>(
-      topk_ids, T, k, E, ct, nchunks, w.table, dest_row, w.counter, status);
-  permute_scan_kernel<<<E, kPermThreads, 0, s>>>(w.table, nchunks, E, w.counter, w.totals,
-                                                 expert_offsets, sf_row_offsets);
+  launch_pdl(permute_rank_kernel, dim3(rank_blocks), dim3(32 * kRankWarps),
+             kRankWarps * E * sizeof(int32_t), s, topk_ids, T, static_cast<int>(k),
+             static_cast<int>(E), ct, nchunks, w.table, dest_row, w.counter, status);
+  launch_pdl(permute_scan_kernel, dim3(E), dim3(kPermThreads), 0, s, w.table, nchunks,
+             static_cast<int>(E), w.counter, w.totals, expert_offsets, sf_row_offsets);
   const int64_t pairs = T * k;
-  permute_route_kernel<<<static_cast<unsigned>((pairs + kPermThreads - 1) / kPermThreads),
-                         kPermThreads, 0, s>>>(topk_ids, topk_w, T, E, k, ct, nchunks, w.table,
-                                               expert_offsets, perm_src, dest_row, perm_w);
+  launch_pdl(permute_route_kernel, dim3(static_cast<unsigned>((pairs + kPermThreads - 1) / kPermThreads)),
+             dim3(kPermThreads), 0, s, topk_ids, topk_w, T, static_cast<int>(E),
+             static_cast<int>(k), ct, nchunks, static_cast<const int32_t*>(w.table),
+             static_cast<const int32_t*>(expert_offsets), perm_src, dest_row, perm_w);
   const int rc = launch_quant_gather(x, topk_ids, T, H, E, k, expert_offsets, sf_row_offsets,
                                      perm_src, dest_row, codes, sf, row_g, w, compact, status, s);
   if (rc != MINITE_OK) return rc;

@@ -26,6 +26,7 @@ constexpr int kAmaxU = 4;
 __global__ void __launch_bounds__(256) group_amax_kernel(const uint16_t* __restrict__ x,
                                                          int64_t elems_per_group,
                                                          uint32_t* __restrict__ amax_bits) {
+  pdl_wait();
   const int64_t grp = blockIdx.y;
   const uint16_t* base = x + grp * elems_per_group;
   const int64_t nvec = elems_per_group / 16;                    // 32-byte vectors
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(256, 4) quantize_group_blocks_kernel(
     const uint16_t* __restrict__ x, int64_t groups, int64_t rows, int nb, uint32_t nb_magic,
     const float* __restrict__ g_in, const uint32_t* __restrict__ amax_bits,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -421,6 +423,7 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
     uint8_t* __restrict__ sf_k, uint8_t* __restrict__ codes_n, uint8_t* __restrict__ sf_n,
     float* __restrict__ g_out) {
   __shared__ __align__(16) uint16_t tiles[2][kDTile];
+  pdl_wait();
   const int t = threadIdx.x;
   const DualGeom G = dual_geom(rows, cols, codes_k, codes_n);
   const int64_t per_group = static_cast<int64_t>(G.tr) * G.tc;
@@ -492,11 +495,11 @@ static void launch_group_blocks(const uint16_t* x, int64_t groups, int64_t rows,
   if (blocks < min_blocks) blocks = min_blocks;
   if (blocks < 1) blocks = 1;
   if (a32)
-    quantize_group_blocks_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, groups, rows, nb, magic, g_in, amax, codes, sf, g_out);
+    launch_pdl(quantize_group_blocks_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256),
+               0, s, x, groups, rows, nb, magic, g_in, amax, codes, sf, g_out);
   else
-    quantize_group_blocks_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, groups, rows, nb, magic, g_in, amax, codes, sf, g_out);
+    launch_pdl(quantize_group_blocks_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256),
+               0, s, x, groups, rows, nb, magic, g_in, amax, codes, sf, g_out);
 }
 
 // Per-group |x| maxima into amax (zeroed first), one grid over all groups.
@@ -509,7 +512,8 @@ static int launch_group_amax(const uint16_t* x, int64_t groups, int64_t per_grou
   if (bx > want) bx = want;
   if (bx < 1) bx = 1;
   dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(groups));
-  group_amax_kernel<<<grid, 256, 0, s>>>(x, per_group, amax);
+  if (launch_pdl(group_amax_kernel, grid, dim3(256), 0, s, x, per_group, amax) != cudaSuccess)
+    return MINITE_ERR_CUDA;
   return MINITE_OK;
 }
 
@@ -544,9 +548,9 @@ extern "C" int minite_quantize_nvfp4_dual(const void* x, int64_t groups, int64_t
   int64_t blocks = static_cast<int64_t>(num_sms()) * 6;
   if (blocks > tiles) blocks = tiles;
   if (blocks * 256 < groups) blocks = (groups + 255) / 256;
-  quantize_dual_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      xb, groups, static_cast<int>(rows), static_cast<int>(cols), amax, codes_k, sf_k, codes_n,
-      sf_n, gscale_out);
+  launch_pdl(quantize_dual_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, xb, groups,
+             static_cast<int>(rows), static_cast<int>(cols), static_cast<const uint32_t*>(amax),
+             codes_k, sf_k, codes_n, sf_n, gscale_out);
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
 

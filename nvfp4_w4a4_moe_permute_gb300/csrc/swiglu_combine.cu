@@ -126,11 +126,12 @@ __global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
   float* lut = smf;
   int32_t* s_off = reinterpret_cast<int32_t*>(smf + kLutEntries);
   int32_t* s_sfoff = s_off + (E + 1);
+  build_silu_lut_part(lut, threadIdx.x, blockDim.x);  // no global memory: overlaps the producer
+  pdl_wait();
   for (int i = threadIdx.x; i <= E; i += blockDim.x) {
     s_off[i] = expert_offsets[i];
     s_sfoff[i] = sf_row_offsets[i];
   }
-  build_silu_lut_part(lut, threadIdx.x, blockDim.x);
   __syncthreads();
   if (!offsets_consistent(s_off, s_sfoff, E, M)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MINITE_ERR_INVALID_ARG);
@@ -228,12 +229,14 @@ static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int 
   const int64_t cap = static_cast<int64_t>(num_sms());
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (h_out)
-    swiglu_quant_kernel<LPR, NCH, true><<<static_cast<unsigned>(blocks), kSwThreads, smem, s>>>(
-        g, perm_w, M, I, E, off, sfoff, codes, sf, row_g, h_out, status);
-  else
-    swiglu_quant_kernel<LPR, NCH, false><<<static_cast<unsigned>(blocks), kSwThreads, smem, s>>>(
-        g, perm_w, M, I, E, off, sfoff, codes, sf, row_g, nullptr, status);
+  const dim3 grid(static_cast<unsigned>(blocks)), block(kSwThreads);
+  const cudaError_t e =
+      h_out ? launch_pdl(swiglu_quant_kernel<LPR, NCH, true>, grid, block, smem, s, g, perm_w, M, I,
+                         E, off, sfoff, codes, sf, row_g, h_out, status)
+            : launch_pdl(swiglu_quant_kernel<LPR, NCH, false>, grid, block, smem, s, g, perm_w, M,
+                         I, E, off, sfoff, codes, sf, row_g, static_cast<uint16_t*>(nullptr),
+                         status);
+  if (e != cudaSuccess) return MINITE_ERR_CUDA;
   return MINITE_OK;
 }
 
@@ -469,6 +472,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
                                                          int64_t T, int64_t M, int N, int k,
                                                          uint16_t* __restrict__ y,
                                                          int32_t* status) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -661,11 +665,12 @@ extern "C" int minite_moe_combine(const void* expert_out, const int32_t* dest_ro
   const uint16_t* d = static_cast<const uint16_t*>(expert_out);
   uint16_t* yy = static_cast<uint16_t*>(y);
   const int n = static_cast<int>(N);
+  const dim3 grid(static_cast<unsigned>(blocks)), block(256);
   if (N % 16 == 0 && aligned(expert_out, 32))
-    combine_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(d, dest_row, T, M, n, k,
-                                                                       yy, status);
+    launch_pdl(combine_kernel<true>, grid, block, 0, s, d, dest_row, T, M, n, static_cast<int>(k),
+               yy, status);
   else
-    combine_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(d, dest_row, T, M, n, k,
-                                                                        yy, status);
+    launch_pdl(combine_kernel<false>, grid, block, 0, s, d, dest_row, T, M, n, static_cast<int>(k),
+               yy, status);
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
