@@ -150,13 +150,16 @@ __global__ void __launch_bounds__(256, 4) quantize_group_blocks_kernel(
   if (t < groups) g_out[t] = g_in ? g_in[t] : global_scale(__uint_as_float(amax_bits[t]));
 }
 
-// Per-row (activation) quantization along columns: one warp per row, lane l
-// owning blocks 32j + l, the row held in registers between its amax and its
-// encoding.
-template <int NCH, bool A32>
+// Quantization along columns, one warp per row, lane l owning blocks 32j + l,
+// the row held in registers between its amax and its encoding. Per-row
+// (activation) scales, or with PG the group's scale (g_in[grp], else from
+// the group maximum in amax_bits).
+template <int NCH, bool A32, bool PG>
 __global__ void __launch_bounds__(256) quantize_token_rows_kernel(
     const uint16_t* __restrict__ x, int64_t groups, int64_t rows, int cols,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out) {
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out,
+    const float* __restrict__ g_in, const uint32_t* __restrict__ amax_bits) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -171,11 +174,13 @@ __global__ void __launch_bounds__(256) quantize_token_rows_kernel(
     uint32_t w[NCH][8];
     float am[NCH];
     const float m = load_row_blocks<NCH, A32>(x + row * cols, nb, w, am);
-    const float g = global_scale(warp_max(m));
+    float g;
+    if (PG) g = g_in ? g_in[grp] : global_scale(__uint_as_float(amax_bits[grp]));
+    else g = global_scale(warp_max(m));
     QBlock qb[NCH];
     quant_row_blocks<NCH>(w, am, nb, g, qb);
     store_row_blocks<NCH>(qb, nb, codes + row * (cols / 2), sf + grp * sf_group_bytes, r, kc);
-    if (lane == 0) g_out[row] = g;
+    if (lane == 0 && (!PG || r == 0)) g_out[PG ? grp : row] = g;
   }
   const int64_t pad_rows = rows_pad - rows;
   for (int64_t p = warp; p < groups * pad_rows; p += nwarps) {
@@ -466,19 +471,21 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
   if (gt < groups) g_out[gt] = global_scale(__uint_as_float(amax_bits[gt]));
 }
 
-template <int NCH>
+template <int NCH, bool PG>
 static void launch_token_rows(const uint16_t* x, int64_t groups, int64_t rows, int cols, bool a32,
-                              uint8_t* codes, uint8_t* sf, float* g_out, cudaStream_t s) {
+                              uint8_t* codes, uint8_t* sf, float* g_out, const float* g_in,
+                              const uint32_t* amax, cudaStream_t s) {
   const int64_t total = groups * ((rows + 127) & ~int64_t(127));
   int64_t blocks = (total + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
+  const dim3 grid(static_cast<unsigned>(blocks)), block(256);
   if (a32)
-    quantize_token_rows_kernel<NCH, true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, groups, rows, cols, codes, sf, g_out);
+    launch_pdl(quantize_token_rows_kernel<NCH, true, PG>, grid, block, 0, s, x, groups, rows, cols,
+               codes, sf, g_out, g_in, amax);
   else
-    quantize_token_rows_kernel<NCH, false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, groups, rows, cols, codes, sf, g_out);
+    launch_pdl(quantize_token_rows_kernel<NCH, false, PG>, grid, block, 0, s, x, groups, rows, cols,
+               codes, sf, g_out, g_in, amax);
 }
 
 static void launch_group_blocks(const uint16_t* x, int64_t groups, int64_t rows, int cols,
@@ -591,11 +598,25 @@ extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows
     const int c = static_cast<int>(cols);
     const bool a32 = aligned(x, 32);
     if (per_group) {
-      launch_group_blocks(xb, groups, rows, c, a32, gscale_in, amax, codes, sf, gscale_out, s);
+      // one warp per row when the row fits in registers, else the flat block stream
+      switch ((cols / 16 + 31) / 32) {
+#define MINITE_CASE(N)                                                                   \
+  case N:                                                                                \
+    launch_token_rows<N, true>(xb, groups, rows, c, a32, codes, sf, gscale_out, gscale_in, \
+                               amax, s);                                                 \
+    break;
+        MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4)
+#undef MINITE_CASE
+        default:
+          launch_group_blocks(xb, groups, rows, c, a32, gscale_in, amax, codes, sf, gscale_out, s);
+      }
     } else {
       switch ((cols / 16 + 31) / 32) {
 #define MINITE_CASE(N) \
-  case N: launch_token_rows<N>(xb, groups, rows, c, a32, codes, sf, gscale_out, s); break;
+  case N:                                                                                \
+    launch_token_rows<N, false>(xb, groups, rows, c, a32, codes, sf, gscale_out, nullptr,  \
+                                nullptr, s);                                             \
+    break;
         MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5)
         MINITE_CASE(6) MINITE_CASE(7) MINITE_CASE(8)
 #undef MINITE_CASE
