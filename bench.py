@@ -200,8 +200,8 @@ class Step:
         self.bwd.status = self.status
 
     def bind(self, inputs, y):
-        """Use the device tensors in `inputs` (x, ids, w, wgu_bf, wd_bf, dy) as
-        this step's inputs and `y` as its output."""
+        """Use the device tensors in `inputs` (any of x, ids, w, wgu_bf, wd_bf, dy)
+        as this step's inputs and `y` as its output."""
         for n, t in inputs.items():
             setattr(self, n, t)
         self.mlp.y = y
@@ -474,13 +474,16 @@ def run_gpu(args):
             "gpu_launches": Step.BWD_LAUNCHES * args.steps,
         }
 
-    # end to end: every step copies its inputs in from pinned host memory and
-    # its result y out to pinned host memory. Inputs and y are double-buffered
-    # on the device, so the copies of step i+1 (copy stream) and the read-back
-    # of step i (a second copy stream) overlap the compute of step i.
+    # end to end: every step copies its inputs (the token batch x, the routing
+    # ids and weights, the incoming gradient dY) in from pinned host memory
+    # and its result y out to pinned host memory; the BF16 weights are model
+    # state that stays on the device between steps (an optimizer updates them
+    # there), so they are not copied. Inputs and y are double-buffered on the
+    # device, so the copies of step i+1 (copy stream) and the read-back of
+    # step i (a second copy stream) overlap the compute of step i.
     e2e = None
     if not args.no_e2e:
-        names = ("x", "ids", "w", "wgu_bf", "wd_bf", "dy")
+        names = ("x", "ids", "w", "dy")
         host = {n: getattr(step, n).cpu().pin_memory() for n in names}
         bufs = [{n: getattr(step, n) for n in names},
                 {n: torch.empty_like(getattr(step, n)) for n in names}]
