@@ -280,7 +280,8 @@ class Step:
                               ("dgu", self.dgu_bf, None), ("x", self.x, mlp.perm_src)):
             self.tok[name] = (src, rs, self.M.quantize_tokens(src, mlp.offsets, E, row_src=rs,
                                                               m_cap=M_))
-        self.ws_tok = torch.empty(max(4, self.M.minite_workspace_bytes(self.M.OP_QUANTIZE_TOKENS, E)),
+        self.ws_tok = torch.empty(max(4, self.M.minite_workspace_bytes(self.M.OP_QUANTIZE_TOKENS, E,
+                                                                       T)),
                                   dtype=u8, device=dev)
         self.dWd = torch.empty((E, H, I), dtype=f32, device=dev)
         self.dWgu = torch.empty((E, 2 * I, H), dtype=f32, device=dev)
@@ -345,8 +346,8 @@ class Step:
             swiglu_keep_h=Mu * 2 * I * 2 + Mu * (I / 2 + I / 16 + 4) + Mu * I * 2,
             swiglu_bwd_keep=Mu * (2 * I * 2 + I * 2 + 4) + Mu * (I + 2 * I / 16 + 4) + Mu * 2 * I * 2,
             combine_dx=Mu * H * 2 + T * H * 2 + T * k * 4,
-            # four operands: each reads its rows twice (amax, encode) and writes codes + scales
-            quant_tokens=sum(2 * Mu * C * 2 + Mu * C / 2 + Mu * C / 16 for C in (H, I, 2 * I, H)),
+            # four operands: each permuted row read once, codes + scales written
+            quant_tokens=sum(Mu * C * 2 + Mu * C / 2 + Mu * C / 16 for C in (H, I, 2 * I, H)),
         )
 
     def algorithmic_bytes(self):

@@ -456,8 +456,9 @@ int minite_moe_combine_backward_quant(const void* dy, int64_t T, int64_t H, int3
  *            128-row x 4-column atoms with k_cap / 16 scale columns; rows past
  *            C are zeroed up to column kofs[E] / 16.
  * g_out:     device, float [E]. kofs_out: device, int32 [E+1].
- * workspace: device, >= minite_workspace_bytes(MINITE_OP_QUANTIZE_TOKENS, E),
- *            4-byte aligned.
+ * workspace: device, >= minite_workspace_bytes(MINITE_OP_QUANTIZE_TOKENS, E,
+ *            row_src ? x_rows : 0), 4-byte aligned (per-expert maxima, and
+ *            for gathered rows one maximum per source row).
  * Device checks: offsets that do not start at 0, decrease or pass m_cap,
  * and kofs[E] > k_cap make the kernels write nothing; a row_src entry
  * outside [0, x_rows) reads as zeros; each sets bit 1<<MINITE_ERR_INVALID_ARG.
@@ -472,7 +473,8 @@ int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const int32_t* r
 
 /* Workspace bytes needed by `op` (MINITE_OP_QUANTIZE: a = groups;
  * MINITE_OP_PERMUTE_QUANT: a = T, b = H, E, k; MINITE_OP_COMBINE_BACKWARD_QUANT:
- * a = T, b = H; MINITE_OP_QUANTIZE_TOKENS: a = E). 0 means none needed. */
+ * a = T, b = H; MINITE_OP_QUANTIZE_TOKENS: a = E, b = source rows when
+ * they are gathered, else 0). 0 means none needed. */
 size_t minite_workspace_bytes(int op, int64_t a, int64_t b, int32_t E, int32_t k);
 
 /* Static description of a status code. */

@@ -20,6 +20,11 @@
 //                        range of permuted rows (rows are expert-contiguous,
 //                        so a range spans few experts) and issues one atomic
 //                        per expert it touched.
+//   token_rowmax_kernel, tokens_amax_gathered_kernel
+//                        the same maximum when rows are gathered: each source
+//                        row's maximum once, then the experts' maxima over
+//                        their rows' sources (a token routed to k experts is
+//                        read once instead of k times).
 //   tokens_quant_kernel  64-token x 256-channel tiles of one expert, gathered
 //                        row by row into shared memory with per-thread
 //                        asynchronous copies (two buffers); thread c quantizes
@@ -116,6 +121,66 @@ __global__ void __launch_bounds__(kTokThreads) tokens_amax_kernel(
     }
     const float v = warp_max(m);
     if (cur >= 0 && lane == 0 && v > 0.0f) atomicMax(amax_bits + cur, __float_as_uint(v));
+  }
+}
+
+// |x| maximum of each source row, one warp per row.
+__global__ void __launch_bounds__(kTokThreads) token_rowmax_kernel(
+    const uint16_t* __restrict__ x, int64_t x_rows, int C, float* __restrict__ rowmax) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int nvec = C / 8;
+  for (int64_t r = warp; r < x_rows; r += nwarps) {
+    const uint4* row = reinterpret_cast<const uint4*>(x + r * C);
+    uint32_t m = 0;  // packed |x| maximum of two BF16 halves
+    for (int i = lane; i < nvec; i += 32) {
+      const uint4 u = __ldg(row + i);
+      m = max_abs_bf16x2(m, max_abs_bf16x2(max_abs_bf16x2(u.x, u.y), max_abs_bf16x2(u.z, u.w)));
+    }
+    float v = fmaxf(bf16lo(m & 0x7FFF7FFFu), bf16hi(m & 0x7FFF7FFFu));
+    v = warp_max(v);
+    if (lane == 0) rowmax[r] = v;
+  }
+}
+
+// Per-expert maxima over the permuted rows' source-row maxima. A warp takes
+// 32 consecutive permuted rows; when they share an expert (the usual case,
+// rows being expert-contiguous) it issues one atomic.
+__global__ void __launch_bounds__(kTokThreads) tokens_amax_gathered_kernel(
+    const float* __restrict__ rowmax, int64_t x_rows, const int32_t* __restrict__ row_src,
+    int64_t m_cap, int E, const int32_t* __restrict__ expert_offsets,
+    uint32_t* __restrict__ amax_bits, int32_t* status) {
+  extern __shared__ int32_t s_off[];  // [E+1]
+  pdl_wait();
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = expert_offsets[i];
+  __syncthreads();
+  if (!token_offsets_ok(s_off, E, m_cap)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MINITE_ERR_INVALID_ARG);
+    return;
+  }
+  const int64_t used = s_off[E];
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t base = warp * 32; base < used; base += nwarps * 32) {
+    const int64_t m = base + lane;
+    float v = 0.0f;
+    int e = -1;
+    if (m < used) {
+      e = expert_of(s_off, E, m);
+      const int32_t src = row_src[m];
+      if (src >= 0 && src < x_rows) v = rowmax[src];
+      else set_status(status, MINITE_ERR_INVALID_ARG);
+    }
+    const int e0 = __shfl_sync(0xffffffffu, e, 0);
+    if (__all_sync(0xffffffffu, e == e0 || e < 0)) {
+      v = warp_max(v);
+      if (lane == 0 && e0 >= 0 && v > 0.0f) atomicMax(amax_bits + e0, __float_as_uint(v));
+    } else if (e >= 0 && v > 0.0f) {
+      atomicMax(amax_bits + e, __float_as_uint(v));
+    }
   }
 }
 
@@ -278,7 +343,11 @@ __global__ void __launch_bounds__(kTokThreads) tokens_quant_kernel(
 using namespace minite;
 
 namespace minite {
-size_t tokens_workspace_bytes(int32_t E) { return static_cast<size_t>(E) * sizeof(uint32_t); }
+// Per-expert maxima, then (for gathered rows) one maximum per source row.
+size_t tokens_workspace_bytes(int32_t E, int64_t x_rows) {
+  const size_t a = (static_cast<size_t>(E) * sizeof(uint32_t) + 255) & ~size_t(255);
+  return a + (x_rows > 0 ? static_cast<size_t>(x_rows) * sizeof(float) : 0);
+}
 }  // namespace minite
 
 extern "C" int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const int32_t* row_src,
@@ -297,7 +366,7 @@ extern "C" int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const
     return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(x, 16) || !aligned(codes, 32) || !aligned(sf, 4) || !aligned(workspace, 4))
     return MINITE_ERR_INVALID_ARG;
-  if (ws_bytes < tokens_workspace_bytes(E)) return MINITE_ERR_INVALID_ARG;
+  if (ws_bytes < tokens_workspace_bytes(E, row_src ? x_rows : 0)) return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   uint32_t* amax = static_cast<uint32_t*>(workspace);
@@ -306,8 +375,22 @@ extern "C" int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const
   int64_t ablocks = (m_cap + kAmaxRows - 1) / kAmaxRows;
   const int64_t acap = static_cast<int64_t>(num_sms()) * 8;
   if (ablocks > acap) ablocks = acap;
-  tokens_amax_kernel<<<static_cast<unsigned>(ablocks), kTokThreads, (E + 1) * sizeof(int32_t),
-                       s>>>(xb, x_rows, row_src, m_cap, c, E, expert_offsets, amax, status);
+  if (row_src) {
+    float* rowmax = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             tokens_workspace_bytes(E, 0));
+    int64_t rblocks = (x_rows + kTokThreads / 32 - 1) / (kTokThreads / 32);
+    if (rblocks > acap) rblocks = acap;
+    token_rowmax_kernel<<<static_cast<unsigned>(rblocks), kTokThreads, 0, s>>>(xb, x_rows, c,
+                                                                              rowmax);
+    int64_t gblocks = (m_cap + kTokThreads - 1) / kTokThreads;
+    if (gblocks > acap) gblocks = acap;
+    tokens_amax_gathered_kernel<<<static_cast<unsigned>(gblocks), kTokThreads,
+                                  (E + 1) * sizeof(int32_t), s>>>(
+        rowmax, x_rows, row_src, m_cap, E, expert_offsets, amax, status);
+  } else {
+    tokens_amax_kernel<<<static_cast<unsigned>(ablocks), kTokThreads, (E + 1) * sizeof(int32_t),
+                         s>>>(xb, x_rows, row_src, m_cap, c, E, expert_offsets, amax, status);
+  }
   const size_t smem = 2 * kTokT * kTokPitch * sizeof(uint16_t) +
                       2 * (E + 1) * sizeof(int64_t) + (E + 1) * sizeof(int32_t);
   static std::once_flag once;

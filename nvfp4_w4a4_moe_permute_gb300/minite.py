@@ -304,8 +304,9 @@ def quantize_tokens(x, expert_offsets, E, row_src=None, m_cap=None, stream=None)
                sf=torch.empty(((C + 127) // 128 * 128) * (k_cap // 16), dtype=torch.uint8, device=dev),
                g=torch.empty(E, dtype=torch.float32, device=dev),
                kofs=torch.empty(E + 1, dtype=torch.int32, device=dev), k_cap=k_cap)
-    ws = torch.empty(max(4, minite_workspace_bytes(OP_QUANTIZE_TOKENS, E)), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.empty(max(4, minite_workspace_bytes(OP_QUANTIZE_TOKENS, E,
+                                                   x_rows if row_src is not None else 0)),
+                     dtype=torch.uint8, device=dev)
     minite_quantize_tokens_nvfp4(x, row_src, m_cap, E, expert_offsets, k_cap, out["codes"],
                                  out["sf"], out["g"], out["kofs"], ws, stream=stream)
     return out

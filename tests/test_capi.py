@@ -58,6 +58,8 @@ def test_workspace_sizes(lib):
     assert M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, 4096, 2048) == 4096 * 128 + 4096 * 4
     assert M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, 0, 2048) == 0
     assert M.minite_workspace_bytes(M.OP_QUANTIZE_TOKENS, 128) == 512
+    # plus one float per source row when rows are gathered
+    assert M.minite_workspace_bytes(M.OP_QUANTIZE_TOKENS, 128, 1000) == 512 + 4000
     assert M.minite_workspace_bytes(M.OP_QUANTIZE_TOKENS, 2000) == 0
 
 
