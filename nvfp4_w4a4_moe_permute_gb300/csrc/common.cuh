@@ -699,6 +699,13 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
                :: "r"(taddr), "r"(ncols) : "memory");
 }
+// Issued by the even CTA of the pair: each CTA's 512-byte scale atom at the
+// descriptor's shared-memory offset into 4 of its own TMEM columns,
+// replicated into the four 32-lane quarters.
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;"
+               :: "r"(taddr), "l"(sdesc) : "memory");
+}
 // Track the pair MMAs issued so far; arrive once on `bar` in every CTA of `mask`.
 __device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t mask) {
   asm volatile(

@@ -945,12 +945,13 @@ constexpr int Q_THREADS = (NUM_WARPS + 1) * 32;
 static_assert(Q_STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
 static_assert(SF_COL0 + Q_NSF * P_SF_COLS <= TMEM_COLS, "TMEM budget");
 
+
 struct QSmem {
   uint64_t full[Q_STAGES];
   uint64_t empty[Q_STAGES];
   uint64_t sfdata[Q_SLOTS];
   uint64_t sfread[Q_SLOTS];
-  uint64_t sf_full[Q_NSF];
+  uint64_t sfready[Q_SLOTS];
   uint64_t sf_empty[Q_NSF];
   uint64_t acc_full;
   uint64_t acc_empty;
@@ -961,8 +962,14 @@ struct QSmem {
   int pad_;
 };
 
-// 23 warps: 6 sit on some sub-partition, whose 16K registers then allow 85
-// per thread.
+// The CTA-pair kernel with two-chunk stages. Its scale factors reach TMEM by
+// tcgen05.cp.cta_group::2 (each CTA's shared memory into its own TMEM),
+// issued by the leader's MMA thread right before the MMAs that read them:
+// 12 copies per chunk, 4 atoms of this CTA's A rows and 8 of B's two 128-row
+// blocks (the single-CTA kernels use scale warps and tcgen05.st instead).
+// Each CTA's scale producer fills its own slot with bulk copies; a relay
+// thread in each CTA forwards the slot's completion to the leader; the
+// leader's commits free the A/B stages and the slots of both CTAs.
 __global__ void __maxnreg__(80)
 grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -996,13 +1003,11 @@ grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmap_a,
       mbar_init(&S.empty[s], 1);
     }
     for (int s = 0; s < Q_SLOTS; ++s) {
-      mbar_init(&S.sfdata[s], 1);
-      mbar_init(&S.sfread[s], 4);
+      mbar_init(&S.sfdata[s], 1);   // this CTA's scale copies
+      mbar_init(&S.sfread[s], 1);   // the leader's commit: both CTAs' copies consumed
+      mbar_init(&S.sfready[s], 2);  // leader: both CTAs' relays
     }
-    for (int b = 0; b < Q_NSF; ++b) {
-      mbar_init(&S.sf_full[b], 8);
-      mbar_init(&S.sf_empty[b], 1);
-    }
+    for (int b = 0; b < Q_NSF; ++b) mbar_init(&S.sf_empty[b], 1);
     mbar_init(&S.acc_full, 1);
     mbar_init(&S.acc_empty, 2 * NUM_EPI_WARPS);
     mbar_init(&S.drain, 1);
@@ -1054,7 +1059,7 @@ grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmap_a,
   volatile int* abort_flag = &S.abort_flag;
   const uint32_t peer_abort = mapa_shared(smem_u32(&S.abort_flag), rank ^ 1u);
   const uint32_t leader_full0 = mapa_shared(smem_u32(&S.full[0]), 0);
-  const uint32_t leader_sf_full0 = mapa_shared(smem_u32(&S.sf_full[0]), 0);
+  const uint32_t leader_sfready0 = mapa_shared(smem_u32(&S.sfready[0]), 0);
   const uint32_t leader_acc_empty = mapa_shared(smem_u32(&S.acc_empty), 0);
   const uint64_t budget = p.budget_ns;
   constexpr uint64_t kDrainBudget = 200000000ull;
@@ -1151,8 +1156,8 @@ grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmap_a,
       constexpr uint32_t idesc = make_idesc_pair();
       const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
       const uint64_t bdesc0 = smem_desc(smem_u32(stages + Q_A_BYTES), 16, 1024, kLayoutSwizzle128B);
-      int stage = 0, sfb = 0;
-      uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
+      int stage = 0, sfb = 0, slot = 0;
+      uint32_t phase = 0, sf_phase = 0, slot_phase = 0, acc_phase = 0;
       bool ok = true;
       bool issued = false;
       for (int t = cid; t < total && ok; t += ncl) {
@@ -1160,25 +1165,42 @@ grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tc_fence_after();
         for (int kd = 0; kd < KD && ok; ++kd) {
           if (!mbar_wait(&S.full[stage], phase, budget, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&S.sfready[slot], slot_phase, budget, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
+          const uint8_t* sSFB = sSFA + Q_SFA_BYTES;
           const int nch = min(Q_CH, KT - Q_CH * kd);
           for (int c = 0; c < nch; ++c) {
-            if (!mbar_wait(&S.sf_full[sfb], sf_phase, budget, abort_flag)) { ok = false; break; }
+            // the ring entry's previous MMAs have completed
+            if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const int kt = Q_CH * kd + c;
             const int ks = min(4, KSTEPS - 4 * kt);
             const uint64_t soff =
                 static_cast<uint64_t>(stage * Q_STAGE_BYTES + c * 128 * BK_BYTES) >> 4;
             const uint32_t sf_t = tmem + SF_COL0 + sfb * P_SF_COLS;
+            for (int s = 0; s < ks; ++s) {
+              // scale atoms of k-step s: this CTA's A rows, then B's two 128-row blocks
+              tc_cp_sf_pair(sf_t + 4 * s,
+                            smem_desc(smem_u32(sSFA + (4 * c + s) * SF_ATOM), 0, 128, kLayoutNone));
+              tc_cp_sf_pair(sf_t + 16 + 8 * s,
+                            smem_desc(smem_u32(sSFB + (4 * c + s) * SF_ATOM), 0, 128, kLayoutNone));
+              tc_cp_sf_pair(sf_t + 16 + 8 * s + 4,
+                            smem_desc(smem_u32(sSFB + (4 * Q_CH + 4 * c + s) * SF_ATOM), 0, 128,
+                                      kLayoutNone));
+            }
             for (int s = 0; s < ks; ++s)
               tc_mma_nvfp4_pair(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc,
                                 sf_t + 4 * s, sf_t + 16 + 8 * s, (kt | s) != 0);
             issued = true;
-            tc_commit_pair_mc(&S.sf_empty[sfb], kPairMask);
+            tc_commit_pair_mc(&S.sf_empty[sfb], 0x1);
             if (++sfb == Q_NSF) { sfb = 0; sf_phase ^= 1u; }
           }
           if (!ok) break;
           tc_commit_pair_mc(&S.empty[stage], kPairMask);
+          tc_commit_pair_mc(&S.sfread[slot], kPairMask);  // both CTAs' slots consumed
           if (++stage == Q_STAGES) { stage = 0; phase ^= 1u; }
+          if (++slot == Q_SLOTS) { slot = 0; slot_phase ^= 1u; }
         }
         if (!ok) break;
         tc_commit_pair_mc(&S.acc_full, kPairMask);
@@ -1191,62 +1213,24 @@ grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmap_a,
         mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
       }
     }
-  } else if (warp < EPI_WARP0) {
-    // ------------------------------------------------------------ scale warps
-    const int quarter = warp & 3;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    int slot = 0, sfb = 0;
-    uint32_t slot_phase = 0, sf_phase = 0;
-    bool ok = true;
-    KIter it;
-    it.start(cid, ncl, total, KD, n_tiles, tiles_prefix, s_off, s_sfb, p);
-    while (it.valid() && ok) {
-      const bool a_ok = static_cast<int>(rank) < it.tl.sf_rbs;
-      const int nrb = min(2, rb_per_expert - it.tl.nt * 2);
-      const int nch = min(Q_CH, KT - Q_CH * it.kt);
-      if (!mbar_wait(&S.sfdata[slot], slot_phase, budget, abort_flag)) ok = false;
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      const uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
-      const uint8_t* sSFB = sSFA + Q_SFA_BYTES;
-      for (int c = 0; c < nch; ++c) {
-        const int ks = min(4, KSTEPS - 4 * (Q_CH * it.kt + c));
-        // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
-        uint32_t ra[16], rbv[32];
-#pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          const int a = 4 * c + st;   // atom index within the slot's 8
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (a_ok && st < ks) v = lds128(sSFA + a * SF_ATOM + lane * 16);
-          ra[4 * st] = v.x; ra[4 * st + 1] = v.y; ra[4 * st + 2] = v.z; ra[4 * st + 3] = v.w;
-#pragma unroll
-          for (int rb = 0; rb < 2; ++rb) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (rb < nrb && st < ks)
-              w = lds128(sSFB + (rb * 4 * Q_CH + a) * SF_ATOM + lane * 16);
-            const int cc = 8 * st + 4 * rb;
-            rbv[cc] = w.x; rbv[cc + 1] = w.y; rbv[cc + 2] = w.z; rbv[cc + 3] = w.w;
-          }
-        }
-        if (c == nch - 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.sfread[slot]);
-        }
-        if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag)) ok = false;
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const uint32_t col = tmem + lane_base + SF_COL0 + sfb * P_SF_COLS;
-        tmem_st_16cols(col, ra);
-        tmem_st_16cols(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[0]));
-        tmem_st_16cols(col + 32, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[16]));
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(leader_sf_full0 + 8u * sfb);
-        if (++sfb == Q_NSF) { sfb = 0; sf_phase ^= 1u; }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ relay: slot filled -> leader
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t slot_phase = 0;
+      bool ok = true;
+      KIter it;
+      it.start(cid, ncl, total, KD, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      while (it.valid()) {
+        if (!mbar_wait(&S.sfdata[slot], slot_phase, budget, abort_flag)) { ok = false; break; }
+        mbar_arrive_cluster(leader_sfready0 + 8u * slot);
+        if (++slot == Q_SLOTS) { slot = 0; slot_phase ^= 1u; }
+        it.advance(p);
       }
-      if (++slot == Q_SLOTS) { slot = 0; slot_phase ^= 1u; }
-      it.advance(p);
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
     }
-    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  } else if (warp < EPI_WARP0) {
+    // warps 3..5 have no role in this kernel
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
