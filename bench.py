@@ -255,8 +255,10 @@ class Step:
     # combine of dX back into token order.
     BWD_STAGES = ["wq_gate_up_dual", "swiglu_keep_h", "swiglu_bwd_keep", "gemm_dgrad_gate_up",
                   "combine_dx", "quant_tokens", "gemm_wgrad_down", "gemm_wgrad_gate_up"]
-    # dual 2, SwiGLU 1, SwiGLU backward 1, GEMM 1, combine 1, 4 token-axis operands x 2, 2 GEMMs
-    BWD_LAUNCHES = 2 + 1 + 1 + 1 + 1 + 8 + 2
+    # dual 2, SwiGLU 1, SwiGLU backward 1, GEMM 1, combine 1, token-axis operands (gathered dY
+    # and x: source-row maxima, expert maxima, encoding; h and [dg | du] with their producers'
+    # row maxima: expert maxima, encoding) 3 + 2 + 2 + 3, 2 GEMMs
+    BWD_LAUNCHES = 2 + 1 + 1 + 1 + 1 + 10 + 2
 
     def init_backward(self):
         import torch
@@ -274,12 +276,17 @@ class Step:
         # weight gradients: BF16 h and [dg | du] kept, their token-axis operands
         self.h_bf = torch.zeros((M_, I), dtype=torch.bfloat16, device=dev)
         self.dgu_bf = torch.zeros((M_, 2 * I), dtype=torch.bfloat16, device=dev)
+        # their row maxima, written by the SwiGLU passes that produce them
+        self.h_amax = torch.zeros(M_, dtype=f32, device=dev)
+        self.dgu_amax = torch.zeros(M_, dtype=f32, device=dev)
         mlp = self.mlp
         self.tok = {}
-        for name, src, rs in (("dy", self.dy, mlp.perm_src), ("h", self.h_bf, None),
-                              ("dgu", self.dgu_bf, None), ("x", self.x, mlp.perm_src)):
-            self.tok[name] = (src, rs, self.M.quantize_tokens(src, mlp.offsets, E, row_src=rs,
-                                                              m_cap=M_))
+        for name, src, rs, ra in (("dy", self.dy, mlp.perm_src, None),
+                                  ("h", self.h_bf, None, self.h_amax),
+                                  ("dgu", self.dgu_bf, None, self.dgu_amax),
+                                  ("x", self.x, mlp.perm_src, None)):
+            self.tok[name] = (src, rs, ra, self.M.quantize_tokens(src, mlp.offsets, E, row_src=rs,
+                                                                  m_cap=M_))
         self.ws_tok = torch.empty(max(4, self.M.minite_workspace_bytes(self.M.OP_QUANTIZE_TOKENS, E,
                                                                        T)),
                                   dtype=u8, device=dev)
@@ -301,11 +308,12 @@ class Step:
         # the forward's SwiGLU keeping BF16 h for the down projection's weight gradient
         M.minite_swiglu_weighted_quant_keep_h(mlp.gate_up, mlp.perm_w, self.E, mlp.offsets,
                                               mlp.sf_offsets, mlp.h_codes, mlp.h_sf, mlp.h_g,
-                                              self.h_bf, self.status, s)
+                                              self.h_bf, self.status, s, h_amax=self.h_amax)
         mark(2)
         M.minite_swiglu_backward_quant_keep(mlp.gate_up, self.dh, mlp.perm_w, self.E, mlp.offsets,
                                             mlp.sf_offsets, self.dgu["codes"], self.dgu["sf"],
-                                            self.dgu["g"], self.dgu_bf, self.status, s)
+                                            self.dgu["g"], self.dgu_bf, self.status, s,
+                                            dgu_amax=self.dgu_amax)
         mark(3)
         M.minite_grouped_gemm_nvfp4(self.dgu["codes"], self.dgu["sf"], self.dgu["g"],
                                     self.wguT["codes"], self.wguT["sf"], self.wgu["g"],
@@ -314,14 +322,15 @@ class Step:
         M.minite_moe_combine(self.dx_perm, mlp.dest_row, self.dx, self.status, s)
         mark(5)
         M_ = self.T * self.k
-        for src, rs, q in self.tok.values():
+        for src, rs, ra, q in self.tok.values():
             M.minite_quantize_tokens_nvfp4(src, rs, M_, self.E, mlp.offsets, q["k_cap"], q["codes"],
-                                           q["sf"], q["g"], q["kofs"], self.ws_tok, self.status, s)
+                                           q["sf"], q["g"], q["kofs"], self.ws_tok, self.status, s,
+                                           row_amax=ra)
         mark(6)
-        M.minite_grouped_gemm_wgrad_nvfp4(self.tok["dy"][2], self.tok["h"][2], self.dWd,
+        M.minite_grouped_gemm_wgrad_nvfp4(self.tok["dy"][3], self.tok["h"][3], self.dWd,
                                           self.status, s)
         mark(7)
-        M.minite_grouped_gemm_wgrad_nvfp4(self.tok["dgu"][2], self.tok["x"][2], self.dWgu,
+        M.minite_grouped_gemm_wgrad_nvfp4(self.tok["dgu"][3], self.tok["x"][3], self.dWgu,
                                           self.status, s)
         mark(8)
 
@@ -343,8 +352,10 @@ class Step:
         sfb = lambda r, c: r * c / 16  # noqa: E731
         return dict(
             wq_gate_up_dual=E * 2 * I * H * 2 + 2 * (E * 2 * I * H / 2 + sfb(E * 2 * I, H)),
-            swiglu_keep_h=Mu * 2 * I * 2 + Mu * (I / 2 + I / 16 + 4) + Mu * I * 2,
-            swiglu_bwd_keep=Mu * (2 * I * 2 + I * 2 + 4) + Mu * (I + 2 * I / 16 + 4) + Mu * 2 * I * 2,
+            # + the kept BF16 rows and their row maxima
+            swiglu_keep_h=Mu * 2 * I * 2 + Mu * (I / 2 + I / 16 + 4) + Mu * (I * 2 + 4),
+            swiglu_bwd_keep=Mu * (2 * I * 2 + I * 2 + 4) + Mu * (I + 2 * I / 16 + 4) +
+            Mu * (2 * I * 2 + 4),
             combine_dx=Mu * H * 2 + T * H * 2 + T * k * 4,
             # four operands: each permuted row read once, codes + scales written
             quant_tokens=sum(Mu * C * 2 + Mu * C / 2 + Mu * C / 16 for C in (H, I, 2 * I, H)),

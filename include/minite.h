@@ -310,14 +310,18 @@ int minite_swiglu_weighted_quant(const void* gate_up, const float* perm_w,
  * nearest even) in h_out, device BF16 [M, I], 32-byte aligned, rows in
  * permuted order; rows at or beyond expert_offsets[E] are not written. h is
  * what the down projection's weight gradient needs from the forward (see
- * minite_quantize_tokens_nvfp4). Same arguments, rules and errors otherwise;
+ * minite_quantize_tokens_nvfp4). h_amax, device float [M] or NULL: when
+ * given, h_amax[m] = max |h_out[m, :]| for every row written (the row's FP32
+ * maximum rounded to BF16, which is the maximum of the rounded row because
+ * rounding is monotone), the per-row maxima that minite_quantize_tokens_nvfp4
+ * takes instead of re-reading h. Same arguments, rules and errors otherwise;
  * h_out may not be NULL.
  */
 int minite_swiglu_weighted_quant_keep_h(const void* gate_up, const float* perm_w, int64_t M,
                                         int64_t I, int32_t E, const int32_t* expert_offsets,
                                         const int32_t* sf_row_offsets, uint8_t* codes,
-                                        uint8_t* sf, float* row_g, void* h_out, int32_t* status,
-                                        minite_stream_t stream);
+                                        uint8_t* sf, float* row_g, void* h_out, float* h_amax,
+                                        int32_t* status, minite_stream_t stream);
 
 /*
  * minite_swiglu_backward_quant -- gradient of the routing-weighted SwiGLU
@@ -366,14 +370,16 @@ int minite_swiglu_backward_quant(const void* gate_up, const void* dh, const floa
  * nearest even) in dgu_out, device BF16 [M, 2I], 32-byte aligned, rows in
  * permuted order; rows at or beyond expert_offsets[E] are not written. The
  * gate_up projection's weight gradient takes its token-axis operand from it
- * (see minite_quantize_tokens_nvfp4). Same arguments, rules and errors
- * otherwise; dgu_out may not be NULL.
+ * (see minite_quantize_tokens_nvfp4). dgu_amax, device float [M] or NULL:
+ * when given, dgu_amax[m] = max |dgu_out[m, :]| for every row written (as
+ * h_amax of minite_swiglu_weighted_quant_keep_h). Same arguments, rules and
+ * errors otherwise; dgu_out may not be NULL.
  */
 int minite_swiglu_backward_quant_keep(const void* gate_up, const void* dh, const float* perm_w,
                                       int64_t M, int64_t I, int32_t E,
                                       const int32_t* expert_offsets, const int32_t* sf_row_offsets,
                                       uint8_t* codes, uint8_t* sf, float* row_g, void* dgu_out,
-                                      int32_t* status, minite_stream_t stream);
+                                      float* dgu_amax, int32_t* status, minite_stream_t stream);
 
 /*
  * minite_moe_combine -- unpermute: y[t] = BF16(sum_{j<k} D[dest_row[t,j]]),
@@ -447,6 +453,11 @@ int minite_moe_combine_backward_quant(const void* dy, int64_t T, int64_t H, int3
  * x:         device, BF16 [x_rows, C], 16-byte aligned.
  * row_src:   device, int32 [m_cap] (e.g. perm_src of the permutation), or
  *            NULL (then rows are x's own and m_cap <= x_rows).
+ * row_amax:  device, float [x_rows], or NULL. When given, row_amax[r] must
+ *            be max_c |x[r, c]| (as the SwiGLU entries that keep their BF16
+ *            output write it); the experts' maxima are then taken from it
+ *            and x is read once (by the encoding) instead of twice. The
+ *            results equal those of a NULL row_amax.
  * m_cap:     permuted rows available (>= expert_offsets[E]).
  * expert_offsets: device, int32 [E+1] (the permutation's).
  * k_cap:     token columns allocated, a multiple of 256 and >= kofs[E]
@@ -457,8 +468,9 @@ int minite_moe_combine_backward_quant(const void* dy, int64_t T, int64_t H, int3
  *            C are zeroed up to column kofs[E] / 16.
  * g_out:     device, float [E]. kofs_out: device, int32 [E+1].
  * workspace: device, >= minite_workspace_bytes(MINITE_OP_QUANTIZE_TOKENS, E,
- *            row_src ? x_rows : 0), 4-byte aligned (per-expert maxima, and
- *            for gathered rows one maximum per source row).
+ *            row_src && !row_amax ? x_rows : 0), 4-byte aligned (per-expert
+ *            maxima, and for gathered rows without row_amax one maximum per
+ *            source row).
  * Device checks: offsets that do not start at 0, decrease or pass m_cap,
  * and kofs[E] > k_cap make the kernels write nothing; a row_src entry
  * outside [0, x_rows) reads as zeros; each sets bit 1<<MINITE_ERR_INVALID_ARG.
@@ -466,7 +478,7 @@ int minite_moe_combine_backward_quant(const void* dy, int64_t T, int64_t H, int3
  * x_rows, m_cap < 2^31.
  */
 int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const int32_t* row_src,
-                                 int64_t m_cap, int64_t C, int32_t E,
+                                 const float* row_amax, int64_t m_cap, int64_t C, int32_t E,
                                  const int32_t* expert_offsets, int64_t k_cap, uint8_t* codes,
                                  uint8_t* sf, float* g_out, int32_t* kofs_out, void* workspace,
                                  size_t ws_bytes, int32_t* status, minite_stream_t stream);
@@ -474,7 +486,8 @@ int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const int32_t* r
 /* Workspace bytes needed by `op` (MINITE_OP_QUANTIZE: a = groups;
  * MINITE_OP_PERMUTE_QUANT: a = T, b = H, E, k; MINITE_OP_COMBINE_BACKWARD_QUANT:
  * a = T, b = H; MINITE_OP_QUANTIZE_TOKENS: a = E, b = source rows when
- * they are gathered, else 0). 0 means none needed. */
+ * they are gathered and no row maxima are passed, else 0). 0 means none
+ * needed. */
 size_t minite_workspace_bytes(int op, int64_t a, int64_t b, int32_t E, int32_t k);
 
 /* Static description of a status code. */

@@ -36,6 +36,12 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+// v rounded to the nearest BF16 (ties to even), as a float. Rounding is
+// monotone and odd, so the |x| maximum of a row rounded to BF16 is the
+// rounded |x| maximum of the row.
+__device__ __forceinline__ float bf16_round(float v) {
+  return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << 16);
+}
 
 // Round to nearest even onto the E2M1 grid, saturating at +-6, sign kept.
 // Returns one byte holding `lo` in bits 0..3 and `hi` in bits 4..7.

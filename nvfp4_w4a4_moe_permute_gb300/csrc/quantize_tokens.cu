@@ -24,12 +24,18 @@
 //                        the same maximum when rows are gathered: each source
 //                        row's maximum once, then the experts' maxima over
 //                        their rows' sources (a token routed to k experts is
-//                        read once instead of k times).
+//                        read once instead of k times). With caller-given
+//                        row maxima (the SwiGLU entries that keep their BF16
+//                        output write them) only the second kernel runs, and
+//                        the operand is read once, by the encoding.
 //   tokens_quant_kernel  64-token x 256-channel tiles of one expert, gathered
 //                        row by row into shared memory with per-thread
-//                        asynchronous copies (two buffers); thread c quantizes
-//                        channel c's four 16-token blocks and writes 32 code
-//                        bytes and 4 scale bytes, all contiguous.
+//                        asynchronous copies (two buffers). Each tile's
+//                        position is decoded once and its source rows are
+//                        looked up one tile ahead of its copies; thread c
+//                        quantizes channel c's four 16-token blocks and
+//                        writes 32 code bytes and 4 scale bytes, all
+//                        contiguous.
 #include <mutex>
 
 #include "common.cuh"
@@ -43,6 +49,7 @@ constexpr int kTokT = 64;                   // tokens per tile
 constexpr int kTokC = 256;                  // channels per tile (one per thread)
 constexpr int kTokPitch = kTokC + 8;        // BF16 per staged row, 16-byte aligned rows
 constexpr int kTokThreads = 256;
+constexpr int kTokCtasPerSm = 3;           // resident CTAs per SM (shared memory)
 constexpr int kTokAlign = 256;              // tokens: K alignment of each expert
 constexpr int kAmaxRows = 64;               // permuted rows per CTA of the amax pass
 
@@ -145,9 +152,10 @@ __global__ void __launch_bounds__(kTokThreads) token_rowmax_kernel(
   }
 }
 
-// Per-expert maxima over the permuted rows' source-row maxima. A warp takes
-// 32 consecutive permuted rows; when they share an expert (the usual case,
-// rows being expert-contiguous) it issues one atomic.
+// Per-expert maxima over the permuted rows' source-row maxima (row m's
+// source is row_src[m], or m itself without row_src). A warp takes 32
+// consecutive permuted rows; when they share an expert (the usual case, rows
+// being expert-contiguous) it issues one atomic.
 __global__ void __launch_bounds__(kTokThreads) tokens_amax_gathered_kernel(
     const float* __restrict__ rowmax, int64_t x_rows, const int32_t* __restrict__ row_src,
     int64_t m_cap, int E, const int32_t* __restrict__ expert_offsets,
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(kTokThreads) tokens_amax_gathered_kernel(
     int e = -1;
     if (m < used) {
       e = expert_of(s_off, E, m);
-      const int32_t src = row_src[m];
+      const int64_t src = row_src ? row_src[m] : m;
       if (src >= 0 && src < x_rows) v = rowmax[src];
       else set_status(status, MINITE_ERR_INVALID_ARG);
     }
@@ -250,61 +258,86 @@ __global__ void __launch_bounds__(kTokThreads) tokens_quant_kernel(
   const int64_t pitch = k_cap / 2;      // code bytes per channel row
   const int64_t units = s_upre[E];
 
-  // unit u -> (expert, token tile, channel tile)
-  auto unit_pos = [&](int64_t u, int& e, int& tt, int& ct) {
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_upre[mid] <= u) lo = mid; else hi = mid;
-    }
-    e = lo;
-    const int64_t rem = u - s_upre[lo];
-    tt = static_cast<int>(rem / nct);
-    ct = static_cast<int>(rem - static_cast<int64_t>(tt) * nct);
+  // unit u -> (expert, token tile, channel tile); expert -1 past the last unit
+  struct Unit {
+    int e, tt, ct;
   };
-  auto fetch = [&](int64_t u, uint16_t* buf) {
+  auto unit_pos = [&](int64_t u) {
+    Unit d{-1, 0, 0};
     if (u < units) {
-      int e, tt, ct;
-      unit_pos(u, e, tt, ct);
-      const int cnt = s_off[e + 1] - s_off[e];
-      const int c0 = ct * kTokC;
+      int lo = 0, hi = E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_upre[mid] <= u) lo = mid; else hi = mid;
+      }
+      const int64_t rem = u - s_upre[lo];
+      d.e = lo;
+      d.tt = static_cast<int>(rem / nct);
+      d.ct = static_cast<int>(rem - static_cast<int64_t>(d.tt) * nct);
+    }
+    return d;
+  };
+  // This thread's 8 rows of a unit (rows warp + 8 i, 16-byte piece lane):
+  // their source rows, looked up one tile ahead of the copies.
+  auto srcs_of = [&](const Unit& d, int32_t (&sr)[8], uint32_t& vmask) {
+    vmask = 0;
+    if (d.e >= 0) {
+      const int cnt = s_off[d.e + 1] - s_off[d.e];
+      const bool cval = d.ct * kTokC + 8 * (t & 31) < C;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int lr = (t >> 5) + 8 * i, seg = t & 31;  // row lr, 16-byte piece seg
-        const int tok = tt * kTokT + lr;
-        bool valid = tok < cnt && c0 + 8 * seg < C;
-        int64_t src = static_cast<int64_t>(s_off[e]) + tok;
-        if (valid && row_src) {
-          src = row_src[src];
-          if (src < 0 || src >= x_rows) {
-            set_status(status, MINITE_ERR_INVALID_ARG);
-            valid = false;
-          }
+        const int tok = d.tt * kTokT + (t >> 5) + 8 * i;
+        sr[i] = s_off[d.e] + tok;
+        if (cval && tok < cnt) {
+          vmask |= 1u << i;
+          if (row_src) sr[i] = row_src[sr[i]];
         }
-        cp_async16(buf + lr * kTokPitch + 8 * seg, valid ? x + src * C + c0 + 8 * seg : x, valid);
+      }
+    }
+  };
+  auto issue = [&](const Unit& d, const int32_t (&sr)[8], uint32_t vmask, uint16_t* buf) {
+    if (d.e >= 0) {
+      const uint16_t* xs = x + d.ct * kTokC + 8 * (t & 31);
+      uint16_t* bs = buf + (t >> 5) * kTokPitch + 8 * (t & 31);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        bool valid = (vmask >> i) & 1u;
+        const int64_t src = sr[i];
+        if (valid && (src < 0 || src >= x_rows)) {
+          set_status(status, MINITE_ERR_INVALID_ARG);
+          valid = false;
+        }
+        cp_async16(bs + 8 * i * kTokPitch, valid ? xs + src * C : x, valid);
       }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
 
+  const int64_t G = gridDim.x;
   int64_t u = blockIdx.x;
-  fetch(u, tiles);
+  Unit d0 = unit_pos(u), d1 = unit_pos(u + G);
+  int32_t sr[8];  // source rows of the next tile to copy (valid where vm has the bit)
+  uint32_t vm;
+  srcs_of(d0, sr, vm);
+  issue(d0, sr, vm, tiles);
+  srcs_of(d1, sr, vm);
   int cur = 0;
   int ecur = -1;
   float g = 1.0f, tk = 1.0f;
-  for (; u < units; u += gridDim.x, cur ^= 1) {
-    fetch(u + gridDim.x, tiles + (cur ^ 1) * kTokT * kTokPitch);
+  for (; u < units; u += G, cur ^= 1) {
+    issue(d1, sr, vm, tiles + (cur ^ 1) * kTokT * kTokPitch);
+    const Unit d2 = unit_pos(u + 2 * G);
+    srcs_of(d2, sr, vm);
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncthreads();
-    int e, tt, ct;
-    unit_pos(u, e, tt, ct);
+    const int e = d0.e, tt = d0.tt;
     if (e != ecur) {  // block-uniform
       ecur = e;
       g = global_scale(__uint_as_float(amax_bits[e]));
       tk = enc_table_entry(g);
     }
     const uint16_t* tile = tiles + cur * kTokT * kTokPitch;
-    const int c = ct * kTokC + t;
+    const int c = d0.ct * kTokC + t;
     const bool valid = c < C;
     uint2 code[4];
     uint32_t sfw = 0;
@@ -325,7 +358,9 @@ __global__ void __launch_bounds__(kTokThreads) tokens_quant_kernel(
                    code[3].x, code[3].y);
       *reinterpret_cast<uint32_t*>(sf + sf_offset(c, k0 / 16, kc)) = sfw;
     }
-    __syncthreads();  // the buffer is refilled two units from now
+    __syncthreads();  // the next iteration refills this buffer
+    d0 = d1;
+    d1 = d2;
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 
@@ -351,7 +386,7 @@ size_t tokens_workspace_bytes(int32_t E, int64_t x_rows) {
 }  // namespace minite
 
 extern "C" int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const int32_t* row_src,
-                                            int64_t m_cap, int64_t C, int32_t E,
+                                            const float* row_amax, int64_t m_cap, int64_t C, int32_t E,
                                             const int32_t* expert_offsets, int64_t k_cap,
                                             uint8_t* codes, uint8_t* sf, float* g_out,
                                             int32_t* kofs_out, void* workspace, size_t ws_bytes,
@@ -364,9 +399,11 @@ extern "C" int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const
   if (k_cap < kTokAlign || k_cap % kTokAlign != 0 || x_rows >= (int64_t(1) << 31) ||
       m_cap >= (int64_t(1) << 31) || C * (k_cap / 2) >= (int64_t(1) << 40))
     return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(x, 16) || !aligned(codes, 32) || !aligned(sf, 4) || !aligned(workspace, 4))
+  if (!aligned(x, 16) || !aligned(codes, 32) || !aligned(sf, 4) || !aligned(workspace, 4) ||
+      !aligned(row_amax, 4))
     return MINITE_ERR_INVALID_ARG;
-  if (ws_bytes < tokens_workspace_bytes(E, row_src ? x_rows : 0)) return MINITE_ERR_INVALID_ARG;
+  if (ws_bytes < tokens_workspace_bytes(E, row_src && !row_amax ? x_rows : 0))
+    return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   uint32_t* amax = static_cast<uint32_t*>(workspace);
@@ -375,13 +412,17 @@ extern "C" int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const
   int64_t ablocks = (m_cap + kAmaxRows - 1) / kAmaxRows;
   const int64_t acap = static_cast<int64_t>(num_sms()) * 8;
   if (ablocks > acap) ablocks = acap;
-  if (row_src) {
-    float* rowmax = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                             tokens_workspace_bytes(E, 0));
-    int64_t rblocks = (x_rows + kTokThreads / 32 - 1) / (kTokThreads / 32);
-    if (rblocks > acap) rblocks = acap;
-    token_rowmax_kernel<<<static_cast<unsigned>(rblocks), kTokThreads, 0, s>>>(xb, x_rows, c,
-                                                                              rowmax);
+  if (row_src || row_amax) {
+    const float* rowmax = row_amax;
+    if (!rowmax) {  // each source row's maximum once
+      float* rm = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           tokens_workspace_bytes(E, 0));
+      int64_t rblocks = (x_rows + kTokThreads / 32 - 1) / (kTokThreads / 32);
+      if (rblocks > acap) rblocks = acap;
+      token_rowmax_kernel<<<static_cast<unsigned>(rblocks), kTokThreads, 0, s>>>(xb, x_rows, c,
+                                                                                rm);
+      rowmax = rm;
+    }
     int64_t gblocks = (m_cap + kTokThreads - 1) / kTokThreads;
     if (gblocks > acap) gblocks = acap;
     tokens_amax_gathered_kernel<<<static_cast<unsigned>(gblocks), kTokThreads,
@@ -401,7 +442,7 @@ extern "C" int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const
                                                  2 * 1025 * sizeof(int64_t) + 1025 * 4));
   });
   if (attr != cudaSuccess) return MINITE_ERR_CUDA;
-  const int64_t qblocks = static_cast<int64_t>(num_sms()) * 3;
+  const int64_t qblocks = static_cast<int64_t>(num_sms()) * kTokCtasPerSm;
   tokens_quant_kernel<<<static_cast<unsigned>(qblocks), kTokThreads, smem, s>>>(
       xb, x_rows, row_src, m_cap, c, E, expert_offsets, amax, k_cap, codes, sf, g_out, kofs_out,
       status);

@@ -103,7 +103,8 @@ __device__ __forceinline__ float group_max(float v) {
 // of a row owns blocks l + LPR*j (j < NCH) of the row's intermediate, with
 // the gates at [0, I) and the ups at [I, 2I) of the gate_up row. Every row's
 // 4I input bytes are requested before any of them is used.
-// KEEP_H: h is also stored as BF16 (round to nearest even) in h_out [M, I].
+// KEEP_H: h is also stored as BF16 (round to nearest even) in h_out [M, I],
+// and, when h_amax is given, each stored row's |h| maximum in h_amax [M].
 constexpr int kSwThreads = 512;
 
 __device__ __forceinline__ void st_bf16x16(uint16_t* p, const float (&v)[16]) {
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
     const uint16_t* __restrict__ gu, const float* __restrict__ perm_w, int64_t M, int I, int E,
     const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ sf_row_offsets,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
-    uint16_t* __restrict__ h_out, int32_t* status) {
+    uint16_t* __restrict__ h_out, float* __restrict__ h_amax, int32_t* status) {
   extern __shared__ __align__(16) float smf[];
   float* lut = smf;
   int32_t* s_off = reinterpret_cast<int32_t*>(smf + kLutEntries);
@@ -175,7 +176,8 @@ __global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
       am[j] = amax_f32x16(h[j]);
       rm = fmaxf(rm, am[j]);
     }
-    const float g = global_scale(group_max<LPR>(rm));
+    const float rmax = group_max<LPR>(rm);
+    const float g = global_scale(rmax);
     const float tk = enc_table_entry(g);
     QBlock qb[NCH];
 #pragma unroll
@@ -203,6 +205,7 @@ __global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
         if (c < kc) sf[sf_offset(r, c, kc)] = static_cast<uint8_t>(qb[j].sf);
       }
       if (l == 0) row_g[m] = g;
+      if (KEEP_H && h_amax && l == 0) h_amax[m] = bf16_round(rmax);
     }
   }
 
@@ -221,7 +224,8 @@ __global__ void __launch_bounds__(kSwThreads, 1) swiglu_quant_kernel(
 template <int LPR, int NCH>
 static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int I, int E,
                          const int32_t* off, const int32_t* sfoff, uint8_t* codes, uint8_t* sf,
-                         float* row_g, uint16_t* h_out, int32_t* status, cudaStream_t s) {
+                         float* row_g, uint16_t* h_out, float* h_amax, int32_t* status,
+                         cudaStream_t s) {
   const size_t smem = kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
   // table (32 KB) + offsets stay under the default 48 KB of dynamic shared memory
   constexpr int rows_per_cta = kSwThreads / 32 * (32 / LPR);
@@ -232,10 +236,10 @@ static int launch_swiglu(const uint16_t* g, const float* perm_w, int64_t M, int 
   const dim3 grid(static_cast<unsigned>(blocks)), block(kSwThreads);
   const cudaError_t e =
       h_out ? launch_pdl(swiglu_quant_kernel<LPR, NCH, true>, grid, block, smem, s, g, perm_w, M, I,
-                         E, off, sfoff, codes, sf, row_g, h_out, status)
+                         E, off, sfoff, codes, sf, row_g, h_out, h_amax, status)
             : launch_pdl(swiglu_quant_kernel<LPR, NCH, false>, grid, block, smem, s, g, perm_w, M,
                          I, E, off, sfoff, codes, sf, row_g, static_cast<uint16_t*>(nullptr),
-                         status);
+                         static_cast<float*>(nullptr), status);
   if (e != cudaSuccess) return MINITE_ERR_CUDA;
   return MINITE_OK;
 }
@@ -323,14 +327,15 @@ __device__ __forceinline__ void swiglu_bwd_block(const float* lut_s, const float
 template <int NCH>
 constexpr int bwd_threads() { return NCH <= 2 ? 512 : 256; }
 
-// KEEP: [dg | du] is also stored as BF16 in dgu_out [M, 2I].
+// KEEP: [dg | du] is also stored as BF16 in dgu_out [M, 2I], and, when
+// dgu_amax is given, each stored row's |x| maximum in dgu_amax [M].
 template <int NCH, bool KEEP>
 __global__ void __launch_bounds__(bwd_threads<NCH>(), 1) swiglu_bwd_quant_kernel(
     const uint16_t* __restrict__ gu, const uint16_t* __restrict__ dh,
     const float* __restrict__ perm_w, int64_t M, int I, int E,
     const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ sf_row_offsets,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
-    uint16_t* __restrict__ dgu_out, int32_t* status) {
+    uint16_t* __restrict__ dgu_out, float* __restrict__ dgu_amax, int32_t* status) {
   extern __shared__ __align__(16) float smf[];
   float* lut_s = smf;
   float* lut_d = smf + kLutEntries;
@@ -380,7 +385,8 @@ __global__ void __launch_bounds__(bwd_threads<NCH>(), 1) swiglu_bwd_quant_kernel
       amu[j] = amax_f32x16(duv[j]);
       rm = fmaxf(rm, fmaxf(amg[j], amu[j]));
     }
-    const float g = global_scale(warp_max(rm));
+    const float rmax = warp_max(rm);
+    const float g = global_scale(rmax);
     const float tk = enc_table_entry(g);
     QBlock qg[NCH], qu[NCH];
 #pragma unroll
@@ -413,6 +419,7 @@ __global__ void __launch_bounds__(bwd_threads<NCH>(), 1) swiglu_bwd_quant_kernel
       }
     }
     if (lane == 0) row_g[m] = g;
+    if (KEEP && dgu_amax && lane == 0) dgu_amax[m] = bf16_round(rmax);
   }
 
   // zero the scale bytes of each expert's padding rows
@@ -443,7 +450,7 @@ template <int NCH>
 static int launch_swiglu_bwd(const uint16_t* g, const uint16_t* dh, const float* perm_w,
                              int64_t M, int I, int E, const int32_t* off, const int32_t* sfoff,
                              uint8_t* codes, uint8_t* sf, float* row_g, uint16_t* dgu_out,
-                             int32_t* status, cudaStream_t s) {
+                             float* dgu_amax, int32_t* status, cudaStream_t s) {
   const size_t smem = 2 * kLutEntries * sizeof(float) + 2 * (E + 1) * sizeof(int32_t);
   if ((dgu_out ? bwd_smem_attr<NCH, true>() : bwd_smem_attr<NCH, false>()) != cudaSuccess)
     return MINITE_ERR_CUDA;
@@ -454,10 +461,10 @@ static int launch_swiglu_bwd(const uint16_t* g, const uint16_t* dh, const float*
   if (blocks < 1) blocks = 1;
   if (dgu_out)
     swiglu_bwd_quant_kernel<NCH, true><<<static_cast<unsigned>(blocks), threads, smem, s>>>(
-        g, dh, perm_w, M, I, E, off, sfoff, codes, sf, row_g, dgu_out, status);
+        g, dh, perm_w, M, I, E, off, sfoff, codes, sf, row_g, dgu_out, dgu_amax, status);
   else
     swiglu_bwd_quant_kernel<NCH, false><<<static_cast<unsigned>(blocks), threads, smem, s>>>(
-        g, dh, perm_w, M, I, E, off, sfoff, codes, sf, row_g, nullptr, status);
+        g, dh, perm_w, M, I, E, off, sfoff, codes, sf, row_g, nullptr, nullptr, status);
   return MINITE_OK;
 }
 
@@ -545,14 +552,15 @@ using namespace minite;
 static int swiglu_weighted_quant_impl(const void* gate_up, const float* perm_w, int64_t M,
                                       int64_t I, int32_t E, const int32_t* expert_offsets,
                                       const int32_t* sf_row_offsets, uint8_t* codes, uint8_t* sf,
-                                      float* row_g, void* h_out, int32_t* status,
-                                      minite_stream_t stream) {
+                                      float* row_g, void* h_out, float* h_amax,
+                                      int32_t* status, minite_stream_t stream) {
   if (!gate_up || !expert_offsets || !sf_row_offsets || !codes || !sf || !row_g)
     return MINITE_ERR_INVALID_ARG;
   if (M < 1 || I < 64 || I % 64 != 0 || I > 2048 || E < 1 || E > 1024)
     return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (M >= (int64_t(1) << 31)) return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(gate_up, 32) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(h_out, 32))
+  if (!aligned(gate_up, 32) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(h_out, 32) ||
+      !aligned(h_amax, 4))
     return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* g = static_cast<const uint16_t*>(gate_up);
@@ -562,17 +570,17 @@ static int swiglu_weighted_quant_impl(const void* gate_up, const float* perm_w, 
   int rc;
   // 16 lanes per row when that leaves no lane idle or the row is short
   if (nb <= 16) rc = launch_swiglu<16, 1>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets,
-                                           codes, sf, row_g, h, status, s);
+                                           codes, sf, row_g, h, h_amax, status, s);
   else if (nb <= 32) rc = launch_swiglu<16, 2>(g, perm_w, M, i, E, expert_offsets,
-                                                sf_row_offsets, codes, sf, row_g, h, status, s);
+                                                sf_row_offsets, codes, sf, row_g, h, h_amax, status, s);
   else if (nb <= 48) rc = launch_swiglu<16, 3>(g, perm_w, M, i, E, expert_offsets,
-                                                sf_row_offsets, codes, sf, row_g, h, status, s);
+                                                sf_row_offsets, codes, sf, row_g, h, h_amax, status, s);
   else if (nb <= 64) rc = launch_swiglu<32, 2>(g, perm_w, M, i, E, expert_offsets,
-                                                sf_row_offsets, codes, sf, row_g, h, status, s);
+                                                sf_row_offsets, codes, sf, row_g, h, h_amax, status, s);
   else if (nb <= 96) rc = launch_swiglu<32, 3>(g, perm_w, M, i, E, expert_offsets,
-                                                sf_row_offsets, codes, sf, row_g, h, status, s);
+                                                sf_row_offsets, codes, sf, row_g, h, h_amax, status, s);
   else rc = launch_swiglu<32, 4>(g, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes, sf,
-                                 row_g, h, status, s);
+                                 row_g, h, h_amax, status, s);
   if (rc != MINITE_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
@@ -584,31 +592,31 @@ extern "C" int minite_swiglu_weighted_quant(const void* gate_up, const float* pe
                                             uint8_t* sf, float* row_g, int32_t* status,
                                             minite_stream_t stream) {
   return swiglu_weighted_quant_impl(gate_up, perm_w, M, I, E, expert_offsets, sf_row_offsets,
-                                    codes, sf, row_g, nullptr, status, stream);
+                                    codes, sf, row_g, nullptr, nullptr, status, stream);
 }
 
 extern "C" int minite_swiglu_weighted_quant_keep_h(
     const void* gate_up, const float* perm_w, int64_t M, int64_t I, int32_t E,
     const int32_t* expert_offsets, const int32_t* sf_row_offsets, uint8_t* codes, uint8_t* sf,
-    float* row_g, void* h_out, int32_t* status, minite_stream_t stream) {
+    float* row_g, void* h_out, float* h_amax, int32_t* status, minite_stream_t stream) {
   if (!h_out) return MINITE_ERR_INVALID_ARG;
   return swiglu_weighted_quant_impl(gate_up, perm_w, M, I, E, expert_offsets, sf_row_offsets,
-                                    codes, sf, row_g, h_out, status, stream);
+                                    codes, sf, row_g, h_out, h_amax, status, stream);
 }
 
 static int swiglu_backward_quant_impl(const void* gate_up, const void* dh, const float* perm_w,
                                       int64_t M, int64_t I, int32_t E,
                                       const int32_t* expert_offsets,
                                       const int32_t* sf_row_offsets, uint8_t* codes, uint8_t* sf,
-                                      float* row_g, void* dgu_out, int32_t* status,
-                                      minite_stream_t stream) {
+                                      float* row_g, void* dgu_out, float* dgu_amax,
+                                      int32_t* status, minite_stream_t stream) {
   if (!gate_up || !dh || !expert_offsets || !sf_row_offsets || !codes || !sf || !row_g)
     return MINITE_ERR_INVALID_ARG;
   if (M < 1 || I < 64 || I % 64 != 0 || I > 2048 || E < 1 || E > 1024)
     return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (M >= (int64_t(1) << 31)) return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(gate_up, 32) || !aligned(dh, 32) || !aligned(codes, 16) || !aligned(sf, 16) ||
-      !aligned(dgu_out, 32))
+      !aligned(dgu_out, 32) || !aligned(dgu_amax, 4))
     return MINITE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* g = static_cast<const uint16_t*>(gate_up);
@@ -618,13 +626,13 @@ static int swiglu_backward_quant_impl(const void* gate_up, const void* dh, const
   const int nb = i / 16;
   int rc;
   if (nb <= 32) rc = launch_swiglu_bwd<1>(g, d, perm_w, M, i, E, expert_offsets, sf_row_offsets,
-                                          codes, sf, row_g, k, status, s);
+                                          codes, sf, row_g, k, dgu_amax, status, s);
   else if (nb <= 64) rc = launch_swiglu_bwd<2>(g, d, perm_w, M, i, E, expert_offsets,
-                                               sf_row_offsets, codes, sf, row_g, k, status, s);
+                                               sf_row_offsets, codes, sf, row_g, k, dgu_amax, status, s);
   else if (nb <= 96) rc = launch_swiglu_bwd<3>(g, d, perm_w, M, i, E, expert_offsets,
-                                               sf_row_offsets, codes, sf, row_g, k, status, s);
+                                               sf_row_offsets, codes, sf, row_g, k, dgu_amax, status, s);
   else rc = launch_swiglu_bwd<4>(g, d, perm_w, M, i, E, expert_offsets, sf_row_offsets, codes,
-                                 sf, row_g, k, status, s);
+                                 sf, row_g, k, dgu_amax, status, s);
   if (rc != MINITE_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
@@ -636,7 +644,7 @@ extern "C" int minite_swiglu_backward_quant(const void* gate_up, const void* dh,
                                             uint8_t* sf, float* row_g, int32_t* status,
                                             minite_stream_t stream) {
   return swiglu_backward_quant_impl(gate_up, dh, perm_w, M, I, E, expert_offsets, sf_row_offsets,
-                                    codes, sf, row_g, nullptr, status, stream);
+                                    codes, sf, row_g, nullptr, nullptr, status, stream);
 }
 
 extern "C" int minite_swiglu_backward_quant_keep(const void* gate_up, const void* dh,
@@ -644,10 +652,11 @@ extern "C" int minite_swiglu_backward_quant_keep(const void* gate_up, const void
                                                  int32_t E, const int32_t* expert_offsets,
                                                  const int32_t* sf_row_offsets, uint8_t* codes,
                                                  uint8_t* sf, float* row_g, void* dgu_out,
-                                                 int32_t* status, minite_stream_t stream) {
+                                                 float* dgu_amax, int32_t* status,
+                                                 minite_stream_t stream) {
   if (!dgu_out) return MINITE_ERR_INVALID_ARG;
   return swiglu_backward_quant_impl(gate_up, dh, perm_w, M, I, E, expert_offsets, sf_row_offsets,
-                                    codes, sf, row_g, dgu_out, status, stream);
+                                    codes, sf, row_g, dgu_out, dgu_amax, status, stream);
 }
 
 extern "C" int minite_moe_combine(const void* expert_out, const int32_t* dest_row, int64_t T,

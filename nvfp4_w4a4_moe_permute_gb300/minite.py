@@ -62,19 +62,19 @@ def load(path: str | None = None):
                                              _vp, _vp, _vp, _vp, _vp, _vp, _vp],
         "minite_moe_combine_backward_quant": [_vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                               _vp, _vp, _vp, _sz, _vp, _vp],
-        "minite_quantize_tokens_nvfp4": [_vp, _i64, _vp, _i64, _i64, _i32, _vp, _i64, _vp, _vp, _vp,
-                                         _vp, _vp, _sz, _vp, _vp],
+        "minite_quantize_tokens_nvfp4": [_vp, _i64, _vp, _vp, _i64, _i64, _i32, _vp, _i64, _vp, _vp,
+                                         _vp, _vp, _vp, _sz, _vp, _vp],
         "minite_grouped_gemm_wgrad_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64,
                                             _vp, _int, _vp, _vp],
         "minite_grouped_gemm_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                       _vp, _int, _vp, _vp],
         "minite_swiglu_weighted_quant": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
         "minite_swiglu_weighted_quant_keep_h": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp,
-                                                _vp, _vp, _vp],
+                                                _vp, _vp, _vp, _vp],
         "minite_swiglu_backward_quant": [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp],
         "minite_swiglu_backward_quant_keep": [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp,
-                                              _vp, _vp, _vp, _vp],
+                                              _vp, _vp, _vp, _vp, _vp],
         "minite_moe_combine": [_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp],
         "minite_test_convert": [_vp, _i64, _vp, _vp, _vp, _vp],
         "minite_test_div6_exhaustive": [_vp, _vp],
@@ -228,12 +228,12 @@ def minite_swiglu_weighted_quant(gate_up, perm_w, E, expert_offsets, sf_row_offs
 
 
 def minite_swiglu_weighted_quant_keep_h(gate_up, perm_w, E, expert_offsets, sf_row_offsets, codes,
-                                        sf, row_g, h_out, status=None, stream=None):
+                                        sf, row_g, h_out, status=None, stream=None, h_amax=None):
     M, I2 = gate_up.shape
     rc = load().minite_swiglu_weighted_quant_keep_h(_p(gate_up), _p(perm_w), M, I2 // 2, E,
                                                     _p(expert_offsets), _p(sf_row_offsets),
                                                     _p(codes), _p(sf), _p(row_g), _p(h_out),
-                                                    _p(status), _s(stream))
+                                                    _p(h_amax), _p(status), _s(stream))
     _check(rc, "minite_swiglu_weighted_quant_keep_h")
 
 
@@ -247,12 +247,13 @@ def minite_swiglu_backward_quant(gate_up, dh, perm_w, E, expert_offsets, sf_row_
 
 
 def minite_swiglu_backward_quant_keep(gate_up, dh, perm_w, E, expert_offsets, sf_row_offsets,
-                                      codes, sf, row_g, dgu_out, status=None, stream=None):
+                                      codes, sf, row_g, dgu_out, status=None, stream=None,
+                                      dgu_amax=None):
     M, I2 = gate_up.shape
     rc = load().minite_swiglu_backward_quant_keep(_p(gate_up), _p(dh), _p(perm_w), M, I2 // 2, E,
                                                   _p(expert_offsets), _p(sf_row_offsets),
                                                   _p(codes), _p(sf), _p(row_g), _p(dgu_out),
-                                                  _p(status), _s(stream))
+                                                  _p(dgu_amax), _p(status), _s(stream))
     _check(rc, "minite_swiglu_backward_quant_keep")
 
 
@@ -269,10 +270,10 @@ def minite_moe_combine_backward_quant(dy, E, dest_row, expert_offsets, sf_row_of
 
 
 def minite_quantize_tokens_nvfp4(x, row_src, m_cap, E, expert_offsets, k_cap, codes, sf, g, kofs,
-                                 workspace, status=None, stream=None):
+                                 workspace, status=None, stream=None, row_amax=None):
     x_rows, C = x.shape
     ws_bytes = workspace.numel() * workspace.element_size()
-    rc = load().minite_quantize_tokens_nvfp4(_p(x), x_rows, _p(row_src), m_cap, C, E,
+    rc = load().minite_quantize_tokens_nvfp4(_p(x), x_rows, _p(row_src), _p(row_amax), m_cap, C, E,
                                              _p(expert_offsets), k_cap, _p(codes), _p(sf), _p(g),
                                              _p(kofs), _p(workspace), ws_bytes, _p(status),
                                              _s(stream))
@@ -292,10 +293,11 @@ def minite_grouped_gemm_wgrad_nvfp4(a, b, out, status=None, stream=None):
     _check(rc, "minite_grouped_gemm_wgrad_nvfp4")
 
 
-def quantize_tokens(x, expert_offsets, E, row_src=None, m_cap=None, stream=None):
+def quantize_tokens(x, expert_offsets, E, row_src=None, m_cap=None, stream=None, row_amax=None):
     """Weight-gradient operand of x's permuted rows (x[row_src[m]] or x[m]):
     dict(codes [C, k_cap/2], sf, g [E], kofs [E+1], k_cap) with
-    k_cap = m_cap + 256 E rounded up to 256."""
+    k_cap = m_cap + 256 E rounded up to 256. ``row_amax`` [x_rows]: each row's
+    |x| maximum when the producer wrote it (x is then read once)."""
     dev = x.device
     x_rows, C = x.shape
     m_cap = (row_src.numel() if row_src is not None else x_rows) if m_cap is None else m_cap
@@ -304,11 +306,12 @@ def quantize_tokens(x, expert_offsets, E, row_src=None, m_cap=None, stream=None)
                sf=torch.empty(((C + 127) // 128 * 128) * (k_cap // 16), dtype=torch.uint8, device=dev),
                g=torch.empty(E, dtype=torch.float32, device=dev),
                kofs=torch.empty(E + 1, dtype=torch.int32, device=dev), k_cap=k_cap)
-    ws = torch.empty(max(4, minite_workspace_bytes(OP_QUANTIZE_TOKENS, E,
-                                                   x_rows if row_src is not None else 0)),
+    gathered = row_src is not None and row_amax is None
+    ws = torch.empty(max(4, minite_workspace_bytes(OP_QUANTIZE_TOKENS, E, x_rows if gathered else 0)),
                      dtype=torch.uint8, device=dev)
     minite_quantize_tokens_nvfp4(x, row_src, m_cap, E, expert_offsets, k_cap, out["codes"],
-                                 out["sf"], out["g"], out["kofs"], ws, stream=stream)
+                                 out["sf"], out["g"], out["kofs"], ws, stream=stream,
+                                 row_amax=row_amax)
     return out
 
 

@@ -116,20 +116,29 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert cb(16, 96, 2, 2, fake, 1 << 20) == 2
     assert cb(16, 128, 2, 2, None, 1 << 20) == 1
     assert cb(16, 128, 2, 2, fake, 8) == 1
-    # token-axis quantizer: C not a multiple of 16, k_cap not a multiple of 256, misaligned codes
-    qt = lambda C, kcap, codes: lib.minite_quantize_tokens_nvfp4(  # noqa: E731
-        fake, 64, None, 64, C, 2, fake, kcap, codes, fake, fake, fake, fake, 1024, None, None)
+    # token-axis quantizer: C not a multiple of 16, k_cap not a multiple of 256, misaligned
+    # codes, misaligned row maxima
+    qt = lambda C, kcap, codes, ra=None: lib.minite_quantize_tokens_nvfp4(  # noqa: E731
+        fake, 64, None, ra, 64, C, 2, fake, kcap, codes, fake, fake, fake, fake, 1024, None, None)
     assert qt(40, 1024, fake) == 2
     assert qt(64, 1000, fake) == 2
     assert qt(64, 1024, vp(4112)) == 1
+    assert qt(64, 1024, fake, vp(4098)) == 1
     # weight-gradient GEMM: N not a multiple of 32, bad out dtype
     wg = lambda N, dt: lib.minite_grouped_gemm_wgrad_nvfp4(  # noqa: E731
         fake, fake, fake, fake, fake, fake, fake, 2, 128, N, 1024, fake, dt, None, None)
     assert wg(100, 0) == 2
     assert wg(128, 7) == 1
-    # SwiGLU keeping h: h_out missing
+    # SwiGLU keeping h: h_out missing; misaligned row maxima
     assert lib.minite_swiglu_weighted_quant_keep_h(fake, None, 16, 128, 1, fake, fake, fake, fake,
-                                                   fake, None, None, None) == 1
+                                                   fake, None, None, None, None) == 1
+    assert lib.minite_swiglu_weighted_quant_keep_h(fake, None, 16, 128, 1, fake, fake, fake, fake,
+                                                   fake, fake, vp(4098), None, None) == 1
+    # SwiGLU backward keeping [dg | du]: dgu_out missing; misaligned row maxima
+    assert lib.minite_swiglu_backward_quant_keep(fake, fake, None, 16, 128, 1, fake, fake, fake,
+                                                 fake, fake, None, None, None, None) == 1
+    assert lib.minite_swiglu_backward_quant_keep(fake, fake, None, 16, 128, 1, fake, fake, fake,
+                                                 fake, fake, fake, vp(4098), None, None) == 1
     # combine: N not a multiple of 8, k too large
     assert lib.minite_moe_combine(fake, fake, 4, 8, 12, 2, fake, None, None) == 2
     assert lib.minite_moe_combine(fake, fake, 4, 8, 16, 64, fake, None, None) == 2

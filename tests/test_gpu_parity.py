@@ -748,7 +748,11 @@ def check_token_operand(q, ref, C):
 @pytest.mark.parametrize("counts,C,gather", [([3, 0, 260, 17], 48, True), ([1], 16, False),
                                               ([700, 5, 0, 0, 129], 256, True),
                                               ([64, 64], 2048, False), ([300, 1000], 768, True)])
-def test_quantize_tokens_bit_exact(counts, C, gather):
+@pytest.mark.parametrize("given_amax", [False, True])
+def test_quantize_tokens_bit_exact(counts, C, gather, given_amax):
+    """Token-axis operand against the oracle, the experts' maxima taken from
+    the rows themselves or from caller-given per-row maxima (as the SwiGLU
+    entries that keep BF16 output write them)."""
     rng = np.random.default_rng(sum(counts) + C)
     E = len(counts)
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
@@ -758,12 +762,16 @@ def test_quantize_tokens_bit_exact(counts, C, gather):
         x = _rand_bf16(rng, (T, C))
         src = rng.integers(0, T, Mu + 5).astype(np.int32)
         rows = O.bf16_to_f32(x)[src[:Mu]]
-        q = M.quantize_tokens(bf16_dev(x), np_dev(off), E, row_src=np_dev(src))
+        xd = bf16_dev(x)
+        ra = xd.float().abs().amax(dim=1) if given_amax else None
+        q = M.quantize_tokens(xd, np_dev(off), E, row_src=np_dev(src), row_amax=ra)
     else:
         x = _rand_bf16(rng, (Mu + 7, C))
         x[:, 3] = 0  # a zero channel
         rows = O.bf16_to_f32(x)[:Mu]
-        q = M.quantize_tokens(bf16_dev(x), np_dev(off), E)
+        xd = bf16_dev(x)
+        ra = xd.float().abs().amax(dim=1) if given_amax else None
+        q = M.quantize_tokens(xd, np_dev(off), E, row_amax=ra)
     torch.cuda.synchronize()
     check_token_operand(q, O.quantize_tokens_per_expert(rows, off), C)
 
@@ -831,8 +839,9 @@ def test_weight_gradients_stagewise(T, H, I, E, k):
     M.minite_grouped_gemm_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"], wgu["sf"], wgu["g"],
                                 mlp.offsets, mlp.sf_offsets, mlp.gate_up, st)
     h = torch.zeros((Mt, I), dtype=torch.bfloat16, device=dev)
+    h_amax = torch.full((Mt,), float("nan"), dtype=torch.float32, device=dev)
     M.minite_swiglu_weighted_quant_keep_h(mlp.gate_up, mlp.perm_w, E, mlp.offsets, mlp.sf_offsets,
-                                          mlp.h_codes, mlp.h_sf, mlp.h_g, h, st)
+                                          mlp.h_codes, mlp.h_sf, mlp.h_g, h, st, h_amax=h_amax)
     bwd = M.MoEMLP(T, H, I, E, k)
     ws = torch.empty(M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, T, H), dtype=torch.uint8,
                      device=dev)
@@ -845,11 +854,13 @@ def test_weight_gradients_stagewise(T, H, I, E, k):
     dgu_sf = torch.empty((M.sf_bytes(Mt + 128 * E, 2 * I),), dtype=torch.uint8, device=dev)
     dgu_g = torch.empty(Mt, dtype=torch.float32, device=dev)
     dgu = torch.zeros((Mt, 2 * I), dtype=torch.bfloat16, device=dev)
+    dgu_amax = torch.full((Mt,), float("nan"), dtype=torch.float32, device=dev)
     M.minite_swiglu_backward_quant_keep(mlp.gate_up, dh, mlp.perm_w, E, mlp.offsets,
-                                        mlp.sf_offsets, dgu_codes, dgu_sf, dgu_g, dgu, st)
+                                        mlp.sf_offsets, dgu_codes, dgu_sf, dgu_g, dgu, st,
+                                        dgu_amax=dgu_amax)
     q_dy = M.quantize_tokens(dy, mlp.offsets, E, row_src=mlp.perm_src, m_cap=Mt)
-    q_h = M.quantize_tokens(h, mlp.offsets, E, m_cap=Mt)
-    q_dgu = M.quantize_tokens(dgu, mlp.offsets, E, m_cap=Mt)
+    q_h = M.quantize_tokens(h, mlp.offsets, E, m_cap=Mt, row_amax=h_amax)
+    q_dgu = M.quantize_tokens(dgu, mlp.offsets, E, m_cap=Mt, row_amax=dgu_amax)
     q_x = M.quantize_tokens(x, mlp.offsets, E, row_src=mlp.perm_src, m_cap=Mt)
     dWd = torch.full((E, H, I), float("nan"), dtype=torch.float32, device=dev)
     dWgu = torch.full((E, 2 * I, H), float("nan"), dtype=torch.float32, device=dev)
@@ -866,6 +877,11 @@ def test_weight_gradients_stagewise(T, H, I, E, k):
     assert np.array_equal(u16(h)[:Mu], O.f32_to_bf16(O.swiglu_weighted(O.bf16_to_f32(u16(mlp.gate_up)[:Mu]), perm_w)))
     assert np.array_equal(u16(dgu)[:Mu], O.f32_to_bf16(O.swiglu_backward(
         O.bf16_to_f32(u16(mlp.gate_up)[:Mu]), O.bf16_to_f32(u16(dh)[:Mu]), perm_w)))
+    # the row maxima written beside them: max |row| of the kept BF16 rows, rows past Mu untouched
+    for amax, kept in ((h_amax, h), (dgu_amax, dgu)):
+        a = amax.cpu().numpy()
+        assert np.array_equal(a[:Mu], np.abs(O.bf16_to_f32(u16(kept)[:Mu])).max(axis=1))
+        assert np.isnan(a[Mu:]).all()
     r_dy = O.quantize_tokens_per_expert(O.bf16_to_f32(d["dy"])[src], off)
     r_h = O.quantize_tokens_per_expert(O.bf16_to_f32(u16(h)[:Mu]), off)
     r_dgu = O.quantize_tokens_per_expert(O.bf16_to_f32(u16(dgu)[:Mu]), off)
@@ -896,7 +912,7 @@ def test_wgrad_gemm_rejects_bad_token_offsets():
 
 
 @pytest.mark.parametrize("I", [64, 768, 2048])
-def test_swiglu_keep_h_stores_rounded_h_and_the_same_codes(I):
+def test_swiglu_keep_h_stores_rounded_h_its_row_maxima_and_the_same_codes(I):
     rng = np.random.default_rng(I)
     counts = [5, 130, 0, 40]
     E = len(counts)
@@ -912,21 +928,26 @@ def test_swiglu_keep_h_stores_rounded_h_and_the_same_codes(I):
         sf = torch.zeros(((Mt + 128 * E) * (I // 16),), dtype=torch.uint8, device="cuda")
         g = torch.zeros(Mt, dtype=torch.float32, device="cuda")
         h = torch.zeros((Mt, I), dtype=torch.bfloat16, device="cuda")
+        h_amax = torch.full((Mt,), float("nan"), dtype=torch.float32, device="cuda")
         st = _status()
         if keep:
             M.minite_swiglu_weighted_quant_keep_h(bf16_dev(gu), np_dev(pw), E, np_dev(off),
-                                                  np_dev(sfo), codes, sf, g, h, st)
+                                                  np_dev(sfo), codes, sf, g, h, st, h_amax=h_amax)
         else:
             M.minite_swiglu_weighted_quant(bf16_dev(gu), np_dev(pw), E, np_dev(off), np_dev(sfo),
                                            codes, sf, g, st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        res.append((codes, sf, g, h))
+        res.append((codes, sf, g, h, h_amax))
     for a, b in zip(res[0][:3], res[1][:3]):
         assert torch.equal(a, b)
     ref = O.f32_to_bf16(O.swiglu_weighted(O.bf16_to_f32(gu[:Mu]), pw[:Mu]))
     assert np.array_equal(u16(res[1][3])[:Mu], ref)
     assert (u16(res[1][3])[Mu:] == 0).all()
+    # each kept row's |h| maximum; rows past the routed ones untouched
+    amax = res[1][4].cpu().numpy()
+    assert np.array_equal(amax[:Mu], np.abs(O.bf16_to_f32(ref)).max(axis=1))
+    assert np.isnan(amax[Mu:]).all()
 
 
 # --------------------------------------------------------------------- failure detection
