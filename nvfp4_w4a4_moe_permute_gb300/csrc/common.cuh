@@ -150,6 +150,14 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&v)[8]) {
   v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
 }
 
+// a / b for a >= 0, b > 0: the 32-bit division when both fit in 32 bits (the
+// usual case; a 64-bit division is a long instruction sequence).
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
+  if (((a | b) >> 32) == 0)
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(256) quantize_token_rows_kernel(
   const int64_t sf_group_bytes = rows_pad * kc;
   const int64_t total = groups * rows;
   for (int64_t row = warp; row < total; row += nwarps) {
-    const int64_t grp = row / rows;
+    const int64_t grp = div_nonneg(row, rows);
     const int64_t r = row - grp * rows;
     uint32_t w[NCH][8];
     float am[NCH];
@@ -433,35 +433,49 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
   const DualGeom G = dual_geom(rows, cols, codes_k, codes_n);
   const int64_t per_group = static_cast<int64_t>(G.tr) * G.tc;
   const int64_t ntiles = groups * per_group;
-  auto fetch = [&](int64_t ti, uint16_t* buf) {
+  // tile ti -> (group, first row, first column), decoded once per tile and
+  // carried from its copies to its quantization
+  struct TilePos {
+    int64_t grp;
+    int r0, c0;
+  };
+  auto pos = [&](int64_t ti) {
+    TilePos p{-1, 0, 0};
     if (ti < ntiles) {
-      const int64_t grp = ti / per_group;
-      const int rem = static_cast<int>(ti - grp * per_group);
-      dual_fetch(x + grp * static_cast<int64_t>(rows) * cols, G, (rem / G.tc) * kDR,
-                 (rem % G.tc) * kDC, buf, x);
+      p.grp = div_nonneg(ti, per_group);
+      const int rem = static_cast<int>(ti - p.grp * per_group);
+      const int tr = rem / G.tc;
+      p.r0 = tr * kDR;
+      p.c0 = (rem - tr * G.tc) * kDC;
     }
+    return p;
+  };
+  auto fetch = [&](const TilePos& p, uint16_t* buf) {
+    if (p.grp >= 0)
+      dual_fetch(x + p.grp * static_cast<int64_t>(rows) * cols, G, p.r0, p.c0, buf, x);
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
 
   int64_t ti = blockIdx.x;
-  fetch(ti, tiles[0]);
+  TilePos p0 = pos(ti), p1 = pos(ti + gridDim.x);
+  fetch(p0, tiles[0]);
   int cur = 0;
   int64_t gcur = -1;
   float g = 1.0f, tk = 1.0f;
   for (; ti < ntiles; ti += gridDim.x, cur ^= 1) {
-    fetch(ti + gridDim.x, tiles[cur ^ 1]);
+    fetch(p1, tiles[cur ^ 1]);
+    const TilePos p2 = pos(ti + 2 * static_cast<int64_t>(gridDim.x));
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncthreads();
-    const int64_t grp = ti / per_group;
-    const int rem = static_cast<int>(ti - grp * per_group);
-    if (grp != gcur) {  // block-uniform
-      gcur = grp;
-      g = global_scale(__uint_as_float(amax_bits[grp]));
+    if (p0.grp != gcur) {  // block-uniform
+      gcur = p0.grp;
+      g = global_scale(__uint_as_float(amax_bits[p0.grp]));
       tk = enc_table_entry(g);
     }
-    dual_tile_quant(tiles[cur], G, grp, (rem / G.tc) * kDR, (rem % G.tc) * kDC, g, tk, codes_k,
-                    sf_k, codes_n, sf_n);
-    __syncthreads();  // the buffer is refilled two tiles from now
+    dual_tile_quant(tiles[cur], G, p0.grp, p0.r0, p0.c0, g, tk, codes_k, sf_k, codes_n, sf_n);
+    __syncthreads();  // the next iteration refills this buffer
+    p0 = p1;
+    p1 = p2;
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kTokThreads) tokens_quant_kernel(
       }
       const int64_t rem = u - s_upre[lo];
       d.e = lo;
-      d.tt = static_cast<int>(rem / nct);
+      d.tt = static_cast<int>(div_nonneg(rem, nct));
       d.ct = static_cast<int>(rem - static_cast<int64_t>(d.tt) * nct);
     }
     return d;

@@ -487,13 +487,13 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
   const int64_t units = T * upt;
   int64_t u = warp;
   int nxt = -1;
-  if (u < units && lane < k) nxt = dest_row[(u / upt) * k + lane];
+  if (u < units && lane < k) nxt = dest_row[div_nonneg(u, upt) * k + lane];
   for (; u < units; u += nwarps) {
-    const int64_t t = u / upt;
+    const int64_t t = div_nonneg(u, upt);
     const int ch = static_cast<int>(u - t * upt);
     int my = nxt;
     const int64_t un = u + nwarps;
-    if (un < units && lane < k) nxt = dest_row[(un / upt) * k + lane];
+    if (un < units && lane < k) nxt = dest_row[div_nonneg(un, upt) * k + lane];
     if (my >= M) {
       set_status(status, MINITE_ERR_BAD_ROUTING);
       my = -1;
