@@ -345,6 +345,16 @@ class Step:
         return dict(gemm_gate_up=2.0 * Mu * 2 * I * H, gemm_down=2.0 * Mu * H * I,
                     gemm_dgrad=2.0 * Mu * I * H, used_rows=Mu)
 
+    def gemm_gate_up_bytes(self):
+        """Bytes the gate_up GEMM must move at minimum: A codes and scales (rows
+        padded to 128 per expert), every expert's W codes and scales once, the
+        BF16 output."""
+        Mu = int(self.mlp.offsets[-1].item())
+        Mp = int(self.mlp.sf_offsets[-1].item())
+        H, I, E = self.H, self.I, self.E
+        return (Mu * H / 2 + Mp * H / 16 + E * 2 * I * H / 2 + E * 2 * I * H / 16 +
+                Mu * 2 * I * 2)
+
     def backward_algorithmic_bytes(self):
         """Bytes each backward stage must move at minimum (read once + write once)."""
         T, H, E, k, I = self.T, self.H, self.E, self.k, self.I
@@ -554,6 +564,10 @@ def run_gpu(args):
     fp4_peak = peaks["bf16_sus"] * FP4_OVER_BF16
     gemm_s = stage_ms["gemm_gate_up"] / 1e3
     achieved = fl["gemm_gate_up"] / gemm_s / 1e12
+    # the same launch against min(FP4 peak, arithmetic intensity x HBM bandwidth)
+    gemm_bytes = step.gemm_gate_up_bytes()
+    ai = fl["gemm_gate_up"] / gemm_bytes
+    attainable = min(fp4_peak, ai * peaks["hbm"] / 1e3)
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
@@ -592,7 +606,10 @@ def run_gpu(args):
         "roofline": {"kernel": "grouped_gemm_dc_kernel (gate_up)", "bound": "tensor",
                      "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp4_peak, "traffic": traffic,
-                     "peak_source": f"{peaks['source']} bf16 sustained x {FP4_OVER_BF16:g} (nominal FP4/BF16)"},
+                     "peak_source": f"{peaks['source']} bf16 sustained x {FP4_OVER_BF16:g} (nominal FP4/BF16)",
+                     "algorithmic_bytes": gemm_bytes, "flop_per_byte": ai,
+                     "attainable": attainable, "frac_of_attainable": achieved / attainable,
+                     "achieved_hbm_gbs": gemm_bytes / gemm_s / 1e9},
         "clocks": clk,
         "gpu_launches": Step.LAUNCHES * args.steps,
         "backward": backward,
