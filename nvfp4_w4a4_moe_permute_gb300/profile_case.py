@@ -8,6 +8,7 @@ command line, without the memory of a whole layer step.
         --rows 131072 --cols 2048 --experts 128 --gather 16384
     python -m nvfp4_w4a4_moe_permute_gb300.profile_case quantize_weights \\
         --experts 16 --rows 1536 --cols 2048 [--dual]
+    python -m nvfp4_w4a4_moe_permute_gb300.profile_case permute_swiglu --tokens 16384
 
 Expert sizes follow a Zipf(1.5) draw over the experts (a skewed routing);
 every call's device status is checked at the end.
@@ -74,7 +75,37 @@ def quantize_weights(args, M, dev, status):
                                     status)
 
 
-CASES = {"quantize_tokens": quantize_tokens, "quantize_weights": quantize_weights}
+def permute_swiglu(args, M, dev, status):
+    """The permutation with fused quantization of x and the weighted SwiGLU
+    with requantization, on the skewed layer's recipe at `--tokens` tokens
+    (the SwiGLU's input is seeded N(0, 2) BF16 in place of the gate_up GEMM's
+    output)."""
+    from . import inputs as IN
+    d = IN.make_moe_inputs("skewed", seed=args.seed, T=args.tokens, with_weights=False)
+    c = d["cfg"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x = bf16(d["x"])
+    ids = torch.from_numpy(d["topk_ids"]).to(dev)
+    w = torch.from_numpy(d["topk_w"]).to(dev)
+    mlp = M.MoEMLP(T, H, I, E, k)
+    gen = torch.Generator(device=dev).manual_seed(args.seed)
+    mlp.gate_up.copy_((torch.randn(mlp.gate_up.shape, device=dev, generator=gen) * 2.0)
+                      .to(torch.bfloat16))
+    for _ in range(args.reps):
+        mlp.permute_quant(x, ids, w)
+        M.minite_swiglu_weighted_quant(mlp.gate_up, mlp.perm_w, E, mlp.offsets, mlp.sf_offsets,
+                                       mlp.h_codes, mlp.h_sf, mlp.h_g, status)
+    torch.cuda.synchronize(dev)
+    if int(mlp.status.item()) != 0:
+        status.fill_(int(mlp.status.item()))
+
+
+CASES = {"quantize_tokens": quantize_tokens, "quantize_weights": quantize_weights,
+         "permute_swiglu": permute_swiglu}
 
 
 def main(argv=None) -> int:
@@ -83,6 +114,7 @@ def main(argv=None) -> int:
     ap.add_argument("--rows", type=int, default=131072)
     ap.add_argument("--cols", type=int, default=1536)
     ap.add_argument("--experts", type=int, default=128)
+    ap.add_argument("--tokens", type=int, default=16384, help="permute_swiglu: tokens")
     ap.add_argument("--gather", type=int, default=0, help="source rows (0: rows in place)")
     ap.add_argument("--dual", action="store_true", help="weights: both orientations")
     ap.add_argument("--reps", type=int, default=3)
