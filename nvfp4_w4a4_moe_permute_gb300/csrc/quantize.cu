@@ -168,7 +168,11 @@ __global__ void __launch_bounds__(256) quantize_token_rows_kernel(
   const int64_t rows_pad = (rows + 127) & ~int64_t(127);
   const int64_t sf_group_bytes = rows_pad * kc;
   const int64_t total = groups * rows;
-  for (int64_t row = warp; row < total; row += nwarps) {
+  for (int64_t i = warp; i < total; i += nwarps) {
+    // per-group scales follow the group-maxima pass, which reads the groups in
+    // order: taking the rows last to first starts where that pass ended, on
+    // bytes still in L2
+    const int64_t row = PG ? total - 1 - i : i;
     const int64_t grp = div_nonneg(row, rows);
     const int64_t r = row - grp * rows;
     uint32_t w[NCH][8];
@@ -442,8 +446,11 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
   auto pos = [&](int64_t ti) {
     TilePos p{-1, 0, 0};
     if (ti < ntiles) {
-      p.grp = div_nonneg(ti, per_group);
-      const int rem = static_cast<int>(ti - p.grp * per_group);
+      // last tile first: the group-maxima pass just read the groups in order,
+      // so the end of the weight is the part still in L2
+      const int64_t tr_ = ntiles - 1 - ti;
+      p.grp = div_nonneg(tr_, per_group);
+      const int rem = static_cast<int>(tr_ - p.grp * per_group);
       const int tr = rem / G.tc;
       p.r0 = tr * kDR;
       p.c0 = (rem - tr * G.tc) * kDC;
