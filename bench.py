@@ -250,15 +250,16 @@ class Step:
         mark(9)
 
     # The rest of the NVFP4 backward of the expert MLP, timed beside the step:
-    # W_gate_up in both orientations (one pass), SwiGLU backward with its
-    # per-row requantization, the gate_up dgrad GEMM (K = 2I, N = H) and the
-    # combine of dX back into token order.
-    BWD_STAGES = ["wq_gate_up_dual", "swiglu_keep_h", "swiglu_bwd_keep", "gemm_dgrad_gate_up",
+    # W_gate_up's dgrad copy (blocks along N, with the global scales the
+    # forward step computed), SwiGLU backward with its per-row requantization,
+    # the gate_up dgrad GEMM (K = 2I, N = H), the combine of dX back into token
+    # order, the token-axis operands and the two weight-gradient GEMMs.
+    BWD_STAGES = ["wq_gate_up_T", "swiglu_keep_h", "swiglu_bwd_keep", "gemm_dgrad_gate_up",
                   "combine_dx", "quant_tokens", "gemm_wgrad_down", "gemm_wgrad_gate_up"]
-    # dual 2, SwiGLU 1, SwiGLU backward 1, GEMM 1, combine 1, token-axis operands (gathered dY
+    # W_gate_up along N 1 (no maxima pass), SwiGLU 1, SwiGLU backward 1, GEMM 1, combine 1, token-axis operands (gathered dY
     # and x: source-row maxima, expert maxima, encoding; h and [dg | du] with their producers'
     # row maxima: expert maxima, encoding) 3 + 2 + 2 + 3, 2 GEMMs
-    BWD_LAUNCHES = 2 + 1 + 1 + 1 + 1 + 10 + 2
+    BWD_LAUNCHES = 1 + 1 + 1 + 1 + 1 + 10 + 2
 
     def init_backward(self):
         import torch
@@ -301,9 +302,9 @@ class Step:
                 events[i].record(s)
 
         mark(0)
-        M.minite_quantize_nvfp4_dual(self.wgu_bf, self.wgu["codes"], self.wgu["sf"],
-                                     self.wguT["codes"], self.wguT["sf"], self.wgu["g"], self.ws_q,
-                                     self.status, s)
+        # the dgrad copy of W_gate_up, with the forward step's per-expert g
+        M.minite_quantize_nvfp4(self.wgu_bf, M.SCALE_PER_GROUP, M.ALONG_ROWS, self.wguT["codes"],
+                                self.wguT["sf"], self.wgu["g"], self.wgu["g"], None, self.status, s)
         mark(1)
         # the forward's SwiGLU keeping BF16 h for the down projection's weight gradient
         M.minite_swiglu_weighted_quant_keep_h(mlp.gate_up, mlp.perm_w, self.E, mlp.offsets,
@@ -361,7 +362,7 @@ class Step:
         Mu = int(self.mlp.offsets[-1].item())
         sfb = lambda r, c: r * c / 16  # noqa: E731
         return dict(
-            wq_gate_up_dual=E * 2 * I * H * 2 + 2 * (E * 2 * I * H / 2 + sfb(E * 2 * I, H)),
+            wq_gate_up_T=E * 2 * I * H * 2 + E * 2 * I * H / 2 + sfb(E * 2 * I, H),
             # + the kept BF16 rows and their row maxima
             swiglu_keep_h=Mu * 2 * I * 2 + Mu * (I / 2 + I / 16 + 4) + Mu * (I * 2 + 4),
             swiglu_bwd_keep=Mu * (2 * I * 2 + I * 2 + 4) + Mu * (I + 2 * I / 16 + 4) +
@@ -482,7 +483,7 @@ def run_gpu(args):
         Mu = int(step.mlp.offsets[-1].item())
         dg_fl = 2.0 * Mu * 2 * step.I * step.H
         backward = {
-            "stages": "W_gate_up quantization in both orientations (one pass) + forward SwiGLU"
+            "stages": "W_gate_up dgrad copy (along N, the forward's global scales) + forward SwiGLU"
                       " keeping BF16 h + SwiGLU backward with per-row requant keeping BF16 dGU"
                       " + gate_up dgrad GEMM (K=2I, N=H) + combine of dX + token-axis NVFP4"
                       " operands (dY, h, dGU, x) + weight-gradient GEMMs of both projections",

@@ -101,7 +101,7 @@ enum {
  * workspace:   device, >= minite_workspace_bytes(MINITE_OP_QUANTIZE, groups,
  *              0, 0, 0) bytes (PER_GROUP without gscale_in only; else NULL ok).
  * Shape rules: Cq % 16 == 0 (blocks), cols % 8 == 0, all > 0; ALONG_COLS:
- * cols <= 4096; ALONG_ROWS: PER_GROUP only; PER_GROUP: rows * cols / 16 <
+ * cols <= 4096; ALONG_ROWS: PER_GROUP only, rows, cols < 2^30; PER_GROUP: rows * cols / 16 <
  * 2^32; groups * rows * cols < 2^40. Misaligned pointers: INVALID_ARG;
  * other shapes: UNSUPPORTED_SHAPE (nothing enqueued in either case).
  */

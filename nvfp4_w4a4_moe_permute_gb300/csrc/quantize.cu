@@ -13,8 +13,11 @@
 //   quantize_rows_kernel   one warp per row, blocks of 16 along the row, the
 //                          row held in registers (coalesced 16-byte loads).
 //   quantize_cols_kernel   blocks of 16 along the rows of a group (the
-//                          transposed, dgrad-layout copy of a weight): a
-//                          64 x 128 tile is staged through shared memory.
+//                          transposed, dgrad-layout copy of a weight): 128 x
+//                          128 tiles staged through shared memory with
+//                          per-thread asynchronous copies (two buffers).
+#include <mutex>
+
 #include "common.cuh"
 #include "host_util.h"
 
@@ -193,84 +196,6 @@ __global__ void __launch_bounds__(256) quantize_token_rows_kernel(
     for (int a = lane; a < kc / 4; a += 32)
       *reinterpret_cast<uint32_t*>(sf + gp * sf_group_bytes + sf_offset(r, 4 * a, kc)) = 0u;
   }
-}
-
-// Transposed quantization of group matrices [rows, cols]: quantized row q is
-// column q of the group, blocks of 16 run along the original rows.
-// Tile: 64 original rows x 128 original columns; thread t handles quantized
-// row q = tile_c0 + t/2 and the 32 original rows tile_r0 + 32*(t%2) + [0,32).
-constexpr int kTR = 64, kTC = 128;
-__global__ void __launch_bounds__(256) quantize_cols_kernel(
-    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, const float* __restrict__ g_in,
-    const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-    float* __restrict__ g_out) {
-  __shared__ uint16_t tile[kTR][kTC + 1];
-  const int64_t grp = blockIdx.z;
-  const int64_t r0 = (int64_t)blockIdx.x * kTR;
-  const int64_t c0 = (int64_t)blockIdx.y * kTC;
-  const uint16_t* xg = x + grp * rows * cols;
-  const int t = threadIdx.x;
-
-  // load: 16 threads per row segment of 128 columns, 16 rows per pass
-#pragma unroll
-  for (int pass = 0; pass < kTR / 16; ++pass) {
-    const int lr = pass * 16 + t / 16;
-    const int lc = (t % 16) * 8;
-    const int64_t gr = r0 + lr, gc = c0 + lc;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (gr < rows && gc < cols) u = __ldcs(reinterpret_cast<const uint4*>(xg + gr * cols + gc));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      tile[lr][lc + 2 * i] = static_cast<uint16_t>(w[i] & 0xFFFF);
-      tile[lr][lc + 2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
-    }
-  }
-  __syncthreads();
-
-  const float g = g_in ? g_in[grp] : global_scale(__uint_as_float(amax_bits[grp]));
-  const float tk = enc_table_entry(g);
-  const int lq = t / 2, half = t % 2;
-  const int64_t q = c0 + lq;               // quantized row
-  const int64_t e0 = r0 + 32 * half;       // first quantized column of this thread
-  const int kc = static_cast<int>(((rows / 16) + 3) & ~int64_t(3));
-  const int64_t rows_pad_q = (cols + 127) & ~int64_t(127);
-  uint32_t packed[4];
-  uint32_t sfpair = 0;
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    float v[16];
-    float am = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      v[i] = __uint_as_float(static_cast<uint32_t>(tile[32 * half + 16 * b + i][lq]) << 16);
-      am = fmaxf(am, fabsf(v[i]));
-    }
-    const bool valid = (e0 + 16 * b) < rows;
-    BlockScale bs = block_scale(am, g, tk);
-    const uint32_t s = valid ? bs.sf : 0u;
-    const bool zero = !valid || s == 0;
-    float lo[8], hi[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { lo[i] = v[i]; hi[i] = v[8 + i]; }
-    packed[2 * b] = encode8(lo, bs.enc, zero);
-    packed[2 * b + 1] = encode8(hi, bs.enc, zero);
-    sfpair |= s << (8 * b);
-  }
-  const uint32_t other = __shfl_down_sync(0xffffffffu, sfpair, 1);
-  const size_t sf_group_bytes = static_cast<size_t>(rows_pad_q) * kc;
-  if (q < cols) {
-    uint8_t* crow = codes + (grp * cols + q) * (rows / 2);
-    if (e0 < rows) *reinterpret_cast<uint2*>(crow + e0 / 2) = make_uint2(packed[0], packed[1]);
-    if (e0 + 16 < rows)
-      *reinterpret_cast<uint2*>(crow + e0 / 2 + 8) = make_uint2(packed[2], packed[3]);
-  }
-  const int64_t col = r0 / 16;  // SF column of this tile's first block (multiple of 4)
-  if (half == 0 && q < rows_pad_q && col < kc) {
-    const uint32_t word = (q < cols) ? (sfpair | (other << 16)) : 0u;
-    *reinterpret_cast<uint32_t*>(sf + grp * sf_group_bytes + sf_offset(q, col, kc)) = word;
-  }
-  if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) g_out[grp] = g;
 }
 
 // Both orientations of per-group quantization from one read of each weight:
@@ -492,6 +417,134 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
   if (gt < groups) g_out[gt] = global_scale(__uint_as_float(amax_bits[gt]));
 }
 
+// Transposed quantization of group matrices [rows, cols] (the dgrad copy of a
+// weight): quantized row q is column q of the group, blocks of 16 along the
+// original rows, one global scale per group (g_in, else from amax_bits).
+// 128 x 128 tiles are staged in shared memory (two buffers, the next tile's
+// per-thread asynchronous copies in flight while the current one is
+// quantized); thread t takes column t % 128 of the tile and its rows
+// 64 (t / 128) .. + 64: four blocks, 32 contiguous code bytes and one 4-byte
+// scale word. After a group-maxima pass the tiles are taken last to first,
+// starting on the bytes that pass left in L2.
+constexpr int kCR = 128, kCC = 128, kCPitch = kCC + 8;  // pitch in BF16, rows 16-byte aligned
+constexpr int kCTile = kCR * kCPitch;
+constexpr size_t kColsSmem = 2 * kCTile * sizeof(uint16_t);
+
+__global__ void __launch_bounds__(256) quantize_cols_kernel(
+    const uint16_t* __restrict__ x, int64_t groups, int rows, int cols,
+    const float* __restrict__ g_in, const uint32_t* __restrict__ amax_bits,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out) {
+  extern __shared__ __align__(16) uint16_t ctiles[];  // [2][kCTile]
+  pdl_wait();
+  const int t = threadIdx.x;
+  const int tr = (rows + kCR - 1) / kCR, tc = (cols + kCC - 1) / kCC;
+  const int nbn = rows / 16;                 // blocks per quantized row
+  const int kcn = (nbn + 3) & ~3;            // SF columns
+  const int64_t sf_group = static_cast<int64_t>((cols + 127) & ~127) * kcn;
+  const bool v8 = (rows / 2) % 32 == 0 && (reinterpret_cast<uintptr_t>(codes) & 31) == 0;
+  const int64_t per_group = static_cast<int64_t>(tr) * tc;
+  const int64_t ntiles = groups * per_group;
+  struct TilePos {
+    int64_t grp;
+    int r0, c0;
+  };
+  auto pos = [&](int64_t ti) {
+    TilePos p{-1, 0, 0};
+    if (ti < ntiles) {
+      const int64_t k = g_in ? ti : ntiles - 1 - ti;
+      p.grp = div_nonneg(k, per_group);
+      const int rem = static_cast<int>(k - p.grp * per_group);
+      const int a = rem / tc;
+      p.r0 = a * kCR;
+      p.c0 = (rem - a * tc) * kCC;
+    }
+    return p;
+  };
+  auto fetch = [&](const TilePos& p, uint16_t* buf) {
+    if (p.grp >= 0) {
+      const uint16_t* xg = x + p.grp * static_cast<int64_t>(rows) * cols;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = t + 256 * i;  // 16-byte piece q: row q / 16, piece q % 16
+        const int lr = q >> 4, seg = q & 15;
+        const bool valid = p.r0 + lr < rows && p.c0 + 8 * seg < cols;
+        const uint16_t* src =
+            valid ? xg + static_cast<int64_t>(p.r0 + lr) * cols + p.c0 + 8 * seg : x;
+        cp_async16_zfill(buf + lr * kCPitch + 8 * seg, src, valid);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+  int64_t ti = blockIdx.x;
+  TilePos p0 = pos(ti), p1 = pos(ti + gridDim.x);
+  fetch(p0, ctiles);
+  int cur = 0;
+  int64_t gcur = -1;
+  float g = 1.0f, tk = 1.0f;
+  const int lc = t & (kCC - 1), rb0 = 4 * (t >> 7);  // this thread's column, first row block
+  for (; ti < ntiles; ti += gridDim.x, cur ^= 1) {
+    fetch(p1, ctiles + (cur ^ 1) * kCTile);
+    const TilePos p2 = pos(ti + 2 * static_cast<int64_t>(gridDim.x));
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+    if (p0.grp != gcur) {  // block-uniform
+      gcur = p0.grp;
+      g = g_in ? g_in[gcur] : global_scale(__uint_as_float(amax_bits[gcur]));
+      tk = enc_table_entry(g);
+    }
+    const uint16_t* tile = ctiles + cur * kCTile;
+    const int c = p0.c0 + lc;
+    const int gr = p0.r0 / 16 + rb0;  // first block (SF column) of this thread, a multiple of 4
+    uint2 code[4];
+    uint32_t sfw = 0;
+#pragma unroll
+    for (int rb = 0; rb < 4; ++rb) {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j] = __uint_as_float(static_cast<uint32_t>(tile[(16 * (rb0 + rb) + j) * kCPitch + lc])
+                               << 16);
+      const bool valid = c < cols && gr + rb < nbn;
+      const QBlock qb = quant_block(v, amax_f32x16(v), g, tk, valid);
+      code[rb] = qb.codes;
+      sfw |= qb.sf << (8 * rb);
+    }
+    if (c < cols && gr < kcn) {
+      if (gr < nbn) {
+        uint8_t* dst = codes + (p0.grp * cols + c) * static_cast<int64_t>(rows / 2) + 8 * gr;
+        if (v8 && gr + 4 <= nbn) {
+          st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
+                       code[3].x, code[3].y);
+        } else {
+#pragma unroll
+          for (int rb = 0; rb < 4; ++rb)
+            if (gr + rb < nbn) st_u64(dst + 8 * rb, code[rb]);
+        }
+      }
+      *reinterpret_cast<uint32_t*>(sf + p0.grp * sf_group + sf_offset(c, gr, kcn)) = sfw;
+    }
+    __syncthreads();  // the next iteration refills this buffer
+    p0 = p1;
+    p1 = p2;
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+  // scale bytes of the padding rows [cols, roundup(cols, 128)); the global scales
+  const int64_t gt = blockIdx.x * static_cast<int64_t>(blockDim.x) + t;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t pn = ((cols + 127) & ~127) - cols;
+  const int wn = kcn / 4;
+  for (int64_t i = gt; i < groups * pn * wn; i += nthreads) {
+    const int64_t grp = i / (pn * wn);
+    const int64_t rem = i % (pn * wn);
+    *reinterpret_cast<uint32_t*>(sf + grp * sf_group +
+                                 sf_offset(cols + rem / wn, 4 * (rem % wn), kcn)) = 0u;
+  }
+  for (int64_t grp = gt; grp < groups; grp += nthreads)
+    g_out[grp] = g_in ? g_in[grp] : global_scale(__uint_as_float(amax_bits[grp]));
+}
+
 template <int NCH, bool PG>
 static void launch_token_rows(const uint16_t* x, int64_t groups, int64_t rows, int cols, bool a32,
                               uint8_t* codes, uint8_t* sf, float* g_out, const float* g_in,
@@ -601,7 +654,9 @@ extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   const int64_t Cq = orientation == MINITE_ALONG_COLS ? cols : rows;
   if (Cq % 16 != 0 || cols % 8 != 0) return MINITE_ERR_UNSUPPORTED_SHAPE;
-  if (orientation == MINITE_ALONG_ROWS && !per_group) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (orientation == MINITE_ALONG_ROWS &&
+      (!per_group || rows >= (int64_t(1) << 30) || cols >= (int64_t(1) << 30)))
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (orientation == MINITE_ALONG_COLS && cols > 4096) return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (groups * rows * cols >= (int64_t(1) << 40)) return MINITE_ERR_UNSUPPORTED_SHAPE;
   if (per_group && rows * (cols / 16) >= (int64_t(1) << 32)) return MINITE_ERR_UNSUPPORTED_SHAPE;
@@ -645,10 +700,22 @@ extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows
       }
     }
   } else {
-    dim3 grid(static_cast<unsigned>((rows + kTR - 1) / kTR),
-              static_cast<unsigned>((cols + kTC - 1) / kTC), static_cast<unsigned>(groups));
-    quantize_cols_kernel<<<grid, 256, 0, s>>>(xb, rows, cols, gscale_in, amax, codes, sf,
-                                              gscale_out);
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+      attr = cudaFuncSetAttribute(quantize_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kColsSmem));
+    });
+    if (attr != cudaSuccess) return MINITE_ERR_CUDA;
+    const int64_t tiles = groups * ((rows + kCR - 1) / kCR) * ((cols + kCC - 1) / kCC);
+    int64_t blocks = static_cast<int64_t>(num_sms()) * 3;
+    if (blocks > tiles) blocks = tiles;
+    if (blocks * 256 < groups) blocks = (groups + 255) / 256;  // g_out: thread t < groups
+    if (launch_pdl(quantize_cols_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                   kColsSmem, s, xb, groups, static_cast<int>(rows), static_cast<int>(cols),
+                   gscale_in, static_cast<const uint32_t*>(amax), codes, sf, gscale_out) !=
+        cudaSuccess)
+      return MINITE_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
