@@ -12,9 +12,10 @@
 //                          equals float order).
 //   quantize_rows_kernel   one warp per row, blocks of 16 along the row, the
 //                          row held in registers (coalesced 16-byte loads).
-//   quantize_cols_kernel   blocks of 16 along the rows of a group (the
-//                          transposed, dgrad-layout copy of a weight): 128 x
-//                          128 tiles staged through shared memory with
+//   quantize_tiles_kernel  blocks of 16 along the rows of a group (the
+//                          transposed, dgrad-layout copy of a weight), and
+//                          optionally the forward copy from the same read:
+//                          128 x 128 tiles staged through shared memory with
 //                          per-thread asynchronous copies (two buffers).
 #include <mutex>
 
@@ -198,16 +199,20 @@ __global__ void __launch_bounds__(256) quantize_token_rows_kernel(
   }
 }
 
-// Both orientations of per-group quantization from one read of each weight:
-// 64 x 128 tiles of x[grp] are staged in shared memory (two buffers, the next
-// tile's per-thread asynchronous copies in flight while the current one is
-// quantized). Warps 0-3 take one tile column each (its 4 blocks along the
-// rows: 32 contiguous code bytes and 4 contiguous scale bytes of the
-// transposed copy); warps 4-7 take half a tile row each (4 blocks along the
-// columns: 32 contiguous code bytes and 4 contiguous scale bytes of the
-// forward copy). Both copies use the group's global scale.
-constexpr int kDR = 64, kDC = 128, kDPitch = kDC + 8;  // pitch in BF16, rows 16-byte aligned
+// Per-group quantization of weights [rows, cols] in the transposed (dgrad)
+// orientation, and with FWD also in the forward one, from one read of each
+// weight: 128 x 128 tiles of x[grp] are staged in shared memory (two buffers,
+// the next tile's per-thread asynchronous copies in flight while the current
+// one is quantized). Every thread takes four blocks of each copy it writes:
+// of the transposed copy, column t % 128 of the tile and its rows
+// 64 (t / 128) .. + 64; of the forward copy, row t / 2 and its columns
+// 64 (t % 2) .. + 64; each gives 32 contiguous code bytes and one 4-byte
+// scale word. Both copies use the group's global scale (g_in, else from the
+// group maxima in amax_bits; after that maxima pass the tiles are taken last
+// to first, starting on the bytes it left in L2).
+constexpr int kDR = 128, kDC = 128, kDPitch = kDC + 8;  // pitch in BF16, rows 16-byte aligned
 constexpr int kDTile = kDR * kDPitch;
+constexpr size_t kDualSmem = 2 * kDTile * sizeof(uint16_t);
 
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
@@ -215,7 +220,7 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
                : "memory");
 }
 
-// Shape constants of the two-orientation quantization of one weight shape.
+// Shape constants of the quantization of one weight shape.
 struct DualGeom {
   int rows, cols, tr, tc;        // tiles per group: tr x tc
   int nbk, nbn, kck, kcn;        // blocks per quantized row, SF columns (forward, transposed)
@@ -238,14 +243,14 @@ __device__ __forceinline__ DualGeom dual_geom(int rows, int cols, const uint8_t*
   return G;
 }
 
-// Every thread of the block: per-thread asynchronous copies of the 64 x 128
+// Every thread of the block: per-thread asynchronous copies of the 128 x 128
 // tile (r0, c0) of group xg into buf (zero-filled outside the matrix), as
 // one commit group.
 __device__ __forceinline__ void dual_fetch(const uint16_t* xg, const DualGeom& G, int r0, int c0,
                                            uint16_t* buf, const uint16_t* any_valid) {
   const int t = threadIdx.x;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 8; ++i) {
     const int q = t + 256 * i;  // 16-byte piece q of the tile: row q / 16, piece q % 16
     const int lr = q >> 4, seg = q & 15;
     const bool valid = r0 + lr < G.rows && c0 + 8 * seg < G.cols;
@@ -255,8 +260,24 @@ __device__ __forceinline__ void dual_fetch(const uint16_t* xg, const DualGeom& G
   }
 }
 
+// Four 8-byte code blocks at dst (blocks g0 .. g0 + 3 of a row of nb): one
+// 32-byte store where allowed, else the blocks below nb one by one.
+__device__ __forceinline__ void store_code4(uint8_t* dst, const uint2 (&code)[4], int g0, int nb,
+                                            bool v8) {
+  if (v8 && g0 + 4 <= nb) {
+    st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
+                 code[3].x, code[3].y);
+  } else {
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      if (g0 + b < nb) st_u64(dst + 8 * b, code[b]);
+  }
+}
+
 // Every thread of the block (256): quantize the staged tile (r0, c0) of
-// group grp in both orientations with the group's global scale g.
+// group grp in the transposed orientation and, with FWD, the forward one,
+// with the group's global scale g.
+template <bool FWD>
 __device__ __forceinline__ void dual_tile_quant(const uint16_t* tile, const DualGeom& G,
                                                 int64_t grp, int r0, int c0, float g, float tk,
                                                 uint8_t* __restrict__ codes_k,
@@ -264,9 +285,11 @@ __device__ __forceinline__ void dual_tile_quant(const uint16_t* tile, const Dual
                                                 uint8_t* __restrict__ codes_n,
                                                 uint8_t* __restrict__ sf_n) {
   const int t = threadIdx.x;
-  if (t < 128) {
+  {
     // ---- one tile column, 4 blocks along the rows (transposed copy)
-    const int c = c0 + t;
+    const int lc = t & (kDC - 1), rb0 = 4 * (t >> 7);
+    const int c = c0 + lc;
+    const int gr = r0 / 16 + rb0;  // multiple of 4
     uint2 code[4];
     uint32_t sfw = 0;
 #pragma unroll
@@ -274,29 +297,23 @@ __device__ __forceinline__ void dual_tile_quant(const uint16_t* tile, const Dual
       float v[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        v[j] = __uint_as_float(static_cast<uint32_t>(tile[(16 * rb + j) * kDPitch + t]) << 16);
-      const bool valid = c < G.cols && r0 / 16 + rb < G.nbn;
+        v[j] = __uint_as_float(static_cast<uint32_t>(tile[(16 * (rb0 + rb) + j) * kDPitch + lc])
+                               << 16);
+      const bool valid = c < G.cols && gr + rb < G.nbn;
       const QBlock q = quant_block(v, amax_f32x16(v), g, tk, valid);
       code[rb] = q.codes;
       sfw |= q.sf << (8 * rb);
     }
-    if (c < G.cols) {
-      const int gr = r0 / 16;  // multiple of 4
-      uint8_t* dst = codes_n + (grp * G.cols + c) * static_cast<int64_t>(G.rows / 2) + 8 * gr;
-      if (G.v8n && gr + 4 <= G.nbn) {
-        st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
-                     code[3].x, code[3].y);
-      } else {
-#pragma unroll
-        for (int rb = 0; rb < 4; ++rb)
-          if (gr + rb < G.nbn) st_u64(dst + 8 * rb, code[rb]);
-      }
+    if (c < G.cols && gr < G.kcn) {
+      if (gr < G.nbn)
+        store_code4(codes_n + (grp * G.cols + c) * static_cast<int64_t>(G.rows / 2) + 8 * gr, code,
+                    gr, G.nbn, G.v8n);
       *reinterpret_cast<uint32_t*>(sf_n + grp * G.sfn_group + sf_offset(c, gr, G.kcn)) = sfw;
     }
-  } else {
+  }
+  if (FWD) {
     // ---- half a tile row, 4 blocks along the columns (forward copy)
-    const int u = t - 128;
-    const int lr = u >> 1, half = u & 1;
+    const int lr = t >> 1, half = t & 1;
     const int r = r0 + lr;
     uint2 code[4];
     uint32_t sfw = 0;
@@ -315,33 +332,29 @@ __device__ __forceinline__ void dual_tile_quant(const uint16_t* tile, const Dual
     }
     const int gc = c0 / 16 + 4 * half;  // multiple of 4
     if (r < G.rows && gc < G.nbk) {
-      uint8_t* dst = codes_k + (grp * G.rows + r) * static_cast<int64_t>(G.cols / 2) + 8 * gc;
-      if (G.v8k && gc + 4 <= G.nbk) {
-        st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
-                     code[3].x, code[3].y);
-      } else {
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb)
-          if (gc + cb < G.nbk) st_u64(dst + 8 * cb, code[cb]);
-      }
+      store_code4(codes_k + (grp * G.rows + r) * static_cast<int64_t>(G.cols / 2) + 8 * gc, code,
+                  gc, G.nbk, G.v8k);
       *reinterpret_cast<uint32_t*>(sf_k + grp * G.sfk_group + sf_offset(r, gc, G.kck)) = sfw;
     }
   }
 }
 
-// Scale bytes of the padding rows of both copies of groups [g0, g1), split
-// over `nthreads` threads numbered from `gt`.
+// Scale bytes of the padding rows of the copies written (the forward one with
+// FWD), groups [g0, g1), split over `nthreads` threads numbered from `gt`.
+template <bool FWD>
 __device__ __forceinline__ void dual_zero_padding(const DualGeom& G, int64_t g0, int64_t g1,
                                                   int64_t gt, int64_t nthreads,
                                                   uint8_t* __restrict__ sf_k,
                                                   uint8_t* __restrict__ sf_n) {
   const int64_t pk = ((G.rows + 127) & ~127) - G.rows, pn = ((G.cols + 127) & ~127) - G.cols;
   const int wk = G.kck / 4, wn = G.kcn / 4;
-  for (int64_t i = gt; i < (g1 - g0) * pk * wk; i += nthreads) {
-    const int64_t grp = g0 + i / (pk * wk);
-    const int64_t rem = i % (pk * wk);
-    *reinterpret_cast<uint32_t*>(sf_k + grp * G.sfk_group +
-                                 sf_offset(G.rows + rem / wk, 4 * (rem % wk), G.kck)) = 0u;
+  if (FWD) {
+    for (int64_t i = gt; i < (g1 - g0) * pk * wk; i += nthreads) {
+      const int64_t grp = g0 + i / (pk * wk);
+      const int64_t rem = i % (pk * wk);
+      *reinterpret_cast<uint32_t*>(sf_k + grp * G.sfk_group +
+                                   sf_offset(G.rows + rem / wk, 4 * (rem % wk), G.kck)) = 0u;
+    }
   }
   for (int64_t i = gt; i < (g1 - g0) * pn * wn; i += nthreads) {
     const int64_t grp = g0 + i / (pn * wn);
@@ -351,12 +364,13 @@ __device__ __forceinline__ void dual_zero_padding(const DualGeom& G, int64_t g0,
   }
 }
 
-__global__ void __launch_bounds__(256) quantize_dual_kernel(
+template <bool FWD>
+__global__ void __launch_bounds__(256) quantize_tiles_kernel(
     const uint16_t* __restrict__ x, int64_t groups, int rows, int cols,
-    const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes_k,
-    uint8_t* __restrict__ sf_k, uint8_t* __restrict__ codes_n, uint8_t* __restrict__ sf_n,
-    float* __restrict__ g_out) {
-  __shared__ __align__(16) uint16_t tiles[2][kDTile];
+    const float* __restrict__ g_in, const uint32_t* __restrict__ amax_bits,
+    uint8_t* __restrict__ codes_k, uint8_t* __restrict__ sf_k, uint8_t* __restrict__ codes_n,
+    uint8_t* __restrict__ sf_n, float* __restrict__ g_out) {
+  extern __shared__ __align__(16) uint16_t dtiles[];  // [2][kDTile]
   pdl_wait();
   const int t = threadIdx.x;
   const DualGeom G = dual_geom(rows, cols, codes_k, codes_n);
@@ -371,14 +385,12 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
   auto pos = [&](int64_t ti) {
     TilePos p{-1, 0, 0};
     if (ti < ntiles) {
-      // last tile first: the group-maxima pass just read the groups in order,
-      // so the end of the weight is the part still in L2
-      const int64_t tr_ = ntiles - 1 - ti;
-      p.grp = div_nonneg(tr_, per_group);
-      const int rem = static_cast<int>(tr_ - p.grp * per_group);
-      const int tr = rem / G.tc;
-      p.r0 = tr * kDR;
-      p.c0 = (rem - tr * G.tc) * kDC;
+      const int64_t k = g_in ? ti : ntiles - 1 - ti;
+      p.grp = div_nonneg(k, per_group);
+      const int rem = static_cast<int>(k - p.grp * per_group);
+      const int a = rem / G.tc;
+      p.r0 = a * kDR;
+      p.c0 = (rem - a * G.tc) * kDC;
     }
     return p;
   };
@@ -390,101 +402,12 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(
 
   int64_t ti = blockIdx.x;
   TilePos p0 = pos(ti), p1 = pos(ti + gridDim.x);
-  fetch(p0, tiles[0]);
+  fetch(p0, dtiles);
   int cur = 0;
   int64_t gcur = -1;
   float g = 1.0f, tk = 1.0f;
   for (; ti < ntiles; ti += gridDim.x, cur ^= 1) {
-    fetch(p1, tiles[cur ^ 1]);
-    const TilePos p2 = pos(ti + 2 * static_cast<int64_t>(gridDim.x));
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-    __syncthreads();
-    if (p0.grp != gcur) {  // block-uniform
-      gcur = p0.grp;
-      g = global_scale(__uint_as_float(amax_bits[p0.grp]));
-      tk = enc_table_entry(g);
-    }
-    dual_tile_quant(tiles[cur], G, p0.grp, p0.r0, p0.c0, g, tk, codes_k, sf_k, codes_n, sf_n);
-    __syncthreads();  // the next iteration refills this buffer
-    p0 = p1;
-    p1 = p2;
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-
-  // zero the scale bytes of the padding rows of both copies, and publish g
-  const int64_t gt = blockIdx.x * (int64_t)blockDim.x + t;
-  dual_zero_padding(G, 0, groups, gt, (int64_t)gridDim.x * blockDim.x, sf_k, sf_n);
-  if (gt < groups) g_out[gt] = global_scale(__uint_as_float(amax_bits[gt]));
-}
-
-// Transposed quantization of group matrices [rows, cols] (the dgrad copy of a
-// weight): quantized row q is column q of the group, blocks of 16 along the
-// original rows, one global scale per group (g_in, else from amax_bits).
-// 128 x 128 tiles are staged in shared memory (two buffers, the next tile's
-// per-thread asynchronous copies in flight while the current one is
-// quantized); thread t takes column t % 128 of the tile and its rows
-// 64 (t / 128) .. + 64: four blocks, 32 contiguous code bytes and one 4-byte
-// scale word. After a group-maxima pass the tiles are taken last to first,
-// starting on the bytes that pass left in L2.
-constexpr int kCR = 128, kCC = 128, kCPitch = kCC + 8;  // pitch in BF16, rows 16-byte aligned
-constexpr int kCTile = kCR * kCPitch;
-constexpr size_t kColsSmem = 2 * kCTile * sizeof(uint16_t);
-
-__global__ void __launch_bounds__(256) quantize_cols_kernel(
-    const uint16_t* __restrict__ x, int64_t groups, int rows, int cols,
-    const float* __restrict__ g_in, const uint32_t* __restrict__ amax_bits,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ g_out) {
-  extern __shared__ __align__(16) uint16_t ctiles[];  // [2][kCTile]
-  pdl_wait();
-  const int t = threadIdx.x;
-  const int tr = (rows + kCR - 1) / kCR, tc = (cols + kCC - 1) / kCC;
-  const int nbn = rows / 16;                 // blocks per quantized row
-  const int kcn = (nbn + 3) & ~3;            // SF columns
-  const int64_t sf_group = static_cast<int64_t>((cols + 127) & ~127) * kcn;
-  const bool v8 = (rows / 2) % 32 == 0 && (reinterpret_cast<uintptr_t>(codes) & 31) == 0;
-  const int64_t per_group = static_cast<int64_t>(tr) * tc;
-  const int64_t ntiles = groups * per_group;
-  struct TilePos {
-    int64_t grp;
-    int r0, c0;
-  };
-  auto pos = [&](int64_t ti) {
-    TilePos p{-1, 0, 0};
-    if (ti < ntiles) {
-      const int64_t k = g_in ? ti : ntiles - 1 - ti;
-      p.grp = div_nonneg(k, per_group);
-      const int rem = static_cast<int>(k - p.grp * per_group);
-      const int a = rem / tc;
-      p.r0 = a * kCR;
-      p.c0 = (rem - a * tc) * kCC;
-    }
-    return p;
-  };
-  auto fetch = [&](const TilePos& p, uint16_t* buf) {
-    if (p.grp >= 0) {
-      const uint16_t* xg = x + p.grp * static_cast<int64_t>(rows) * cols;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int q = t + 256 * i;  // 16-byte piece q: row q / 16, piece q % 16
-        const int lr = q >> 4, seg = q & 15;
-        const bool valid = p.r0 + lr < rows && p.c0 + 8 * seg < cols;
-        const uint16_t* src =
-            valid ? xg + static_cast<int64_t>(p.r0 + lr) * cols + p.c0 + 8 * seg : x;
-        cp_async16_zfill(buf + lr * kCPitch + 8 * seg, src, valid);
-      }
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
-
-  int64_t ti = blockIdx.x;
-  TilePos p0 = pos(ti), p1 = pos(ti + gridDim.x);
-  fetch(p0, ctiles);
-  int cur = 0;
-  int64_t gcur = -1;
-  float g = 1.0f, tk = 1.0f;
-  const int lc = t & (kCC - 1), rb0 = 4 * (t >> 7);  // this thread's column, first row block
-  for (; ti < ntiles; ti += gridDim.x, cur ^= 1) {
-    fetch(p1, ctiles + (cur ^ 1) * kCTile);
+    fetch(p1, dtiles + (cur ^ 1) * kDTile);
     const TilePos p2 = pos(ti + 2 * static_cast<int64_t>(gridDim.x));
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncthreads();
@@ -493,56 +416,45 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(
       g = g_in ? g_in[gcur] : global_scale(__uint_as_float(amax_bits[gcur]));
       tk = enc_table_entry(g);
     }
-    const uint16_t* tile = ctiles + cur * kCTile;
-    const int c = p0.c0 + lc;
-    const int gr = p0.r0 / 16 + rb0;  // first block (SF column) of this thread, a multiple of 4
-    uint2 code[4];
-    uint32_t sfw = 0;
-#pragma unroll
-    for (int rb = 0; rb < 4; ++rb) {
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        v[j] = __uint_as_float(static_cast<uint32_t>(tile[(16 * (rb0 + rb) + j) * kCPitch + lc])
-                               << 16);
-      const bool valid = c < cols && gr + rb < nbn;
-      const QBlock qb = quant_block(v, amax_f32x16(v), g, tk, valid);
-      code[rb] = qb.codes;
-      sfw |= qb.sf << (8 * rb);
-    }
-    if (c < cols && gr < kcn) {
-      if (gr < nbn) {
-        uint8_t* dst = codes + (p0.grp * cols + c) * static_cast<int64_t>(rows / 2) + 8 * gr;
-        if (v8 && gr + 4 <= nbn) {
-          st_global_v8(dst, code[0].x, code[0].y, code[1].x, code[1].y, code[2].x, code[2].y,
-                       code[3].x, code[3].y);
-        } else {
-#pragma unroll
-          for (int rb = 0; rb < 4; ++rb)
-            if (gr + rb < nbn) st_u64(dst + 8 * rb, code[rb]);
-        }
-      }
-      *reinterpret_cast<uint32_t*>(sf + p0.grp * sf_group + sf_offset(c, gr, kcn)) = sfw;
-    }
+    dual_tile_quant<FWD>(dtiles + cur * kDTile, G, p0.grp, p0.r0, p0.c0, g, tk, codes_k, sf_k,
+                         codes_n, sf_n);
     __syncthreads();  // the next iteration refills this buffer
     p0 = p1;
     p1 = p2;
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 
-  // scale bytes of the padding rows [cols, roundup(cols, 128)); the global scales
+  // zero the scale bytes of the padding rows, and publish g
   const int64_t gt = blockIdx.x * static_cast<int64_t>(blockDim.x) + t;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t pn = ((cols + 127) & ~127) - cols;
-  const int wn = kcn / 4;
-  for (int64_t i = gt; i < groups * pn * wn; i += nthreads) {
-    const int64_t grp = i / (pn * wn);
-    const int64_t rem = i % (pn * wn);
-    *reinterpret_cast<uint32_t*>(sf + grp * sf_group +
-                                 sf_offset(cols + rem / wn, 4 * (rem % wn), kcn)) = 0u;
-  }
+  dual_zero_padding<FWD>(G, 0, groups, gt, nthreads, sf_k, sf_n);
   for (int64_t grp = gt; grp < groups; grp += nthreads)
     g_out[grp] = g_in ? g_in[grp] : global_scale(__uint_as_float(amax_bits[grp]));
+}
+
+// One launch of quantize_tiles_kernel<FWD> (three CTAs per SM: two 34 KB tile
+// buffers each).
+template <bool FWD>
+static int launch_tiles(const uint16_t* x, int64_t groups, int64_t rows, int64_t cols,
+                        const float* g_in, const uint32_t* amax, uint8_t* codes_k, uint8_t* sf_k,
+                        uint8_t* codes_n, uint8_t* sf_n, float* g_out, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(quantize_tiles_kernel<FWD>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kDualSmem));
+  });
+  if (attr != cudaSuccess) return MINITE_ERR_CUDA;
+  const int64_t tiles = groups * ((rows + kDR - 1) / kDR) * ((cols + kDC - 1) / kDC);
+  int64_t blocks = static_cast<int64_t>(num_sms()) * 3;
+  if (blocks > tiles) blocks = tiles;
+  if (blocks * 256 < groups) blocks = (groups + 255) / 256;  // g_out: thread t < groups
+  if (launch_pdl(quantize_tiles_kernel<FWD>, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                 kDualSmem, s, x, groups, static_cast<int>(rows), static_cast<int>(cols), g_in,
+                 amax, codes_k, sf_k, codes_n, sf_n, g_out) != cudaSuccess)
+    return MINITE_ERR_CUDA;
+  return MINITE_OK;
 }
 
 template <int NCH, bool PG>
@@ -625,14 +537,8 @@ extern "C" int minite_quantize_nvfp4_dual(const void* x, int64_t groups, int64_t
   uint32_t* amax = static_cast<uint32_t*>(workspace);
   const int rc = launch_group_amax(xb, groups, rows * cols, amax, s);
   if (rc != MINITE_OK) return rc;
-  const int64_t tiles = groups * ((rows + kDR - 1) / kDR) * ((cols + kDC - 1) / kDC);
-  int64_t blocks = static_cast<int64_t>(num_sms()) * 6;
-  if (blocks > tiles) blocks = tiles;
-  if (blocks * 256 < groups) blocks = (groups + 255) / 256;
-  launch_pdl(quantize_dual_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, xb, groups,
-             static_cast<int>(rows), static_cast<int>(cols), static_cast<const uint32_t*>(amax),
-             codes_k, sf_k, codes_n, sf_n, gscale_out);
-  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+  return launch_tiles<true>(xb, groups, rows, cols, nullptr, amax, codes_k, sf_k, codes_n, sf_n,
+                            gscale_out, s);
 }
 
 extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows, int64_t cols,
@@ -700,22 +606,9 @@ extern "C" int minite_quantize_nvfp4(const void* x, int64_t groups, int64_t rows
       }
     }
   } else {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-      attr = cudaFuncSetAttribute(quantize_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(kColsSmem));
-    });
-    if (attr != cudaSuccess) return MINITE_ERR_CUDA;
-    const int64_t tiles = groups * ((rows + kCR - 1) / kCR) * ((cols + kCC - 1) / kCC);
-    int64_t blocks = static_cast<int64_t>(num_sms()) * 3;
-    if (blocks > tiles) blocks = tiles;
-    if (blocks * 256 < groups) blocks = (groups + 255) / 256;  // g_out: thread t < groups
-    if (launch_pdl(quantize_cols_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256),
-                   kColsSmem, s, xb, groups, static_cast<int>(rows), static_cast<int>(cols),
-                   gscale_in, static_cast<const uint32_t*>(amax), codes, sf, gscale_out) !=
-        cudaSuccess)
-      return MINITE_ERR_CUDA;
+    const int rc = launch_tiles<false>(xb, groups, rows, cols, gscale_in, amax, nullptr, nullptr,
+                                       codes, sf, gscale_out, s);
+    if (rc != MINITE_OK) return rc;
   }
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
