@@ -668,6 +668,55 @@ def test_mlp_forward_full_size_sampled_tokens_match_oracle_chain():
     assert same > 0.9, same
 
 
+def test_benchmarked_step_full_size_graph_replay_matches_oracle_on_sampled_tokens():
+    """The step the benchmark times: the skewed 32768-token layer (weight
+    quantization, permutation, both GEMMs, SwiGLU, combine, the combine
+    backward with dY quantization and the down projection's dgrad GEMM),
+    captured as one CUDA graph and replayed. Per-token scaling makes a
+    token's rows independent of the batch, so the oracle runs on sampled
+    tokens alone: their y against the oracle chain (chain tolerance), and
+    their dgrad rows dH = dY_hat W_down_hat within 1 BF16 ulp of the exact
+    product (rows located through the oracle's own permutation)."""
+    import bench
+    d = IN.make_moe_inputs("skewed")
+    c = d["cfg"]
+    T, E = c["T"], c["E"]
+    dev = torch.device("cuda", 0)
+    step = bench.Step(d, dev)
+    s = torch.cuda.current_stream(dev)
+    step.run(s)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(s)
+    with torch.cuda.graph(graph, stream=cap):
+        step.run(torch.cuda.current_stream(dev))
+    s.wait_stream(cap)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    rng = np.random.default_rng(11)
+    tok = np.sort(rng.choice(T, 24, replace=False))
+    # forward output of the sampled tokens
+    ref = O.moe_mlp_forward(d["x"][tok], d["topk_ids"][tok], d["topk_w"][tok], E,
+                            O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
+    yv = O.bf16_to_f32(u16(step.mlp.y)[tok]).astype(np.float64)
+    yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
+    rel = np.linalg.norm(yv - yr, axis=1) / np.linalg.norm(yr, axis=1)
+    assert rel.max() < 2e-2, rel.max()
+    assert (u16(step.mlp.y)[tok] == ref["y"]).mean() > 0.9
+    # dgrad rows of the sampled tokens: per-token dY quantization, W_down's dgrad copy
+    pq = O.moe_permute_quant(d["dy"][tok], d["topk_ids"][tok], None, E)
+    wdT = O.quantize_weights(d["w_down"], along_rows=True)
+    dh_s, _ = O.grouped_gemm_exact(pq["codes"], pq["sf"], pq["row_g"], wdT[0], wdT[1], wdT[3],
+                                   pq["expert_offsets"])
+    full = O.moe_permute(d["topk_ids"], E)
+    gpu_rows = full["dest_row"][tok].ravel()
+    mini_rows = pq["dest_row"].ravel()
+    assert (gpu_rows >= 0).all() and (mini_rows >= 0).all()
+    assert_bf16_within_one_ulp(u16(step.dh)[gpu_rows], dh_s[mini_rows], "dH (sampled rows)")
+
+
 @pytest.mark.parametrize("name,T", [("tiny", None), ("mlp", 256)])
 def test_backward_chain_stagewise(name, T):
     """The NVFP4 backward of the expert MLP, stage by stage: permute+quant of
