@@ -15,6 +15,13 @@ def u16(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def gpu_bf16_values(u: np.ndarray) -> np.ndarray:
+    """Float64 values of BF16 bit patterns read back from the device (decoded
+    here, so that no device output passes through the oracle)."""
+    bits = np.asarray(u, dtype=np.uint16).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
 def np_dev(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
 
@@ -30,7 +37,7 @@ def assert_bf16_within_one_ulp(got_u16, exact_f64, what=""):
     """BF16 output within 1 BF16 ulp of the correctly rounded exact result."""
     from oracle import nvfp4_moe_oracle as O
     ref = O.bf16_to_f32(O.f64_to_bf16(exact_f64)).astype(np.float64)
-    got = O.bf16_to_f32(got_u16).astype(np.float64)
+    got = gpu_bf16_values(got_u16)
     ulp = np.maximum(bf16_ulp(ref), bf16_ulp(got))
     bad = np.abs(got - ref) > ulp
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside 1 BF16 ulp; worst " \

@@ -10,8 +10,8 @@ import numpy as np
 import pytest
 import torch
 
-from _helpers import (assert_bf16_within_one_ulp, assert_fp32_within_bound, bf16_dev, np_dev,
-                      u16)
+from _helpers import (assert_bf16_within_one_ulp, assert_fp32_within_bound, bf16_dev,
+                      gpu_bf16_values, np_dev, u16)
 from nvfp4_w4a4_moe_permute_gb300 import inputs as IN
 from nvfp4_w4a4_moe_permute_gb300 import minite as M
 from oracle import nvfp4_moe_oracle as O
@@ -638,7 +638,7 @@ def test_mlp_tiny_stagewise_and_end_to_end():
                                        *[O.quantize_weights(d["w_gate_up"])[i] for i in (0, 1)],
                                        O.quantize_weights(d["w_gate_up"])[3], p["expert_offsets"])
     assert_bf16_within_one_ulp(u16(mlp.gate_up)[:Mu], gu_exact, "gate_up")
-    yv = O.bf16_to_f32(u16(y)).astype(np.float64)
+    yv = gpu_bf16_values(u16(y))
     yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
     assert np.linalg.norm(yv - yr) / np.linalg.norm(yr) < 2e-2
 
@@ -660,7 +660,7 @@ def test_mlp_forward_full_size_sampled_tokens_match_oracle_chain():
     tok = np.sort(rng.choice(T, 64, replace=False))
     ref = O.moe_mlp_forward(d["x"][tok], d["topk_ids"][tok], d["topk_w"][tok], E,
                             O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
-    yv = O.bf16_to_f32(u16(y)[tok]).astype(np.float64)
+    yv = gpu_bf16_values(u16(y)[tok])
     yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
     rel = np.linalg.norm(yv - yr, axis=1) / np.linalg.norm(yr, axis=1)
     assert rel.max() < 2e-2, rel.max()
@@ -700,7 +700,7 @@ def test_benchmarked_step_full_size_graph_replay_matches_oracle_on_sampled_token
     # forward output of the sampled tokens
     ref = O.moe_mlp_forward(d["x"][tok], d["topk_ids"][tok], d["topk_w"][tok], E,
                             O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
-    yv = O.bf16_to_f32(u16(step.mlp.y)[tok]).astype(np.float64)
+    yv = gpu_bf16_values(u16(step.mlp.y)[tok])
     yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
     rel = np.linalg.norm(yv - yr, axis=1) / np.linalg.norm(yr, axis=1)
     assert rel.max() < 2e-2, rel.max()
@@ -717,25 +717,51 @@ def test_benchmarked_step_full_size_graph_replay_matches_oracle_on_sampled_token
     assert_bf16_within_one_ulp(u16(step.dh)[gpu_rows], dh_s[mini_rows], "dH (sampled rows)")
 
 
+def _dev_rows(a, rows, dtype=None):
+    """Device copy of oracle array `a` in a zeroed buffer of `rows` rows (the
+    rows past a's are the unused capacity a stage's buffers have)."""
+    out = np.zeros((rows,) + a.shape[1:], dtype=a.dtype if dtype is None else dtype)
+    out[:a.shape[0]] = a
+    return bf16_dev(out) if out.dtype == np.uint16 else np_dev(out)
+
+
 @pytest.mark.parametrize("name,T", [("tiny", None), ("mlp", 256)])
 def test_backward_chain_stagewise(name, T):
     """The NVFP4 backward of the expert MLP, stage by stage: permute+quant of
     dY, down dgrad GEMM (W_down quantized along N), SwiGLU backward with
     per-row requantization, gate_up dgrad GEMM (W_gate_up quantized along N),
-    combine of dX. Each stage is checked against the oracle fed with the
-    GPU's inputs to that stage: codes, scales and the combine bit-exact, GEMM
-    outputs within one BF16 ulp of the exact result."""
+    combine of dX. The oracle runs the whole chain from the layer's inputs;
+    a GPU stage whose input is an earlier stage's result takes the oracle's
+    value of it (uploaded), so no expected value depends on GPU output.
+    Codes, scales and the combine bit-exact, GEMM outputs within one BF16 ulp
+    of the exact result."""
     d = IN.make_moe_inputs(name, T=T)
     c = d["cfg"]
     T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
     rng = np.random.default_rng(9)
     dy = O.f32_to_bf16(rng.standard_normal((T, H)).astype(np.float32))
-    ids, w = np_dev(d["topk_ids"]), np_dev(d["topk_w"])
-    wgu, wd = _weights(d)
+    # the oracle's chain
+    fwd = O.moe_mlp_forward(d["x"], d["topk_ids"], d["topk_w"], E,
+                            O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
+    pf = fwd["permute"]
+    p = O.moe_permute_quant(dy, d["topk_ids"], None, E)
+    off, sfo = p["expert_offsets"], p["sf_row_offsets"]
+    assert np.array_equal(off, pf["expert_offsets"])
+    Mu = int(off[-1])
+    qdT = O.quantize_weights(d["w_down"], along_rows=True)
+    dh_exact, _ = O.grouped_gemm_exact(p["codes"], p["sf"], p["row_g"], qdT[0], qdT[1], qdT[3], off)
+    dh_o = O.f64_to_bf16(dh_exact)
+    sb = O.swiglu_backward_quant(fwd["gate_up"], dh_o, pf["perm_w"], off, sfo)
+    qguT = O.quantize_weights(d["w_gate_up"], along_rows=True)
+    dx_exact, _ = O.grouped_gemm_exact(sb["codes"], sb["sf"], sb["row_g"], qguT[0], qguT[1],
+                                       qguT[3], off)
+    dxp_o = O.f64_to_bf16(dx_exact)
+    dx_o = O.moe_combine(dxp_o, pf["dest_row"])
+
+    # the GPU's stages
+    ids = np_dev(d["topk_ids"])
     _, wdT = M.quantize_dual(bf16_dev(d["w_down"]))
     _, wguT = M.quantize_dual(bf16_dev(d["w_gate_up"]))
-    mlp = M.MoEMLP(T, H, I, E, k)
-    mlp.forward(bf16_dev(d["x"]), ids, w, wgu, wd)
     bwd = M.MoEMLP(T, H, I, E, k)
     bwd.permute_quant(bf16_dev(dy), ids, None)
     Mt = T * k
@@ -743,54 +769,45 @@ def test_backward_chain_stagewise(name, T):
     dh = torch.empty((Mt, I), dtype=torch.bfloat16, device="cuda")
     M.minite_grouped_gemm_nvfp4(bwd.a_codes, bwd.a_sf, bwd.a_g, wdT["codes"], wdT["sf"], wdT["g"],
                                 bwd.offsets, bwd.sf_offsets, dh, st)
+    off_d, sfo_d = np_dev(off), np_dev(sfo)
     dgu_codes = torch.zeros((Mt, I), dtype=torch.uint8, device="cuda")
     dgu_sf = torch.full((M.sf_bytes(Mt + 128 * E, 2 * I),), 0xAB, dtype=torch.uint8, device="cuda")
     dgu_g = torch.zeros(Mt, dtype=torch.float32, device="cuda")
-    M.minite_swiglu_backward_quant(mlp.gate_up, dh, mlp.perm_w, E, mlp.offsets, mlp.sf_offsets,
-                                   dgu_codes, dgu_sf, dgu_g, st)
+    M.minite_swiglu_backward_quant(_dev_rows(fwd["gate_up"], Mt), _dev_rows(dh_o, Mt),
+                                   _dev_rows(pf["perm_w"], Mt), E, off_d, sfo_d, dgu_codes, dgu_sf,
+                                   dgu_g, st)
     dx_perm = torch.empty((Mt, H), dtype=torch.bfloat16, device="cuda")
     M.minite_grouped_gemm_nvfp4(dgu_codes, dgu_sf, dgu_g, wguT["codes"], wguT["sf"], wguT["g"],
-                                mlp.offsets, mlp.sf_offsets, dx_perm, st)
+                                off_d, sfo_d, dx_perm, st)
     dx = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    M.minite_moe_combine(dx_perm, mlp.dest_row, dx, st)
+    M.minite_moe_combine(_dev_rows(dxp_o, Mt), np_dev(pf["dest_row"]), dx, st)
     torch.cuda.synchronize()
-    assert int(st.item()) == 0 and int(mlp.status.item()) == 0 and int(bwd.status.item()) == 0
+    assert int(st.item()) == 0 and int(bwd.status.item()) == 0
 
-    p = O.moe_permute_quant(dy, d["topk_ids"], None, E)
     check_permute(bwd, p, H)
-    off, sfo = p["expert_offsets"], p["sf_row_offsets"]
-    Mu = int(off[-1])
-    qdT = O.quantize_weights(d["w_down"], along_rows=True)
-    dh_exact, _ = O.grouped_gemm_exact(p["codes"], p["sf"], p["row_g"], qdT[0], qdT[1], qdT[3], off)
     assert_bf16_within_one_ulp(u16(dh)[:Mu], dh_exact, "dh")
-    perm_w = mlp.perm_w.cpu().numpy()
-    sb = O.swiglu_backward_quant(u16(mlp.gate_up), u16(dh), perm_w, off, sfo)
     assert np.array_equal(dgu_codes.cpu().numpy()[:Mu], sb["codes"])
     assert np.array_equal(dgu_sf.cpu().numpy()[:sb["sf_swizzled"].size], sb["sf_swizzled"])
     assert np.array_equal(dgu_g.cpu().numpy()[:Mu].view(np.uint32), sb["row_g"].view(np.uint32))
-    qguT = O.quantize_weights(d["w_gate_up"], along_rows=True)
-    dx_exact, _ = O.grouped_gemm_exact(sb["codes"], sb["sf"], sb["row_g"], qguT[0], qguT[1],
-                                       qguT[3], off)
     assert_bf16_within_one_ulp(u16(dx_perm)[:Mu], dx_exact, "dx_perm")
-    assert np.array_equal(u16(dx), O.moe_combine(u16(dx_perm), mlp.dest_row.cpu().numpy()))
+    assert np.array_equal(u16(dx), dx_o)
 
 
 # --------------------------------------------------------------------- weight gradient
 
-def _tok_sf_rows(q, C):
-    """Row-major [C, kofs[E]/16] scales of a GPU token-axis operand."""
-    K = int(q["kofs"][-1].item())
-    full = O.unswizzle_sf(q["sf"].cpu().numpy(), (C + 127) // 128 * 128, q["k_cap"] // 16)
-    return full[:C, :K // 16], full[C:, :K // 16]
-
-
 def check_token_operand(q, ref, C):
+    """A GPU token-axis operand against the oracle's: K offsets, codes and
+    global scales equal; every scale byte up to column kofs[E] / 16 equal
+    (rows past C zero), read at the layout's offsets."""
     K = int(ref["kofs"][-1])
     assert np.array_equal(q["kofs"].cpu().numpy(), ref["kofs"])
     assert np.array_equal(q["codes"].cpu().numpy()[:, :K // 2], ref["codes"])
-    rows, pad = _tok_sf_rows(q, C)
-    assert np.array_equal(rows, ref["sf"])
-    assert (pad == 0).all()
+    rp = (C + 127) // 128 * 128
+    r, col = np.meshgrid(np.arange(rp), np.arange(K // 16), indexing="ij")
+    want = np.zeros((rp, K // 16), dtype=np.uint8)
+    want[:C] = ref["sf"]
+    got = q["sf"].cpu().numpy()[O.sf_swizzle_offset(r, col, q["k_cap"] // 16)]
+    assert np.array_equal(got, want)
     assert np.array_equal(q["g"].cpu().numpy().view(np.uint32), ref["g"].view(np.uint32))
 
 
@@ -877,34 +894,44 @@ def test_weight_gradients_stagewise(T, H, I, E, k):
     token-axis NVFP4 operands. Operands bit-exact, gradients within
     2^-20 sum|ab| of the exact result."""
     d = _small_moe(T + H, T, H, I, E, k)
+    # the oracle's chain from the layer's inputs
+    fwd = O.moe_mlp_forward(d["x"], d["ids"], d["w"], E, O.quantize_weights(d["wgu"]),
+                            O.quantize_weights(d["wd"]))
+    pf = fwd["permute"]
+    off, src, perm_w = pf["expert_offsets"], pf["perm_src"], pf["perm_w"]
+    Mu = int(off[-1])
+    gu_f = O.bf16_to_f32(fwd["gate_up"])
+    h_o = O.f32_to_bf16(O.swiglu_weighted(gu_f, perm_w))
+    p_dy = O.moe_permute_quant(d["dy"], d["ids"], None, E)
+    qdT = O.quantize_weights(d["wd"], along_rows=True)
+    dh_exact, _ = O.grouped_gemm_exact(p_dy["codes"], p_dy["sf"], p_dy["row_g"], qdT[0], qdT[1],
+                                       qdT[3], off)
+    dh_o = O.f64_to_bf16(dh_exact)
+    dgu_o = O.f32_to_bf16(O.swiglu_backward(gu_f, O.bf16_to_f32(dh_o), perm_w))
+    r_dy = O.quantize_tokens_per_expert(O.bf16_to_f32(d["dy"])[src], off)
+    r_h = O.quantize_tokens_per_expert(O.bf16_to_f32(h_o), off)
+    r_dgu = O.quantize_tokens_per_expert(O.bf16_to_f32(dgu_o), off)
+    r_x = O.quantize_tokens_per_expert(O.bf16_to_f32(d["x"])[src], off)
+
+    # the GPU's stages; a stage whose input is an earlier stage's result takes
+    # the oracle's value of it
     dev = "cuda"
     x, ids, w, dy = bf16_dev(d["x"]), np_dev(d["ids"]), np_dev(d["w"]), bf16_dev(d["dy"])
-    wgu = M.quantize(bf16_dev(d["wgu"]), per_group=True)
-    _, wdT = M.quantize_dual(bf16_dev(d["wd"]))
     mlp = M.MoEMLP(T, H, I, E, k)
     Mt = T * k
     st = _status()
     mlp.permute_quant(x, ids, w)
-    M.minite_grouped_gemm_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"], wgu["sf"], wgu["g"],
-                                mlp.offsets, mlp.sf_offsets, mlp.gate_up, st)
+    gu_in, pw_in = _dev_rows(fwd["gate_up"], Mt), _dev_rows(perm_w, Mt)
     h = torch.zeros((Mt, I), dtype=torch.bfloat16, device=dev)
     h_amax = torch.full((Mt,), float("nan"), dtype=torch.float32, device=dev)
-    M.minite_swiglu_weighted_quant_keep_h(mlp.gate_up, mlp.perm_w, E, mlp.offsets, mlp.sf_offsets,
+    M.minite_swiglu_weighted_quant_keep_h(gu_in, pw_in, E, mlp.offsets, mlp.sf_offsets,
                                           mlp.h_codes, mlp.h_sf, mlp.h_g, h, st, h_amax=h_amax)
-    bwd = M.MoEMLP(T, H, I, E, k)
-    ws = torch.empty(M.minite_workspace_bytes(M.OP_COMBINE_BACKWARD_QUANT, T, H), dtype=torch.uint8,
-                     device=dev)
-    M.minite_moe_combine_backward_quant(dy, E, mlp.dest_row, mlp.offsets, mlp.sf_offsets,
-                                        mlp.perm_src, bwd.a_codes, bwd.a_sf, bwd.a_g, ws, st)
-    dh = torch.empty((Mt, I), dtype=torch.bfloat16, device=dev)
-    M.minite_grouped_gemm_nvfp4(bwd.a_codes, bwd.a_sf, bwd.a_g, wdT["codes"], wdT["sf"], wdT["g"],
-                                mlp.offsets, mlp.sf_offsets, dh, st)
     dgu_codes = torch.empty((Mt, I), dtype=torch.uint8, device=dev)
     dgu_sf = torch.empty((M.sf_bytes(Mt + 128 * E, 2 * I),), dtype=torch.uint8, device=dev)
     dgu_g = torch.empty(Mt, dtype=torch.float32, device=dev)
     dgu = torch.zeros((Mt, 2 * I), dtype=torch.bfloat16, device=dev)
     dgu_amax = torch.full((Mt,), float("nan"), dtype=torch.float32, device=dev)
-    M.minite_swiglu_backward_quant_keep(mlp.gate_up, dh, mlp.perm_w, E, mlp.offsets,
+    M.minite_swiglu_backward_quant_keep(gu_in, _dev_rows(dh_o, Mt), pw_in, E, mlp.offsets,
                                         mlp.sf_offsets, dgu_codes, dgu_sf, dgu_g, dgu, st,
                                         dgu_amax=dgu_amax)
     q_dy = M.quantize_tokens(dy, mlp.offsets, E, row_src=mlp.perm_src, m_cap=Mt)
@@ -918,23 +945,16 @@ def test_weight_gradients_stagewise(T, H, I, E, k):
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and int(mlp.status.item()) == 0
 
-    off = mlp.offsets.cpu().numpy()
-    Mu = int(off[-1])
-    src = mlp.perm_src.cpu().numpy()[:Mu]
-    perm_w = mlp.perm_w.cpu().numpy()[:Mu]
+    assert np.array_equal(mlp.offsets.cpu().numpy(), off)
+    assert np.array_equal(mlp.perm_src.cpu().numpy()[:Mu], src)
     # the kept BF16 tensors are the roundings of what the stages quantize
-    assert np.array_equal(u16(h)[:Mu], O.f32_to_bf16(O.swiglu_weighted(O.bf16_to_f32(u16(mlp.gate_up)[:Mu]), perm_w)))
-    assert np.array_equal(u16(dgu)[:Mu], O.f32_to_bf16(O.swiglu_backward(
-        O.bf16_to_f32(u16(mlp.gate_up)[:Mu]), O.bf16_to_f32(u16(dh)[:Mu]), perm_w)))
-    # the row maxima written beside them: max |row| of the kept BF16 rows, rows past Mu untouched
-    for amax, kept in ((h_amax, h), (dgu_amax, dgu)):
-        a = amax.cpu().numpy()
-        assert np.array_equal(a[:Mu], np.abs(O.bf16_to_f32(u16(kept)[:Mu])).max(axis=1))
-        assert np.isnan(a[Mu:]).all()
-    r_dy = O.quantize_tokens_per_expert(O.bf16_to_f32(d["dy"])[src], off)
-    r_h = O.quantize_tokens_per_expert(O.bf16_to_f32(u16(h)[:Mu]), off)
-    r_dgu = O.quantize_tokens_per_expert(O.bf16_to_f32(u16(dgu)[:Mu]), off)
-    r_x = O.quantize_tokens_per_expert(O.bf16_to_f32(d["x"])[src], off)
+    assert np.array_equal(u16(h)[:Mu], h_o)
+    assert np.array_equal(u16(dgu)[:Mu], dgu_o)
+    # the row maxima written beside them: max |row| of the kept rows, rows past Mu untouched
+    for amax, kept in ((h_amax, h_o), (dgu_amax, dgu_o)):
+        a_ = amax.cpu().numpy()
+        assert np.array_equal(a_[:Mu], np.abs(O.bf16_to_f32(kept)).max(axis=1))
+        assert np.isnan(a_[Mu:]).all()
     for q, r, C in ((q_dy, r_dy, H), (q_h, r_h, I), (q_dgu, r_dgu, 2 * I), (q_x, r_x, H)):
         check_token_operand(q, r, C)
     for out, ra, rb in ((dWd, r_dy, r_h), (dWgu, r_dgu, r_x)):
