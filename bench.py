@@ -4,18 +4,21 @@ One step = one pass of the whole path over one batch of the skewed-load
 Qwen3-30B-A3B-shaped layer (32768 tokens, hidden 2048, 128 experts top-8,
 intermediate 768, Zipf(1.2) expert load with empty experts):
 
-  weight quant (W_gate_up and W_down, per expert, along K)
+  weight quant (W_gate_up along K; W_down along K and along N, the dgrad
+  layout with the same global scales, from one read)
   -> permute + per-token amax + NVFP4 quant of x
   -> grouped gate_up GEMM -> weighted SwiGLU + requant -> grouped down GEMM
   -> combine
-  -> requant of W_down along N (dgrad layout, same global scales)
-  -> permute + quant of dY -> grouped dgrad GEMM.
+  -> combine backward: dY to the forward's permuted rows, quantized per token
+  -> grouped dgrad GEMM (dH).
 
 Prints one JSON line. ``value`` is tokens/s over all ranks with inputs
 resident in HBM; ``e2e`` repeats the step through the same C-ABI calls with
 inputs in pinned host memory, copied in (and y copied out) inside the timed
-region. ``--impl reference`` times the CPU oracle on a bounded sample of the
-same workload instead.
+region; ``backward`` times the rest of the NVFP4 backward beside the step
+(W_gate_up's dgrad copy, SwiGLU backward, gate_up dgrad GEMM, dX combine,
+token-axis operands, weight-gradient GEMMs). ``--impl reference`` times the
+CPU oracle on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
