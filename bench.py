@@ -209,7 +209,11 @@ class Step:
             setattr(self, n, t)
         self.mlp.y = y
 
-    def run(self, stream, events=None):
+    def run(self, stream, events=None, ready=None):
+        """Enqueue the step on `stream`. `ready`: optional CUDA events of the
+        step's input copies; the permutation waits for ready["x"] (x, ids and
+        w) and the combine backward for ready["dy"]; the weight quantization
+        needs neither (the weights are device-resident model state)."""
         M, s = self.M, stream
 
         def mark(i):
@@ -224,6 +228,8 @@ class Step:
         M.minite_quantize_nvfp4_dual(self.wd_bf, self.wd["codes"], self.wd["sf"], self.wdT["codes"],
                                      self.wdT["sf"], self.wd["g"], self.ws_q, self.status, s)
         mark(2)
+        if ready is not None:
+            s.wait_event(ready["x"])
         mlp = self.mlp
         mlp.permute_quant(self.x, self.ids, self.w, s)
         mark(3)
@@ -241,6 +247,8 @@ class Step:
         mark(6)
         M.minite_moe_combine(mlp.down, mlp.dest_row, mlp.y, self.status, s)
         mark(7)
+        if ready is not None:
+            s.wait_event(ready["dy"])
         # backward of the combine: dY to the forward's permuted rows, quantized
         b = self.bwd
         M.minite_moe_combine_backward_quant(self.dy, self.E, mlp.dest_row, mlp.offsets,
@@ -506,7 +514,9 @@ def run_gpu(args):
     # state that stays on the device between steps (an optimizer updates them
     # there), so they are not copied. Inputs and y are double-buffered on the
     # device, so the copies of step i+1 (copy stream) and the read-back of
-    # step i (a second copy stream) overlap the compute of step i.
+    # step i (a second copy stream) overlap the compute of step i; each step
+    # waits for its inputs where it first reads them (x, ids and w at the
+    # permutation, dY at the combine backward), after the weight quantization.
     e2e = None
     if not args.no_e2e:
         names = ("x", "ids", "w", "dy")
@@ -518,15 +528,18 @@ def run_gpu(args):
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = y_host.numel() * y_host.element_size()
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_in_x = [torch.cuda.Event() for _ in range(2)]  # x, ids, w of buffer b copied in
+        ev_in_dy = [torch.cuda.Event() for _ in range(2)]  # dy of buffer b copied in
         ev_done = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
 
         def copy_in(b):
             with torch.cuda.stream(s_in):
-                for n, t in host.items():
-                    bufs[b][n].copy_(t, non_blocking=True)
-                ev_in[b].record(s_in)
+                for n in ("x", "ids", "w"):
+                    bufs[b][n].copy_(host[n], non_blocking=True)
+                ev_in_x[b].record(s_in)
+                bufs[b]["dy"].copy_(host["dy"], non_blocking=True)
+                ev_in_dy[b].record(s_in)
 
         def e2e_run(n_steps):
             copy_in(0)
@@ -536,11 +549,11 @@ def run_gpu(args):
                     if i > 0:
                         s_in.wait_event(ev_done[nxt])  # step i-1 is done with buffer nxt
                     copy_in(nxt)
-                stream.wait_event(ev_in[cur])
                 if i >= 2:
                     stream.wait_event(ev_out[cur])  # y of step i-2 has been read back
                 step.bind(bufs[cur], ys[cur])
-                step.run(stream)
+                # the step waits for its inputs where it first reads them
+                step.run(stream, ready={"x": ev_in_x[cur], "dy": ev_in_dy[cur]})
                 ev_done[cur].record(stream)
                 s_out.wait_event(ev_done[cur])
                 with torch.cuda.stream(s_out):
