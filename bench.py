@@ -209,11 +209,13 @@ class Step:
             setattr(self, n, t)
         self.mlp.y = y
 
-    def run(self, stream, events=None, ready=None):
+    def run(self, stream, events=None, ready=None, y_done=None):
         """Enqueue the step on `stream`. `ready`: optional CUDA events of the
         step's input copies; the permutation waits for ready["x"] (x, ids and
         w) and the combine backward for ready["dy"]; the weight quantization
-        needs neither (the weights are device-resident model state)."""
+        needs neither (the weights are device-resident model state).
+        `y_done`: optional event recorded once y is complete (after the
+        combine), so that its read-back can overlap the rest of the step."""
         M, s = self.M, stream
 
         def mark(i):
@@ -246,6 +248,8 @@ class Step:
                                     mlp.down, self.status, s)
         mark(6)
         M.minite_moe_combine(mlp.down, mlp.dest_row, mlp.y, self.status, s)
+        if y_done is not None:
+            y_done.record(s)
         mark(7)
         if ready is not None:
             s.wait_event(ready["dy"])
@@ -532,6 +536,7 @@ def run_gpu(args):
         ev_in_dy = [torch.cuda.Event() for _ in range(2)]  # dy of buffer b copied in
         ev_done = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_y = [torch.cuda.Event() for _ in range(2)]  # y of buffer b complete
 
         def copy_in(b):
             with torch.cuda.stream(s_in):
@@ -553,9 +558,10 @@ def run_gpu(args):
                     stream.wait_event(ev_out[cur])  # y of step i-2 has been read back
                 step.bind(bufs[cur], ys[cur])
                 # the step waits for its inputs where it first reads them
-                step.run(stream, ready={"x": ev_in_x[cur], "dy": ev_in_dy[cur]})
+                step.run(stream, ready={"x": ev_in_x[cur], "dy": ev_in_dy[cur]},
+                         y_done=ev_y[cur])
                 ev_done[cur].record(stream)
-                s_out.wait_event(ev_done[cur])
+                s_out.wait_event(ev_y[cur])
                 with torch.cuda.stream(s_out):
                     y_host.copy_(ys[cur], non_blocking=True)
                     ev_out[cur].record(s_out)
