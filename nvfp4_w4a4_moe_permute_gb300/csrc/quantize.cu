@@ -10,8 +10,14 @@
 //   group_amax_kernel      per-group |x| maximum (weights), atomicMax on the
 //                          float bits (all values are >= 0, so integer order
 //                          equals float order).
-//   quantize_rows_kernel   one warp per row, blocks of 16 along the row, the
-//                          row held in registers (coalesced 16-byte loads).
+//   quantize_token_rows_kernel
+//                          one warp per row, blocks of 16 along the row, the
+//                          row held in registers between its maximum and its
+//                          encoding: per-row scales (activations) or the
+//                          group's scale (weights along K).
+//   quantize_group_blocks_kernel
+//                          the group-scaled form for rows longer than 2048: a
+//                          flat stream of 32-block chunks per warp.
 //   quantize_tiles_kernel  blocks of 16 along the rows of a group (the
 //                          transposed, dgrad-layout copy of a weight), and
 //                          optionally the forward copy from the same read:
