@@ -182,8 +182,8 @@ int minite_moe_permute_quant(const void* x, const int32_t* topk_ids, const float
 
 /*
  * minite_moe_permute_quant_noalloc -- minite_moe_permute_quant for callers
- * that cannot allocate device memory. The paper has no counterpart to this
- * entry point; it exists for deployment only.
+ * that cannot allocate device memory. The sources describe no counterpart
+ * to this entry point; it exists for deployment only.
  *
  * Same arguments, outputs and results as minite_moe_permute_quant, minus the
  * workspace: the scratch lives in a 2 MiB array inside the library's device
