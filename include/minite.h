@@ -314,8 +314,10 @@ int minite_swiglu_weighted_quant(const void* gate_up, const float* perm_w,
  * given, h_amax[m] = max |h_out[m, :]| for every row written (the row's FP32
  * maximum rounded to BF16, which is the maximum of the rounded row because
  * rounding is monotone), the per-row maxima that minite_quantize_tokens_nvfp4
- * takes instead of re-reading h. Same arguments, rules and errors otherwise;
- * h_out may not be NULL.
+ * takes instead of re-reading h: the maximum taken inside the pass that
+ * produces the values, as the miniTE report summary's "Two complementary
+ * interventions" does for the permutation and the weighted SwiGLU. Same
+ * arguments, rules and errors otherwise; h_out may not be NULL.
  */
 int minite_swiglu_weighted_quant_keep_h(const void* gate_up, const float* perm_w, int64_t M,
                                         int64_t I, int32_t E, const int32_t* expert_offsets,
