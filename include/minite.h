@@ -191,11 +191,20 @@ int minite_moe_permute_quant(const void* x, const int32_t* topk_ids, const float
  * Use it where calling cudaMalloc is not possible: a fixed memory plan, a
  * plugin that only receives its inputs and outputs, a loop that must not
  * enter the allocator. It allocates nothing and calls no allocating routine.
- *  - Limit: minite_workspace_bytes(MINITE_OP_PERMUTE_QUANT, T, H, E, k) must
- *    not exceed 2 MiB (about T*E <= 32M at k = 8); larger problems return
+ *  - Limit: the ranking scratch must fit in the 2 MiB array. It takes
+ *    4*E*ceil(T / floor(512/k)) bytes (one expert histogram per chunk of
+ *    floor(512/k) tokens) plus 4*E + 256 bytes, each part rounded up to 256
+ *    bytes (at k = 8 about T*E <= 32M). Larger problems return
  *    MINITE_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *    minite_workspace_bytes(MINITE_OP_PERMUTE_QUANT, ...) also counts the
+ *    token-order staging of the scales; when that staging does not fit in
+ *    the array as well, each token's scales are written straight to its k
+ *    rows instead, with identical results.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
+ *    The address is kept for the life of the process: after
+ *    cudaDeviceReset the library's module is reloaded elsewhere, so do not
+ *    call this entry point again in a process that reset its device.
  *  - All calls on a device share the array: calls that overlap on the GPU
  *    (different streams with no ordering between them) race. Nothing needs
  *    clearing between calls; every scratch word read is rewritten first.
@@ -507,6 +516,23 @@ const char* minite_version(void);
  */
 int minite_test_convert(const float* in, int64_t n, uint8_t* out_e2m1, uint8_t* out_e4m3,
                         float* out_exp, minite_stream_t stream);
+
+/*
+ * Test hook: digests of the element converters over every float32 bit
+ * pattern, so that a test can compare them with a CPU reference on all 2^32
+ * inputs without moving the results. Chunk c holds the patterns
+ * [c * 2^20, (c + 1) * 2^20); for each chunk in [first_chunk, first_chunk +
+ * n_chunks) this adds into digests[3 * (c - first_chunk) + j] (device,
+ * caller zeroes) the sum modulo 2^64 of SplitMix64(((pattern << 32) |
+ * result) ^ salt_j) over the chunk's finite inputs: j = 0 the E2M1 code
+ * (salt 0x243F6A8885A308D3), j = 1 the E4M3 scale code of +0 and the
+ * positive inputs (salt 0x13198A2E03707344), j = 2 the bits of the
+ * specified exponential (salt 0xA4093822299F31D0). The converters are the
+ * ones the kernels use. Returns MINITE_ERR_INVALID_ARG when the range
+ * passes chunk 4095 or n_chunks exceeds 65536.
+ */
+int minite_test_convert_digest(unsigned long long first_chunk, unsigned long long n_chunks,
+                               unsigned long long* digests, minite_stream_t stream);
 
 /*
  * Test hook: the quantizers divide a block amax by 6 with an FMA-corrected

@@ -35,6 +35,53 @@ __global__ void convert_test_kernel(const float* __restrict__ in, int64_t n,
   }
 }
 
+// SplitMix64 finaliser (Steele, Lea and Flood, 2014), for the converter digests.
+__device__ __forceinline__ unsigned long long splitmix64(unsigned long long z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Digests of the converters over chunks of 2^20 consecutive float32 bit
+// patterns: per chunk and converter, the sum modulo 2^64 of
+// splitmix64(((pattern << 32) | result) ^ salt) over the finite inputs (E4M3:
+// +0 and the positive ones). 16 blocks of 256 threads per chunk.
+constexpr int kDigestChunkBits = 20;
+constexpr int kDigestBlocksPerChunk = 16;
+__global__ void __launch_bounds__(256) convert_digest_kernel(unsigned long long first_chunk,
+                                                             unsigned long long* __restrict__ digests) {
+  const unsigned long long chunk = first_chunk + blockIdx.x / kDigestBlocksPerChunk;
+  const uint32_t per_block = (1u << kDigestChunkBits) / kDigestBlocksPerChunk;
+  const uint32_t base = static_cast<uint32_t>(chunk << kDigestChunkBits) +
+                        (blockIdx.x % kDigestBlocksPerChunk) * per_block;
+  unsigned long long d0 = 0, d1 = 0, d2 = 0;
+  for (uint32_t i = threadIdx.x; i < per_block; i += blockDim.x) {
+    const uint32_t b = base + i;
+    if ((b & 0x7F800000u) == 0x7F800000u) continue;  // inf / NaN
+    const float v = __uint_as_float(b);
+    const unsigned long long key = static_cast<unsigned long long>(b) << 32;
+    d0 += splitmix64((key | (cvt_e2m1x2(v, 0.0f) & 0xFu)) ^ 0x243F6A8885A308D3ull);
+    if (v > 0.0f || b == 0u) d1 += splitmix64((key | cvt_e4m3(v)) ^ 0x13198A2E03707344ull);
+    d2 += splitmix64((key | __float_as_uint(exp_spec(v))) ^ 0xA4093822299F31D0ull);
+  }
+  d0 = warp_sum_u64(d0);
+  d1 = warp_sum_u64(d1);
+  d2 = warp_sum_u64(d2);
+  if ((threadIdx.x & 31) == 0) {
+    unsigned long long* out = digests + 3 * (blockIdx.x / kDigestBlocksPerChunk);
+    atomicAdd(out, d0);
+    atomicAdd(out + 1, d1);
+    atomicAdd(out + 2, d2);
+  }
+}
+
 // Every non-negative finite float x: count x with div6_rn(x) != IEEE x / 6.
 __global__ void div6_exhaustive_kernel(unsigned long long* mismatches) {
   unsigned long long bad = 0;
@@ -90,6 +137,18 @@ extern "C" int minite_test_convert(const float* in, int64_t n, uint8_t* out_e2m1
   convert_test_kernel<<<static_cast<unsigned>(blocks), 256, 0,
                         reinterpret_cast<cudaStream_t>(stream)>>>(in, n, out_e2m1, out_e4m3,
                                                                   out_exp);
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
+extern "C" int minite_test_convert_digest(unsigned long long first_chunk,
+                                          unsigned long long n_chunks,
+                                          unsigned long long* digests, minite_stream_t stream) {
+  if (!digests || first_chunk + n_chunks > (1ull << (32 - kDigestChunkBits)) ||
+      n_chunks > (1ull << 16))
+    return MINITE_ERR_INVALID_ARG;
+  if (n_chunks == 0) return MINITE_OK;
+  convert_digest_kernel<<<static_cast<unsigned>(n_chunks * kDigestBlocksPerChunk), 256, 0,
+                          reinterpret_cast<cudaStream_t>(stream)>>>(first_chunk, digests);
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
 

@@ -570,7 +570,10 @@ extern "C" int minite_moe_combine_backward_quant(
 // holds it until the process exits. Its device address is looked up once
 // per device (cudaGetSymbolAddress, under a mutex) on the first call made
 // while that device is current; make that first call before capturing a
-// stream. All calls on a device share the array, so two calls whose work
+// stream. The address is kept for the life of the process, so it does not
+// survive cudaDeviceReset (which unloads the module holding the array); a
+// process that resets its device must not call this entry point again. All
+// calls on a device share the array, so two calls whose work
 // overlaps on the GPU (different streams, no ordering between them) race
 // and must not be issued. The kernels rewrite every scratch word they read
 // on each call (histogram entries, the counter and, when they fit, the

@@ -28,7 +28,7 @@ EXPORTS = [
     "minite_workspace_bytes",
     "minite_status_string", "minite_version", "minite_test_convert",
     "minite_set_wait_budget_ns", "minite_moe_permute_quant_noalloc", "minite_set_gemm_variant",
-    "minite_test_div6_exhaustive", "minite_quantize_nvfp4_dual",
+    "minite_test_div6_exhaustive", "minite_test_convert_digest", "minite_quantize_nvfp4_dual",
     "minite_moe_combine_backward_quant", "minite_quantize_tokens_nvfp4",
     "minite_swiglu_weighted_quant_keep_h", "minite_grouped_gemm_wgrad_nvfp4",
     "minite_swiglu_backward_quant_keep",
@@ -78,6 +78,7 @@ def load(path: str | None = None):
         "minite_moe_combine": [_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp],
         "minite_test_convert": [_vp, _i64, _vp, _vp, _vp, _vp],
         "minite_test_div6_exhaustive": [_vp, _vp],
+        "minite_test_convert_digest": [ctypes.c_ulonglong, ctypes.c_ulonglong, _vp, _vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -327,6 +328,13 @@ def minite_test_convert(x, out_e2m1=None, out_e4m3=None, out_exp=None, stream=No
     rc = load().minite_test_convert(_p(x), x.numel(), _p(out_e2m1), _p(out_e4m3), _p(out_exp),
                                     _s(stream))
     _check(rc, "minite_test_convert")
+
+
+def minite_test_convert_digest(first_chunk, n_chunks, digests, stream=None):
+    """Adds the device converters' digests of chunks [first_chunk, first_chunk
+    + n_chunks) of 2^20 float32 bit patterns into digests (int64 [n_chunks, 3])."""
+    rc = load().minite_test_convert_digest(first_chunk, n_chunks, _p(digests), _s(stream))
+    _check(rc, "minite_test_convert_digest")
 
 
 def minite_test_div6_exhaustive(counter, stream=None):

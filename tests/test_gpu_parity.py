@@ -11,7 +11,8 @@ import pytest
 import torch
 
 from _helpers import (assert_bf16_within_one_ulp, assert_fp32_within_bound, bf16_dev,
-                      gpu_bf16_values, np_dev, u16)
+                      np_dev, u16)
+from _stagewise import check_forward_stagewise
 from nvfp4_w4a4_moe_permute_gb300 import inputs as IN
 from nvfp4_w4a4_moe_permute_gb300 import minite as M
 from oracle import nvfp4_moe_oracle as O
@@ -84,6 +85,45 @@ def test_converters_bit_exact_over_float32_sweep():
         assert np.array_equal(e4.cpu().numpy()[pos], O.e4m3_rn_satfinite(c[pos])), "E4M3"
         got = ex.cpu().numpy().view(np.uint32)
         assert np.array_equal(got, O.exp_spec(c).view(np.uint32)), "exp_spec"
+
+
+def test_converters_bit_exact_over_every_float32():
+    """Every finite float32 input: the kernels' E2M1 and E4M3 converters and
+    the specified exponential against the oracle's. The device reduces its
+    results per chunk of 2^20 bit patterns to digests; the oracle's digests
+    come from a pool of host processes (spawned) over the same chunks. A
+    differing chunk is then compared element by element to name the input."""
+    import multiprocessing as mp
+    import os
+    import _digest as DG
+    n_chunks = 1 << (32 - DG.CHUNK_BITS)
+    dev = torch.zeros((n_chunks, 3), dtype=torch.int64, device="cuda")
+    M.minite_test_convert_digest(0, n_chunks, dev)
+    procs = max(1, min(os.cpu_count() or 1, 64))
+    parts = [list(range(i, n_chunks, procs)) for i in range(procs)]
+    with mp.get_context("spawn").Pool(procs) as pool:
+        res = pool.map(DG.chunk_digests, parts)
+    host = np.zeros((n_chunks, 3), dtype=np.uint64)
+    for part, r in zip(parts, res):
+        host[part] = np.array(r, dtype=np.uint64)
+    got = dev.cpu().numpy().view(np.uint64)
+    bad = np.nonzero((got != host).any(axis=1))[0]
+    if bad.size:
+        c = int(bad[0])
+        b = np.arange(c << DG.CHUNK_BITS, (c + 1) << DG.CHUNK_BITS, dtype=np.uint64).astype(np.uint32)
+        f = b.view(np.float32)
+        f = f[np.isfinite(f)]
+        e2 = torch.empty(f.size, dtype=torch.uint8, device="cuda")
+        e4 = torch.empty(f.size, dtype=torch.uint8, device="cuda")
+        ex = torch.empty(f.size, dtype=torch.float32, device="cuda")
+        M.minite_test_convert(np_dev(f), e2, e4, ex)
+        torch.cuda.synchronize()
+        pos = (f > 0) | ((f == 0) & ~np.signbit(f))
+        d2 = np.nonzero(e2.cpu().numpy() != O.e2m1_rn(f))[0]
+        d4 = np.nonzero(e4.cpu().numpy()[pos] != O.e4m3_rn_satfinite(f[pos]))[0]
+        dx = np.nonzero(ex.cpu().numpy().view(np.uint32) != O.exp_spec(f).view(np.uint32))[0]
+        pytest.fail(f"{bad.size} chunks differ; chunk {c}: e2m1 at {f[d2[:3]]}, "
+                    f"e4m3 at {f[pos][d4[:3]]}, exp at {f[dx[:3]]}")
 
 
 def test_division_by_six_is_exact_for_every_nonnegative_float():
@@ -621,100 +661,21 @@ def _weights(d):
 
 
 def test_mlp_tiny_stagewise_and_end_to_end():
+    """The tiny configuration through every stage, all 64 tokens: permutation
+    bit-exact, both GEMMs within one BF16 ulp of the exact product, SwiGLU
+    codes and the combine bit-exact (each stage given the oracle's input)."""
     d = IN.make_moe_inputs("tiny")
     c = d["cfg"]
     T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
     wgu, wd = _weights(d)
     mlp = M.MoEMLP(T, H, I, E, k)
-    y = mlp.forward(bf16_dev(d["x"]), np_dev(d["topk_ids"]), np_dev(d["topk_w"]), wgu, wd)
+    mlp.forward(bf16_dev(d["x"]), np_dev(d["topk_ids"]), np_dev(d["topk_w"]), wgu, wd)
     torch.cuda.synchronize()
     assert int(mlp.status.item()) == 0
-    ref = O.moe_mlp_forward(d["x"], d["topk_ids"], d["topk_w"], E,
-                            O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
-    p = ref["permute"]
-    Mu = int(p["expert_offsets"][-1])
-    check_permute(mlp, p, H)
-    gu_exact, _ = O.grouped_gemm_exact(p["codes"], p["sf"], p["row_g"],
-                                       *[O.quantize_weights(d["w_gate_up"])[i] for i in (0, 1)],
-                                       O.quantize_weights(d["w_gate_up"])[3], p["expert_offsets"])
-    assert_bf16_within_one_ulp(u16(mlp.gate_up)[:Mu], gu_exact, "gate_up")
-    yv = gpu_bf16_values(u16(y))
-    yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
-    assert np.linalg.norm(yv - yr) / np.linalg.norm(yr) < 2e-2
-
-
-def test_mlp_forward_full_size_sampled_tokens_match_oracle_chain():
-    """Full Qwen3-30B-A3B expert-MLP forward (4096 tokens). Per-token scaling
-    makes a token's output independent of the rest of the batch, so the oracle
-    runs the chain on a sample of tokens alone and the GPU's full-batch rows of
-    those tokens must agree within the chain tolerance."""
-    d = IN.make_moe_inputs("mlp")
-    c = d["cfg"]
-    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
-    wgu, wd = _weights(d)
-    mlp = M.MoEMLP(T, H, I, E, k)
-    y = mlp.forward(bf16_dev(d["x"]), np_dev(d["topk_ids"]), np_dev(d["topk_w"]), wgu, wd)
-    torch.cuda.synchronize()
-    assert int(mlp.status.item()) == 0
-    rng = np.random.default_rng(5)
-    tok = np.sort(rng.choice(T, 64, replace=False))
-    ref = O.moe_mlp_forward(d["x"][tok], d["topk_ids"][tok], d["topk_w"][tok], E,
-                            O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
-    yv = gpu_bf16_values(u16(y)[tok])
-    yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
-    rel = np.linalg.norm(yv - yr, axis=1) / np.linalg.norm(yr, axis=1)
-    assert rel.max() < 2e-2, rel.max()
-    same = (u16(y)[tok] == ref["y"]).mean()
-    assert same > 0.9, same
-
-
-def test_benchmarked_step_full_size_graph_replay_matches_oracle_on_sampled_tokens():
-    """The step the benchmark times: the skewed 32768-token layer (weight
-    quantization, permutation, both GEMMs, SwiGLU, combine, the combine
-    backward with dY quantization and the down projection's dgrad GEMM),
-    captured as one CUDA graph and replayed. Per-token scaling makes a
-    token's rows independent of the batch, so the oracle runs on sampled
-    tokens alone: their y against the oracle chain (chain tolerance), and
-    their dgrad rows dH = dY_hat W_down_hat within 1 BF16 ulp of the exact
-    product (rows located through the oracle's own permutation)."""
-    import bench
-    d = IN.make_moe_inputs("skewed")
-    c = d["cfg"]
-    T, E = c["T"], c["E"]
-    dev = torch.device("cuda", 0)
-    step = bench.Step(d, dev)
-    s = torch.cuda.current_stream(dev)
-    step.run(s)
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(s)
-    with torch.cuda.graph(graph, stream=cap):
-        step.run(torch.cuda.current_stream(dev))
-    s.wait_stream(cap)
-    for _ in range(2):
-        graph.replay()
-    torch.cuda.synchronize()
-    assert int(step.status.item()) == 0
-    rng = np.random.default_rng(11)
-    tok = np.sort(rng.choice(T, 24, replace=False))
-    # forward output of the sampled tokens
-    ref = O.moe_mlp_forward(d["x"][tok], d["topk_ids"][tok], d["topk_w"][tok], E,
-                            O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
-    yv = gpu_bf16_values(u16(step.mlp.y)[tok])
-    yr = O.bf16_to_f32(ref["y"]).astype(np.float64)
-    rel = np.linalg.norm(yv - yr, axis=1) / np.linalg.norm(yr, axis=1)
-    assert rel.max() < 2e-2, rel.max()
-    assert (u16(step.mlp.y)[tok] == ref["y"]).mean() > 0.9
-    # dgrad rows of the sampled tokens: per-token dY quantization, W_down's dgrad copy
-    pq = O.moe_permute_quant(d["dy"][tok], d["topk_ids"][tok], None, E)
-    wdT = O.quantize_weights(d["w_down"], along_rows=True)
-    dh_s, _ = O.grouped_gemm_exact(pq["codes"], pq["sf"], pq["row_g"], wdT[0], wdT[1], wdT[3],
-                                   pq["expert_offsets"])
-    full = O.moe_permute(d["topk_ids"], E)
-    gpu_rows = full["dest_row"][tok].ravel()
-    mini_rows = pq["dest_row"].ravel()
-    assert (gpu_rows >= 0).all() and (mini_rows >= 0).all()
-    assert_bf16_within_one_ulp(u16(step.dh)[gpu_rows], dh_s[mini_rows], "dH (sampled rows)")
+    wq = (O.quantize_weights(d["w_gate_up"]), O.quantize_weights(d["w_down"]))
+    ref = O.moe_mlp_forward(d["x"], d["topk_ids"], d["topk_w"], E, *wq)
+    check_permute(mlp, ref["permute"], H)
+    check_forward_stagewise(d, np.arange(T), wq, mlp, wgu, wd, mlp.status)
 
 
 def _dev_rows(a, rows, dtype=None):

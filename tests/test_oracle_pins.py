@@ -342,6 +342,116 @@ def test_grouped_gemm_brute_force_rational():
         assert np.all(bound >= np.abs(y))
 
 
+def _exact_rational_abs(a_codes, a_sf, a_g, b_codes, b_sf, b_g, off, m, n):
+    """sum_k |ahat_k * bhat_k| of output (m, n), in rational arithmetic."""
+    e = int(np.searchsorted(off, m, side="right") - 1)
+    K = a_codes.shape[1] * 2
+    qa = O.unpack_codes(a_codes[m:m + 1])[0]
+    qb = O.unpack_codes(b_codes[e][n:n + 1])[0]
+    mags = [Fraction(v).limit_denominator(4) for v in FMT["e2m1_magnitudes"]]
+    tot = Fraction(0)
+    for kk in range(K):
+        sa = Fraction(float(O.e4m3_decode(a_sf[m, kk // 16])))
+        sb = Fraction(float(O.e4m3_decode(b_sf[e][n, kk // 16])))
+        tot += mags[int(qa[kk]) & 7] * sa * mags[int(qb[kk]) & 7] * sb
+    return tot / (Fraction(float(a_g[m])) * Fraction(float(b_g[e])))
+
+
+def _f32_nearest(q: Fraction) -> float:
+    """The float32 nearest to the rational q (ties to even), by integer arithmetic."""
+    if q == 0:
+        return 0.0
+    sign = -1.0 if q < 0 else 1.0
+    q = abs(q)
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1
+    e = max(e, -126)
+    ulp = Fraction(2) ** (e - 23)
+    m = q / ulp
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * float(n * ulp)
+
+
+def _fp32_gemm_case(rng, counts, N, K):
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M = int(off[-1])
+    xa = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-4, 5, (M, 1)))).astype(np.float32)
+    ac, asf, ag = O.quantize_per_row(xa)
+    wb = (rng.standard_normal((len(counts), N, K)) * 0.05).astype(np.float32)
+    bq = [O.quantize_per_tensor(wb[e]) for e in range(len(counts))]
+    bc = np.stack([q[0] for q in bq]); bsf = np.stack([q[1] for q in bq])
+    bg = np.array([q[2] for q in bq], dtype=np.float32)
+    return ac, asf, ag, bc, bsf, bg, off
+
+
+def _fp32_accumulate_bound(K):
+    # each dequantized operand is one float32 rounding of an exact value (its
+    # product with the other: two roundings), then K products are summed in
+    # float32 in some order: at most (K + 1) further roundings per term
+    u = 2.0 ** -24
+    return (K + 2) * u * (1 + 2.0 ** -20)
+
+
+def test_grouped_gemm_fp32_accumulate_brute_force_rational():
+    """The float32-accumulate GEMM (the timed CPU baseline) lies within the
+    float32 summation bound of the exact rational result, row by row and
+    expert by expert (including empty experts)."""
+    rng = np.random.default_rng(61)
+    for trial in range(5):
+        counts = rng.integers(0, 5, int(rng.integers(1, 4)))
+        if counts.sum() == 0:
+            counts[0] = 2
+        N, K = int(rng.integers(1, 8)), 64 * int(rng.integers(1, 3))
+        ac, asf, ag, bc, bsf, bg, off = _fp32_gemm_case(rng, counts, N, K)
+        y = O.grouped_gemm_fp32_accumulate(ac, asf, ag, bc, bsf, bg, off)
+        assert y.dtype == np.float32 and y.shape == (int(off[-1]), N)
+        lim = _fp32_accumulate_bound(K)
+        for m in range(int(off[-1])):
+            for n in range(N):
+                ex = _exact_rational(ac, asf, ag, bc, bsf, bg, off, m, n)
+                ab = _exact_rational_abs(ac, asf, ag, bc, bsf, bg, off, m, n)
+                assert abs(Fraction(float(y[m, n])) - ex) <= Fraction(lim) * ab
+
+
+def test_grouped_gemm_fp32_accumulate_one_hot_weights_give_float32_dequantized_activations():
+    """One-hot weight rows of value 1 (quantized exactly: code 6, scale 448,
+    global scale 2688) make each output a single product, so the result is
+    the float32 nearest to the exact dequantized activation."""
+    rng = np.random.default_rng(62)
+    M, K, N = 12, 128, 8
+    xa = (rng.standard_normal((M, K)) * 3).astype(np.float32)
+    ac, asf, ag = O.quantize_per_row(xa)
+    cols = rng.choice(K, N, replace=False)
+    w = np.zeros((1, N, K), dtype=np.float32)
+    w[0, np.arange(N), cols] = 1.0
+    bc, bsf, _, bg = O.quantize_weights(O.f32_to_bf16(w))
+    assert bg[0] == 2688.0
+    y = O.grouped_gemm_fp32_accumulate(ac, asf, ag, bc, bsf, bg, np.array([0, M], dtype=np.int32))
+    mags = [Fraction(v).limit_denominator(4) for v in FMT["e2m1_magnitudes"]]
+    q = O.unpack_codes(ac)
+    for m in range(M):
+        for j, c in enumerate(cols):
+            v = mags[int(q[m, c]) & 7] * (-1 if int(q[m, c]) & 8 else 1)
+            xh = v * Fraction(float(O.e4m3_decode(asf[m, c // 16]))) / Fraction(float(ag[m]))
+            assert float(y[m, j]) == _f32_nearest(xh)
+
+
+def test_grouped_gemm_fp32_accumulate_within_bound_of_exact_at_larger_sizes():
+    """Several experts (one empty), K = 512: within the float32 summation bound
+    of the pinned exact grouped GEMM."""
+    rng = np.random.default_rng(63)
+    ac, asf, ag, bc, bsf, bg, off = _fp32_gemm_case(rng, [37, 0, 80, 5], 48, 512)
+    y = O.grouped_gemm_fp32_accumulate(ac, asf, ag, bc, bsf, bg, off)
+    ex, ab = O.grouped_gemm_exact(ac, asf, ag, bc, bsf, bg, off)
+    assert np.all(np.abs(y.astype(np.float64) - ex) <= _fp32_accumulate_bound(512) * ab + 1e-300)
+    # and it is not the exact result computed in float64 under another name
+    assert not np.array_equal(y.astype(np.float64), ex)
+
+
 # ---------------------------------------------------------------- weight gradient
 
 def _token_operand_case(rng, counts, C, spread=True):

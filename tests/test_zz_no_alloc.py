@@ -76,6 +76,33 @@ def test_noalloc_permute_matches_workspace_entry_point_on_consecutive_calls():
         assert int(got["status"].item()) == 0
 
 
+def test_noalloc_repeat_of_the_same_shape_with_new_routing():
+    """Two calls in a row with the same shape (100000 tokens over 128
+    experts, so the per-chunk histograms take about 0.8 MiB of the array)
+    but different routing and inputs: anything the first call left in the
+    shared array that the second call failed to rewrite would show here,
+    since the shapes do not change. Outputs start from sentinels each time."""
+    dev = torch.device("cuda:0")
+    T, H, E, k = 100000, 64, 128, 8
+    assert (1 << 19) < 4 * E * -(-T // (512 // k)) < (2 << 20)
+    for seed in (21, 22):
+        rng = np.random.default_rng(seed)
+        x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(dev).to(torch.bfloat16)
+        ids_np, w_np = IN.topk_softmax_routing(rng.standard_normal((T, E)).astype(np.float32), k)
+        ids = torch.from_numpy(ids_np).to(dev)
+        w = torch.from_numpy(w_np).to(dev)
+        ref = _outputs(T, H, E, k, dev)
+        ws = torch.empty(M.minite_workspace_bytes(M.OP_PERMUTE_QUANT, T, H, E, k),
+                         dtype=torch.uint8, device=dev)
+        _run("ws", x, ids, w, E, ref, ws)
+        got = _outputs(T, H, E, k, dev)
+        _run("noalloc", x, ids, w, E, got)
+        torch.cuda.synchronize()
+        for key in ref:
+            assert torch.equal(ref[key], got[key]), f"seed {seed}: {key} differs"
+        assert int(got["status"].item()) == 0
+
+
 def test_noalloc_scatters_scales_directly_when_token_order_staging_does_not_fit():
     """T * (H/16 + 4) bytes of token-order scales exceed the 2 MiB array here,
     so the allocation-free entry writes each token's scales straight to its
