@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD, choices=["skewed", "mlp", "gate_up", "tiny"])
     ap.add_argument("--gemm-variant", type=int, default=0,
                     help="grouped-GEMM kernel: 0 automatic, 1 single-CTA one-chunk stages,"
-                         " 2 CTA pair, 4 CTA pair two-chunk stages, 5 single-CTA two-chunk stages")
+                         " 5 single-CTA two-chunk stages, 6 CTA pair with five stages")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip timing the rest of the NVFP4 backward beside the step")

@@ -555,12 +555,12 @@ void minite_set_wait_budget_ns(uint64_t ns);
 
 /*
  * Test hook: which grouped-GEMM kernel minite_grouped_gemm_nvfp4 launches.
- * 0 = automatic (currently 5 where it applies, else 1), 1 = single-CTA kernel
- * (128 x 256 tiles), 2 = CTA-pair kernel (256 x 256 tiles on two SMs),
- * 4 = CTA-pair kernel with two-chunk stages, 5 = single-CTA kernel with
- * two-chunk stages (4 and 5: K a multiple of 256 and at most about 830
- * experts; otherwise the single-CTA kernel runs). All give identical
- * results.
+ * 0 = automatic (currently 6 where it applies, else 1), 1 = single-CTA kernel
+ * (128 x 256 tiles, one-chunk stages), 5 = single-CTA kernel with two-chunk
+ * stages (K a multiple of 256 and at most about 830 experts; otherwise the
+ * single-CTA kernel runs), 6 = CTA-pair kernel (256 x 256 tiles on the two
+ * SMs of a cluster, five stages; at most about 1000 experts). Any other value
+ * selects automatic. All give identical results.
  * Process-wide; takes effect at the next call.
  */
 void minite_set_gemm_variant(int variant);

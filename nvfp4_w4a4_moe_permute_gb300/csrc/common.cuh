@@ -479,12 +479,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One wait attempt. The thread sleeps in the hardware until the phase
+// completes or about `hint_ns` nanoseconds pass (suspend-time hint), so
+// waiting warps do not spin on the barrier word that the copy engine and the
+// tensor pipe update.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t hint_ns = 20000u) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"
-               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
   return ok != 0;
 }
 
@@ -498,11 +503,13 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // `budget_ns` passed since the wait began, or *abort became non-zero first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
                                           volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  // try_wait itself suspends the thread for a while before failing, so the
-  // abort flag and the clock are checked after every failed attempt
+  // each attempt sleeps at most min(budget, 20 us), so a short budget still
+  // runs out on time
+  const uint32_t hint = budget_ns < 20000u ? static_cast<uint32_t>(budget_ns) : 20000u;
+  if (mbar_try_wait(bar, parity, hint)) return true;
+  // the abort flag and the clock are checked after every failed attempt
   const uint64_t start = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait(bar, parity, hint)) {
     if (*abort) return false;
     if (globaltimer() - start > budget_ns) return false;
   }
@@ -677,6 +684,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
                :: "r"(cluster_addr) : "memory");
+}
+// Arrive on an mbarrier of the peer CTA with the default (release, CTA scope)
+// semantics. Used after tcgen05.wait::st / wait::ld and
+// tcgen05.fence::before_thread_sync to hand TMEM to the peer's MMA thread; a
+// cluster-scope release costs ~1.4k cycles here (it waits for this SM's
+// outstanding memory traffic), this form ~0.1k.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(cluster_addr), "r"(v) : "memory");

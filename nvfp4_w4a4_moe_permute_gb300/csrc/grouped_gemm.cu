@@ -36,15 +36,15 @@
 //    CTA records MINITE_ERR_TIMEOUT, drains its in-flight copies and MMAs,
 //    frees TMEM and exits.
 //
-// Kernels (all bit-identical; the automatic choice is the fourth where it
-// applies): grouped_gemm_kernel (above, one-chunk stages),
-// grouped_gemm_pair_kernel and grouped_gemm_pair2_kernel (256 x 256 tiles
-// with tcgen05.mma.cta_group::2 on the two SMs of a cluster, one- and
-// two-chunk stages), grouped_gemm_dc_kernel (128 x 256 tiles, two-chunk
-// stages loaded with one 3-D box per operand and scale atoms from a separate
-// producer warp). A copy instruction costs the issuing thread a roughly
-// fixed time whatever its size, so fewer, larger copies per tensor cycle
-// keep the producer ahead of the MMA.
+// Kernels (all bit-identical; the automatic choice is the third where it
+// applies): grouped_gemm_kernel (above, one-chunk stages; any K % 64 == 0),
+// grouped_gemm_dc_kernel (128 x 256 tiles, two-chunk stages loaded with one
+// 3-D box per operand and scale atoms from a separate producer warp) and
+// grouped_gemm_pair_deep_kernel (256 x 256 tiles with tcgen05.mma.cta_group::2
+// on the two SMs of a cluster, five one-chunk stages that carry their scale
+// atoms). Each SM's copy engine delivers about 100 GB/s on these operands
+// whatever the box shape, the stage count or the number of SMs loading, so
+// the loads, not the tensor pipe, set the pace of all three.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -514,56 +514,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 }
 
 // ============================================================================
-// CTA-pair kernel (cta_group::2): a cluster of two CTAs on the two SMs of a
-// TPC computes a 256 x 256 output tile with tcgen05.mma.cta_group::2
-// (M = 256: each CTA holds 128 rows of A; N = 256: each CTA holds 128 rows of
-// B), so each SM stages half the B bytes of the single-CTA kernel for the same
-// MMA work. Roles per CTA as in the single-CTA kernel; the MMA thread of the
-// even CTA issues for the pair and its commits are multicast to both CTAs'
-// barriers. Both CTAs' A/B TMA loads count on the even CTA's full barrier.
-// Each CTA's scale atoms (A: its own 128 rows; B: all 256 rows, since each
-// SM's half of the MMA reads them from its own TMEM) go to a separate ring of
-// shared-memory slots, loaded P_LEAD k-tiles ahead of the A/B tiles, so the
-// scale warps have written them into their CTA's TMEM ring before the A/B
-// data lands and their latency stays off the MMA's critical path.
+// CTA-pair building blocks (cta_group::2): a cluster of two CTAs on the two
+// SMs of a TPC computes a 256 x 256 output tile (M = 256: each CTA holds 128
+// rows of A; N = 256: each CTA holds 128 rows of B). The MMA thread of the
+// even CTA issues for the pair; both CTAs' A/B loads count on its barriers.
+// Each CTA's TMEM needs its own 128 rows' A scales and all 256 rows' B scales.
 // ============================================================================
 
-constexpr int P_STAGES = 5;                           // A/B stages
 constexpr int P_A_BYTES = 128 * BK_BYTES;             // this CTA's 128 rows of A
 constexpr int P_B_BYTES = 128 * BK_BYTES;             // this CTA's 128 rows of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;  // 32 KB, counted on the even CTA's barrier
 constexpr int P_SFA_BYTES = 4 * SF_ATOM;              // this CTA's A scales, 4 K-steps
 constexpr int P_SFB_BYTES = 8 * SF_ATOM;              // both 128-row blocks of B scales
-constexpr int P_SLOT_BYTES = P_SFA_BYTES + P_SFB_BYTES;  // 6 KB scale slot
-constexpr int P_SLOTS = 8;                            // scale slots in shared memory
-constexpr int P_LEAD = 3;                             // scale loads run this many k-tiles ahead
-constexpr int P_NSF = 5;                              // TMEM scale ring
+constexpr int P_SLOT_BYTES = P_SFA_BYTES + P_SFB_BYTES;  // 6 KB of scale atoms per chunk
 constexpr uint32_t P_SF_COLS = 16 + 32;               // A: 4 x 4, B: 4 x 8 (256 rows)
 static_assert(P_STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
-static_assert(SF_COL0 + P_NSF * P_SF_COLS <= TMEM_COLS, "TMEM budget");
-static_assert(P_LEAD < P_SLOTS, "scale lead");
 constexpr uint16_t kPairMask = 0x3;
 
 constexpr uint32_t make_idesc_pair() {
   return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
          (static_cast<uint32_t>(256 >> 4) << 24);
 }
-
-struct PSmem {
-  uint64_t full[P_STAGES];
-  uint64_t empty[P_STAGES];
-  uint64_t sfdata[P_SLOTS];
-  uint64_t sfread[P_SLOTS];
-  uint64_t sf_full[P_NSF];
-  uint64_t sf_empty[P_NSF];
-  uint64_t acc_full;
-  uint64_t acc_empty;
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort_flag;
-  int total_tiles;
-  int pad_;
-};
 
 struct PTile {
   int e, nt;
@@ -618,650 +589,12 @@ struct KIter {
   }
 };
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                         const __grid_constant__ CUtensorMap tmap_b, const Params p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* stages = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* slots = stages + P_STAGES * P_STAGE_BYTES;
-  PSmem& S = *reinterpret_cast<PSmem*>(slots + P_SLOTS * P_SLOT_BYTES);
-  int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
-  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
-  int32_t* s_sfb = s_off + (p.E + 1);                           // [E+1] sf_row_offsets / 128
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const int cid = static_cast<int>(cluster_id_x());
-  const int ncl = static_cast<int>(num_clusters_x());
-  const int KT = (p.K + 255) / 256;
-  const int KSTEPS = p.K / 64;
-  const int atoms_per_rb = p.K / 64;
-  const int n_tiles = (p.N + BN - 1) / BN;
-  const int rb_per_expert = (p.N + 127) / 128;
-  const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
-
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmap_a);
-    tma_prefetch_desc(&tmap_b);
-    for (int s = 0; s < P_STAGES; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
-    }
-    for (int s = 0; s < P_SLOTS; ++s) {
-      mbar_init(&S.sfdata[s], 1);
-      mbar_init(&S.sfread[s], 4);
-    }
-    for (int b = 0; b < P_NSF; ++b) {
-      mbar_init(&S.sf_full[b], 8);
-      mbar_init(&S.sf_empty[b], 1);
-    }
-    mbar_init(&S.acc_full, 1);
-    mbar_init(&S.acc_empty, 2 * NUM_EPI_WARPS);
-    mbar_init(&S.drain, 1);
-    S.abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
-  if (warp == 2) {
-    int carry = 0;
-    bool bad = false;
-    if (lane == 0) tiles_prefix[0] = 0;
-    for (int base = 0; base < p.E; base += 32) {
-      const int e = base + lane;
-      int cnt = 0;
-      if (e < p.E) {
-        const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
-        const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
-        s_off[e + 1] = o1;
-        s_sfb[e + 1] = s1 / 128;
-        if (e == 0) { s_off[0] = o0; s_sfb[0] = s0 / 128; }
-        cnt = o1 - o0;
-        if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
-            (e == p.E - 1 && o1 > p.M))
-          bad = true;
-        cnt = cnt > 0 ? (cnt + 255) / 256 : 0;
-      }
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (e < p.E) tiles_prefix[e + 1] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-      S.total_tiles = bad ? 0 : carry * n_tiles;
-      if (bad && blockIdx.x == 0) set_status(p.status, MINITE_ERR_INVALID_ARG);
-    }
-  }
-  // both CTAs' barriers exist and TMEM is allocated before any cross-CTA traffic
-  tc_fence_before();
-  cluster_sync_all();
-  tc_fence_after();
-
-  const uint32_t tmem = S.tmem_base;
-  const int total = S.total_tiles;
-  volatile int* abort_flag = &S.abort_flag;
-  const uint32_t peer_abort = mapa_shared(smem_u32(&S.abort_flag), rank ^ 1u);
-  const uint32_t leader_full0 = mapa_shared(smem_u32(&S.full[0]), 0);
-  const uint32_t leader_sf_full0 = mapa_shared(smem_u32(&S.sf_full[0]), 0);
-  const uint32_t leader_acc_empty = mapa_shared(smem_u32(&S.acc_empty), 0);
-  const uint64_t budget = p.budget_ns;
-  constexpr uint64_t kDrainBudget = 200000000ull;
-  auto fail = [&](int code) {
-    *abort_flag = 1;
-    st_shared_cluster(peer_abort, 1u);
-    set_status(p.status, code);
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t armed_mask = 0, armed_parity = 0;            // A/B stages
-      uint32_t slot_mask = 0, slot_parity = 0;              // scale slots
-      int stage = 0, slot = 0;
-      uint32_t phase = 0, slot_phase = 0;
-      bool ok = true;
-      KIter ab, sf;
-      ab.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
-      sf.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
-      // scale atoms of k-tile `it` into the next slot, once the scale warps
-      // have read that slot's previous contents
-      auto issue_scales = [&](const KIter& it) -> bool {
-        if (!mbar_wait(&S.sfread[slot], slot_phase ^ 1u, budget, abort_flag)) return false;
-        const PTile& tl = it.tl;
-        const int ks = min(4, KSTEPS - 4 * it.kt);
-        const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;   // this CTA's A block exists
-        const int nrb = min(2, rb_per_expert - tl.nt * 2);      // B blocks inside the weight
-        uint8_t* sSFA = slots + slot * P_SLOT_BYTES;
-        uint8_t* sSFB = sSFA + P_SFA_BYTES;
-        mbar_arrive_expect_tx(&S.sfdata[slot],
-                              static_cast<uint32_t>(ks * ((a_ok ? 1 : 0) + nrb)) * SF_ATOM);
-        if (a_ok)
-          bulk_load(sSFA,
-                    p.a_sf + (static_cast<size_t>(tl.sf_rb0 + static_cast<int>(rank)) * atoms_per_rb +
-                              4 * it.kt) * SF_ATOM,
-                    ks * SF_ATOM, &S.sfdata[slot]);
-        for (int rb = 0; rb < nrb; ++rb)
-          bulk_load(sSFB + rb * 4 * SF_ATOM,
-                    p.b_sf + tl.e * sfb_expert +
-                        (static_cast<size_t>(tl.nt * 2 + rb) * atoms_per_rb + 4 * it.kt) * SF_ATOM,
-                    ks * SF_ATOM, &S.sfdata[slot]);
-        slot_mask |= 1u << slot;
-        slot_parity = (slot_parity & ~(1u << slot)) | (slot_phase << slot);
-        if (++slot == P_SLOTS) { slot = 0; slot_phase ^= 1u; }
-        return true;
-      };
-      for (int i = 0; i < P_LEAD && sf.valid() && ok; ++i) {
-        ok = issue_scales(sf);
-        sf.advance(p);
-      }
-      while (ab.valid() && ok) {
-        if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
-        uint8_t* sA = stages + stage * P_STAGE_BYTES;
-        uint8_t* sB = sA + P_A_BYTES;
-        if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], 2 * P_STAGE_BYTES);
-        const uint32_t fb = leader_full0 + 8u * stage;
-        tma_load_2d_pair(sA, &tmap_a, fb, ab.kt * BK_BYTES, ab.tl.row0 + 128 * static_cast<int>(rank));
-        tma_load_2d_pair(sB, &tmap_b, fb, ab.kt * BK_BYTES,
-                         ab.tl.e * p.N + ab.tl.nt * BN + 128 * static_cast<int>(rank));
-        armed_mask |= 1u << stage;
-        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
-        ab.advance(p);
-        if (sf.valid()) {
-          if (!issue_scales(sf)) { ok = false; break; }
-          sf.advance(p);
-        }
-      }
-      if (!ok) fail(MINITE_ERR_TIMEOUT);
-      volatile int no_abort = 0;
-      // this CTA's scale copies count on its own barriers
-      for (int s = 0; s < P_SLOTS; ++s)
-        if (slot_mask & (1u << s))
-          mbar_wait(&S.sfdata[s], (slot_parity >> s) & 1u, kDrainBudget, &no_abort);
-      if (rank == 0) {
-        // both CTAs' A/B copies count on these barriers: all armed stages landed
-        for (int s = 0; s < P_STAGES; ++s)
-          if (armed_mask & (1u << s))
-            mbar_wait(&S.full[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
-      } else if (!ok) {
-        // this CTA's A/B copies count on the other CTA's barriers: give any
-        // copy still in flight time to land before the CTA can exit
-        const uint64_t t0 = globaltimer();
-        while (globaltimer() - t0 < 100000ull) {}
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (rank == 0 && lane == 0) {
-      constexpr uint32_t idesc = make_idesc_pair();
-      const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
-      const uint64_t bdesc0 = smem_desc(smem_u32(stages + P_A_BYTES), 16, 1024, kLayoutSwizzle128B);
-      int stage = 0, sfb = 0;
-      uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
-      bool ok = true;
-      bool issued = false;
-      for (int t = cid; t < total && ok; t += ncl) {
-        if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag) ||
-              !mbar_wait(&S.sf_full[sfb], sf_phase, budget, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const int ks = min(4, KSTEPS - 4 * kt);
-          const uint64_t soff = static_cast<uint64_t>(stage * P_STAGE_BYTES) >> 4;
-          const uint32_t sf_t = tmem + SF_COL0 + sfb * P_SF_COLS;
-          for (int s = 0; s < ks; ++s)
-            tc_mma_nvfp4_pair(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc,
-                              sf_t + 4 * s, sf_t + 16 + 8 * s, (kt | s) != 0);
-          issued = true;
-          tc_commit_pair_mc(&S.empty[stage], kPairMask);
-          tc_commit_pair_mc(&S.sf_empty[sfb], kPairMask);
-          if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
-          if (++sfb == P_NSF) { sfb = 0; sf_phase ^= 1u; }
-        }
-        if (!ok) break;
-        tc_commit_pair_mc(&S.acc_full, kPairMask);
-        acc_phase ^= 1u;
-      }
-      if (!ok) fail(MINITE_ERR_TIMEOUT);
-      if (issued) {
-        tc_commit_pair_mc(&S.drain, 0x1);
-        volatile int no_abort = 0;
-        mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
-      }
-    }
-  } else if (warp < EPI_WARP0) {
-    // ------------------------------------------------------------ scale warps
-    const int quarter = warp & 3;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    int slot = 0, sfb = 0;
-    uint32_t slot_phase = 0, sf_phase = 0;
-    bool ok = true;
-    KIter it;
-    it.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
-    while (it.valid()) {
-      const bool a_ok = static_cast<int>(rank) < it.tl.sf_rbs;
-      const int nrb = min(2, rb_per_expert - it.tl.nt * 2);
-      const int ks = min(4, KSTEPS - 4 * it.kt);
-      if (!mbar_wait(&S.sfdata[slot], slot_phase, budget, abort_flag)) ok = false;
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      const uint8_t* sSFA = slots + slot * P_SLOT_BYTES;
-      const uint8_t* sSFB = sSFA + P_SFA_BYTES;
-      // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
-      uint32_t ra[16], rbv[32];
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (a_ok && s < ks) v = lds128(sSFA + s * SF_ATOM + lane * 16);
-        ra[4 * s] = v.x; ra[4 * s + 1] = v.y; ra[4 * s + 2] = v.z; ra[4 * s + 3] = v.w;
-#pragma unroll
-        for (int rb = 0; rb < 2; ++rb) {
-          uint4 w = make_uint4(0, 0, 0, 0);
-          if (rb < nrb && s < ks) w = lds128(sSFB + (rb * 4 + s) * SF_ATOM + lane * 16);
-          const int c = 8 * s + 4 * rb;
-          rbv[c] = w.x; rbv[c + 1] = w.y; rbv[c + 2] = w.z; rbv[c + 3] = w.w;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.sfread[slot]);
-      if (++slot == P_SLOTS) { slot = 0; slot_phase ^= 1u; }
-      if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag)) ok = false;
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      const uint32_t col = tmem + lane_base + SF_COL0 + sfb * P_SF_COLS;
-      tmem_st_16cols(col, ra);
-      tmem_st_16cols(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[0]));
-      tmem_st_16cols(col + 32, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[16]));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_sf_full0 + 8u * sfb);
-      if (++sfb == P_NSF) { sfb = 0; sf_phase ^= 1u; }
-      it.advance(p);
-    }
-    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
-    const int cb = (warp - EPI_WARP0) >> 2;
-    const int r_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int t = cid; t < total; t += ncl) {
-      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, s_off, s_sfb, p);
-      const bool valid = r_in_tile < tl.rows;
-      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
-      float scale = 0.0f;
-      if (valid) scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
-      if (!mbar_wait(&S.acc_full, acc_phase, budget, abort_flag)) ok = false;
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      acc_phase ^= 1u;
-      tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * EPI_COLS;
-      epilogue_slice(p, tbase, valid, row, tl.nt * BN + cb * EPI_COLS, scale,
-                     [&] { mbar_arrive_cluster(leader_acc_empty); });
-    }
-    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
-  }
-
-  // no cross-CTA traffic may target a CTA that has left: both wait here, then
-  // free the pair's TMEM together
-  tc_fence_before();
-  cluster_sync_all();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
-}
-
-// ============================================================================
-// CTA-pair kernel with two-chunk stages. Each TMA copy instruction costs the
-// issuing thread a roughly fixed time, whatever its size, so a stage covers
-// two 128-byte K chunks (K = 512, eight pair MMAs, 1024 tensor cycles) and
-// is loaded with one 3-D box per operand: a box {128 bytes, 128 rows, 2
-// chunks} lands as two consecutive 128-byte-swizzled chunk tiles. Per stage
-// and CTA that is two A/B copies from warp 0 and three scale copies (A: 8
-// atoms of its 128 rows; B: 8 atoms of each of the two 128-row blocks, all
-// contiguous) from a separate scale-producer warp, into two 12 KB slots.
-// MMA, scale-warp and epilogue roles are those of the CTA-pair kernel, with
-// the scale warps walking a slot chunk by chunk into the per-chunk TMEM ring.
-// ============================================================================
-
 constexpr int Q_CH = 2;                                  // 128-byte K chunks per stage
-constexpr int Q_STAGES = 3;
-constexpr int Q_A_BYTES = Q_CH * 128 * BK_BYTES;         // 32 KB: this CTA's 128 rows of A
-constexpr int Q_B_BYTES = Q_CH * 128 * BK_BYTES;         // 32 KB: this CTA's 128 rows of B
-constexpr int Q_STAGE_BYTES = Q_A_BYTES + Q_B_BYTES;     // 64 KB, counted on the even CTA
-constexpr int Q_SFA_BYTES = 4 * Q_CH * SF_ATOM;          // 4 KB: 8 k-steps of this CTA's A scales
+constexpr int Q_SFA_BYTES = 4 * Q_CH * SF_ATOM;          // 4 KB: 8 k-steps of A scales
 constexpr int Q_SFB_BYTES = 2 * 4 * Q_CH * SF_ATOM;      // 8 KB: 8 k-steps of both B blocks
 constexpr int Q_SLOT_BYTES = Q_SFA_BYTES + Q_SFB_BYTES;  // 12 KB
-constexpr int Q_SLOTS = 2;
-constexpr int Q_NSF = 5;                                 // TMEM scale ring (per chunk)
 constexpr int Q_SF_WARP = NUM_WARPS;                     // the scale-slot producer warp
 constexpr int Q_THREADS = (NUM_WARPS + 1) * 32;
-static_assert(Q_STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
-static_assert(SF_COL0 + Q_NSF * P_SF_COLS <= TMEM_COLS, "TMEM budget");
-
-
-struct QSmem {
-  uint64_t full[Q_STAGES];
-  uint64_t empty[Q_STAGES];
-  uint64_t sfdata[Q_SLOTS];
-  uint64_t sfread[Q_SLOTS];
-  uint64_t sfready[Q_SLOTS];
-  uint64_t sf_empty[Q_NSF];
-  uint64_t acc_full;
-  uint64_t acc_empty;
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort_flag;
-  int total_tiles;
-  int pad_;
-};
-
-// The CTA-pair kernel with two-chunk stages. Its scale factors reach TMEM by
-// tcgen05.cp.cta_group::2 (each CTA's shared memory into its own TMEM),
-// issued by the leader's MMA thread right before the MMAs that read them:
-// 12 copies per chunk, 4 atoms of this CTA's A rows and 8 of B's two 128-row
-// blocks (the single-CTA kernels use scale warps and tcgen05.st instead).
-// Each CTA's scale producer fills its own slot with bulk copies; a relay
-// thread in each CTA forwards the slot's completion to the leader; the
-// leader's commits free the A/B stages and the slots of both CTAs.
-__global__ void __maxnreg__(80)
-grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                          const __grid_constant__ CUtensorMap tmap_b, const Params p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* stages = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* slots = stages + Q_STAGES * Q_STAGE_BYTES;
-  QSmem& S = *reinterpret_cast<QSmem*>(slots + Q_SLOTS * Q_SLOT_BYTES);
-  int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
-  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
-  int32_t* s_sfb = s_off + (p.E + 1);                           // [E+1] sf_row_offsets / 128
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const int cid = static_cast<int>(cluster_id_x());
-  const int ncl = static_cast<int>(num_clusters_x());
-  const int KT = (p.K + 255) / 256;        // 128-byte chunks per tile
-  const int KD = (KT + Q_CH - 1) / Q_CH;   // stages per tile
-  const int KSTEPS = p.K / 64;
-  const int atoms_per_rb = p.K / 64;
-  const int n_tiles = (p.N + BN - 1) / BN;
-  const int rb_per_expert = (p.N + 127) / 128;
-  const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
-
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmap_a);
-    tma_prefetch_desc(&tmap_b);
-    for (int s = 0; s < Q_STAGES; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
-    }
-    for (int s = 0; s < Q_SLOTS; ++s) {
-      mbar_init(&S.sfdata[s], 1);   // this CTA's scale copies
-      mbar_init(&S.sfread[s], 1);   // the leader's commit: both CTAs' copies consumed
-      mbar_init(&S.sfready[s], 2);  // leader: both CTAs' relays
-    }
-    for (int b = 0; b < Q_NSF; ++b) mbar_init(&S.sf_empty[b], 1);
-    mbar_init(&S.acc_full, 1);
-    mbar_init(&S.acc_empty, 2 * NUM_EPI_WARPS);
-    mbar_init(&S.drain, 1);
-    S.abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
-  if (warp == 2) {
-    int carry = 0;
-    bool bad = false;
-    if (lane == 0) tiles_prefix[0] = 0;
-    for (int base = 0; base < p.E; base += 32) {
-      const int e = base + lane;
-      int cnt = 0;
-      if (e < p.E) {
-        const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
-        const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
-        s_off[e + 1] = o1;
-        s_sfb[e + 1] = s1 / 128;
-        if (e == 0) { s_off[0] = o0; s_sfb[0] = s0 / 128; }
-        cnt = o1 - o0;
-        if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
-            (e == p.E - 1 && o1 > p.M))
-          bad = true;
-        cnt = cnt > 0 ? (cnt + 255) / 256 : 0;
-      }
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (e < p.E) tiles_prefix[e + 1] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-      S.total_tiles = bad ? 0 : carry * n_tiles;
-      if (bad && blockIdx.x == 0) set_status(p.status, MINITE_ERR_INVALID_ARG);
-    }
-  }
-  // both CTAs' barriers exist and TMEM is allocated before any cross-CTA traffic
-  tc_fence_before();
-  cluster_sync_all();
-  tc_fence_after();
-
-  const uint32_t tmem = S.tmem_base;
-  const int total = S.total_tiles;
-  volatile int* abort_flag = &S.abort_flag;
-  const uint32_t peer_abort = mapa_shared(smem_u32(&S.abort_flag), rank ^ 1u);
-  const uint32_t leader_full0 = mapa_shared(smem_u32(&S.full[0]), 0);
-  const uint32_t leader_sfready0 = mapa_shared(smem_u32(&S.sfready[0]), 0);
-  const uint32_t leader_acc_empty = mapa_shared(smem_u32(&S.acc_empty), 0);
-  const uint64_t budget = p.budget_ns;
-  constexpr uint64_t kDrainBudget = 200000000ull;
-  auto fail = [&](int code) {
-    *abort_flag = 1;
-    st_shared_cluster(peer_abort, 1u);
-    set_status(p.status, code);
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ A/B producer
-    if (lane == 0) {
-      uint32_t armed_mask = 0, armed_parity = 0;
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      KIter it;
-      it.start(cid, ncl, total, KD, n_tiles, tiles_prefix, s_off, s_sfb, p);
-      while (it.valid()) {
-        if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
-        uint8_t* sA = stages + stage * Q_STAGE_BYTES;
-        uint8_t* sB = sA + Q_A_BYTES;
-        if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], 2 * Q_STAGE_BYTES);
-        const uint32_t fb = leader_full0 + 8u * stage;
-        tma_load_3d_pair(sA, &tmap_a, fb, 0, it.tl.row0 + 128 * static_cast<int>(rank),
-                         Q_CH * it.kt);
-        tma_load_3d_pair(sB, &tmap_b, fb, 0,
-                         it.tl.e * p.N + it.tl.nt * BN + 128 * static_cast<int>(rank),
-                         Q_CH * it.kt);
-        armed_mask |= 1u << stage;
-        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == Q_STAGES) { stage = 0; phase ^= 1u; }
-        it.advance(p);
-      }
-      if (!ok) fail(MINITE_ERR_TIMEOUT);
-      volatile int no_abort = 0;
-      if (rank == 0) {
-        // both CTAs' A/B copies count on these barriers: all armed stages landed
-        for (int s = 0; s < Q_STAGES; ++s)
-          if (armed_mask & (1u << s))
-            mbar_wait(&S.full[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
-      } else if (!ok) {
-        // this CTA's copies count on the other CTA's barriers: give any copy
-        // still in flight time to land before the CTA can exit
-        const uint64_t t0 = globaltimer();
-        while (globaltimer() - t0 < 100000ull) {}
-      }
-    }
-  } else if (warp == Q_SF_WARP) {
-    // ------------------------------------------------------------ scale-slot producer
-    if (lane == 0) {
-      uint32_t slot_mask = 0, slot_parity = 0;
-      int slot = 0;
-      uint32_t slot_phase = 0;
-      bool ok = true;
-      KIter it;
-      it.start(cid, ncl, total, KD, n_tiles, tiles_prefix, s_off, s_sfb, p);
-      while (it.valid()) {
-        if (!mbar_wait(&S.sfread[slot], slot_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
-        const PTile& tl = it.tl;
-        const int na = min(4 * Q_CH, KSTEPS - 4 * Q_CH * it.kt);   // atoms (k-steps) in this stage
-        const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;     // this CTA's A block exists
-        const int nrb = min(2, rb_per_expert - tl.nt * 2);        // B blocks inside the weight
-        uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
-        uint8_t* sSFB = sSFA + Q_SFA_BYTES;
-        mbar_arrive_expect_tx(&S.sfdata[slot],
-                              static_cast<uint32_t>(na * ((a_ok ? 1 : 0) + nrb)) * SF_ATOM);
-        if (a_ok)
-          bulk_load(sSFA,
-                    p.a_sf + (static_cast<size_t>(tl.sf_rb0 + static_cast<int>(rank)) * atoms_per_rb +
-                              4 * Q_CH * it.kt) * SF_ATOM,
-                    na * SF_ATOM, &S.sfdata[slot]);
-        for (int rb = 0; rb < nrb; ++rb)
-          bulk_load(sSFB + rb * 4 * Q_CH * SF_ATOM,
-                    p.b_sf + tl.e * sfb_expert +
-                        (static_cast<size_t>(tl.nt * 2 + rb) * atoms_per_rb + 4 * Q_CH * it.kt) *
-                            SF_ATOM,
-                    na * SF_ATOM, &S.sfdata[slot]);
-        slot_mask |= 1u << slot;
-        slot_parity = (slot_parity & ~(1u << slot)) | (slot_phase << slot);
-        if (++slot == Q_SLOTS) { slot = 0; slot_phase ^= 1u; }
-        it.advance(p);
-      }
-      if (!ok) fail(MINITE_ERR_TIMEOUT);
-      // this CTA's scale copies count on its own barriers
-      volatile int no_abort = 0;
-      for (int s = 0; s < Q_SLOTS; ++s)
-        if (slot_mask & (1u << s))
-          mbar_wait(&S.sfdata[s], (slot_parity >> s) & 1u, kDrainBudget, &no_abort);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (rank == 0 && lane == 0) {
-      constexpr uint32_t idesc = make_idesc_pair();
-      const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
-      const uint64_t bdesc0 = smem_desc(smem_u32(stages + Q_A_BYTES), 16, 1024, kLayoutSwizzle128B);
-      int stage = 0, sfb = 0, slot = 0;
-      uint32_t phase = 0, sf_phase = 0, slot_phase = 0, acc_phase = 0;
-      bool ok = true;
-      bool issued = false;
-      for (int t = cid; t < total && ok; t += ncl) {
-        if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        for (int kd = 0; kd < KD && ok; ++kd) {
-          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&S.sfready[slot], slot_phase, budget, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint8_t* sSFA = slots + slot * Q_SLOT_BYTES;
-          const uint8_t* sSFB = sSFA + Q_SFA_BYTES;
-          const int nch = min(Q_CH, KT - Q_CH * kd);
-          for (int c = 0; c < nch; ++c) {
-            // the ring entry's previous MMAs have completed
-            if (!mbar_wait(&S.sf_empty[sfb], sf_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            const int kt = Q_CH * kd + c;
-            const int ks = min(4, KSTEPS - 4 * kt);
-            const uint64_t soff =
-                static_cast<uint64_t>(stage * Q_STAGE_BYTES + c * 128 * BK_BYTES) >> 4;
-            const uint32_t sf_t = tmem + SF_COL0 + sfb * P_SF_COLS;
-            for (int s = 0; s < ks; ++s) {
-              // scale atoms of k-step s: this CTA's A rows, then B's two 128-row blocks
-              tc_cp_sf_pair(sf_t + 4 * s,
-                            smem_desc(smem_u32(sSFA + (4 * c + s) * SF_ATOM), 0, 128, kLayoutNone));
-              tc_cp_sf_pair(sf_t + 16 + 8 * s,
-                            smem_desc(smem_u32(sSFB + (4 * c + s) * SF_ATOM), 0, 128, kLayoutNone));
-              tc_cp_sf_pair(sf_t + 16 + 8 * s + 4,
-                            smem_desc(smem_u32(sSFB + (4 * Q_CH + 4 * c + s) * SF_ATOM), 0, 128,
-                                      kLayoutNone));
-            }
-            for (int s = 0; s < ks; ++s)
-              tc_mma_nvfp4_pair(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc,
-                                sf_t + 4 * s, sf_t + 16 + 8 * s, (kt | s) != 0);
-            issued = true;
-            tc_commit_pair_mc(&S.sf_empty[sfb], 0x1);
-            if (++sfb == Q_NSF) { sfb = 0; sf_phase ^= 1u; }
-          }
-          if (!ok) break;
-          tc_commit_pair_mc(&S.empty[stage], kPairMask);
-          tc_commit_pair_mc(&S.sfread[slot], kPairMask);  // both CTAs' slots consumed
-          if (++stage == Q_STAGES) { stage = 0; phase ^= 1u; }
-          if (++slot == Q_SLOTS) { slot = 0; slot_phase ^= 1u; }
-        }
-        if (!ok) break;
-        tc_commit_pair_mc(&S.acc_full, kPairMask);
-        acc_phase ^= 1u;
-      }
-      if (!ok) fail(MINITE_ERR_TIMEOUT);
-      if (issued) {
-        tc_commit_pair_mc(&S.drain, 0x1);
-        volatile int no_abort = 0;
-        mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
-      }
-    }
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ relay: slot filled -> leader
-    if (lane == 0) {
-      int slot = 0;
-      uint32_t slot_phase = 0;
-      bool ok = true;
-      KIter it;
-      it.start(cid, ncl, total, KD, n_tiles, tiles_prefix, s_off, s_sfb, p);
-      while (it.valid()) {
-        if (!mbar_wait(&S.sfdata[slot], slot_phase, budget, abort_flag)) { ok = false; break; }
-        mbar_arrive_cluster(leader_sfready0 + 8u * slot);
-        if (++slot == Q_SLOTS) { slot = 0; slot_phase ^= 1u; }
-        it.advance(p);
-      }
-      if (!ok) fail(MINITE_ERR_TIMEOUT);
-    }
-  } else if (warp < EPI_WARP0) {
-    // warps 3..5 have no role in this kernel
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
-    const int cb = (warp - EPI_WARP0) >> 2;
-    const int r_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int t = cid; t < total; t += ncl) {
-      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, s_off, s_sfb, p);
-      const bool valid = r_in_tile < tl.rows;
-      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
-      float scale = 0.0f;
-      if (valid) scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
-      if (!mbar_wait(&S.acc_full, acc_phase, budget, abort_flag)) ok = false;
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      acc_phase ^= 1u;
-      tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * EPI_COLS;
-      epilogue_slice(p, tbase, valid, row, tl.nt * BN + cb * EPI_COLS, scale,
-                     [&] { mbar_arrive_cluster(leader_acc_empty); });
-    }
-    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
-  }
-
-  // no cross-CTA traffic may target a CTA that has left: both wait here, then
-  // free the pair's TMEM together
-  tc_fence_before();
-  cluster_sync_all();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
-}
 
 // ============================================================================
 // Single-CTA kernel with two-chunk stages: the 128 x 256 tile of the
@@ -1637,6 +970,354 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ============================================================================
+// CTA-pair kernel with a deep operand pipeline (default for the forward and
+// dgrad GEMMs). The pair's two SMs compute a 256 x 256 tile with
+// tcgen05.mma.cta_group::2: each CTA holds 128 rows of A and 128 of the 256
+// B rows, so an SM streams 32 KB of operands per 128-byte K chunk instead of
+// the 48 KB of a single-CTA 128 x 256 tile (64 instead of 96 bytes per
+// tensor cycle). A chunk's scale atoms travel in the same pipeline stage as
+// its A/B tiles and are written to the TMEM slot of that stage, so the stage
+// count (five) is also the scale look-ahead, and a stage's MMA commit frees
+// its shared memory and its TMEM scale slot at once. Copy instructions are
+// split between two producer threads (A/B tiles; scale atoms) so that
+// neither issues more than three per chunk.
+//
+// Per chunk and stage s:
+//   warp 0 (each CTA): waits empty[s]; two TMA boxes (A rows, B rows) whose
+//     bytes count on the leader's full[s] (the leader arms it for both CTAs).
+//   warp 22 (each CTA): waits empty[s]; bulk copies of this CTA's A atoms and
+//     both 128-row blocks of B atoms, counted on its own sfdata[s].
+//   warps 2..5 (each CTA): wait sfdata[s]; write the atoms into TMEM slot s
+//     (tcgen05.st, replicated into the four lane quarters); arrive on the
+//     leader's sf_full[s] (eight arrivals: four warps per CTA).
+//   warp 1 of the leader: waits full[s] and sf_full[s]; four pair MMAs;
+//     commits empty[s] to both CTAs.
+//   warps 6..21 (each CTA): after the tile's last commit (acc_full), drain
+//     the 128 x 256 accumulator of this CTA's rows, arrive on the leader's
+//     acc_empty (32 arrivals), then scale, convert and store.
+// ============================================================================
+
+constexpr int R_STAGES = 5;
+constexpr int R_AB_BYTES = P_STAGE_BYTES;   // 32 KB: this CTA's A and B rows of one chunk
+constexpr int R_SF_BYTES = P_SLOT_BYTES;    // 6 KB: this CTA's A atoms, both B blocks' atoms
+constexpr int R_SF_WARP = NUM_WARPS;        // warp 22: scale-copy producer
+constexpr int R_THREADS = (NUM_WARPS + 1) * 32;
+static_assert(SF_COL0 + R_STAGES * P_SF_COLS <= TMEM_COLS, "TMEM budget");
+static_assert(R_SF_BYTES % 16 == 0, "bulk copy alignment");
+
+struct RSmem {
+  uint64_t full[R_STAGES];     // leader: both CTAs' A/B bytes of the stage
+  uint64_t empty[R_STAGES];    // both CTAs: the stage's MMAs completed
+  uint64_t sfdata[R_STAGES];   // both CTAs: this CTA's scale bytes of the stage
+  uint64_t sf_full[R_STAGES];  // leader: both CTAs' scale warps filled TMEM slot s
+  uint64_t acc_full;           // both CTAs: the tile's MMAs completed
+  uint64_t acc_empty;          // leader: every epilogue warp of both CTAs drained
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_tiles;
+  int pad_;
+};
+
+__global__ void __maxnreg__(80)
+grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                              const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sf_area = stages + R_STAGES * R_AB_BYTES;
+  RSmem& S = *reinterpret_cast<RSmem*>(sf_area + R_STAGES * R_SF_BYTES);
+  int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
+  int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
+  int32_t* s_sfb = s_off + (p.E + 1);                           // [E+1] sf_row_offsets / 128
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(num_clusters_x());
+  const int KT = (p.K + 255) / 256;
+  const int KSTEPS = p.K / 64;
+  const int atoms_per_rb = p.K / 64;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int rb_per_expert = (p.N + 127) / 128;
+  const size_t sfb_expert = static_cast<size_t>(rb_per_expert) * atoms_per_rb * SF_ATOM;
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    for (int s = 0; s < R_STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+      mbar_init(&S.sfdata[s], 1);
+      mbar_init(&S.sf_full[s], 8);
+    }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, 2 * NUM_EPI_WARPS);
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
+  // everything above touches only this CTA's shared memory and TMEM
+  pdl_wait();
+  if (warp == 2) {
+    // 256-row m-block prefix over experts, validating the device offsets
+    int carry = 0;
+    bool bad = false;
+    if (lane == 0) tiles_prefix[0] = 0;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      int cnt = 0;
+      if (e < p.E) {
+        const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
+        const int s0 = __ldg(p.sf_offsets + e), s1 = __ldg(p.sf_offsets + e + 1);
+        s_off[e + 1] = o1;
+        s_sfb[e + 1] = s1 / 128;
+        if (e == 0) { s_off[0] = o0; s_sfb[0] = s0 / 128; }
+        cnt = o1 - o0;
+        if (cnt < 0 || s1 - s0 != ((cnt + 127) & ~127) || (e == 0 && (o0 != 0 || s0 != 0)) ||
+            (e == p.E - 1 && o1 > p.M))
+          bad = true;
+        cnt = cnt > 0 ? (cnt + 255) / 256 : 0;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (e < p.E) tiles_prefix[e + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      S.total_tiles = bad ? 0 : carry * n_tiles;
+      if (bad && blockIdx.x == 0) set_status(p.status, MINITE_ERR_INVALID_ARG);
+    }
+  }
+  // both CTAs' barriers exist and TMEM is allocated before any cross-CTA traffic
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+
+  const uint32_t tmem = S.tmem_base;
+  const int total = S.total_tiles;
+  volatile int* abort_flag = &S.abort_flag;
+  const uint32_t peer_abort = mapa_shared(smem_u32(&S.abort_flag), rank ^ 1u);
+  const uint32_t leader_full0 = mapa_shared(smem_u32(&S.full[0]), 0);
+  const uint32_t leader_sf_full0 = mapa_shared(smem_u32(&S.sf_full[0]), 0);
+  const uint32_t leader_acc_empty = mapa_shared(smem_u32(&S.acc_empty), 0);
+  const uint64_t budget = p.budget_ns;
+  constexpr uint64_t kDrainBudget = 200000000ull;
+  auto fail = [&](int code) {
+    *abort_flag = 1;
+    st_shared_cluster(peer_abort, 1u);
+    set_status(p.status, code);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ A/B producer
+    if (lane == 0) {
+      uint32_t armed_mask = 0, armed_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      KIter it;
+      it.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      while (it.valid()) {
+        if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        uint8_t* sA = stages + stage * R_AB_BYTES;
+        uint8_t* sB = sA + P_A_BYTES;
+        if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], 2 * R_AB_BYTES);
+        const uint32_t fb = leader_full0 + 8u * stage;
+        tma_load_2d_pair(sA, &tmap_a, fb, it.kt * BK_BYTES,
+                         it.tl.row0 + 128 * static_cast<int>(rank));
+        tma_load_2d_pair(sB, &tmap_b, fb, it.kt * BK_BYTES,
+                         it.tl.e * p.N + it.tl.nt * BN + 128 * static_cast<int>(rank));
+        armed_mask |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
+        it.advance(p);
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      volatile int no_abort = 0;
+      if (rank == 0) {
+        // both CTAs' A/B copies count on these barriers: all armed stages landed
+        for (int s = 0; s < R_STAGES; ++s)
+          if (armed_mask & (1u << s))
+            mbar_wait(&S.full[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
+      } else if (!ok) {
+        // this CTA's copies count on the other CTA's barriers: give any copy
+        // still in flight time to land before the CTA can exit
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {}
+      }
+    }
+  } else if (warp == R_SF_WARP) {
+    // ------------------------------------------------------------ scale-copy producer
+    if (lane == 0) {
+      uint32_t armed_mask = 0, armed_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      KIter it;
+      it.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      while (it.valid()) {
+        if (!mbar_wait(&S.empty[stage], phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        const PTile& tl = it.tl;
+        const int ks = min(4, KSTEPS - 4 * it.kt);
+        const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;   // this CTA's A block exists
+        const int nrb = min(2, rb_per_expert - tl.nt * 2);      // B blocks inside the weight
+        uint8_t* sSFA = sf_area + stage * R_SF_BYTES;
+        uint8_t* sSFB = sSFA + P_SFA_BYTES;
+        mbar_arrive_expect_tx(&S.sfdata[stage],
+                              static_cast<uint32_t>(ks * ((a_ok ? 1 : 0) + nrb)) * SF_ATOM);
+        if (a_ok)
+          bulk_load(sSFA,
+                    p.a_sf + (static_cast<size_t>(tl.sf_rb0 + static_cast<int>(rank)) * atoms_per_rb +
+                              4 * it.kt) * SF_ATOM,
+                    ks * SF_ATOM, &S.sfdata[stage]);
+        for (int rb = 0; rb < nrb; ++rb)
+          bulk_load(sSFB + rb * 4 * SF_ATOM,
+                    p.b_sf + tl.e * sfb_expert +
+                        (static_cast<size_t>(tl.nt * 2 + rb) * atoms_per_rb + 4 * it.kt) * SF_ATOM,
+                    ks * SF_ATOM, &S.sfdata[stage]);
+        armed_mask |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
+        it.advance(p);
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      // this CTA's scale copies count on its own barriers
+      volatile int no_abort = 0;
+      for (int s = 0; s < R_STAGES; ++s)
+        if (armed_mask & (1u << s))
+          mbar_wait(&S.sfdata[s], (armed_parity >> s) & 1u, kDrainBudget, &no_abort);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = make_idesc_pair();
+      const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t bdesc0 = smem_desc(smem_u32(stages + P_A_BYTES), 16, 1024, kLayoutSwizzle128B);
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int t = cid; t < total && ok; t += ncl) {
+        if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag) ||
+              !mbar_wait(&S.sf_full[stage], phase, budget, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const int ks = min(4, KSTEPS - 4 * kt);
+          const uint64_t soff = static_cast<uint64_t>(stage * R_AB_BYTES) >> 4;
+          const uint32_t sf_t = tmem + SF_COL0 + stage * P_SF_COLS;
+          for (int s = 0; s < ks; ++s)
+            tc_mma_nvfp4_pair(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc,
+                              sf_t + 4 * s, sf_t + 16 + 8 * s, (kt | s) != 0);
+          issued = true;
+          tc_commit_pair_mc(&S.empty[stage], kPairMask);
+          if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&S.acc_full, kPairMask);
+        acc_phase ^= 1u;
+      }
+      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      if (issued) {
+        tc_commit_pair_mc(&S.drain, 0x1);
+        volatile int no_abort = 0;
+        mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
+      }
+    }
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------------------------------------ scale warps
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    KIter it;
+    it.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
+    while (it.valid()) {
+      const bool a_ok = static_cast<int>(rank) < it.tl.sf_rbs;
+      const int nrb = min(2, rb_per_expert - it.tl.nt * 2);
+      const int ks = min(4, KSTEPS - 4 * it.kt);
+      if (!mbar_wait(&S.sfdata[stage], phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const uint8_t* sSFA = sf_area + stage * R_SF_BYTES;
+      const uint8_t* sSFB = sSFA + P_SFA_BYTES;
+      // lane i of every quarter holds atom row i: the scales of rows i, i+32, i+64, i+96
+      uint32_t ra[16], rbv[32];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (a_ok && s < ks) v = lds128(sSFA + s * SF_ATOM + lane * 16);
+        ra[4 * s] = v.x; ra[4 * s + 1] = v.y; ra[4 * s + 2] = v.z; ra[4 * s + 3] = v.w;
+#pragma unroll
+        for (int rb = 0; rb < 2; ++rb) {
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (rb < nrb && s < ks) w = lds128(sSFB + (rb * 4 + s) * SF_ATOM + lane * 16);
+          const int c = 8 * s + 4 * rb;
+          rbv[c] = w.x; rbv[c + 1] = w.y; rbv[c + 2] = w.z; rbv[c + 3] = w.w;
+        }
+      }
+      // TMEM slot `stage` is free: its previous chunk's MMAs completed before
+      // the scale producer could refill this stage (both wait on empty[stage])
+      const uint32_t col = tmem + lane_base + SF_COL0 + stage * P_SF_COLS;
+      tmem_st_16cols(col, ra);
+      tmem_st_16cols(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[0]));
+      tmem_st_16cols(col + 32, *reinterpret_cast<const uint32_t(*)[16]>(&rbv[16]));
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(&S.sf_full[stage]);
+        else mbar_arrive_remote(leader_sf_full0 + 8u * stage);
+      }
+      if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
+      it.advance(p);
+    }
+    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  } else if (warp < EPI_WARP0 + NUM_EPI_WARPS) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int cb = (warp - EPI_WARP0) >> 2;
+    const int r_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = cid; t < total; t += ncl) {
+      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      const bool valid = r_in_tile < tl.rows;
+      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
+      float scale = 0.0f;
+      if (valid) scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
+      if (!mbar_wait(&S.acc_full, acc_phase, budget, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      acc_phase ^= 1u;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * EPI_COLS;
+      epilogue_slice(p, tbase, valid, row, tl.nt * BN + cb * EPI_COLS, scale,
+                     [&] {
+                       if (rank == 0) mbar_arrive(&S.acc_empty);
+                       else mbar_arrive_remote(leader_acc_empty);
+                     });
+    }
+    if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  }
+
+  // no cross-CTA traffic may target a CTA that has left: both wait here, then
+  // free the pair's TMEM together
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
+}
+
 }  // namespace gemm
 
 // ---------------------------------------------------------------- host side
@@ -1693,6 +1374,58 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t ro
 
 }  // namespace
 
+namespace {
+
+// Clusters of two CTAs of `kernel` that can be resident at once on the
+// current device (queried once per device and kernel).
+template <typename Kernel>
+int resident_pairs(Kernel kernel, int threads, size_t smem) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int v = cache[dev].load();
+  if (v > 0) return v;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * static_cast<unsigned>(num_sms() / 2));
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) return 0;
+  if (n > num_sms() / 2) n = num_sms() / 2;
+  cache[dev].store(n);
+  return n;
+}
+
+// Launch `pairs` clusters of two CTAs with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pair_pdl(void (*kernel)(KArgs...), int pairs, int threads, size_t smem,
+                            cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace
+
 uint64_t wait_budget_ns() {
   const uint64_t v = g_budget_ns.load();
   return v ? v : 2000000000ull;
@@ -1705,7 +1438,7 @@ using namespace minite;
 extern "C" void minite_set_wait_budget_ns(uint64_t ns) { g_budget_ns.store(ns); }
 
 extern "C" void minite_set_gemm_variant(int variant) {
-  g_gemm_variant.store(variant >= 1 && variant <= 5 && variant != 3 ? variant : 0);
+  g_gemm_variant.store(variant == 1 || variant == 5 || variant == 6 ? variant : 0);
 }
 
 extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
@@ -1727,27 +1460,24 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
   if (!aligned(a_codes, 128) || !aligned(b_codes, 128) || !aligned(a_sf, 16) ||
       !aligned(b_sf, 16) || !aligned(out, 32))
     return MINITE_ERR_INVALID_ARG;
-  // automatic choice: the single-CTA kernel (measured faster on every shape so far)
-  // automatic choice: the single-CTA kernel with two-chunk stages where it
-  // applies (measured fastest on the MoE shapes), else the single-CTA kernel
+  // automatic choice: the CTA-pair kernel (measured fastest on the MoE
+  // shapes: gate_up 0.445 against 0.457 ms, dgrad 0.232 against 0.234 ms, down
+  // even), else the single-CTA kernels
   int variant = g_gemm_variant.load();
-  if (variant == 0) variant = 5;
-  const size_t q_smem = 1024 + Q_STAGES * Q_STAGE_BYTES + Q_SLOTS * Q_SLOT_BYTES + sizeof(QSmem) +
-                        3 * (E + 1) * sizeof(int32_t);
+  if (variant == 0) variant = 6;
   const size_t d_smem = 1024 + D_STAGES * D_STAGE_BYTES + D_SLOTS * Q_SLOT_BYTES + sizeof(DSmem) +
                         2 * (E + 1) * sizeof(int32_t);
-  // the two-chunk kernels read whole 128-byte chunks of every row
-  if (variant == 4 && (K % 256 != 0 || q_smem > 232448)) variant = 1;
+  // the two-chunk kernel reads whole 128-byte chunks of every row
   if (variant == 5 && (K % 256 != 0 || d_smem > 232448)) variant = 1;
+  const size_t r_smem = 1024 + R_STAGES * (R_AB_BYTES + R_SF_BYTES) + sizeof(RSmem) +
+                        3 * (E + 1) * sizeof(int32_t);
+  if (variant == 6 && r_smem > 232448) variant = 1;
   CUtensorMap ta, tb;
-  if (variant == 4) {
-    if (!make_map3(&ta, a_codes, K / 2, M_total, 128) || !make_map3(&tb, b_codes, K / 2, N * E, 128))
-      return MINITE_ERR_CUDA;
-  } else if (variant == 5) {
+  if (variant == 5) {
     if (!make_map3(&ta, a_codes, K / 2, M_total, BM) || !make_map3(&tb, b_codes, K / 2, N * E, BN))
       return MINITE_ERR_CUDA;
   } else {
-    const uint32_t b_box = variant == 2 ? 128u : static_cast<uint32_t>(BN);
+    const uint32_t b_box = variant == 6 ? 128u : static_cast<uint32_t>(BN);
     if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, N * E, b_box))
       return MINITE_ERR_CUDA;
   }
@@ -1796,59 +1526,23 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     if (launch_pdl(grouped_gemm_dc_kernel<false>, dim3(grid), dim3(Q_THREADS), d_smem, s, ta, tb,
                    p) != cudaSuccess)
       return MINITE_ERR_CUDA;
-  } else if (variant == 4) {
+  } else if (variant == 6) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-      attr_err = cudaFuncSetAttribute(grouped_gemm_pair2_kernel,
+      attr_err = cudaFuncSetAttribute(grouped_gemm_pair_deep_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     });
     if (attr_err != cudaSuccess) return MINITE_ERR_CUDA;
-    // one CTA per SM in clusters of two, never more pairs than pair tiles
+    // one CTA per SM in clusters of two: as many pairs as can be resident at
+    // once (a GPC with an odd SM count leaves one SM out), never more pairs
+    // than pair tiles
     const int64_t max_pairs = (M_total / 256 + E) * n_tiles;
-    int pairs = num_sms() / 2;
+    int pairs = resident_pairs(grouped_gemm_pair_deep_kernel, R_THREADS, r_smem);
+    if (pairs <= 0) return MINITE_ERR_CUDA;
     if (max_pairs < pairs) pairs = static_cast<int>(max_pairs);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    cfg.blockDim = dim3(Q_THREADS);
-    cfg.dynamicSmemBytes = q_smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair2_kernel, ta, tb, p) != cudaSuccess)
-      return MINITE_ERR_CUDA;
-  } else {
-    const size_t smem = 1024 + P_STAGES * P_STAGE_BYTES + P_SLOTS * P_SLOT_BYTES + sizeof(PSmem) +
-                        3 * (E + 1) * sizeof(int32_t);
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-      attr_err = cudaFuncSetAttribute(grouped_gemm_pair_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    });
-    if (attr_err != cudaSuccess || smem > 232448) return MINITE_ERR_CUDA;
-    // one CTA per SM in clusters of two, never more pairs than pair tiles
-    const int64_t max_pairs = (M_total / 256 + E) * n_tiles;
-    int pairs = num_sms() / 2;
-    if (max_pairs < pairs) pairs = static_cast<int>(max_pairs);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, ta, tb, p) != cudaSuccess)
+    if (launch_pair_pdl(grouped_gemm_pair_deep_kernel, pairs, R_THREADS, r_smem, s, ta, tb, p) !=
+        cudaSuccess)
       return MINITE_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;

@@ -37,7 +37,7 @@ def _automatic_gemm_variant():
     M.minite_set_gemm_variant(0)
 
 
-VARIANTS = [1, 2, 4, 5]  # single-CTA, CTA-pair, and both with two-chunk stages
+VARIANTS = [1, 5, 6]  # single-CTA one- and two-chunk stages, deep-pipeline CTA pair
 
 
 def _status():
