@@ -54,8 +54,12 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches only (default: the step replayed as one CUDA graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=16)
-    ap.add_argument("--cpu-sample-experts", type=int, default=2)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4096,
+                    help="reference arm: tokens of the workload's batch each oracle step runs on")
+    ap.add_argument("--cpu-baseline-reps", type=int, default=2)
+    ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration measurements")
     return ap.parse_args()
 
 
@@ -128,6 +132,20 @@ def measured_peaks():
 
 
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rates
+
+
+def percentile(xs, q):
+    """q-th percentile (linear interpolation) of a non-empty list."""
+    s = sorted(xs)
+    pos = (len(s) - 1) * q / 100.0
+    lo = int(pos)
+    hi = min(lo + 1, len(s) - 1)
+    return s[lo] + (s[hi] - s[lo]) * (pos - lo)
+
+
+# grouped-GEMM kernel of each `--gemm-variant` (0 = automatic = 6 on these shapes)
+GEMM_KERNELS = {1: "grouped_gemm_kernel", 5: "grouped_gemm_dc_kernel",
+                6: "grouped_gemm_pair_deep_kernel"}
 
 
 def max_over_ranks(values, device):
@@ -402,6 +420,125 @@ class Step:
         )
 
 
+def time_launches(fn, stream, reps=10, warmup=3, flush=None):
+    """Per-launch times (ms) of `fn()` on `stream` from CUDA events recorded
+    around each launch; `flush` (a device buffer larger than L2) is
+    overwritten before every launch so that no launch finds its inputs in L2."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    out = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+def per_config(dev, fp4_peak, peaks):
+    """The other configurations the metric names, each timed per launch with
+    L2 flushed before every launch (median, p10, p90 of 10):
+      dense: the single NVFP4 GEMM M=4096 N=1536 K=2048 (A quantized per row,
+        1% outlier channels x20), BF16 and FP32 output, and the quantization
+        of A;
+      gate_up layer (4096 tokens, 128 experts top-8): the permutation with
+        fused quantization and the gate_up grouped GEMM;
+      MLP forward (4096 tokens): permutation -> gate_up GEMM -> SwiGLU ->
+        down GEMM -> combine, as one timed unit (weights quantized before).
+    The gate_up layer and the MLP forward use the same seeded batch."""
+    import numpy as np
+    import torch
+
+    from nvfp4_w4a4_moe_permute_gb300 import inputs as IN
+    from nvfp4_w4a4_moe_permute_gb300 import minite as M
+    s = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    hbm = peaks["hbm"]
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def stats(ts):
+        return {"median": round(statistics.median(ts), 5), "p10": round(percentile(ts, 10), 5),
+                "p90": round(percentile(ts, 90), 5)}
+
+    out = {"peak_basis": f"FP4 {fp4_peak:.0f} TFLOP/s (measured bf16 burst x {FP4_OVER_BF16:g}),"
+                         f" HBM {hbm:.0f} GB/s (measured copy)", "l2": "flushed before every launch"}
+    # ---- dense GEMM
+    dd = IN.make_dense_inputs()
+    c = dd["cfg"]
+    Mr, N, K = c["M"], c["N"], c["K"]
+    a = bf16(dd["a"])
+    w = bf16(dd["w"][None])
+    qw = M.quantize(w, per_group=True)
+    qa = M.quantize(a)
+    torch.cuda.synchronize(dev)
+    off = torch.tensor([0, Mr], dtype=torch.int32, device=dev)
+    sfo = torch.tensor([0, (Mr + 127) // 128 * 128], dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flops = 2.0 * Mr * N * K
+    dense = {"shape": f"M={Mr} N={N} K={K}, E=1"}
+    ta = time_launches(lambda: M.quantize(a, stream=s), s, flush=flush)
+    qbytes = Mr * K * 2 + Mr * K / 2 + Mr * K / 16 + Mr * 4
+    dense["quantize_a"] = dict(stats(ta), gbs=round(qbytes / (statistics.median(ta) / 1e3) / 1e9, 1))
+    for name, dt in (("bf16_out", torch.bfloat16), ("fp32_out", torch.float32)):
+        o = torch.empty((Mr, N), dtype=dt, device=dev)
+        tg = time_launches(lambda: M.minite_grouped_gemm_nvfp4(
+            qa["codes"], qa["sf"], qa["g"], qw["codes"], qw["sf"], qw["g"], off, sfo, o, st, s),
+            s, flush=flush)
+        med = statistics.median(tg)
+        obytes = Mr * N * (2 if dt == torch.bfloat16 else 4)
+        byts = Mr * K / 2 + Mr * K / 16 + N * K / 2 + N * K / 16 + obytes
+        dense[name] = dict(stats(tg), tflops=round(flops / (med / 1e3) / 1e12, 1),
+                           frac_fp4_peak=round(flops / (med / 1e3) / 1e12 / fp4_peak, 4),
+                           attainable_tflops=round(min(fp4_peak, flops / byts * hbm / 1e3), 1))
+    assert int(st.item()) == 0
+    out["dense_gemm"] = dense
+    del a, w, qw, qa, dd
+    # ---- gate_up layer and MLP forward (one seeded batch)
+    d = IN.make_moe_inputs("mlp")
+    c = d["cfg"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    wgu = M.quantize(bf16(d["w_gate_up"]), per_group=True)
+    wd = M.quantize(bf16(d["w_down"]), per_group=True)
+    x, ids, tw = bf16(d["x"]), torch.from_numpy(d["topk_ids"]).to(dev), torch.from_numpy(d["topk_w"]).to(dev)
+    mlp = M.MoEMLP(T, H, I, E, k, dev)
+    mlp.forward(x, ids, tw, wgu, wd, s)
+    torch.cuda.synchronize(dev)
+    assert int(mlp.status.item()) == 0
+    Mu = int(mlp.offsets[-1].item())
+    tp = time_launches(lambda: mlp.permute_quant(x, ids, tw, s), s, flush=flush)
+    pbytes = T * H * 2 + T * k * 8 + Mu * (H / 2 + H / 16 + 4 + 12)
+    tgu = time_launches(lambda: M.minite_grouped_gemm_nvfp4(
+        mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"], wgu["sf"], wgu["g"], mlp.offsets,
+        mlp.sf_offsets, mlp.gate_up, mlp.status, s), s, flush=flush)
+    gfl = 2.0 * Mu * 2 * I * H
+    gbytes = Mu * H / 2 + int(mlp.sf_offsets[-1].item()) * H / 16 + E * 2 * I * H * (1 / 2 + 1 / 16) \
+        + Mu * 2 * I * 2
+    gmed = statistics.median(tgu)
+    out["gate_up_layer"] = {
+        "workload": workload_name("gate_up", c),
+        "permute_quant": dict(stats(tp), gbs=round(pbytes / (statistics.median(tp) / 1e3) / 1e9, 1),
+                              frac_hbm=round(pbytes / (statistics.median(tp) / 1e3) / 1e9 / hbm, 3)),
+        "gemm_gate_up": dict(stats(tgu), tflops=round(gfl / (gmed / 1e3) / 1e12, 1),
+                             frac_fp4_peak=round(gfl / (gmed / 1e3) / 1e12 / fp4_peak, 4),
+                             attainable_tflops=round(min(fp4_peak, gfl / gbytes * hbm / 1e3), 1),
+                             hbm_gbs=round(gbytes / (gmed / 1e3) / 1e9, 1))}
+    tf = time_launches(lambda: mlp.forward(x, ids, tw, wgu, wd, s), s, flush=flush)
+    fmed = statistics.median(tf)
+    out["mlp_forward"] = {"workload": workload_name("mlp", c), **stats(tf),
+                          "tokens_per_s": round(T / (fmed / 1e3)),
+                          "launches": 5 + 1 + 1 + 1 + 1}
+    assert int(mlp.status.item()) == 0
+    return out
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -450,6 +587,7 @@ def run_gpu(args):
     ms_eager = t0.elapsed_time(t1)
     # the same step captured once as a CUDA graph and replayed: no launch gaps
     ms_graph = None
+    step_ms_list = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps)]
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
@@ -460,14 +598,14 @@ def run_gpu(args):
         for _ in range(args.warmup):
             graph.replay()
         barrier()
-        g0 = torch.cuda.Event(enable_timing=True)
-        g1 = torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(args.steps):
+        gev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        gev[0].record(stream)
+        for i in range(args.steps):
             graph.replay()
-        g1.record(stream)
+            gev[i + 1].record(stream)
         barrier()
-        ms_graph = g0.elapsed_time(g1)
+        ms_graph = gev[0].elapsed_time(gev[-1])
+        step_ms_list = [gev[i].elapsed_time(gev[i + 1]) for i in range(args.steps)]
         assert int(step.status.item()) == 0, f"device status {int(step.status.item())}"
     clk = clocks.stop()
     ms = ms_graph if ms_graph is not None else ms_eager
@@ -584,7 +722,13 @@ def run_gpu(args):
 
     fl = step.flops()
     peaks = measured_peaks()
-    fp4_peak = peaks["bf16_sus"] * FP4_OVER_BF16
+    # each GEMM launch is timed alone (CUDA events around it), so the burst
+    # BF16 figure is the basis; the sustained one is reported beside it
+    fp4_peak = peaks["bf16"] * FP4_OVER_BF16
+    fp4_peak_sus = peaks["bf16_sus"] * FP4_OVER_BF16
+    per_cfg = None
+    if not args.no_per_config and rank == 0:
+        per_cfg = per_config(dev, fp4_peak, peaks)
     gemm_s = stage_ms["gemm_gate_up"] / 1e3
     achieved = fl["gemm_gate_up"] / gemm_s / 1e12
     # the same launch against min(FP4 peak, arithmetic intensity x HBM bandwidth)
@@ -622,20 +766,28 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (each step streams ~5 GB)",
                    "launch": "eager" if args.no_graph else "CUDA graph of the step, replayed",
                    "parallelism": f"replicas{world}"},
+        "step_ms": {"median": round(statistics.median(step_ms_list), 4),
+                    "p10": round(percentile(step_ms_list, 10), 4),
+                    "p90": round(percentile(step_ms_list, 90), 4),
+                    "of": "graph replays" if ms_graph is not None else "eager steps"},
         "gemm_gate_up_tflops": achieved,
         "gemm_gate_up_frac_fp4_peak": achieved / fp4_peak,
         "stages_ms": {s: round(v, 4) for s, v in stage_ms.items()},
         "stages_hbm_gbs": {s: round(v, 1) for s, v in hbm.items()},
-        "roofline": {"kernel": "grouped_gemm_dc_kernel (gate_up)", "bound": "tensor",
+        "roofline": {"kernel": f"{GEMM_KERNELS.get(args.gemm_variant or 6)} (gate_up)",
+                     "bound": "tensor",
                      "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp4_peak, "traffic": traffic,
-                     "peak_source": f"{peaks['source']} bf16 sustained x {FP4_OVER_BF16:g} (nominal FP4/BF16)",
+                     "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal"
+                                    f" dense FP4/BF16); the launch is timed alone",
+                     "frac_of_sustained_basis": achieved / fp4_peak_sus,
                      "algorithmic_bytes": gemm_bytes, "flop_per_byte": ai,
                      "attainable": attainable, "frac_of_attainable": achieved / attainable,
                      "achieved_hbm_gbs": gemm_bytes / gemm_s / 1e9},
         "clocks": clk,
         "gpu_launches": Step.LAUNCHES * args.steps,
         "backward": backward,
+        "per_config": per_cfg,
         "e2e": e2e,
         "cpu_baseline": None,
     }
@@ -647,75 +799,235 @@ def run_gpu(args):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+#
+# The oracle (plain NumPy) timed on the host's cores. Work is sharded by
+# expert over spawned processes (never forked from a CUDA process), each
+# driving the unchanged oracle functions for its experts: the quantization of
+# their weights and their permuted rows through the gate_up GEMM
+# (float32-accumulate variant), the weighted SwiGLU with requantization, the
+# down GEMM and, for the benchmarked step, the dgrad GEMM. The parent runs
+# the permutations and the combine. Arrays travel through .npy files in
+# shared memory. The oracle runs on a whole batch of the stated size; nothing
+# is scaled.
 
-class CpuSample:
-    """The oracle on a bounded sample of the step, scaled to one full step:
-    the per-token chain (forward + dY permute/quant + dgrad GEMM) on n_tok
-    tokens scaled by T/n_tok, plus the weight quantizations (both
-    orientations) of n_exp experts scaled by E/n_exp."""
+def cpu_info():
+    """(logical cores, CPU model string) of this host."""
+    import platform
+    model = platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return os.cpu_count() or 1, model
 
-    def __init__(self, workload: str, n_tok: int, n_exp: int):
+
+_ORC = {}
+
+
+def _orc_init(dirpath):
+    from oracle import nvfp4_moe_oracle as O
+    _ORC["O"] = O
+    _ORC["dir"] = dirpath
+
+
+def _mm(name, mode="r"):
+    import numpy as np
+    return np.load(os.path.join(_ORC["dir"], name + ".npy"), mmap_mode=mode)
+
+
+def _orc_quantize_weights(experts, dgrad):
+    """Weights of `experts`: W_gate_up and W_down along K (forward), and W_down
+    along N with the same global scales (dgrad copy) when `dgrad`."""
+    O = _ORC["O"]
+    wgu, wd = _mm("w_gate_up"), _mm("w_down")
+    out = {n: _mm(n, "r+") for n in ("gu_c", "gu_sf", "gu_g", "d_c", "d_sf", "d_g")}
+    if dgrad:
+        out.update({n: _mm(n, "r+") for n in ("dT_c", "dT_sf")})
+    for e in experts:
+        c, sf, _, g = O.quantize_weights(wgu[e:e + 1])
+        out["gu_c"][e], out["gu_sf"][e], out["gu_g"][e] = c[0], sf[0], g[0]
+        c, sf, _, g = O.quantize_weights(wd[e:e + 1])
+        out["d_c"][e], out["d_sf"][e], out["d_g"][e] = c[0], sf[0], g[0]
+        if dgrad:
+            c, sf, _, _ = O.quantize_weights(wd[e:e + 1], along_rows=True, g_in=g)
+            out["dT_c"][e], out["dT_sf"][e] = c[0], sf[0]
+    for m in out.values():
+        m.flush()
+    return len(experts)
+
+
+def _orc_expert_rows(experts, dgrad):
+    """The permuted rows of `experts` through gate_up GEMM -> BF16 -> weighted
+    SwiGLU + requant -> down GEMM -> BF16 (and dY's rows through the dgrad
+    GEMM when `dgrad`), each expert as a one-expert problem of the oracle."""
+    import numpy as np
+    O = _ORC["O"]
+    off = _mm("offsets")
+    a_c, a_sf, a_g, pw = _mm("a_c"), _mm("a_sf"), _mm("a_g"), _mm("perm_w")
+    gu_c, gu_sf, gu_g = _mm("gu_c"), _mm("gu_sf"), _mm("gu_g")
+    d_c, d_sf, d_g = _mm("d_c"), _mm("d_sf"), _mm("d_g")
+    down = _mm("down", "r+")
+    if dgrad:
+        y_c, y_sf, y_g = _mm("dy_c"), _mm("dy_sf"), _mm("dy_g")
+        dT_c, dT_sf = _mm("dT_c"), _mm("dT_sf")
+        dh = _mm("dh", "r+")
+    for e in experts:
+        a, b = int(off[e]), int(off[e + 1])
+        if a == b:
+            continue
+        o1 = np.array([0, b - a], dtype=np.int64)
+        s1 = np.array([0, (b - a + 127) // 128 * 128], dtype=np.int64)
+        gu = O.grouped_gemm_fp32_accumulate(a_c[a:b], a_sf[a:b], a_g[a:b], gu_c[e:e + 1],
+                                            gu_sf[e:e + 1], gu_g[e:e + 1], o1)
+        sw = O.swiglu_weighted_quant(O.f32_to_bf16(gu), pw[a:b], o1, s1)
+        d = O.grouped_gemm_fp32_accumulate(sw["codes"], sw["sf"], sw["row_g"], d_c[e:e + 1],
+                                           d_sf[e:e + 1], d_g[e:e + 1], o1)
+        down[a:b] = O.f32_to_bf16(d)
+        if dgrad:
+            h = O.grouped_gemm_fp32_accumulate(y_c[a:b], y_sf[a:b], y_g[a:b], dT_c[e:e + 1],
+                                               dT_sf[e:e + 1], d_g[e:e + 1], o1)
+            dh[a:b] = O.f32_to_bf16(h)
+    down.flush()
+    if dgrad:
+        dh.flush()
+    return len(experts)
+
+
+class OracleRunner:
+    """The oracle on the host's cores for one MoE workload. `tokens` selects
+    the batch (the first `tokens` tokens of the workload's seeded batch, with
+    their routing); `dgrad` adds the combine backward's dY quantization and
+    the dgrad GEMM; `weights_in_step` makes the weight quantization part of
+    each timed step (else it runs once at set-up)."""
+
+    def __init__(self, workload, tokens=None, dgrad=False, weights_in_step=False, procs=None):
+        import multiprocessing as mp
+        import tempfile
+
         import numpy as np
 
         from nvfp4_w4a4_moe_permute_gb300 import inputs as IN
         from oracle import nvfp4_moe_oracle as O
-        self.O = O
+        self.O, self.np = O, np
         d = IN.make_moe_inputs(workload, seed=0)
         c = d["cfg"]
-        self.T, self.E = c["T"], c["E"]
-        self.n_tok, self.n_exp = n_tok, n_exp
-        self.d = d
-        self.tok = np.arange(n_tok)
-        used = np.unique(d["topk_ids"][self.tok])
-        # untimed: quantized weights of the experts the sampled tokens reach
-        self.wgu = self._partial(d["w_gate_up"], used)
-        self.wd = self._partial(d["w_down"], used)
-        self.wdT = self._partial(d["w_down"], used, along_rows=True, g_in=self.wd[3])
+        self.cfg = c
+        T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+        self.tokens = T if tokens is None else min(int(tokens), T)
+        self.E, self.dgrad, self.weights_in_step = E, dgrad, weights_in_step
+        tok = np.arange(self.tokens)
+        self.x, self.ids, self.w = d["x"][tok], d["topk_ids"][tok], d["topk_w"][tok]
+        # the incoming gradient (workloads without one use x in its place)
+        self.dy = d.get("dy", d["x"])[tok] if dgrad else None
+        base = "/dev/shm" if os.path.isdir("/dev/shm") else None
+        self.dir = tempfile.mkdtemp(prefix="minite_oracle_", dir=base)
+        M = self.tokens * k
 
-    def _partial(self, w, used, along_rows=False, g_in=None):
-        import numpy as np
-        O = self.O
-        q = O.quantize_weights(w[used], along_rows=along_rows,
-                               g_in=None if g_in is None else g_in[used])
-        full = []
-        for a in q:
-            z = np.zeros((self.E,) + a.shape[1:], dtype=a.dtype)
-            z[used] = a
-            full.append(z)
-        return tuple(full)
+        def put(name, arr):
+            np.save(os.path.join(self.dir, name + ".npy"), arr)
 
-    def run(self):
-        O, d, tok, E = self.O, self.d, self.tok, self.E
+        def blank(name, shape, dtype):
+            np.save(os.path.join(self.dir, name + ".npy"), np.zeros(shape, dtype=dtype))
+
+        put("w_gate_up", d["w_gate_up"])
+        put("w_down", d["w_down"])
+        del d
+        blank("gu_c", (E, 2 * I, H // 2), np.uint8)
+        blank("gu_sf", (E, 2 * I, H // 16), np.uint8)
+        blank("gu_g", (E,), np.float32)
+        blank("d_c", (E, H, I // 2), np.uint8)
+        blank("d_sf", (E, H, I // 16), np.uint8)
+        blank("d_g", (E,), np.float32)
+        if dgrad:
+            blank("dT_c", (E, I, H // 2), np.uint8)
+            blank("dT_sf", (E, I, H // 16), np.uint8)
+        blank("down", (M, H), np.uint16)
+        if dgrad:
+            blank("dh", (M, I), np.uint16)
+        self.procs = max(1, min(procs or os.cpu_count() or 1, 64))
+        # experts spread over processes by their row counts plus a fixed cost
+        # per expert (its weights are dequantized once per GEMM)
+        rows = np.bincount(self.ids.ravel(), minlength=E)
+        cost = rows / max(1.0, rows.mean()) + 1.0
+        loads = [0.0] * self.procs
+        self.shards = [[] for _ in range(self.procs)]
+        for e in np.argsort(-cost, kind="stable"):
+            i = int(np.argmin(loads))
+            self.shards[i].append(int(e))
+            loads[i] += float(cost[e])
+        self.shards = [s for s in self.shards if s]
+        ctx = mp.get_context("spawn")
+        self.pool = ctx.Pool(len(self.shards), initializer=_orc_init, initargs=(self.dir,))
+        if not weights_in_step:
+            self.pool.starmap(_orc_quantize_weights, [(s, dgrad) for s in self.shards])
+
+    def step(self):
+        """One timed pass; returns seconds."""
+        O, np = self.O, self.np
         t0 = time.perf_counter()
-        O.quantize_weights(d["w_gate_up"][:self.n_exp])
-        wd = O.quantize_weights(d["w_down"][:self.n_exp])
-        O.quantize_weights(d["w_down"][:self.n_exp], along_rows=True, g_in=wd[3])
-        t_w = time.perf_counter() - t0
-        t1 = time.perf_counter()
-        O.moe_mlp_forward(d["x"][tok], d["topk_ids"][tok], d["topk_w"][tok], E, self.wgu, self.wd)
-        dy = d.get("dy", d["x"])
-        pq = O.moe_permute_quant(dy[tok], d["topk_ids"][tok], None, E)
-        dh, _ = O.grouped_gemm_exact(pq["codes"], pq["sf"], pq["row_g"], self.wdT[0], self.wdT[1],
-                                     self.wdT[3], pq["expert_offsets"])
-        O.f64_to_bf16(dh)
-        t_chain = time.perf_counter() - t1
-        step_s = t_w * E / self.n_exp + t_chain * self.T / self.n_tok
-        return step_s, dict(weights_s=round(t_w, 3), chain_s=round(t_chain, 3))
+        if self.weights_in_step:
+            self.pool.starmap(_orc_quantize_weights, [(s, self.dgrad) for s in self.shards])
+        pq = O.moe_permute_quant(self.x, self.ids, self.w, self.E)
+        for name, arr in (("a_c", pq["codes"]), ("a_sf", pq["sf"]), ("a_g", pq["row_g"]),
+                          ("perm_w", pq["perm_w"]),
+                          ("offsets", np.asarray(pq["expert_offsets"], dtype=np.int64))):
+            np.save(os.path.join(self.dir, name + ".npy"), arr)
+        if self.dgrad:
+            pd = O.moe_permute_quant(self.dy, self.ids, None, self.E)
+            for name, arr in (("dy_c", pd["codes"]), ("dy_sf", pd["sf"]), ("dy_g", pd["row_g"])):
+                np.save(os.path.join(self.dir, name + ".npy"), arr)
+        self.pool.starmap(_orc_expert_rows, [(s, self.dgrad) for s in self.shards])
+        down = np.load(os.path.join(self.dir, "down.npy"), mmap_mode="r")
+        O.moe_combine(np.asarray(down[:int(pq["expert_offsets"][-1])]), pq["dest_row"])
+        return time.perf_counter() - t0
+
+    def close(self):
+        import shutil
+        self.pool.terminate()
+        self.pool.join()
+        shutil.rmtree(self.dir, ignore_errors=True)
+
+
+def cpu_baseline_run(args):
+    """The oracle's whole 4096-token expert-MLP forward (Qwen3-30B-A3B layer:
+    permutation + quantization, gate_up GEMM, weighted SwiGLU + requant,
+    down GEMM, combine) on all host cores; one warm-up pass and
+    `--cpu-baseline-reps` timed passes. Prints one JSON object."""
+    cores, model = cpu_info()
+    r = OracleRunner("mlp", procs=cores)
+    try:
+        r.step()
+        times = [r.step() for _ in range(max(1, args.cpu_baseline_reps))]
+    finally:
+        r.close()
+    s = statistics.median(times)
+    print(json.dumps({"cpu_baseline": {
+        "value": r.tokens / s, "unit": "tokens/s", "cores": len(r.shards), "cpu_model": model,
+        "kind": "oracle", "extrapolated": False, "seconds": round(s, 3),
+        "workload": workload_name("mlp", r.cfg),
+        "sample": f"the whole {r.tokens}-token expert-MLP forward (not scaled), weights quantized"
+                  f" beforehand; GEMMs in the oracle's float32-accumulate variant; expert shards"
+                  f" over {len(r.shards)} spawned processes; median of {len(times)} passes"}}),
+          flush=True)
 
 
 def cpu_baseline_subprocess(args):
-    """Run the oracle in a fresh single-threaded process (spawned, never forked
-    from this CUDA process) and return its cpu_baseline object."""
+    """Run cpu_baseline_run in a fresh process with no GPU visible (its process
+    pool is spawned there, never forked from this CUDA process)."""
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--steps", "1",
-           "--warmup", "0", "--workload", args.workload, "--cpu-sample-tokens",
-           str(args.cpu_sample_tokens), "--cpu-sample-experts", str(args.cpu_sample_experts)]
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only",
+           "--cpu-baseline-reps", str(args.cpu_baseline_reps)]
     try:
         r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
-                           timeout=900)
+                           timeout=1200)
         line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1]
         return json.loads(line)["cpu_baseline"]
     except Exception as exc:  # noqa: BLE001
@@ -723,33 +1035,44 @@ def cpu_baseline_subprocess(args):
 
 
 def run_reference(args):
+    """The reference arm: the oracle timed on the host's cores on the
+    benchmark's workload and step (weight quantization of every expert, the
+    permutation, both GEMMs, SwiGLU, combine, dY quantization and the dgrad
+    GEMM), on a batch of the first `--cpu-sample-tokens` tokens of the seeded
+    batch (with their routing) so that a step takes seconds, not minutes.
+    Every step is measured; nothing is scaled."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ.setdefault(v, "1")
-    smp = CpuSample(args.workload, args.cpu_sample_tokens, args.cpu_sample_experts)
-    T = smp.T
-    times = []
-    parts = None
-    for i in range(args.warmup + args.steps):
-        step_s, parts = smp.run()
-        if i >= args.warmup:
-            times.append(step_s)
+        os.environ[v] = "1"
+    cores, model = cpu_info()
+    r = OracleRunner(args.workload, tokens=args.cpu_sample_tokens, dgrad=True,
+                     weights_in_step=True, procs=cores)
+    try:
+        for _ in range(args.warmup):
+            r.step()
+        times = [r.step() for _ in range(args.steps)]
+    finally:
+        r.close()
     ms = statistics.mean(times) * 1e3
-    value = T / (ms / 1e3)
-    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
-    sample = (f"oracle chain (fwd + dY permute/quant + dgrad GEMM) on {args.cpu_sample_tokens} "
-              f"tokens scaled x{T // args.cpu_sample_tokens}, plus weight quantization of "
-              f"{args.cpu_sample_experts} experts scaled to all; last sample {parts}")
+    value = r.tokens / (ms / 1e3)
+    T = r.cfg["T"]
+    sample = (f"the benchmark's step on the first {r.tokens} of the workload's {T} tokens (their"
+              f" routing; every expert's weights quantized each step, as in the GPU step), not"
+              f" scaled; expert shards over {len(r.shards)} spawned processes")
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "fp32 quantization / fp64 GEMM (numpy)",
+           "vs_baseline": None,
+           "dtype": "fp32 quantization, float32-accumulate GEMMs (numpy)",
            "data": "synthetic (seeded numpy)", "impl": "reference",
-           "config": {"workload": workload_name(args.workload, smp.d["cfg"]),
-                      "parallelism": "host cpu"},
-           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
-                            "kind": "oracle", "sample": sample},
+           "config": {"workload": workload_name(args.workload, r.cfg),
+                      "batch_tokens": r.tokens, "parallelism": f"host cpu, {len(r.shards)} processes"},
+           "step_seconds": {"median": round(statistics.median(times), 3),
+                            "min": round(min(times), 3), "max": round(max(times), 3)},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": len(r.shards),
+                            "cpu_model": model, "kind": "oracle", "extrapolated": False,
+                            "seconds": round(ms / 1e3, 3), "sample": sample},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -757,7 +1080,9 @@ def run_reference(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.cpu_baseline_only:
+        cpu_baseline_run(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

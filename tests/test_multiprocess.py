@@ -64,7 +64,7 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
            "reference", "--gpus", "2", "--steps", "1", "--warmup", "0", "--workload", "tiny",
-           "--cpu-sample-tokens", "4", "--cpu-sample-experts", "1"]
+           "--cpu-sample-tokens", "4"]
     env = dict(os.environ, OMP_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
     r = subprocess.run(cmd, cwd=ROOT, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
                        text=True, timeout=600)
