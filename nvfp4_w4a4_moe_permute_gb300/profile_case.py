@@ -9,6 +9,7 @@ command line, without the memory of a whole layer step.
     python -m nvfp4_w4a4_moe_permute_gb300.profile_case quantize_weights \\
         --experts 16 --rows 1536 --cols 2048 [--dual]
     python -m nvfp4_w4a4_moe_permute_gb300.profile_case permute_swiglu --tokens 16384
+    python -m nvfp4_w4a4_moe_permute_gb300.profile_case gemm --tokens 8192 --gemm gate_up
 
 Expert sizes follow a Zipf(1.5) draw over the experts (a skewed routing);
 every call's device status is checked at the end.
@@ -104,8 +105,45 @@ def permute_swiglu(args, M, dev, status):
         status.fill_(int(mlp.status.item()))
 
 
+def gemm(args, M, dev, status):
+    """One grouped GEMM of the skewed layer's recipe at `--tokens` tokens
+    (`--gemm` gate_up, down or dgrad), its operands produced by the library
+    (weight quantization, permutation, SwiGLU), with the automatic kernel or
+    `--variant`. The GEMM is the last `--reps` launches."""
+    from . import inputs as IN
+    d = IN.make_moe_inputs("skewed", seed=args.seed, T=args.tokens)
+    c = d["cfg"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    wgu = M.quantize(bf16(d["w_gate_up"]), per_group=True)
+    wd_bf = bf16(d["w_down"])
+    wd = M.quantize(wd_bf, per_group=True)
+    wdT = M.quantize(wd_bf, per_group=True, along_rows=True, g_in=wd["g"])
+    mlp = M.MoEMLP(T, H, I, E, k)
+    mlp.status = status
+    mlp.forward(bf16(d["x"]), torch.from_numpy(d["topk_ids"]).to(dev),
+                torch.from_numpy(d["topk_w"]).to(dev), wgu, wd)
+    dh = torch.empty((T * k, I), dtype=torch.bfloat16, device=dev)
+    M.minite_set_gemm_variant(args.variant)
+    for _ in range(args.reps):
+        if args.gemm == "gate_up":
+            M.minite_grouped_gemm_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"], wgu["sf"],
+                                        wgu["g"], mlp.offsets, mlp.sf_offsets, mlp.gate_up, status)
+        elif args.gemm == "down":
+            M.minite_grouped_gemm_nvfp4(mlp.h_codes, mlp.h_sf, mlp.h_g, wd["codes"], wd["sf"],
+                                        wd["g"], mlp.offsets, mlp.sf_offsets, mlp.down, status)
+        else:
+            # the permuted x stands in for the permuted dY (same layout and routing)
+            M.minite_grouped_gemm_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wdT["codes"], wdT["sf"],
+                                        wd["g"], mlp.offsets, mlp.sf_offsets, dh, status)
+    M.minite_set_gemm_variant(0)
+
+
 CASES = {"quantize_tokens": quantize_tokens, "quantize_weights": quantize_weights,
-         "permute_swiglu": permute_swiglu}
+         "permute_swiglu": permute_swiglu, "gemm": gemm}
 
 
 def main(argv=None) -> int:
@@ -117,6 +155,8 @@ def main(argv=None) -> int:
     ap.add_argument("--tokens", type=int, default=16384, help="permute_swiglu: tokens")
     ap.add_argument("--gather", type=int, default=0, help="source rows (0: rows in place)")
     ap.add_argument("--dual", action="store_true", help="weights: both orientations")
+    ap.add_argument("--gemm", default="gate_up", choices=["gate_up", "down", "dgrad"])
+    ap.add_argument("--variant", type=int, default=0, help="gemm: grouped-GEMM kernel (0 automatic)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--seed", type=int, default=0)
     args = ap.parse_args(argv)
