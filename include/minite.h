@@ -68,7 +68,8 @@ enum {
   MINITE_OP_QUANTIZE = 0,
   MINITE_OP_PERMUTE_QUANT = 1,
   MINITE_OP_COMBINE_BACKWARD_QUANT = 2,
-  MINITE_OP_QUANTIZE_TOKENS = 3
+  MINITE_OP_QUANTIZE_TOKENS = 3,
+  MINITE_OP_GATE_UP_SWIGLU = 4
 };
 
 /*
@@ -253,6 +254,56 @@ int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const
                               int64_t M_total, int64_t N, int64_t K, int32_t E,
                               void* out, int out_dtype, int32_t* status,
                               minite_stream_t stream);
+
+/*
+ * minite_gate_up_swiglu_quant_nvfp4 -- the gate_up grouped GEMM with the
+ * routing-weighted SwiGLU and the NVFP4 requantization of its result fused
+ * into the GEMM's epilogue: the gate_up product never goes through memory
+ * unless gate_up is given.
+ *
+ * Cites: "Two complementary interventions" (amax computed during weighted
+ * SwiGLU, fused scale layout) and "Diagnostic, alignement et noyaux rapides"
+ * (grouped GEMMs over experts).
+ *
+ * Bit for bit the composition
+ *   minite_grouped_gemm_nvfp4(a..., b..., N = 2I, out = BF16 gate_up)
+ *   minite_swiglu_weighted_quant(gate_up, perm_w, ...)
+ * on the same arguments: each row's gate and up values are rounded to BF16
+ * exactly as that GEMM stores them before the SwiGLU, and the row's global
+ * scale comes from the |h| maximum over all I columns.
+ *
+ * a_codes, a_sf, a_g, b_codes, b_sf, b_g, expert_offsets, sf_row_offsets,
+ * M_total, K, E: as for minite_grouped_gemm_nvfp4 with N = 2I (b_codes
+ *          [E, 2I, K/2]: gate rows [0, I), up rows [I, 2I); b_g [E]).
+ * perm_w:  device float [M_total] or NULL (weight 1).
+ * gate_up: device BF16 [M_total, 2I], 32-byte aligned, or NULL: when given it
+ *          also receives the GEMM's BF16 output (for a backward pass).
+ * h_codes, h_sf, h_g: as the codes, sf and row_g of
+ *          minite_swiglu_weighted_quant (16-byte aligned); padding rows of
+ *          each expert's scale region are zeroed.
+ * workspace: device, >= minite_workspace_bytes(MINITE_OP_GATE_UP_SWIGLU,
+ *          M_total, I, 0, 0) bytes (4 * M_total * roundup(I/128, 4)),
+ *          16-byte aligned; contents on entry are ignored (the call clears
+ *          what it uses first).
+ * Shape rules: I % 128 == 0, 128 <= I <= 8192, K % 64 == 0, 1 <= E <= 663
+ * (the kernel's shared memory, 219.2 KB + 12 (E+1) bytes, within 227 KB),
+ * M_total < 2^31; otherwise MINITE_ERR_UNSUPPORTED_SHAPE and nothing is
+ * enqueued.
+ * Device errors: invalid offsets set bit 1<<MINITE_ERR_INVALID_ARG; the
+ * I/128 tiles of a 256-row block exchange their rows' maxima through the
+ * workspace, and a wait for that exchange (like every other wait) gives up
+ * after the budget of minite_set_wait_budget_ns with bit
+ * 1<<MINITE_ERR_TIMEOUT. Calls sharing a workspace must not overlap.
+ */
+int minite_gate_up_swiglu_quant_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
+                                      const float* a_g, const uint8_t* b_codes,
+                                      const uint8_t* b_sf, const float* b_g,
+                                      const int32_t* expert_offsets,
+                                      const int32_t* sf_row_offsets, int64_t M_total, int64_t I,
+                                      int64_t K, int32_t E, const float* perm_w, void* gate_up,
+                                      uint8_t* h_codes, uint8_t* h_sf, float* h_g,
+                                      void* workspace, size_t ws_bytes, int32_t* status,
+                                      minite_stream_t stream);
 
 /*
  * minite_grouped_gemm_wgrad_nvfp4 -- weight gradient of a grouped
@@ -497,8 +548,8 @@ int minite_quantize_tokens_nvfp4(const void* x, int64_t x_rows, const int32_t* r
 /* Workspace bytes needed by `op` (MINITE_OP_QUANTIZE: a = groups;
  * MINITE_OP_PERMUTE_QUANT: a = T, b = H, E, k; MINITE_OP_COMBINE_BACKWARD_QUANT:
  * a = T, b = H; MINITE_OP_QUANTIZE_TOKENS: a = E, b = source rows when
- * they are gathered and no row maxima are passed, else 0). 0 means none
- * needed. */
+ * they are gathered and no row maxima are passed, else 0;
+ * MINITE_OP_GATE_UP_SWIGLU: a = M_total, b = I). 0 means none needed. */
 size_t minite_workspace_bytes(int op, int64_t a, int64_t b, int32_t E, int32_t k);
 
 /* Static description of a status code. */

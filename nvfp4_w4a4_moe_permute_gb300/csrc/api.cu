@@ -10,6 +10,7 @@ namespace minite {
 size_t permute_workspace_bytes(int64_t T, int64_t H, int32_t E, int32_t k);
 size_t combine_backward_workspace_bytes(int64_t T, int64_t H);
 size_t tokens_workspace_bytes(int32_t E, int64_t x_rows);
+size_t swiglu_fused_workspace_words(int64_t M, int64_t I);
 
 int num_sms() {
   static std::atomic<int> cache[64];
@@ -108,6 +109,8 @@ extern "C" size_t minite_workspace_bytes(int op, int64_t a, int64_t b, int32_t E
       return (a > 0 && b > 0) ? combine_backward_workspace_bytes(a, b) : 0;
     case MINITE_OP_QUANTIZE_TOKENS:
       return (a > 0 && a <= 1024 && b >= 0) ? tokens_workspace_bytes(static_cast<int32_t>(a), b) : 0;
+    case MINITE_OP_GATE_UP_SWIGLU:
+      return (a > 0 && b >= 128) ? swiglu_fused_workspace_words(a, b) * sizeof(uint32_t) : 0;
     default:
       return 0;
   }

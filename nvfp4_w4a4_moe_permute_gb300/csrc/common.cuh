@@ -452,6 +452,48 @@ __device__ __forceinline__ float exp_spec(float x) {
   return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(ni + 127) << 23));
 }
 
+// silu(g) = g / (1 + exp_spec(-g)), every step an IEEE float operation.
+__device__ __forceinline__ float silu_spec(float g) {
+  return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));
+}
+
+// The gates are BF16, so silu takes at most 2^16 distinct inputs: each CTA
+// tabulates silu_spec in shared memory for |g| in [2^-24, 2^8) (32 binades,
+// both signs, 32 KB) and evaluates the formula only for gates outside it.
+// Entry index: 2 * (|g| bits - bits of 2^-24) + sign.
+constexpr uint32_t kLutLo = (127u - 24u) << 7;  // BF16 bits of 2^-24
+constexpr uint32_t kLutSpan = 32u << 7;          // 4096 magnitudes per sign
+constexpr int kLutEntries = 2 * static_cast<int>(kLutSpan);
+
+__device__ __forceinline__ uint32_t lut_gate_bits(int i) {
+  return (static_cast<uint32_t>(i & 1) << 15) | (kLutLo + static_cast<uint32_t>(i >> 1));
+}
+
+__device__ inline void build_silu_lut_part(float* lut, int t, int nthreads) {
+  for (int i = t; i < kLutEntries; i += nthreads)
+    lut[i] = silu_spec(__uint_as_float(lut_gate_bits(i) << 16));
+}
+
+// A narrower table for kernels short of shared memory: |g| in [2^-16, 2^8)
+// (24 binades, 24 KB), same entry order.
+constexpr uint32_t kLut24Lo = (127u - 16u) << 7;
+constexpr uint32_t kLut24Span = 24u << 7;
+constexpr int kLut24Entries = 2 * static_cast<int>(kLut24Span);
+
+__device__ inline void build_silu_lut24_part(float* lut, int t, int nthreads) {
+  for (int i = t; i < kLut24Entries; i += nthreads)
+    lut[i] = silu_spec(__uint_as_float(
+        ((static_cast<uint32_t>(i & 1) << 15) | (kLut24Lo + static_cast<uint32_t>(i >> 1))) << 16));
+}
+
+// silu_spec of a gate that is a BF16 value (held as a float): the entry of the
+// 24-binade table where |g| lies in [2^-16, 2^8), the formula elsewhere.
+__device__ __forceinline__ float silu_bf16_lut24(const float* lut, float g) {
+  const uint32_t bits = __float_as_uint(g) >> 16;
+  const uint32_t off = (bits & 0x7FFFu) - kLut24Lo;
+  return off < kLut24Span ? lut[2 * off + (bits >> 15)] : silu_spec(g);
+}
+
 // ----------------------------------------------------------------------------
 // mbarrier / TMA / tcgen05 wrappers (inline PTX)
 // ----------------------------------------------------------------------------
@@ -627,6 +669,13 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 16-byte global store (address 16-byte aligned).
+__device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};"
+               :: "l"(ptr), "r"(a0), "r"(a1), "r"(a2), "r"(a3) : "memory");
+}
+
 // 32-byte global store (address 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void* ptr, uint32_t a0, uint32_t a1, uint32_t a2,
                                              uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
@@ -775,6 +824,48 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
+}
+
+// Warp: load 8 consecutive fp32 columns at each of two TMEM addresses of this
+// warp's 32 lanes, then wait; one statement, so that no use of the registers
+// can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_8cols_x2(uint32_t ta, uint32_t tb, uint32_t (&a)[8],
+                                                 uint32_t (&b)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]),
+        "=r"(a[7]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]),
+        "=r"(b[6]), "=r"(b[7])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// Named barrier `id` over `count` threads (whole warps).
+__device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
+// Device-scope stores and loads of global words (served by L2, not L1).
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed_gpu_v4(const uint32_t* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+// block_scale for a thread that holds its own row: the encode factor is the
+// IEEE quotient RN(g / sf) (clamped to FLT_MAX), which is what the table
+// entry scaled by a power of two gives wherever that product is a normal
+// float, and what block_scale computes below it.
+__device__ __forceinline__ BlockScale block_scale_div(float amax_b, float g) {
+  BlockScale r;
+  r.sf = cvt_e4m3(__fmul_rn(div6_rn(amax_b), g));
+  r.enc = r.sf ? fminf(__fdiv_rn(g, e4m3_value(r.sf)), kFltMax) : 0.0f;
+  return r;
 }
 
 }  // namespace minite

@@ -45,9 +45,17 @@
 // atoms). Each SM's copy engine delivers about 100 GB/s on these operands
 // whatever the box shape, the stage count or the number of SMs loading, so
 // the loads, not the tensor pipe, set the pace of all three.
+//
+// minite_gate_up_swiglu_quant_nvfp4 runs the pair kernel's second instance
+// (SWIGLU): the even CTA loads gate rows and the odd CTA the matching up
+// rows, so each accumulator holds gate and up columns of the same 128
+// intermediate columns; the epilogue applies the weighted SwiGLU and, once
+// the I/128 tiles of a 256-row block have published their rows' partial |h|
+// maxima (flagged per-row slots in a workspace), quantizes h to NVFP4.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -103,6 +111,18 @@ struct Smem {
   int pad_;
 };
 
+// Fields of the fused gate_up + weighted SwiGLU + NVFP4 epilogue (unused by
+// the plain GEMMs).
+struct SwigluParams {
+  const float* perm_w;   // [M] routing weights, or null (weight 1)
+  uint8_t* h_codes;      // [M, I/2]
+  uint8_t* h_sf;         // per-expert padded regions, kc = I/16 scale columns
+  float* h_g;            // [M]
+  uint32_t* amax;        // [M, roundup(I/128, 4)] zeroed: per row, each tile's partial |h|
+                         // maximum (float bits) with bit 31 set once written
+  int I;
+};
+
 struct Params {
   const float* a_g;
   const float* b_g;
@@ -116,6 +136,7 @@ struct Params {
   int N, K, E;        // weight gradient: K = token columns allocated per operand row
   int out_fp32;
   uint64_t budget_ns;
+  SwigluParams sw;
 };
 
 struct Tile {
@@ -1020,6 +1041,10 @@ struct RSmem {
   int pad_;
 };
 
+// 80 registers: the 23 warps spread over the SM's four sub-partitions put six
+// on one of them, and 6 x 32 x 80 = 15360 of its 16384 registers is the most
+// that fits (88 would not).
+template <bool SWIGLU>
 __global__ void __maxnreg__(80)
 grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
                               const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -1031,6 +1056,9 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
   int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
   int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
   int32_t* s_sfb = s_off + (p.E + 1);                           // [E+1] sf_row_offsets / 128
+  float* lut = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(s_sfb + (p.E + 1)) + 15) & ~uintptr_t(15));  // SWIGLU: silu table
+  float* epi_part = lut + kLut24Entries;   // SWIGLU: [2][4 quarters][4 warps][32] row partial maxima
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1060,6 +1088,7 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
+  if constexpr (SWIGLU) build_silu_lut24_part(lut, threadIdx.x, R_THREADS);
   // everything above touches only this CTA's shared memory and TMEM
   pdl_wait();
   if (warp == 2) {
@@ -1134,8 +1163,11 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint32_t fb = leader_full0 + 8u * stage;
         tma_load_2d_pair(sA, &tmap_a, fb, it.kt * BK_BYTES,
                          it.tl.row0 + 128 * static_cast<int>(rank));
-        tma_load_2d_pair(sB, &tmap_b, fb, it.kt * BK_BYTES,
-                         it.tl.e * p.N + it.tl.nt * BN + 128 * static_cast<int>(rank));
+        // SWIGLU: the even CTA loads gate rows [128 nt, +128), the odd CTA the
+        // up rows [I + 128 nt, +128) of the expert's [2I, K] weight
+        const int b_row = SWIGLU ? it.tl.e * p.N + static_cast<int>(rank) * (p.N / 2) + it.tl.nt * 128
+                                 : it.tl.e * p.N + it.tl.nt * BN + 128 * static_cast<int>(rank);
+        tma_load_2d_pair(sB, &tmap_b, fb, it.kt * BK_BYTES, b_row);
         armed_mask |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
@@ -1169,7 +1201,7 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const PTile& tl = it.tl;
         const int ks = min(4, KSTEPS - 4 * it.kt);
         const bool a_ok = static_cast<int>(rank) < tl.sf_rbs;   // this CTA's A block exists
-        const int nrb = min(2, rb_per_expert - tl.nt * 2);      // B blocks inside the weight
+        const int nrb = SWIGLU ? 2 : min(2, rb_per_expert - tl.nt * 2);  // B blocks inside the weight
         uint8_t* sSFA = sf_area + stage * R_SF_BYTES;
         uint8_t* sSFB = sSFA + P_SFA_BYTES;
         mbar_arrive_expect_tx(&S.sfdata[stage],
@@ -1179,11 +1211,14 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     p.a_sf + (static_cast<size_t>(tl.sf_rb0 + static_cast<int>(rank)) * atoms_per_rb +
                               4 * it.kt) * SF_ATOM,
                     ks * SF_ATOM, &S.sfdata[stage]);
-        for (int rb = 0; rb < nrb; ++rb)
+        for (int rb = 0; rb < nrb; ++rb) {
+          // SWIGLU: the gate block nt, then the up block I / 128 + nt
+          const int brb = SWIGLU ? (rb == 0 ? tl.nt : p.N / 256 + tl.nt) : tl.nt * 2 + rb;
           bulk_load(sSFB + rb * 4 * SF_ATOM,
                     p.b_sf + tl.e * sfb_expert +
-                        (static_cast<size_t>(tl.nt * 2 + rb) * atoms_per_rb + 4 * it.kt) * SF_ATOM,
+                        (static_cast<size_t>(brb) * atoms_per_rb + 4 * it.kt) * SF_ATOM,
                     ks * SF_ATOM, &S.sfdata[stage]);
+        }
         armed_mask |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
@@ -1245,7 +1280,7 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
     it.start(cid, ncl, total, KT, n_tiles, tiles_prefix, s_off, s_sfb, p);
     while (it.valid()) {
       const bool a_ok = static_cast<int>(rank) < it.tl.sf_rbs;
-      const int nrb = min(2, rb_per_expert - it.tl.nt * 2);
+      const int nrb = SWIGLU ? 2 : min(2, rb_per_expert - it.tl.nt * 2);
       const int ks = min(4, KSTEPS - 4 * it.kt);
       if (!mbar_wait(&S.sfdata[stage], phase, budget, abort_flag)) ok = false;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -1283,6 +1318,155 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
       it.advance(p);
     }
     if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
+  } else if (SWIGLU && warp < EPI_WARP0 + NUM_EPI_WARPS) {
+    // ------------------------------------------------------------ fused SwiGLU epilogue
+    // Warp (quarter, cb) holds TMEM lanes 32 quarter.. of this CTA: gate
+    // columns [32 cb, +32) and the matching up columns [128 + 32 cb, +32),
+    // i.e. intermediate columns 128 nt + 32 cb + [0, 32) of its row, two
+    // NVFP4 blocks. A row's global scale needs the |h| maximum over all I
+    // columns, spread over the n_tiles CTA tiles of its m-block, which
+    // n_tiles clusters run at the same time: the four warps of a quarter
+    // combine their partial maxima in shared memory, one of them publishes the
+    // CTA's value in the row's slot nt (bit 31 set marks it written; the
+    // maxima are non-negative floats), and every warp polls its rows' n_tiles
+    // slots before quantizing. A warp that hits a timeout stops working but
+    // keeps the quarter's barrier cadence, so no barrier is left waiting.
+    const int quarter = warp & 3;
+    const int cb = (warp - EPI_WARP0) >> 2;
+    const int r_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
+    const uint32_t qbar = 2 + static_cast<uint32_t>(quarter);   // named barrier of the quarter
+    const SwigluParams& sw = p.sw;
+    const int I = sw.I;
+    const int kc = I / 16;
+    const int stride = (n_tiles + 3) & ~3;                        // slot words per row
+    uint32_t acc_phase = 0;
+    int it = 0;
+    bool failed = false;
+    for (int t = cid; t < total; t += ncl, ++it) {
+      const PTile tl = decode_pair_tile(t, n_tiles, tiles_prefix, s_off, s_sfb, p);
+      const bool valid = r_in_tile < tl.rows;
+      const int64_t row = static_cast<int64_t>(tl.row0) + r_in_tile;
+      float scale = 0.0f, w = 1.0f;
+      if (valid) {
+        scale = __frcp_rn(__fmul_rn(__ldg(p.a_g + row), __ldg(p.b_g + tl.e)));
+        if (sw.perm_w) w = __ldg(sw.perm_w + row);
+      }
+      bool ok = !failed &&
+                __all_sync(0xffffffffu, mbar_wait(&S.acc_full, acc_phase, budget, abort_flag));
+      if (!ok && !failed) {
+        failed = true;
+        if (lane == 0) fail(MINITE_ERR_TIMEOUT);
+      }
+      float h[2][16];
+      float part = 0.0f;
+      if (ok) {
+        acc_phase ^= 1u;
+        tc_fence_after();
+        const uint32_t tb = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 32 * cb;
+        // 8 gate and 8 up columns at a time: the BF16 values the plain GEMM
+        // would store (kept in gate_up when asked), then h; nothing else stays
+        // live between steps, so the 80 registers hold without spilling
+        uint16_t* o = static_cast<uint16_t*>(p.out) + row * p.N + tl.nt * 128 + 32 * cb;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t rg[8], ru[8];
+          tmem_ld_8cols_x2(tb + 8 * b, tb + 128 + 8 * b, rg, ru);
+          if (b == 3) {
+            // every accumulator column this warp reads is in registers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (rank == 0) mbar_arrive(&S.acc_empty);
+              else mbar_arrive_remote(leader_acc_empty);
+            }
+          }
+          uint32_t gw[4], uw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            gw[j] = static_cast<uint32_t>(__bfloat16_as_ushort(
+                        __float2bfloat16_rn(__fmul_rn(__uint_as_float(rg[2 * j]), scale)))) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(
+                         __float2bfloat16_rn(__fmul_rn(__uint_as_float(rg[2 * j + 1]), scale))))
+                     << 16);
+            uw[j] = static_cast<uint32_t>(__bfloat16_as_ushort(
+                        __float2bfloat16_rn(__fmul_rn(__uint_as_float(ru[2 * j]), scale)))) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(
+                         __float2bfloat16_rn(__fmul_rn(__uint_as_float(ru[2 * j + 1]), scale))))
+                     << 16);
+          }
+          if (p.out && valid) {
+            st_global_v4(o + 8 * b, gw[0], gw[1], gw[2], gw[3]);
+            st_global_v4(o + I + 8 * b, uw[0], uw[1], uw[2], uw[3]);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float h0 = silu_bf16_lut24(lut, bf16lo(gw[j]));
+            float h1 = silu_bf16_lut24(lut, bf16hi(gw[j]));
+            mul_f32x2(h0, h1, bf16lo(uw[j]), bf16hi(uw[j]));
+            mul_f32x2(h0, h1, w, w);
+            h[b >> 1][8 * (b & 1) + 2 * j] = h0;
+            h[b >> 1][8 * (b & 1) + 2 * j + 1] = h1;
+          }
+        }
+        part = fmaxf(fmaxf(part, amax_f32x16(h[0])), amax_f32x16(h[1]));
+      }
+      // the quarter's four partial maxima of each row meet in shared memory
+      // (two buffers: a warp is at most one tile ahead of the others here)
+      float* pm = epi_part + (it & 1) * 512 + quarter * 128;
+      pm[cb * 32 + lane] = part;
+      __syncwarp();
+      bar_sync_named(qbar, 128);
+      uint32_t* slots = sw.amax + row * stride;
+      if (ok && cb == 0 && valid) {
+        const float m = fmaxf(fmaxf(pm[lane], pm[32 + lane]), fmaxf(pm[64 + lane], pm[96 + lane]));
+        st_relaxed_gpu(slots + tl.nt, 0x80000000u | __float_as_uint(m));
+      }
+      if (!ok) continue;
+      // wait for the row's n_tiles slots (all lanes of the warp together)
+      float rmax = 0.0f;
+      bool have = !valid;
+      const uint64_t t0 = globaltimer();
+      while (true) {
+        if (!have) {
+          uint32_t m = 0u, all = 0x80000000u;
+          for (int q = 0; q < n_tiles; q += 4) {
+            const uint4 v = ld_relaxed_gpu_v4(slots + q);
+            const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (q + i < n_tiles) { all &= x[i]; m = max(m, x[i] & 0x7FFFFFFFu); }
+          }
+          if (all) { have = true; rmax = __uint_as_float(m); }
+        }
+        if (__all_sync(0xffffffffu, have)) break;
+        // one decision for the whole warp: every lane must leave together
+        const bool stop = *abort_flag != 0 || globaltimer() - t0 > budget;
+        if (__any_sync(0xffffffffu, stop)) {
+          failed = true;
+          if (lane == 0) fail(MINITE_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(32);
+      }
+      if (failed) continue;
+      const float g = global_scale(rmax);
+      const int64_t sfr = static_cast<int64_t>(tl.sf_rb0) * 128 + r_in_tile;
+      const int c0 = 8 * tl.nt + 2 * cb;   // first of this thread's two block columns
+      if (valid) {
+        const BlockScale s0 = block_scale_div(amax_f32x16(h[0]), g);
+        const BlockScale s1 = block_scale_div(amax_f32x16(h[1]), g);
+        const uint2 q0 = encode16(h[0], s0.enc, s0.sf == 0);
+        const uint2 q1 = encode16(h[1], s1.enc, s1.sf == 0);
+        *reinterpret_cast<uint4*>(sw.h_codes + row * (I / 2) + 64 * tl.nt + 16 * cb) =
+            make_uint4(q0.x, q0.y, q1.x, q1.y);
+        *reinterpret_cast<uint16_t*>(sw.h_sf + sf_offset(sfr, c0, kc)) =
+            static_cast<uint16_t>(s0.sf | (s1.sf << 8));
+        if (tl.nt == 0 && cb == 0) sw.h_g[row] = g;
+      } else if (r_in_tile < 128 * tl.sf_rbs) {
+        // a padding row of the expert's last 128-row scale block
+        *reinterpret_cast<uint16_t*>(sw.h_sf + sf_offset(sfr, c0, kc)) = 0;
+      }
+    }
   } else if (warp < EPI_WARP0 + NUM_EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
@@ -1318,7 +1502,27 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
+// Zero `n` words (the fused epilogue's row maxima and counters) once the
+// previous kernel on the stream has finished with them.
+__global__ void zero_words_kernel(uint32_t* __restrict__ w, int64_t n) {
+  pdl_wait();
+  const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = 4 * i0; i < n; i += 4 * step) {
+    if (i + 4 <= n) *reinterpret_cast<uint4*>(w + i) = make_uint4(0u, 0u, 0u, 0u);
+    else for (int64_t j = i; j < n; ++j) w[j] = 0u;
+  }
+}
+
 }  // namespace gemm
+
+// Workspace of minite_gate_up_swiglu_quant_nvfp4: per row, one slot word for
+// each of the I / 128 tiles of its m-block (the tile's partial |h| maximum
+// with bit 31 set once written), rows padded to 4 words.
+size_t swiglu_fused_workspace_words(int64_t M, int64_t I) {
+  const int64_t stride = (I / 128 + 3) / 4 * 4;
+  return static_cast<size_t>(M * stride);
+}
 
 // ---------------------------------------------------------------- host side
 
@@ -1378,9 +1582,9 @@ namespace {
 
 // Clusters of two CTAs of `kernel` that can be resident at once on the
 // current device (queried once per device and kernel).
-template <typename Kernel>
+template <int Tag, typename Kernel>
 int resident_pairs(Kernel kernel, int threads, size_t smem) {
-  static std::atomic<int> cache[64];
+  static std::atomic<int> cache[64];   // one per Tag: kernels of one type share a type
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   int v = cache[dev].load();
@@ -1530,7 +1734,7 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-      attr_err = cudaFuncSetAttribute(grouped_gemm_pair_deep_kernel,
+      attr_err = cudaFuncSetAttribute(grouped_gemm_pair_deep_kernel<false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     });
     if (attr_err != cudaSuccess) return MINITE_ERR_CUDA;
@@ -1538,13 +1742,90 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     // once (a GPC with an odd SM count leaves one SM out), never more pairs
     // than pair tiles
     const int64_t max_pairs = (M_total / 256 + E) * n_tiles;
-    int pairs = resident_pairs(grouped_gemm_pair_deep_kernel, R_THREADS, r_smem);
+    int pairs = resident_pairs<0>(grouped_gemm_pair_deep_kernel<false>, R_THREADS, r_smem);
     if (pairs <= 0) return MINITE_ERR_CUDA;
     if (max_pairs < pairs) pairs = static_cast<int>(max_pairs);
-    if (launch_pair_pdl(grouped_gemm_pair_deep_kernel, pairs, R_THREADS, r_smem, s, ta, tb, p) !=
-        cudaSuccess)
+    if (launch_pair_pdl(grouped_gemm_pair_deep_kernel<false>, pairs, R_THREADS, r_smem, s, ta, tb,
+                        p) != cudaSuccess)
       return MINITE_ERR_CUDA;
   }
+  return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
+}
+
+extern "C" int minite_gate_up_swiglu_quant_nvfp4(
+    const uint8_t* a_codes, const uint8_t* a_sf, const float* a_g, const uint8_t* b_codes,
+    const uint8_t* b_sf, const float* b_g, const int32_t* expert_offsets,
+    const int32_t* sf_row_offsets, int64_t M_total, int64_t I, int64_t K, int32_t E,
+    const float* perm_w, void* gate_up, uint8_t* h_codes, uint8_t* h_sf, float* h_g,
+    void* workspace, size_t ws_bytes, int32_t* status, minite_stream_t stream) {
+  using namespace gemm;
+  if (!a_codes || !a_sf || !a_g || !b_codes || !b_sf || !b_g || !expert_offsets ||
+      !sf_row_offsets || !h_codes || !h_sf || !h_g || !workspace)
+    return MINITE_ERR_INVALID_ARG;
+  if (M_total < 1 || M_total >= (int64_t(1) << 31) || I < 128 || I % 128 != 0 || I > 8192 ||
+      K < 64 || K % 64 != 0 || K > (1 << 20) || E < 1 || E > 1024 ||
+      2 * I * E >= (int64_t(1) << 31))
+    return MINITE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(a_codes, 128) || !aligned(b_codes, 128) || !aligned(a_sf, 16) ||
+      !aligned(b_sf, 16) || !aligned(h_codes, 16) || !aligned(h_sf, 16) || !aligned(workspace, 16) ||
+      (gate_up && !aligned(gate_up, 32)))
+    return MINITE_ERR_INVALID_ARG;
+  const size_t words = swiglu_fused_workspace_words(M_total, I);
+  if (ws_bytes < words * sizeof(uint32_t)) return MINITE_ERR_INVALID_ARG;
+  // stages, scale slots, barriers, the three offset tables and the silu table
+  const size_t smem = 1024 + R_STAGES * (R_AB_BYTES + R_SF_BYTES) + sizeof(RSmem) +
+                      3 * (E + 1) * sizeof(int32_t) + 16 + kLut24Entries * sizeof(float) +
+                      2 * 512 * sizeof(float);
+  if (smem > 232448) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_pair_deep_kernel<true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  });
+  if (attr_err != cudaSuccess) return MINITE_ERR_CUDA;
+  // every m-block's I/128 tiles run at once on I/128 clusters (consecutive
+  // cluster ids): launch a multiple of I/128 clusters, all resident together
+  const int n_tiles = static_cast<int>(I / 128);
+  int pairs = resident_pairs<1>(grouped_gemm_pair_deep_kernel<true>, R_THREADS, smem);
+  if (pairs <= 0) return MINITE_ERR_CUDA;
+  pairs = pairs / n_tiles * n_tiles;
+  if (pairs == 0) return MINITE_ERR_UNSUPPORTED_SHAPE;
+  const int64_t max_pairs = (M_total / 256 + E) * n_tiles;
+  if (max_pairs < pairs) pairs = static_cast<int>(max_pairs);
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, 2 * I * E, 128))
+    return MINITE_ERR_CUDA;
+  Params p;
+  p.a_g = a_g;
+  p.b_g = b_g;
+  p.a_sf = a_sf;
+  p.b_sf = b_sf;
+  p.offsets = expert_offsets;
+  p.sf_offsets = sf_row_offsets;
+  p.out = gate_up;
+  p.status = status;
+  p.M = M_total;
+  p.N = static_cast<int>(2 * I);
+  p.K = static_cast<int>(K);
+  p.E = E;
+  p.out_fp32 = 0;
+  p.budget_ns = wait_budget_ns();
+  uint32_t* ws = static_cast<uint32_t*>(workspace);
+  p.sw.perm_w = perm_w;
+  p.sw.h_codes = h_codes;
+  p.sw.h_sf = h_sf;
+  p.sw.h_g = h_g;
+  p.sw.amax = ws;
+  p.sw.I = static_cast<int>(I);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t zero_blocks = std::min<int64_t>(num_sms(), (static_cast<int64_t>(words) + 1023) / 1024);
+  if (launch_pdl(zero_words_kernel, dim3(static_cast<unsigned>(zero_blocks)), dim3(256), 0, s, ws,
+                 static_cast<int64_t>(words)) != cudaSuccess)
+    return MINITE_ERR_CUDA;
+  if (launch_pair_pdl(grouped_gemm_pair_deep_kernel<true>, pairs, R_THREADS, smem, s, ta, tb, p) !=
+      cudaSuccess)
+    return MINITE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
 

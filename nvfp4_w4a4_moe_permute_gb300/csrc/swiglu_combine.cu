@@ -11,28 +11,6 @@
 
 namespace minite {
 
-// silu(g) = g / (1 + exp_spec(-g)), every step an IEEE float operation.
-__device__ __forceinline__ float silu_spec(float g) {
-  return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));
-}
-
-// The gates are BF16, so silu takes at most 2^16 distinct inputs: each CTA
-// tabulates silu_spec in shared memory for |g| in [2^-24, 2^8) (32 binades,
-// both signs, 32 KB) and evaluates the formula only for gates outside it.
-// Entry index: 2 * (|g| bits - bits of 2^-24) + sign.
-constexpr uint32_t kLutLo = (127u - 24u) << 7;  // BF16 bits of 2^-24
-constexpr uint32_t kLutSpan = 32u << 7;          // 4096 magnitudes per sign
-constexpr int kLutEntries = 2 * static_cast<int>(kLutSpan);
-
-__device__ __forceinline__ uint32_t lut_gate_bits(int i) {
-  return (static_cast<uint32_t>(i & 1) << 15) | (kLutLo + static_cast<uint32_t>(i >> 1));
-}
-
-__device__ void build_silu_lut_part(float* lut, int t, int nthreads) {
-  for (int i = t; i < kLutEntries; i += nthreads)
-    lut[i] = silu_spec(__uint_as_float(lut_gate_bits(i) << 16));
-}
-
 // Byte offsets into a table of the two gates of a packed BF16 pair whose
 // magnitudes both lie in [2^-24, 2^8): per 16-bit half h, t = h - bits of
 // 2^-24 leaves the sign in bit 15 and the magnitude offset in bits 0..11

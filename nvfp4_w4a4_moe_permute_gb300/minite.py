@@ -20,6 +20,7 @@ SCALE_PER_ROW, SCALE_PER_GROUP = 0, 1
 ALONG_COLS, ALONG_ROWS = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
 OP_QUANTIZE, OP_PERMUTE_QUANT, OP_COMBINE_BACKWARD_QUANT, OP_QUANTIZE_TOKENS = 0, 1, 2, 3
+OP_GATE_UP_SWIGLU = 4
 ERR_TIMEOUT, ERR_BAD_ROUTING = 4, 5
 
 EXPORTS = [
@@ -31,7 +32,7 @@ EXPORTS = [
     "minite_test_div6_exhaustive", "minite_test_convert_digest", "minite_quantize_nvfp4_dual",
     "minite_moe_combine_backward_quant", "minite_quantize_tokens_nvfp4",
     "minite_swiglu_weighted_quant_keep_h", "minite_grouped_gemm_wgrad_nvfp4",
-    "minite_swiglu_backward_quant_keep",
+    "minite_swiglu_backward_quant_keep", "minite_gate_up_swiglu_quant_nvfp4",
 ]
 
 
@@ -68,6 +69,9 @@ def load(path: str | None = None):
                                             _vp, _int, _vp, _vp],
         "minite_grouped_gemm_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
                                       _vp, _int, _vp, _vp],
+        "minite_gate_up_swiglu_quant_nvfp4": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                              _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                                              _vp],
         "minite_swiglu_weighted_quant": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
         "minite_swiglu_weighted_quant_keep_h": [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp,
                                                 _vp, _vp, _vp, _vp],
@@ -217,6 +221,21 @@ def minite_grouped_gemm_nvfp4(a_codes, a_sf, a_g, b_codes, b_sf, b_g, expert_off
                                           _p(b_g), _p(expert_offsets), _p(sf_row_offsets), M, N,
                                           2 * K2, E, _p(out), out_dtype, _p(status), _s(stream))
     _check(rc, "minite_grouped_gemm_nvfp4")
+
+
+def minite_gate_up_swiglu_quant_nvfp4(a_codes, a_sf, a_g, b_codes, b_sf, b_g, expert_offsets,
+                                      sf_row_offsets, perm_w, h_codes, h_sf, h_g, workspace,
+                                      gate_up=None, status=None, stream=None):
+    """b_codes [E, 2I, K/2]; h_codes [M, I/2]; workspace uint8 of at least
+    minite_workspace_bytes(OP_GATE_UP_SWIGLU, M, I, 0, 0) bytes."""
+    M, K2 = a_codes.shape
+    E, N, _ = b_codes.shape
+    rc = load().minite_gate_up_swiglu_quant_nvfp4(
+        _p(a_codes), _p(a_sf), _p(a_g), _p(b_codes), _p(b_sf), _p(b_g), _p(expert_offsets),
+        _p(sf_row_offsets), M, N // 2, 2 * K2, E, _p(perm_w), _p(gate_up), _p(h_codes), _p(h_sf),
+        _p(h_g), _p(workspace), workspace.numel() * workspace.element_size(), _p(status),
+        _s(stream))
+    _check(rc, "minite_gate_up_swiglu_quant_nvfp4")
 
 
 def minite_swiglu_weighted_quant(gate_up, perm_w, E, expert_offsets, sf_row_offsets, codes, sf,
@@ -401,6 +420,10 @@ class MoEMLP:
         self.down = torch.empty((M, H), dtype=torch.bfloat16, device=d)
         self.y = torch.empty((T, H), dtype=torch.bfloat16, device=d)
         self.status = torch.zeros(1, dtype=i32, device=d)
+        # the fused gate_up + SwiGLU kernel takes I % 128 == 0 and E <= 663
+        self.fused_ok = I % 128 == 0 and 128 <= I <= 8192 and E <= 663
+        self.sw_ws = torch.empty(max(16, minite_workspace_bytes(OP_GATE_UP_SWIGLU, M, I, 0, 0)),
+                                 dtype=u8, device=d) if self.fused_ok else None
 
     def permute_quant(self, x, topk_ids, topk_w, stream=None):
         minite_moe_permute_quant(x, topk_ids, topk_w, self.E, self.a_codes, self.a_sf, self.a_g,
@@ -408,16 +431,32 @@ class MoEMLP:
                                  None if topk_w is None else self.perm_w, self.ws, self.status,
                                  stream)
 
-    def forward(self, x, topk_ids, topk_w, wgu, wd, stream=None):
-        """x [T,H] bf16, topk_ids [T,k] int32, topk_w [T,k] f32; wgu / wd are
-        ``quantize(..., per_group=True)`` results of [E,2I,H] and [E,H,I]."""
-        self.permute_quant(x, topk_ids, topk_w, stream)
+    def gate_up_swiglu(self, wgu, stream=None, fused=True, keep_gate_up=False):
+        """h = weighted SwiGLU of the gate_up GEMM, quantized into h_codes /
+        h_sf / h_g: one fused launch (the BF16 gate_up stored only with
+        keep_gate_up), or the GEMM into gate_up followed by the SwiGLU."""
+        if fused:
+            if not self.fused_ok:
+                raise MiniteError("the fused gate_up + SwiGLU kernel needs I % 128 == 0, E <= 663")
+            minite_gate_up_swiglu_quant_nvfp4(
+                self.a_codes, self.a_sf, self.a_g, wgu["codes"], wgu["sf"], wgu["g"],
+                self.offsets, self.sf_offsets, self.perm_w, self.h_codes, self.h_sf, self.h_g,
+                self.sw_ws, gate_up=self.gate_up if keep_gate_up else None, status=self.status,
+                stream=stream)
+            return
         minite_grouped_gemm_nvfp4(self.a_codes, self.a_sf, self.a_g, wgu["codes"], wgu["sf"],
                                   wgu["g"], self.offsets, self.sf_offsets, self.gate_up,
                                   self.status, stream)
         minite_swiglu_weighted_quant(self.gate_up, self.perm_w, self.E, self.offsets,
                                      self.sf_offsets, self.h_codes, self.h_sf, self.h_g,
                                      self.status, stream)
+
+    def forward(self, x, topk_ids, topk_w, wgu, wd, stream=None, fused=False, keep_gate_up=True):
+        """x [T,H] bf16, topk_ids [T,k] int32, topk_w [T,k] f32; wgu / wd are
+        ``quantize(..., per_group=True)`` results of [E,2I,H] and [E,H,I].
+        fused: gate_up GEMM, SwiGLU and requantization in one launch."""
+        self.permute_quant(x, topk_ids, topk_w, stream)
+        self.gate_up_swiglu(wgu, stream, fused=fused, keep_gate_up=keep_gate_up)
         minite_grouped_gemm_nvfp4(self.h_codes, self.h_sf, self.h_g, wd["codes"], wd["sf"],
                                   wd["g"], self.offsets, self.sf_offsets, self.down, self.status,
                                   stream)

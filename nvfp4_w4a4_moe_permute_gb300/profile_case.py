@@ -107,7 +107,8 @@ def permute_swiglu(args, M, dev, status):
 
 def gemm(args, M, dev, status):
     """One grouped GEMM of the skewed layer's recipe at `--tokens` tokens
-    (`--gemm` gate_up, down or dgrad), its operands produced by the library
+    (`--gemm` gate_up, gate_up_swiglu (the fused gate_up GEMM + SwiGLU +
+    requantization), down or dgrad), its operands produced by the library
     (weight quantization, permutation, SwiGLU), with the automatic kernel or
     `--variant`. The GEMM is the last `--reps` launches."""
     from . import inputs as IN
@@ -129,7 +130,9 @@ def gemm(args, M, dev, status):
     dh = torch.empty((T * k, I), dtype=torch.bfloat16, device=dev)
     M.minite_set_gemm_variant(args.variant)
     for _ in range(args.reps):
-        if args.gemm == "gate_up":
+        if args.gemm == "gate_up_swiglu":
+            mlp.gate_up_swiglu(wgu, fused=True)
+        elif args.gemm == "gate_up":
             M.minite_grouped_gemm_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"], wgu["sf"],
                                         wgu["g"], mlp.offsets, mlp.sf_offsets, mlp.gate_up, status)
         elif args.gemm == "down":
@@ -155,7 +158,8 @@ def main(argv=None) -> int:
     ap.add_argument("--tokens", type=int, default=16384, help="permute_swiglu: tokens")
     ap.add_argument("--gather", type=int, default=0, help="source rows (0: rows in place)")
     ap.add_argument("--dual", action="store_true", help="weights: both orientations")
-    ap.add_argument("--gemm", default="gate_up", choices=["gate_up", "down", "dgrad"])
+    ap.add_argument("--gemm", default="gate_up",
+                    choices=["gate_up", "gate_up_swiglu", "down", "dgrad"])
     ap.add_argument("--variant", type=int, default=0, help="gemm: grouped-GEMM kernel (0 automatic)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--seed", type=int, default=0)
