@@ -9,19 +9,25 @@
 // execution path".
 //
 // Four launches, no host synchronization:
-//   permute_rank_kernel   one warp per token chunk: stable in-chunk rank of
-//                         every (token, slot) pair (kept in dest_row) and the
-//                         chunk's expert histogram -> table[e][chunk]; also
-//                         resets the scan's completion counter.
-//   permute_scan_kernel   one block per expert: exclusive prefix of its
-//                         chunk counts; the last block to finish turns the
-//                         expert totals into expert_offsets / sf_row_offsets.
-//   permute_route_kernel  one thread per pair: the pair's permuted row
-//                         (offset + chunk base + local rank), perm_src and
-//                         perm_w.
-//   permute_quant_kernel  one warp per token: reads the token once,
-//                         quantizes it once in registers and writes its
-//                         codes / scales to its k destination rows.
+//   permute_rank_kernel      one warp per token chunk: stable in-chunk rank of
+//                            every (token, slot) pair (kept in dest_row) and
+//                            the chunk's expert histogram -> table[e][chunk];
+//                            also resets the scan's completion counter.
+//   permute_scan_kernel      one block per expert: exclusive prefix of its
+//                            chunk counts; the last block to finish turns the
+//                            expert totals into expert_offsets / sf_row_offsets.
+//   permute_quant_kernel     one warp per token: completes its pairs' permuted
+//                            rows (offset + chunk base + local rank) with
+//                            perm_src and perm_w, reads the token once,
+//                            quantizes it once in registers and writes its
+//                            codes to its k destination rows, its scales and
+//                            global scale in token order.
+//   permute_sf_gather_kernel the swizzled scale layout, one 128-row block of
+//                            whole 512-byte atoms at a time, from the
+//                            token-order scales through perm_src.
+// Without room for the token-order staging (the allocation-free entry point
+// on large problems) the quant kernel writes each row's scales itself, one
+// 4-byte word per lane and row, and there is no gather.
 #include <mutex>
 
 #include "common.cuh"
@@ -200,27 +206,6 @@ __global__ void __launch_bounds__(kPermThreads) permute_scan_kernel(
   }
 }
 
-// Completes every pair's permuted row (expert offset + the chunk's base for
-// the expert + the local rank) and writes the routing outputs; one thread per
-// pair.
-__global__ void __launch_bounds__(kPermThreads) permute_route_kernel(
-    const int32_t* __restrict__ ids, const float* __restrict__ topk_w, int64_t T, int E, int k,
-    int ct, int nchunks, const int32_t* __restrict__ table,
-    const int32_t* __restrict__ expert_offsets, int32_t* __restrict__ perm_src,
-    int32_t* __restrict__ dest_row, float* __restrict__ perm_w) {
-  pdl_wait();
-  const int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (p >= T * k) return;
-  const int e = ids[p];
-  if (e < 0 || e >= E) return;  // dest_row already -1
-  const int64_t t = p / k;
-  const int dest = expert_offsets[e] + table[static_cast<int64_t>(e) * nchunks + t / ct] +
-                   dest_row[p];
-  dest_row[p] = dest;
-  perm_src[dest] = static_cast<int32_t>(t);
-  if (perm_w) perm_w[dest] = topk_w[p];
-}
-
 // Quantize and scatter, one warp per token over a grid of resident blocks:
 // the warp reads the token once (lane l owns blocks 32i + l), quantizes it
 // once in registers and writes its codes, scales and g to each of its k
@@ -229,11 +214,18 @@ __global__ void __launch_bounds__(kPermThreads) permute_route_kernel(
 // ids == nullptr: the routing comes from the caller (dest_row and offsets of
 // an earlier permutation), which is then checked on the device; only the
 // token-order scale mode (sfc != nullptr) is used this way.
+// With ids, the warp also completes its token's routing (what a separate
+// pass would do): each pair's permuted row is the expert's offset plus the
+// chunk's base for the expert (the scan's table) plus the pair's rank within
+// the chunk (left in dest_row by the ranking), written back to dest_row with
+// perm_src and perm_w of that row.
 template <int NCH>
 __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int64_t T, int H, int E,
     int k, const int32_t* __restrict__ expert_offsets,
-    const int32_t* __restrict__ sf_row_offsets, const int32_t* __restrict__ dest_row,
+    const int32_t* __restrict__ sf_row_offsets, int32_t* __restrict__ dest_row,
+    const int32_t* __restrict__ table, int ct, int nchunks, const float* __restrict__ topk_w,
+    int32_t* __restrict__ perm_src, float* __restrict__ perm_w,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ row_g,
     uint8_t* __restrict__ sfc, float* __restrict__ gtok, int32_t* status) {
   pdl_wait();
@@ -255,12 +247,14 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int nb = H / 16;
   const int kc = (nb + 3) & ~3;
-  int cpart[NCH];  // the column part of each owned block's scale offset
-#pragma unroll
-  for (int j = 0; j < NCH; ++j) {
-    const int cc = 32 * j + lane;
-    cpart[j] = (cc >> 2) * 512 + (cc & 3);
-  }
+  // Direct scale stores: lane l writes the 4-byte word of atoms l, l + 32
+  // (scale columns 4a .. 4a + 3) of each destination row. Column c is block
+  // c of the row, held by lane c % 32 in chunk c / 32, so the word of atom
+  // l + 32 m gathers byte (l / 8 + 4 m) of the packed chunk scales of lanes
+  // (4 l + i) % 32, i = 0..3.
+  const int natoms = kc >> 2;
+  const int src0 = (4 * lane) & 31;
+  const uint32_t bsel = static_cast<uint32_t>(lane >> 3);   // byte within a packed word
   const bool a32 = (reinterpret_cast<uintptr_t>(x) & 31) == 0;
   uint32_t w[NCH][8];
   float am[NCH];
@@ -269,7 +263,13 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
   auto fetch = [&](int64_t t) {
     if (lane < k) {
       dest = dest_row[t * k + lane];
-      e = ids ? ids[t * k + lane] : 0;
+      if (ids) {
+        e = ids[t * k + lane];
+        if (dest >= 0)   // a valid id: dest is the pair's rank within its chunk
+          dest += s_off[e] + table[static_cast<int64_t>(e) * nchunks + t / ct];
+      } else {
+        e = 0;
+      }
     }
     const uint16_t* xr = x + t * H;
     m = a32 ? load_row_blocks<NCH, true>(xr, nb, w, am)
@@ -283,6 +283,13 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
     quant_row_blocks<NCH>(w, am, nb, g, qb);
     const int dcur = dest, ecur = e;
     const int64_t tcur = t;
+    if (ids && lane < k) {
+      dest_row[tcur * k + lane] = dcur;
+      if (dcur >= 0) {
+        perm_src[dcur] = static_cast<int32_t>(tcur);
+        if (perm_w) perm_w[dcur] = topk_w[tcur * k + lane];
+      }
+    }
     t += nwarps;
     if (t < T) fetch(t);
     if (sfc) {
@@ -294,6 +301,25 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
       }
       if (lane == 0) gtok[tcur] = g;
     }
+    // this lane's scale words: atom lane + 32 m for m < (natoms + 31) / 32
+    uint32_t sw[(NCH + 3) / 4];
+    if (!sfc) {
+#pragma unroll
+      for (int m = 0; m < (NCH + 3) / 4; ++m) {
+        // packed scales of chunks 4m .. 4m + 3 of this lane (zero past the row)
+        uint32_t pk = 0u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (4 * m + q < NCH) pk |= (qb[4 * m + q].sf & 0xFFu) << (8 * q);
+        uint32_t word = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t v = __shfl_sync(0xffffffffu, pk, src0 + i);
+          word |= ((v >> (8 * bsel)) & 0xFFu) << (8 * i);
+        }
+        sw[m] = word;
+      }
+    }
     for (int j = 0; j < k; ++j) {
       const int d = __shfl_sync(0xffffffffu, dcur, j);
       if (d < 0) continue;  // warp-uniform
@@ -302,16 +328,22 @@ __global__ void __launch_bounds__(kPermThreads, NCH <= 5 ? 3 : 2) permute_quant_
         continue;
       }
       const int ej = __shfl_sync(0xffffffffu, ecur, j);
-      const int64_t r = static_cast<int64_t>(s_sfoff[ej]) + (d - s_off[ej]);
-      uint8_t* srow = sf + ((r >> 7) * (kc >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
       uint8_t* crow = codes + static_cast<int64_t>(d) * (H / 2);
 #pragma unroll
       for (int jj = 0; jj < NCH; ++jj) {
         const int cc = 32 * jj + lane;
         if (cc < nb) st_u64(crow + 8 * cc, qb[jj].codes);
-        if (!sfc && cc < kc) srow[cpart[jj]] = static_cast<uint8_t>(qb[jj].sf);
       }
-      if (!sfc && lane == 0) row_g[d] = g;
+      if (!sfc) {
+        const int64_t r = static_cast<int64_t>(s_sfoff[ej]) + (d - s_off[ej]);
+        uint8_t* srow = sf + ((r >> 7) * natoms) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+#pragma unroll
+        for (int m = 0; m < (NCH + 3) / 4; ++m) {
+          const int a = lane + 32 * m;
+          if (a < natoms) *reinterpret_cast<uint32_t*>(srow + a * 512) = sw[m];
+        }
+        if (lane == 0) row_g[d] = g;
+      }
     }
   }
   if (sfc) return;  // the scale gather writes every scale row, padding included
@@ -430,8 +462,9 @@ size_t combine_backward_workspace_bytes(int64_t T, int64_t H) {
 // compact, the scale gather. ids == nullptr: caller-given routing.
 static int launch_quant_gather(const void* x, const int32_t* topk_ids, int64_t T, int64_t H,
                                int32_t E, int32_t k, const int32_t* expert_offsets,
-                               const int32_t* sf_row_offsets, const int32_t* perm_src,
-                               const int32_t* dest_row, uint8_t* codes, uint8_t* sf,
+                               const int32_t* sf_row_offsets, int32_t* perm_src,
+                               int32_t* dest_row, const int32_t* table, int ct, int nchunks,
+                               const float* topk_w, float* perm_w, uint8_t* codes, uint8_t* sf,
                                float* row_g, const PermWs& w, bool compact, int32_t* status,
                                cudaStream_t s) {
   const size_t smem = 2 * (E + 1) * sizeof(int32_t);
@@ -447,7 +480,8 @@ static int launch_quant_gather(const void* x, const int32_t* topk_ids, int64_t T
   case N:                                                                                  \
     launch_pdl(permute_quant_kernel<N>, dim3(static_cast<unsigned>(qblocks)),              \
                dim3(kPermThreads), smem, s, xb, topk_ids, T, h, E, k, expert_offsets,      \
-               sf_row_offsets, dest_row, codes, sf, row_g, w.sfc, w.gtok, status);         \
+               sf_row_offsets, dest_row, table, ct, nchunks, topk_w, perm_src, perm_w,     \
+               codes, sf, row_g, w.sfc, w.gtok, status);                                   \
     break;
     MINITE_CASE(1) MINITE_CASE(2) MINITE_CASE(3) MINITE_CASE(4) MINITE_CASE(5) MINITE_CASE(6)
     MINITE_CASE(7) MINITE_CASE(8)
@@ -499,13 +533,9 @@ static int permute_quant_impl(const void* x, const int32_t* topk_ids, const floa
              static_cast<int>(E), ct, nchunks, w.table, dest_row, w.counter, status);
   launch_pdl(permute_scan_kernel, dim3(E), dim3(kPermThreads), 0, s, w.table, nchunks,
              static_cast<int>(E), w.counter, w.totals, expert_offsets, sf_row_offsets);
-  const int64_t pairs = T * k;
-  launch_pdl(permute_route_kernel, dim3(static_cast<unsigned>((pairs + kPermThreads - 1) / kPermThreads)),
-             dim3(kPermThreads), 0, s, topk_ids, topk_w, T, static_cast<int>(E),
-             static_cast<int>(k), ct, nchunks, static_cast<const int32_t*>(w.table),
-             static_cast<const int32_t*>(expert_offsets), perm_src, dest_row, perm_w);
   const int rc = launch_quant_gather(x, topk_ids, T, H, E, k, expert_offsets, sf_row_offsets,
-                                     perm_src, dest_row, codes, sf, row_g, w, compact, status, s);
+                                     perm_src, dest_row, w.table, ct, nchunks, topk_w, perm_w,
+                                     codes, sf, row_g, w, compact, status, s);
   if (rc != MINITE_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
@@ -547,9 +577,11 @@ extern "C" int minite_moe_combine_backward_quant(
   const size_t kc = static_cast<size_t>(((H / 16) + 3) & ~int64_t(3));
   w.sfc = static_cast<uint8_t*>(workspace);
   w.gtok = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(T * kc));
+  // the forward's routing, read only (no ids: dest_row, perm_src untouched)
   const int rc = launch_quant_gather(dy, nullptr, T, H, E, k, expert_offsets, sf_row_offsets,
-                                     perm_src, dest_row, codes, sf, row_g, w, true, status,
-                                     reinterpret_cast<cudaStream_t>(stream));
+                                     const_cast<int32_t*>(perm_src), const_cast<int32_t*>(dest_row),
+                                     nullptr, 1, 1, nullptr, nullptr, codes, sf, row_g, w, true,
+                                     status, reinterpret_cast<cudaStream_t>(stream));
   if (rc != MINITE_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
 }
