@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-configuration measurements")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="skip the fused gate_up + SwiGLU comparison")
     return ap.parse_args()
 
 
@@ -369,9 +371,10 @@ class Step:
         mark(8)
 
     # kernels launched per step by the library (memsets not counted): weight
-    # quantization 2 + 2, permutation 5, GEMM 1, SwiGLU 1, GEMM 1, combine 1,
-    # combine backward with dY quantization 2, GEMM 1
-    LAUNCHES = 2 + 2 + 5 + 1 + 1 + 1 + 1 + 2 + 1
+    # quantization 2 + 2, permutation 4 (rank, scan, quant, scale gather),
+    # GEMM 1, SwiGLU 1, GEMM 1, combine 1, combine backward with dY
+    # quantization 2, GEMM 1
+    LAUNCHES = 2 + 2 + 4 + 1 + 1 + 1 + 1 + 2 + 1
 
     def flops(self):
         Mu = int(self.mlp.offsets[-1].item())
@@ -439,6 +442,39 @@ def time_launches(fn, stream, reps=10, warmup=3, flush=None):
         e1.synchronize()
         out.append(e0.elapsed_time(e1))
     return out
+
+
+def fused_gate_up_swiglu(step, stream, dev, reps=10):
+    """The fused gate_up GEMM + weighted SwiGLU + requantization
+    (minite_gate_up_swiglu_quant_nvfp4, no BF16 gate_up kept) against the
+    gate_up GEMM followed by the SwiGLU kernel, both on the step's buffers,
+    L2 flushed before every launch (median, p10, p90 of `reps`)."""
+    import torch
+
+    from nvfp4_w4a4_moe_permute_gb300 import minite as M
+    mlp = step.mlp
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def stats(ts):
+        return {"median": round(statistics.median(ts), 5), "p10": round(percentile(ts, 10), 5),
+                "p90": round(percentile(ts, 90), 5)}
+
+    def unfused():
+        M.minite_grouped_gemm_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, step.wgu["codes"],
+                                    step.wgu["sf"], step.wgu["g"], mlp.offsets, mlp.sf_offsets,
+                                    mlp.gate_up, mlp.status, stream)
+        M.minite_swiglu_weighted_quant(mlp.gate_up, mlp.perm_w, mlp.E, mlp.offsets,
+                                       mlp.sf_offsets, mlp.h_codes, mlp.h_sf, mlp.h_g,
+                                       mlp.status, stream)
+
+    tu = time_launches(unfused, stream, reps=reps, flush=flush)
+    tf = time_launches(lambda: mlp.gate_up_swiglu(step.wgu, stream, fused=True), stream,
+                       reps=reps, flush=flush)
+    torch.cuda.synchronize(dev)
+    assert int(mlp.status.item()) == 0
+    return {"workload": "the benchmarked step's gate_up layer",
+            "fused_ms": stats(tf), "gemm_then_swiglu_ms": stats(tu),
+            "used_in_step": False}
 
 
 def per_config(dev, fp4_peak, peaks):
@@ -535,6 +571,12 @@ def per_config(dev, fp4_peak, peaks):
     out["mlp_forward"] = {"workload": workload_name("mlp", c), **stats(tf),
                           "tokens_per_s": round(T / (fmed / 1e3)),
                           "launches": 5 + 1 + 1 + 1 + 1}
+    if mlp.fused_ok:
+        # the gate_up GEMM + SwiGLU as one fused launch against the two launches
+        tu = time_launches(lambda: mlp.gate_up_swiglu(wgu, s, fused=False), s, flush=flush)
+        tfu = time_launches(lambda: mlp.gate_up_swiglu(wgu, s, fused=True), s, flush=flush)
+        out["mlp_forward"]["gate_up_swiglu"] = {"fused_ms": stats(tfu),
+                                                "gemm_then_swiglu_ms": stats(tu)}
     assert int(mlp.status.item()) == 0
     return out
 
@@ -720,6 +762,12 @@ def run_gpu(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": ems / args.steps}
 
+    # the gate_up GEMM with the SwiGLU and requantization fused into its
+    # epilogue, against the step's two launches, on the step's own buffers
+    fused = None
+    if rank == 0 and step.mlp.fused_ok and not args.no_fused:
+        fused = fused_gate_up_swiglu(step, stream, dev)
+
     fl = step.flops()
     peaks = measured_peaks()
     # each GEMM launch is timed alone (CUDA events around it), so the burst
@@ -788,6 +836,7 @@ def run_gpu(args):
         "gpu_launches": Step.LAUNCHES * args.steps,
         "backward": backward,
         "per_config": per_cfg,
+        "fused_gate_up_swiglu": fused,
         "e2e": e2e,
         "cpu_baseline": None,
     }
