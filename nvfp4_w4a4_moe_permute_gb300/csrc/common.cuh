@@ -298,6 +298,14 @@ __device__ __forceinline__ float amax_f32x16(const float (&v)[16]) {
                fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 
+// Two floats rounded to BF16 (nearest, ties to even) in one instruction: lo
+// in bits 0..15, hi in bits 16..31 (each the same as __float2bfloat16_rn).
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
 // Elementwise a * b (IEEE float products) on pairs of floats.
 __device__ __forceinline__ void mul_f32x2(float& a0, float& a1, float b0, float b1) {
   uint64_t p, q;
@@ -840,6 +848,14 @@ __device__ __forceinline__ void tmem_ld_8cols_x2(uint32_t ta, uint32_t tb, uint3
         "=r"(b[6]), "=r"(b[7])
       : "r"(ta), "r"(tb)
       : "memory");
+}
+
+// One lane of the (converged) warp gets true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(r));
+  return r != 0;
 }
 
 // Named barrier `id` over `count` threads (whole warps).

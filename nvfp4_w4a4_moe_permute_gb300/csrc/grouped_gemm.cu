@@ -208,16 +208,18 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
 }
 
 // One epilogue warp: drain EPI_COLS (= 64) accumulator columns of its 32 TMEM
-// lanes (row `row` on each lane) as two 32-column loads, packing each to
-// BF16 (scaled by `scale`) as it arrives; call `release` on lane 0 as soon
-// as the second load has landed (the MMA may then overwrite the
-// accumulator), then store the row's columns [n0, n0 + 64) below N.
+// lanes (row `row` on each lane) as two 32-column loads, call `release` on
+// lane 0 as soon as the second has landed (the MMA may then overwrite the
+// accumulator), scale by `scale`, round to BF16 (or keep FP32) and store the
+// row's columns [n0, n0 + 64) below N.
 template <typename Release>
 __device__ __forceinline__ void epilogue_slice(const Params& p, uint32_t tbase, bool valid,
                                                int64_t row, int n0, float scale, Release release) {
   static_assert(EPI_COLS == 64, "two 32-column TMEM loads per epilogue warp");
   const int lane = threadIdx.x & 31;
   if (!p.out_fp32) {
+    // the first half is packed (paired products, one two-value conversion)
+    // before the second load, so the accumulator is released soon after
     uint32_t pk[32];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -230,10 +232,9 @@ __device__ __forceinline__ void epilogue_slice(const Params& p, uint32_t tbase, 
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const float lo = __fmul_rn(__uint_as_float(r[2 * j]), scale);
-        const float hi = __fmul_rn(__uint_as_float(r[2 * j + 1]), scale);
-        pk[16 * c + j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-                         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+        float lo = __uint_as_float(r[2 * j]), hi = __uint_as_float(r[2 * j + 1]);
+        mul_f32x2(lo, hi, scale, scale);
+        pk[16 * c + j] = pack_bf16x2_rn(lo, hi);
       }
     }
     if (!valid) return;
@@ -1012,8 +1013,8 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
 //   warps 2..5 (each CTA): wait sfdata[s]; write the atoms into TMEM slot s
 //     (tcgen05.st, replicated into the four lane quarters); arrive on the
 //     leader's sf_full[s] (eight arrivals: four warps per CTA).
-//   warp 1 of the leader: waits full[s] and sf_full[s]; four pair MMAs;
-//     commits empty[s] to both CTAs.
+//   warp 1 of the leader (the whole warp, one elected lane issuing): waits
+//     full[s] and sf_full[s]; four pair MMAs; commits empty[s] to both CTAs.
 //   warps 6..21 (each CTA): after the tile's last commit (acc_full), drain
 //     the 128 x 256 accumulator of this CTA's rows, arrive on the leader's
 //     acc_empty (32 arrivals), then scale, convert and store.
@@ -1233,7 +1234,12 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (rank == 0 && lane == 0) {
+    // The whole warp runs the loop, so the stage, the phases and every
+    // descriptor are warp-uniform values; every lane takes the barrier waits
+    // (one instruction for the warp) and one elected lane issues the MMAs and
+    // commits. Issued from a one-lane branch instead, the per-chunk loop took
+    // ~165 cycles per MMA, above the tensor pipe's 128.
+    if (rank == 0) {
       constexpr uint32_t idesc = make_idesc_pair();
       const uint64_t adesc0 = smem_desc(smem_u32(stages), 16, 1024, kLayoutSwizzle128B);
       const uint64_t bdesc0 = smem_desc(smem_u32(stages + P_A_BYTES), 16, 1024, kLayoutSwizzle128B);
@@ -1242,29 +1248,41 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
       bool ok = true;
       bool issued = false;
       for (int t = cid; t < total && ok; t += ncl) {
-        if (!mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&S.acc_empty, acc_phase ^ 1u, budget, abort_flag))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&S.full[stage], phase, budget, abort_flag) ||
-              !mbar_wait(&S.sf_full[stage], phase, budget, abort_flag)) { ok = false; break; }
+          const bool w_ok = mbar_wait(&S.full[stage], phase, budget, abort_flag) &&
+                            mbar_wait(&S.sf_full[stage], phase, budget, abort_flag);
+          if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
           tc_fence_after();
           const int ks = min(4, KSTEPS - 4 * kt);
           const uint64_t soff = static_cast<uint64_t>(stage * R_AB_BYTES) >> 4;
           const uint32_t sf_t = tmem + SF_COL0 + stage * P_SF_COLS;
-          for (int s = 0; s < ks; ++s)
-            tc_mma_nvfp4_pair(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc,
-                              sf_t + 4 * s, sf_t + 16 + 8 * s, (kt | s) != 0);
+          if (elect_one()) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              if (s < ks)
+                tc_mma_nvfp4_pair(tmem, adesc0 + soff + 2 * s, bdesc0 + soff + 2 * s, idesc,
+                                  sf_t + 4 * s, sf_t + 16 + 8 * s, (kt | s) != 0);
+            tc_commit_pair_mc(&S.empty[stage], kPairMask);
+          }
+          __syncwarp();
           issued = true;
-          tc_commit_pair_mc(&S.empty[stage], kPairMask);
           if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit_pair_mc(&S.acc_full, kPairMask);
+        if (elect_one()) tc_commit_pair_mc(&S.acc_full, kPairMask);
+        __syncwarp();
         acc_phase ^= 1u;
       }
-      if (!ok) fail(MINITE_ERR_TIMEOUT);
+      if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
       if (issued) {
-        tc_commit_pair_mc(&S.drain, 0x1);
+        // all MMAs complete before TMEM is freed
+        if (elect_one()) tc_commit_pair_mc(&S.drain, 0x1);
+        __syncwarp();
         volatile int no_abort = 0;
         mbar_wait(&S.drain, 0, kDrainBudget, &no_abort);
       }
@@ -1383,16 +1401,12 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
           uint32_t gw[4], uw[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            gw[j] = static_cast<uint32_t>(__bfloat16_as_ushort(
-                        __float2bfloat16_rn(__fmul_rn(__uint_as_float(rg[2 * j]), scale)))) |
-                    (static_cast<uint32_t>(__bfloat16_as_ushort(
-                         __float2bfloat16_rn(__fmul_rn(__uint_as_float(rg[2 * j + 1]), scale))))
-                     << 16);
-            uw[j] = static_cast<uint32_t>(__bfloat16_as_ushort(
-                        __float2bfloat16_rn(__fmul_rn(__uint_as_float(ru[2 * j]), scale)))) |
-                    (static_cast<uint32_t>(__bfloat16_as_ushort(
-                         __float2bfloat16_rn(__fmul_rn(__uint_as_float(ru[2 * j + 1]), scale))))
-                     << 16);
+            float g0 = __uint_as_float(rg[2 * j]), g1 = __uint_as_float(rg[2 * j + 1]);
+            float u0 = __uint_as_float(ru[2 * j]), u1 = __uint_as_float(ru[2 * j + 1]);
+            mul_f32x2(g0, g1, scale, scale);
+            mul_f32x2(u0, u1, scale, scale);
+            gw[j] = pack_bf16x2_rn(g0, g1);
+            uw[j] = pack_bf16x2_rn(u0, u1);
           }
           if (p.out && valid) {
             st_global_v4(o + 8 * b, gw[0], gw[1], gw[2], gw[3]);

@@ -250,6 +250,35 @@ def test_fused_full_size_identical_to_unfused_and_oracle_rows(name):
     _oracle_rows(d, fu, off, sfo, rows.astype(np.int64))
 
 
+def test_plain_and_fused_gemm_repeat_bit_identical_full_size():
+    """Races in a pipeline show up as run-to-run differences: three launches
+    of the gate_up GEMM and of the fused kernel on the 4096-token layer give
+    the same bytes each time."""
+    d = IN.make_moe_inputs("mlp")
+    d.pop("w_down", None)
+    c = d["cfg"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    wgu = M.quantize(bf16_dev(d["w_gate_up"]), per_group=True)
+    mlp = M.MoEMLP(T, H, I, E, k)
+    mlp.permute_quant(bf16_dev(d["x"]), np_dev(d["topk_ids"]), np_dev(d["topk_w"]))
+    Mu = int(mlp.offsets[-1].item())
+    plain, fused = [], []
+    for _ in range(3):
+        M.minite_grouped_gemm_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"], wgu["sf"],
+                                    wgu["g"], mlp.offsets, mlp.sf_offsets, mlp.gate_up, mlp.status)
+        torch.cuda.synchronize()
+        plain.append(mlp.gate_up[:Mu].clone())
+        mlp.gate_up_swiglu(wgu, fused=True, keep_gate_up=True)
+        torch.cuda.synchronize()
+        fused.append((mlp.gate_up[:Mu].clone(), mlp.h_codes[:Mu].clone(), mlp.h_g[:Mu].clone()))
+    assert int(mlp.status.item()) == 0
+    for i in (1, 2):
+        assert torch.equal(plain[i], plain[0]), "plain GEMM differs between launches"
+        for a, b in zip(fused[i], fused[0]):
+            assert torch.equal(a, b), "fused kernel differs between launches"
+    assert torch.equal(fused[0][0], plain[0]), "fused gate_up differs from the plain GEMM"
+
+
 def test_fused_rejects_unsupported_shapes():
     d = make_case(64, 256, 192, [64, 64], 2, seed=3)   # I % 128 != 0
     c = d["cfg"]
