@@ -191,51 +191,6 @@ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t kc) {
 // share one 16-element block; lanes 8a..8a+7 share one 4-column SF atom word.
 // ----------------------------------------------------------------------------
 
-template <int NCH>
-struct RowQuant {
-  uint32_t codes[NCH];  // this lane's 4 code bytes per chunk
-  uint32_t sfword[NCH]; // valid on lanes 8a: the 4 SF bytes of blocks 4a..4a+3
-};
-
-// v[j][i]: element (256j + 8*lane + i); elements at or beyond C must be 0.
-template <int NCH>
-__device__ __forceinline__ void quantize_row_warp(const float (&v)[NCH][8], int C, float g,
-                                                  RowQuant<NCH>& out) {
-  const int lane = threadIdx.x & 31;
-  const float tk = enc_table_entry(g);
-#pragma unroll
-  for (int j = 0; j < NCH; ++j) {
-    const bool valid = (256 * j + 8 * lane) < C;
-    float am = amax8(v[j]);
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-    BlockScale bs = block_scale(am, g, tk);
-    uint32_t sf = valid ? bs.sf : 0u;
-    out.codes[j] = encode8(v[j], bs.enc, !valid || sf == 0);
-    // gather the SF bytes of lanes 8a, 8a+2, 8a+4, 8a+6 into lane 8a
-    uint32_t s1 = __shfl_down_sync(0xffffffffu, sf, 2);
-    uint32_t s2 = __shfl_down_sync(0xffffffffu, sf, 4);
-    uint32_t s3 = __shfl_down_sync(0xffffffffu, sf, 6);
-    out.sfword[j] = sf | (s1 << 8) | (s2 << 16) | (s3 << 24);
-  }
-}
-
-// Write one quantized row: codes at codes_row (C/2 bytes), SF words into the
-// swizzled region `sf_base` at local row r with kc SF columns.
-template <int NCH>
-__device__ __forceinline__ void store_row_warp(const RowQuant<NCH>& q, int C, uint8_t* codes_row,
-                                               uint8_t* sf_base, int64_t r, int kc) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < NCH; ++j) {
-    const int e0 = 256 * j + 8 * lane;
-    if (e0 < C) *reinterpret_cast<uint32_t*>(codes_row + e0 / 2) = q.codes[j];
-    const int col = 16 * j + (lane >> 1);  // SF column of this lane's block
-    if ((lane & 7) == 0 && col < kc) {
-      *reinterpret_cast<uint32_t*>(sf_base + sf_offset(r, col, kc)) = q.sfword[j];
-    }
-  }
-}
-
 // ----------------------------------------------------------------------------
 // Lane-per-block quantizer core: one lane owns one whole 16-element block, so
 // the block amax needs no shuffle and the block scale is computed once per
@@ -592,18 +547,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* desc, uint64_
       : "memory");
 }
 
-// L2 prefetch of one 2-D TMA box (no completion tracking).
-__device__ __forceinline__ void tma_prefetch_2d(const void* desc, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-               :: "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y) : "memory");
-}
-
-// L2 prefetch of a contiguous range (16-byte aligned address, size % 16 == 0).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-               :: "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
-}
-
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
@@ -637,13 +580,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
       :: "r"(smem_u32(bar)) : "memory");
-}
-
-// Copy one 512-byte scale-factor atom (32 rows x 16 bytes) from shared memory
-// into 4 TMEM columns, replicated into the four 32-lane quarters.
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
-               :: "r"(taddr), "l"(sdesc) : "memory");
 }
 
 // D(tmem) (+)= A(smem) * B(smem)^T with NVFP4 block scales from TMEM.
@@ -738,10 +674,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
-               :: "r"(cluster_addr) : "memory");
-}
 // Arrive on an mbarrier of the peer CTA with the default (release, CTA scope)
 // semantics. Used after tcgen05.wait::st / wait::ld and
 // tcgen05.fence::before_thread_sync to hand TMEM to the peer's MMA thread; a
@@ -764,17 +696,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* desc, ui
          "r"(y)
       : "memory");
 }
-// 3-D TMA load into this CTA's shared memory, completion counted on an
-// mbarrier that may live in the peer CTA of the pair.
-__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* desc, uint32_t mbar_cluster,
-                                                 int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
-      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
-      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(desc)), "r"(mbar_cluster), "r"(x),
-         "r"(y), "r"(z)
-      : "memory");
-}
 // One warp in each CTA of the pair, collectively.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -784,13 +705,6 @@ __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
                :: "r"(taddr), "r"(ncols) : "memory");
-}
-// Issued by the even CTA of the pair: each CTA's 512-byte scale atom at the
-// descriptor's shared-memory offset into 4 of its own TMEM columns,
-// replicated into the four 32-lane quarters.
-__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;"
-               :: "r"(taddr), "l"(sdesc) : "memory");
 }
 // Track the pair MMAs issued so far; arrive once on `bar` in every CTA of `mask`.
 __device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t mask) {
@@ -810,17 +724,6 @@ __device__ __forceinline__ void tc_mma_nvfp4_pair(uint32_t d_tmem, uint64_t ades
       " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
       :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
          "r"(accumulate)
-      : "memory");
-}
-
-// Warp: load 64 consecutive fp32 columns of this warp's 32 TMEM lanes (one
-// instruction, one wait).
-__device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr)
       : "memory");
 }
 
