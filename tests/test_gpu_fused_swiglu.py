@@ -290,3 +290,34 @@ def test_fused_rejects_unsupported_shapes():
         M.minite_gate_up_swiglu_quant_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"], wgu["sf"],
                                             wgu["g"], mlp.offsets, mlp.sf_offsets, None,
                                             mlp.h_codes, mlp.h_sf, mlp.h_g, ws, status=mlp.status)
+
+
+def test_fused_wait_timeout_sets_status_and_context_survives():
+    """Every wait of the fused kernel (pipeline barriers and the row-maximum
+    exchange) runs out under a 1 ns budget: the call sets the timeout bit and
+    returns, and the next call on the same context gives the right bytes."""
+    d = make_case(T_RAGGED, 256, 384, RAGGED, 2, seed=31)
+    mlp, un, fu, wgu = _run_both(d, True)
+    Mu = int(mlp.offsets[-1].item())
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def call():
+        M.minite_gate_up_swiglu_quant_nvfp4(mlp.a_codes, mlp.a_sf, mlp.a_g, wgu["codes"],
+                                            wgu["sf"], wgu["g"], mlp.offsets, mlp.sf_offsets,
+                                            mlp.perm_w, fu["codes"], fu["sf"], fu["g"], mlp.sw_ws,
+                                            gate_up=fu["gate_up"], status=st)
+
+    try:
+        M.minite_set_wait_budget_ns(1)
+        call()
+        torch.cuda.synchronize()
+    finally:
+        M.minite_set_wait_budget_ns(0)
+    assert int(st.item()) & (1 << M.ERR_TIMEOUT)
+    st.zero_()
+    for key in ("codes", "sf"):
+        fu[key].fill_(SENTINEL)
+    call()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _assert_identical(un, fu, Mu)
