@@ -47,6 +47,14 @@
 // tensor pipe (128 cycles per MMA when fed) sets the pace: each K chunk's
 // MMAs wait for its scale atoms, which are copied only once the stage's
 // previous MMAs complete and then pass through the scale warps into TMEM.
+// The output stores were the other limit: with a lane owning a row, every
+// store instruction touched 32 different 128-byte lines and the epilogue
+// warps fell behind the single-buffered accumulator (with the stores left
+// out, gate_up took 0.32 instead of 0.44 ms and down 0.22 instead of 0.39 ms
+// on the skewed layer). The BF16 epilogue therefore transposes chunks among
+// groups of four lanes so that each instruction writes whole row segments,
+// and the pair kernel hands full 32-row boxes to TMA stores from a 2 KB
+// staging buffer per warp.
 //
 // minite_gate_up_swiglu_quant_nvfp4 runs the pair kernel's second instance
 // (SWIGLU): the even CTA loads gate rows and the odd CTA the matching up
@@ -137,6 +145,7 @@ struct Params {
   int64_t M;          // rows of A / out (weight gradient: rows of A, i.e. channels)
   int N, K, E;        // weight gradient: K = token columns allocated per operand row
   int out_fp32;
+  int c_tma;          // CTA-pair kernel: BF16 output staged per warp, written by TMA stores
   uint64_t budget_ns;
   SwigluParams sw;
 };
@@ -209,48 +218,92 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
+// One epilogue warp's drain of EPI_COLS (= 64) accumulator columns of its 32
+// TMEM lanes into 32 packed BF16 pairs per lane (the row's columns scaled by
+// `scale`), as two 32-column loads; `release` runs on lane 0 once the second
+// has landed (the MMA may then overwrite the accumulator). The first half is
+// packed (paired products, one two-value conversion) before the second load.
+template <typename Release>
+__device__ __forceinline__ void drain_bf16x64(uint32_t tbase, float scale, Release release,
+                                              uint32_t (&pk)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t r[32];
+    tmem_ld_32cols(tbase + 32 * c, r);
+    if (c == 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) release();
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float lo = __uint_as_float(r[2 * j]), hi = __uint_as_float(r[2 * j + 1]);
+      mul_f32x2(lo, hi, scale, scale);
+      pk[16 * c + j] = pack_bf16x2_rn(lo, hi);
+    }
+  }
+}
+
+// Stores a warp's 32 consecutive rows x 64 BF16 columns [n0, n0 + 64) below
+// N; lane L holds row row0 + L as 32 packed words (four 32-byte chunks). A
+// lane owning a whole row would make every store instruction touch 32
+// different 128-byte lines; instead the four lanes of each group g exchange
+// chunks (a 4 x 4 transpose by three shuffles and two rotations on each side)
+// so that lane (g, t) stores chunk t of rows 4g..4g+3, one row per
+// instruction: each instruction writes 8 whole 128-byte row segments.
+// `vmask` has bit L set when row row0 + L exists. Call on all 32 lanes.
+__device__ __forceinline__ void store_rows_bf16x64(uint16_t* out, int64_t ld, int64_t row0,
+                                                   int n0, int N, uint32_t vmask,
+                                                   uint32_t (&pk)[32]) {
+  const int lane = threadIdx.x & 31;
+  const int t = lane & 3;
+  const int gbase = lane & ~3;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    // sender side: y[s] = chunk (t - s) & 3, the chunk lane gbase + ((t - s) & 3) needs
+    const uint32_t c0 = pk[w], c1 = pk[8 + w], c2 = pk[16 + w], c3 = pk[24 + w];
+    const uint32_t a0 = (t & 1) ? c1 : c0, a1 = (t & 1) ? c0 : c3, a2 = (t & 1) ? c3 : c2,
+                   a3 = (t & 1) ? c2 : c1;
+    const uint32_t y1 = (t & 2) ? a3 : a1, y2 = (t & 2) ? a0 : a2, y3 = (t & 2) ? a1 : a3;
+    // r[s] = chunk t of group row (t + s) & 3
+    const uint32_t r0 = (t & 2) ? a2 : a0;
+    const uint32_t r1 = __shfl_sync(0xffffffffu, y1, gbase | ((t + 1) & 3));
+    const uint32_t r2 = __shfl_sync(0xffffffffu, y2, gbase | ((t + 2) & 3));
+    const uint32_t r3 = __shfl_sync(0xffffffffu, y3, gbase | ((t + 3) & 3));
+    // receiver side: chunk t of group row u is r[(u - t) & 3]
+    const uint32_t b0 = (t & 1) ? r3 : r0, b1 = (t & 1) ? r0 : r1, b2 = (t & 1) ? r1 : r2,
+                   b3 = (t & 1) ? r2 : r3;
+    pk[w] = (t & 2) ? b2 : b0;
+    pk[8 + w] = (t & 2) ? b3 : b1;
+    pk[16 + w] = (t & 2) ? b0 : b2;
+    pk[24 + w] = (t & 2) ? b1 : b3;
+  }
+  const int col = n0 + 16 * t;
+  uint16_t* o = out + (row0 + gbase) * ld + col;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (((vmask >> (gbase + u)) & 1u) && col < N)
+      st_global_v8(o + static_cast<int64_t>(u) * ld, pk[8 * u], pk[8 * u + 1], pk[8 * u + 2],
+                   pk[8 * u + 3], pk[8 * u + 4], pk[8 * u + 5], pk[8 * u + 6], pk[8 * u + 7]);
+}
+
 // One epilogue warp: drain EPI_COLS (= 64) accumulator columns of its 32 TMEM
-// lanes (row `row` on each lane) as two 32-column loads, call `release` on
-// lane 0 as soon as the second has landed (the MMA may then overwrite the
-// accumulator), scale by `scale`, round to BF16 (or keep FP32) and store the
-// row's columns [n0, n0 + 64) below N.
+// lanes (row `row` on each lane, consecutive over the lanes) as two 32-column
+// loads, call `release` on lane 0 as soon as the second has landed (the MMA
+// may then overwrite the accumulator), scale by `scale`, round to BF16 (or
+// keep FP32) and store the row's columns [n0, n0 + 64) below N. Call on all
+// 32 lanes.
 template <typename Release>
 __device__ __forceinline__ void epilogue_slice(const Params& p, uint32_t tbase, bool valid,
                                                int64_t row, int n0, float scale, Release release) {
   static_assert(EPI_COLS == 64, "two 32-column TMEM loads per epilogue warp");
   const int lane = threadIdx.x & 31;
   if (!p.out_fp32) {
-    // the first half is packed (paired products, one two-value conversion)
-    // before the second load, so the accumulator is released soon after
     uint32_t pk[32];
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      uint32_t r[32];
-      tmem_ld_32cols(tbase + 32 * c, r);
-      if (c == 1) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) release();
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float lo = __uint_as_float(r[2 * j]), hi = __uint_as_float(r[2 * j + 1]);
-        mul_f32x2(lo, hi, scale, scale);
-        pk[16 * c + j] = pack_bf16x2_rn(lo, hi);
-      }
-    }
-    if (!valid) return;
-    uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.N + n0;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      if (n0 + c * 32 < p.N) {
-        st_global_v8(orow + c * 32, pk[16 * c], pk[16 * c + 1], pk[16 * c + 2], pk[16 * c + 3],
-                     pk[16 * c + 4], pk[16 * c + 5], pk[16 * c + 6], pk[16 * c + 7]);
-        st_global_v8(orow + c * 32 + 16, pk[16 * c + 8], pk[16 * c + 9], pk[16 * c + 10],
-                     pk[16 * c + 11], pk[16 * c + 12], pk[16 * c + 13], pk[16 * c + 14],
-                     pk[16 * c + 15]);
-      }
-    }
+    drain_bf16x64(tbase, scale, release, pk);
+    store_rows_bf16x64(static_cast<uint16_t*>(p.out), p.N, row - lane, n0, p.N,
+                       __ballot_sync(0xffffffffu, valid), pk);
   } else {
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
@@ -1019,7 +1072,10 @@ grouped_gemm_dc_kernel(const __grid_constant__ CUtensorMap tmap_a,
 //     full[s] and sf_full[s]; four pair MMAs; commits empty[s] to both CTAs.
 //   warps 6..21 (each CTA): after the tile's last commit (acc_full), drain
 //     the 128 x 256 accumulator of this CTA's rows, arrive on the leader's
-//     acc_empty (32 arrivals), then scale, convert and store.
+//     acc_empty (32 arrivals), then scale, convert and store: with c_tma
+//     (BF16 output, staging fits) each warp writes its 32 rows x 64 columns
+//     as two 32 x 32 TMA boxes through its 2 KB of staging, rows past the
+//     expert's end by transposed plain stores.
 // ============================================================================
 
 constexpr int R_STAGES = 5;
@@ -1027,6 +1083,8 @@ constexpr int R_AB_BYTES = P_STAGE_BYTES;   // 32 KB: this CTA's A and B rows of
 constexpr int R_SF_BYTES = P_SLOT_BYTES;    // 6 KB: this CTA's A atoms, both B blocks' atoms
 constexpr int R_SF_WARP = NUM_WARPS;        // warp 22: scale-copy producer
 constexpr int R_THREADS = (NUM_WARPS + 1) * 32;
+constexpr int R_C_WARP_BYTES = 2048;                  // 32 rows x 32 BF16 columns
+constexpr int R_C_BYTES = NUM_EPI_WARPS * R_C_WARP_BYTES;
 static_assert(SF_COL0 + R_STAGES * P_SF_COLS <= TMEM_COLS, "TMEM budget");
 static_assert(R_SF_BYTES % 16 == 0, "bulk copy alignment");
 
@@ -1050,12 +1108,14 @@ struct RSmem {
 template <bool SWIGLU>
 __global__ void __maxnreg__(80)
 grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                              const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+                              const __grid_constant__ CUtensorMap tmap_b,
+                              const __grid_constant__ CUtensorMap tmap_c, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sf_area = stages + R_STAGES * R_AB_BYTES;
-  RSmem& S = *reinterpret_cast<RSmem*>(sf_area + R_STAGES * R_SF_BYTES);
+  uint8_t* c_area = sf_area + R_STAGES * R_SF_BYTES;   // c_tma: R_C_WARP_BYTES per epilogue warp
+  RSmem& S = *reinterpret_cast<RSmem*>(c_area + (!SWIGLU && p.c_tma ? R_C_BYTES : 0));
   int32_t* tiles_prefix = reinterpret_cast<int32_t*>(&S + 1);   // [E+1]
   int32_t* s_off = tiles_prefix + (p.E + 1);                    // [E+1] expert_offsets
   int32_t* s_sfb = s_off + (p.E + 1);                           // [E+1] sf_row_offsets / 128
@@ -1501,12 +1561,45 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
       acc_phase ^= 1u;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * EPI_COLS;
-      epilogue_slice(p, tbase, valid, row, tl.nt * BN + cb * EPI_COLS, scale,
-                     [&] {
-                       if (rank == 0) mbar_arrive(&S.acc_empty);
-                       else mbar_arrive_remote(leader_acc_empty);
-                     });
+      auto release = [&] {
+        if (rank == 0) mbar_arrive(&S.acc_empty);
+        else mbar_arrive_remote(leader_acc_empty);
+      };
+      const int n0 = tl.nt * BN + cb * EPI_COLS;
+      if (!p.c_tma) {
+        epilogue_slice(p, tbase, valid, row, n0, scale, release);
+        continue;
+      }
+      uint32_t pk[32];
+      drain_bf16x64(tbase, scale, release, pk);
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      if (vmask != 0xffffffffu || n0 + EPI_COLS > p.N) {
+        // the expert's last rows (a box would cross into the next expert's)
+        store_rows_bf16x64(static_cast<uint16_t*>(p.out), p.N, row - lane, n0, p.N, vmask, pk);
+        continue;
+      }
+      // two 32 x 32 boxes through this warp's 2 KB of staging: lane = row,
+      // its 64 bytes as four 16-byte chunks, chunk c at c ^ ((lane >> 1) & 3)
+      // (the output tensor map's 64-byte swizzle, conflict-free shared stores)
+      uint8_t* cst = c_area + (warp - EPI_WARP0) * R_C_WARP_BYTES;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (lane == 0) bulk_wait_group_read0();   // the previous box has left the buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(cst + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) =
+              make_uint4(pk[16 * h + 4 * c], pk[16 * h + 4 * c + 1], pk[16 * h + 4 * c + 2],
+                         pk[16 * h + 4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, cst, n0 + 32 * h, static_cast<int>(row));
+          bulk_commit_group();
+        }
+      }
     }
+    if (lane == 0) bulk_wait_group0();   // every box written before the CTA exits
     if (!ok && lane == 0) fail(MINITE_ERR_TIMEOUT);
   }
 
@@ -1572,6 +1665,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t r
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// BF16 output [rows, N] for TMA stores: boxes of 32 rows x 32 columns (64
+// bytes, 64-byte swizzle).
+bool make_map_out(CUtensorMap* m, const void* base, uint64_t N, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {N, rows};
+  cuuint64_t strides[1] = {N * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The same operand as 3-D: {128 bytes of a K chunk, rows, K / 128 chunks} with
@@ -1692,6 +1799,10 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
   const size_t r_smem = 1024 + R_STAGES * (R_AB_BYTES + R_SF_BYTES) + sizeof(RSmem) +
                         3 * (E + 1) * sizeof(int32_t);
   if (variant == 6 && r_smem > 232448) variant = 1;
+  // BF16 output of the CTA-pair kernel through TMA stores when the staging fits
+  const bool c_tma = variant == 6 && out_dtype == MINITE_OUT_BF16 && r_smem + R_C_BYTES <= 232448;
+  CUtensorMap tc;
+  if (c_tma && !make_map_out(&tc, out, N, M_total)) return MINITE_ERR_CUDA;
   CUtensorMap ta, tb;
   if (variant == 5) {
     if (!make_map3(&ta, a_codes, K / 2, M_total, BM) || !make_map3(&tb, b_codes, K / 2, N * E, BN))
@@ -1701,7 +1812,7 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, N * E, b_box))
       return MINITE_ERR_CUDA;
   }
-  Params p;
+  Params p = {};
   p.a_g = a_g;
   p.b_g = b_g;
   p.a_sf = a_sf;
@@ -1715,6 +1826,7 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
   p.K = static_cast<int>(K);
   p.E = E;
   p.out_fp32 = out_dtype == MINITE_OUT_FP32;
+  p.c_tma = c_tma ? 1 : 0;
   p.budget_ns = wait_budget_ns();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t n_tiles = (N + BN - 1) / BN;
@@ -1758,11 +1870,14 @@ extern "C" int minite_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* 
     // once (a GPC with an odd SM count leaves one SM out), never more pairs
     // than pair tiles
     const int64_t max_pairs = (M_total / 256 + E) * n_tiles;
-    int pairs = resident_pairs<0>(grouped_gemm_pair_deep_kernel<false>, R_THREADS, r_smem);
+    const size_t smem = r_smem + (c_tma ? R_C_BYTES : 0);
+    int pairs = c_tma ? resident_pairs<2>(grouped_gemm_pair_deep_kernel<false>, R_THREADS, smem)
+                      : resident_pairs<0>(grouped_gemm_pair_deep_kernel<false>, R_THREADS, smem);
     if (pairs <= 0) return MINITE_ERR_CUDA;
     if (max_pairs < pairs) pairs = static_cast<int>(max_pairs);
-    if (launch_pair_pdl(grouped_gemm_pair_deep_kernel<false>, pairs, R_THREADS, r_smem, s, ta, tb,
-                        p) != cudaSuccess)
+    // without c_tma the kernel does not read its third tensor map
+    if (launch_pair_pdl(grouped_gemm_pair_deep_kernel<false>, pairs, R_THREADS, smem, s, ta, tb,
+                        c_tma ? tc : tb, p) != cudaSuccess)
       return MINITE_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
@@ -1812,7 +1927,7 @@ extern "C" int minite_gate_up_swiglu_quant_nvfp4(
   CUtensorMap ta, tb;
   if (!make_map(&ta, a_codes, K / 2, M_total, BM) || !make_map(&tb, b_codes, K / 2, 2 * I * E, 128))
     return MINITE_ERR_CUDA;
-  Params p;
+  Params p = {};
   p.a_g = a_g;
   p.b_g = b_g;
   p.a_sf = a_sf;
@@ -1839,7 +1954,7 @@ extern "C" int minite_gate_up_swiglu_quant_nvfp4(
   if (launch_pdl(zero_words_kernel, dim3(static_cast<unsigned>(zero_blocks)), dim3(256), 0, s, ws,
                  static_cast<int64_t>(words)) != cudaSuccess)
     return MINITE_ERR_CUDA;
-  if (launch_pair_pdl(grouped_gemm_pair_deep_kernel<true>, pairs, R_THREADS, smem, s, ta, tb, p) !=
+  if (launch_pair_pdl(grouped_gemm_pair_deep_kernel<true>, pairs, R_THREADS, smem, s, ta, tb, tb, p) !=
       cudaSuccess)
     return MINITE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MINITE_OK : MINITE_ERR_CUDA;
@@ -1869,7 +1984,7 @@ extern "C" int minite_grouped_gemm_wgrad_nvfp4(const uint8_t* a_codes, const uin
   CUtensorMap ta, tb;
   if (!make_map3(&ta, a_codes, k_cap / 2, M, BM) || !make_map3(&tb, b_codes, k_cap / 2, N, BN))
     return MINITE_ERR_CUDA;
-  Params p;
+  Params p = {};
   p.a_g = a_g;
   p.b_g = b_g;
   p.a_sf = a_sf;

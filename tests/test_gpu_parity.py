@@ -532,6 +532,28 @@ def test_grouped_gemm_kernels_agree_bitwise():
         assert np.array_equal(outs[0], o)
 
 
+@pytest.mark.parametrize("counts,N,K", [
+    ([300, 0, 33, 129, 64, 1], 512, 256),
+    # 401 experts: the CTA-pair kernel's output staging no longer fits beside
+    # the per-expert tables, so every row takes the plain (transposed) stores
+    ([0] * 200 + [97] + [0] * 199 + [260], 256, 128),
+])
+def test_grouped_gemm_bf16_store_paths_agree_bitwise(counts, N, K):
+    """BF16 output of the CTA-pair kernel: whole 32-row boxes by TMA stores,
+    an expert's last rows by plain stores of four-lane transposed chunks. Both
+    agree bit for bit with the single-CTA kernel and within one BF16 ulp with
+    the exact product, and rows past the last expert stay untouched."""
+    c = make_gemm_case(counts, N, K, seed=sum(counts) + len(counts))
+    outs = []
+    for v in (1, 6):
+        M.minite_set_gemm_variant(v)
+        out = run_gemm(c, torch.bfloat16, M_total=c["Mu"] + 40)
+        check_gemm(c, out)
+        assert torch.isnan(out[c["Mu"]:].float()).all()
+        outs.append(u16(out))
+    assert np.array_equal(outs[0], outs[1])
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_grouped_gemm_inconsistent_offsets_are_reported_not_executed(variant):
     M.minite_set_gemm_variant(variant)
