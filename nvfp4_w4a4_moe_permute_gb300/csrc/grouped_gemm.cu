@@ -245,17 +245,20 @@ __device__ __forceinline__ void drain_bf16x64(uint32_t tbase, float scale, Relea
   }
 }
 
-// Stores a warp's 32 consecutive rows x 64 BF16 columns [n0, n0 + 64) below
-// N; lane L holds row row0 + L as 32 packed words (four 32-byte chunks). A
-// lane owning a whole row would make every store instruction touch 32
-// different 128-byte lines; instead the four lanes of each group g exchange
-// chunks (a 4 x 4 transpose by three shuffles and two rotations on each side)
-// so that lane (g, t) stores chunk t of rows 4g..4g+3, one row per
-// instruction: each instruction writes 8 whole 128-byte row segments.
-// `vmask` has bit L set when row row0 + L exists. Call on all 32 lanes.
-__device__ __forceinline__ void store_rows_bf16x64(uint16_t* out, int64_t ld, int64_t row0,
-                                                   int n0, int N, uint32_t vmask,
-                                                   uint32_t (&pk)[32]) {
+// Stores 128 bytes of each of a warp's 32 consecutive rows: the columns
+// [n0, n0 + 128 / sizeof(T)) below N of a row-major [*, ld] array of T (64
+// BF16 or 32 FP32 columns); lane L holds row row0 + L as 32 words (four
+// 32-byte chunks). A lane owning a whole row would make every store
+// instruction touch 32 different 128-byte lines; instead the four lanes of
+// each group g exchange chunks (a 4 x 4 transpose by three shuffles and two
+// rotations on each side) so that lane (g, t) stores chunk t of rows
+// 4g..4g+3, one row per instruction: each instruction writes 8 whole
+// 128-byte row segments. `vmask` has bit L set when row row0 + L exists.
+// Call on all 32 lanes.
+template <typename T>
+__device__ __forceinline__ void store_rows_x4(T* out, int64_t ld, int64_t row0, int n0, int N,
+                                              uint32_t vmask, uint32_t (&pk)[32]) {
+  static_assert(sizeof(T) == 2 || sizeof(T) == 4, "BF16 or FP32 rows");
   const int lane = threadIdx.x & 31;
   const int t = lane & 3;
   const int gbase = lane & ~3;
@@ -279,8 +282,8 @@ __device__ __forceinline__ void store_rows_bf16x64(uint16_t* out, int64_t ld, in
     pk[16 + w] = (t & 2) ? b0 : b2;
     pk[24 + w] = (t & 2) ? b1 : b3;
   }
-  const int col = n0 + 16 * t;
-  uint16_t* o = out + (row0 + gbase) * ld + col;
+  const int col = n0 + (32 / static_cast<int>(sizeof(T))) * t;
+  T* o = out + (row0 + gbase) * ld + col;
 #pragma unroll
   for (int u = 0; u < 4; ++u)
     if (((vmask >> (gbase + u)) & 1u) && col < N)
@@ -302,9 +305,10 @@ __device__ __forceinline__ void epilogue_slice(const Params& p, uint32_t tbase, 
   if (!p.out_fp32) {
     uint32_t pk[32];
     drain_bf16x64(tbase, scale, release, pk);
-    store_rows_bf16x64(static_cast<uint16_t*>(p.out), p.N, row - lane, n0, p.N,
-                       __ballot_sync(0xffffffffu, valid), pk);
+    store_rows_x4(static_cast<uint16_t*>(p.out), p.N, row - lane, n0, p.N,
+                  __ballot_sync(0xffffffffu, valid), pk);
   } else {
+    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
       uint32_t r[32];
@@ -314,17 +318,9 @@ __device__ __forceinline__ void epilogue_slice(const Params& p, uint32_t tbase, 
         __syncwarp();
         if (lane == 0) release();
       }
-      if (valid && n0 + 32 * c < p.N) {
-        float* o = static_cast<float*>(p.out) + row * p.N + n0 + 32 * c;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t w[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            w[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[8 * i + j]), scale));
-          st_global_v8(o + 8 * i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-        }
-      }
+      for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), scale));
+      store_rows_x4(static_cast<float*>(p.out), p.N, row - lane, n0 + 32 * c, p.N, vmask, r);
     }
   }
 }
@@ -1575,7 +1571,7 @@ grouped_gemm_pair_deep_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
       if (vmask != 0xffffffffu || n0 + EPI_COLS > p.N) {
         // the expert's last rows (a box would cross into the next expert's)
-        store_rows_bf16x64(static_cast<uint16_t*>(p.out), p.N, row - lane, n0, p.N, vmask, pk);
+        store_rows_x4(static_cast<uint16_t*>(p.out), p.N, row - lane, n0, p.N, vmask, pk);
         continue;
       }
       // two 32 x 32 boxes through this warp's 2 KB of staging: lane = row,
