@@ -822,6 +822,14 @@ def run_gpu(args):
         "gemm_gate_up_frac_fp4_peak": achieved / fp4_peak,
         "stages_ms": {s: round(v, 4) for s, v in stage_ms.items()},
         "stages_hbm_gbs": {s: round(v, 1) for s, v in hbm.items()},
+        # each stage against its own bound: the measured HBM copy rate for the
+        # bandwidth stages, the FP4 burst basis for the GEMMs
+        "stages_frac_of_peak": dict(
+            {s: round(v / peaks["hbm"], 3) for s, v in hbm.items()},
+            **{g: round(fl[g] / (stage_ms[g] / 1e3) / 1e12 / fp4_peak, 3)
+               for g in ("gemm_gate_up", "gemm_down", "gemm_dgrad")}),
+        "gemms_tflops": {g: round(fl[g] / (stage_ms[g] / 1e3) / 1e12, 1)
+                         for g in ("gemm_gate_up", "gemm_down", "gemm_dgrad")},
         "roofline": {"kernel": f"{GEMM_KERNELS.get(args.gemm_variant or 6)} (gate_up)",
                      "bound": "tensor",
                      "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
