@@ -508,13 +508,13 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // `budget_ns` passed since the wait began, or *abort became non-zero first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
                                           volatile int* abort) {
-  // each attempt sleeps at most min(budget, 20 us), so a short budget still
-  // runs out on time
-  const uint32_t hint = budget_ns < 20000u ? static_cast<uint32_t>(budget_ns) : 20000u;
-  if (mbar_try_wait(bar, parity, hint)) return true;
+  // no suspend-time hint: each attempt returns at once if the phase is not
+  // complete (the grouped GEMMs measured 2-3% faster than with attempts that
+  // may sleep 1 or 20 us), so a short budget also runs out on time
+  if (mbar_try_wait(bar, parity, 0u)) return true;
   // the abort flag and the clock are checked after every failed attempt
   const uint64_t start = globaltimer();
-  while (!mbar_try_wait(bar, parity, hint)) {
+  while (!mbar_try_wait(bar, parity, 0u)) {
     if (*abort) return false;
     if (globaltimer() - start > budget_ns) return false;
   }
